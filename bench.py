@@ -1,0 +1,392 @@
+"""Benchmark: paged GQA decode attention on GB300 through the C-ABI library.
+
+One step = one call of the whole hot path (plan, page-table walk, TMA page
+gather, scores, online softmax, PV, split epilogue, merge) over one batch of
+seeded synthetic inputs resident in HBM.  L2 is flushed (a 2 x L2-size buffer
+is rewritten) before every timed step, outside the step's event pair.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl pkv|reference]
+
+Prints one JSON line (rank 0).  `value` is achieved GB/s of algorithmic bytes
+(K and V of the valid keys, q, out, lse, used block-table entries, lengths)
+summed over all ranks, divided by the max over ranks of the time per step.
+`--impl reference` times the CPU fp64 oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged GQA decode attn: µs/call, achieved HBM GB/s and % of GB300 peak"
+NOMINAL_HBM_GBS = 8000.0
+KERNEL_SOURCES = ["paged_kv_gqa_gb300/csrc/decode_kernel.cuh", "paged_kv_gqa_gb300/csrc/ptx.cuh",
+                  "paged_kv_gqa_gb300/csrc/plan.h"]
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the decode kernel from the committed ncu summary,
+    only if that summary was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "decode_split_kernel_%s.md" % workload)
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if line.startswith("- ") and ":" in line:
+                k, v = line[2:].split(":", 1)
+                fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    try:
+        return int(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.device_index = device_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device_index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append(parts)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm = [float(s[1]) for s in self.samples if s[1].replace(".", "", 1).isdigit()]
+        mx = [float(s[2]) for s in self.samples if s[2].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4) if s[5 + i].lower() == "active"})
+        power = [float(s[3]) for s in self.samples if s[3].replace(".", "", 1).isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples),
+                "power_w_max": max(power) if power else None}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if os.environ.get("PKV_BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+        dist.init_process_group(backend)
+        return dist, rank, world, local
+    return None, rank, world, local
+
+
+def run_reference(args) -> None:
+    """The oracle as it stands, timed on the host cores (one bounded sample per step)."""
+    import numpy as np
+    import oracle
+    from workloads import algorithmic_bytes, make_case
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    case = make_case(args.workload)
+    q, k, v, bt, sl = case.host_bits()
+    rows, sample = _reference_sample(case, args.ref_seconds)
+    ab = algorithmic_bytes(case)
+    frac = len(rows) / (case.B * case.Hq)
+    step_bytes = ab["total"] * frac
+    cores = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        oracle.paged_decode(q, k, v, bt, sl, case.scale, select=rows)
+    t = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.paged_decode(q, k, v, bt, sl, case.scale, select=rows)
+        t.append(time.perf_counter() - t0)
+    sec = sum(t) / len(t)
+    value = step_bytes / sec / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config_block(case, args, plan=None),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _reference_sample(case, seconds_hint):
+    """Rows (b, h) for a bounded CPU sample: every sequence, a stride of heads, so that
+    one oracle pass over them is roughly a second or less on a many-core host."""
+    import numpy as np
+    lens = case.seq_lens.numpy().astype(np.int64)
+    work = float((lens * case.Hq).sum()) * case.D * 4  # fp64 flops of a full pass
+    budget = 2.0e9 * max(0.25, seconds_hint)            # ~2 GFLOP/s/core-ish, times the hint
+    stride = 1
+    while work / stride > budget * (os.cpu_count() or 1) and stride < case.Hq:
+        stride *= 2
+    rows = [(b, h) for b in range(case.B) for h in range(0, case.Hq, stride)]
+    return rows, "all %d sequences, every %d-th query head (%d of %d rows) per step" % (
+        case.B, stride, len(rows), case.B * case.Hq)
+
+
+def _config_block(case, args, plan):
+    lens = case.seq_lens.cpu().numpy()
+    cfg = {"workload": args.workload, "B": case.B, "Hq": case.Hq, "Hkv": case.Hkv, "D": case.D,
+           "page_size": case.P, "num_pages": case.num_pages, "max_pages": case.max_pages,
+           "seq_lens": {"min": int(lens.min()), "max": int(lens.max()), "sum": int(lens.sum())},
+           "seed": case.meta["seed"], "l2": "flushed before every timed step (2 x L2 bytes rewritten)"}
+    if plan is not None:
+        cfg.update({"num_splits": plan["num_splits"], "chunk_tokens": plan["chunk_tokens"],
+                    "grid_blocks": plan["grid_blocks"], "blocks_per_sm": plan["blocks_per_sm"]})
+    return cfg
+
+
+def _cpu_baseline(case, seconds: float) -> dict:
+    """The oracle as it stands on the host cores, on a bounded sample of the workload."""
+    import oracle
+    from workloads import algorithmic_bytes
+    q, k, v, bt, sl = case.host_bits()
+    rows, sample = _reference_sample(case, 1.0)
+    frac = len(rows) / (case.B * case.Hq)
+    step_bytes = algorithmic_bytes(case)["total"] * frac
+    n, t_total = 0, 0.0
+    t_end = time.perf_counter() + seconds
+    while time.perf_counter() < t_end or n == 0:
+        t0 = time.perf_counter()
+        oracle.paged_decode(q, k, v, bt, sl, case.scale, select=rows)
+        t_total += time.perf_counter() - t0
+        n += 1
+    return {"value": round(step_bytes * n / t_total / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count() or 1,
+            "kind": "oracle", "sample": "%s; %d passes in %.1f s" % (sample, n, t_total)}
+
+
+def run_pkv(args) -> None:
+    import torch
+    import paged_kv_gqa_gb300 as pkv
+    from workloads import algorithmic_bytes, make_case
+
+    dist, rank, world, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pkv.load()
+
+    case = make_case(args.workload, device=dev)
+    ab = algorithmic_bytes(case)
+    props = torch.cuda.get_device_properties(dev)
+    plan = pkv.plan_query(case.B, case.Hq, case.Hkv, case.D, case.P, case.max_pages, props.multi_processor_count)
+    ws_bytes = pkv.paged_decode_attn_workspace_size(case.B, case.Hq, case.Hkv, case.D, case.P, case.max_pages)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    out = torch.empty((case.B, case.Hq, case.D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((case.B, case.Hq), dtype=torch.float32, device=dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    launches_per_call = 1 + plan["merge_needed"]
+
+    def call():
+        pkv.paged_decode_attn(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens, case.scale,
+                              out, lse, ws, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        call()
+    torch.cuda.synchronize()
+    if pkv.pkv_check_status(ws) != 0:
+        raise RuntimeError("device status %d after warm-up" % pkv.pkv_check_status(ws))
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xff)
+        starts[i].record(stream)
+        call()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    mean_ms = sum(step_ms) / len(step_ms)
+    if dist:
+        t = torch.tensor([mean_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        mean_ms = float(t.item())
+    status = pkv.pkv_check_status(ws)
+
+    # ---- end to end through the public API with host buffers -------------------
+    e2e = None
+    if not args.no_e2e:
+        e2e = _e2e(args, case, ab, pkv, torch, dev, stream, flush, plan, dist)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = _cpu_baseline(case.to("cpu"), args.cpu_seconds)
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    peaks = measured_peaks()
+    gbs = ab["total"] / (mean_ms * 1e-3) / 1e9
+    traffic = profiled_traffic(args.workload)
+    line = {
+        "metric": METRIC, "value": round(gbs * world, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(mean_ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, shuffled page pool)",
+        "config": _config_block(case, args, plan),
+        "us_per_call": round(mean_ms * 1e3, 3),
+        "us_per_call_p10_p50_p90": [round(x * 1e3, 3) for x in _quantiles(step_ms)],
+        "pct_of_measured_hbm": round(100 * gbs / peaks["hbm_gbs"], 2),
+        "pct_of_nominal_8tbs": round(100 * gbs / NOMINAL_HBM_GBS, 2),
+        "algorithmic_bytes": ab["total"], "tail_bytes_touched": ab["tail_bytes"],
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": traffic,
+                     "kernel": "decode_split_kernel (+ merge_kernel when splits > 1, timed together)",
+                     "peak_source": peaks["source"]},
+        "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches_per_call * args.steps,
+        "clocks": clocks, "device_status": status, "wall_s_timed_region": round(t_wall, 3),
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def _quantiles(xs):
+    s = sorted(xs)
+    return [s[int(0.1 * (len(s) - 1))], s[int(0.5 * (len(s) - 1))], s[int(0.9 * (len(s) - 1))]]
+
+
+def _e2e(args, case, ab, pkv, torch, dev, stream, flush, plan, dist):
+    """Same metric, through the public call with host buffers: each step copies the
+    step's inputs host -> device from pinned memory, runs the call, and reads the
+    result back."""
+    host = {n: getattr(case, n).cpu().pin_memory() for n in ("q", "k_cache", "v_cache", "block_table", "seq_lens")}
+    devb = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+    out_h = torch.empty((case.B, case.Hq, case.D), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty((case.B, case.Hq), dtype=torch.float32).pin_memory()
+    out = torch.empty((case.B, case.Hq, case.D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((case.B, case.Hq), dtype=torch.float32, device=dev)
+    ws = torch.zeros(plan["workspace_bytes"], dtype=torch.uint8, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    steps = max(3, min(args.steps, args.e2e_steps))
+
+    def step():
+        for n in host:
+            devb[n].copy_(host[n], non_blocking=True)
+        pkv.paged_decode_attn(devb["q"], devb["k_cache"], devb["v_cache"], devb["block_table"], devb["seq_lens"],
+                              case.scale, out, lse, ws, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for s, e in ev:
+        flush.fill_(2)
+        s.record(stream)
+        step()
+        e.record(stream)
+    torch.cuda.synchronize()
+    ms = sum(s.elapsed_time(e) for s, e in ev) / steps
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    world = dist.get_world_size() if dist else 1
+    return {"value": round(ab["total"] * world / (ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4), "steps": steps}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="batch",
+                    choices=["tiny", "batch", "ragged", "long", "bigpage", "bigpage_g16"])
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=1.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_pkv(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,216 @@
+/*
+ * pkv.h -- C interface of the paged GQA decode-attention library for GB300
+ * (sm_103a).
+ *
+ * The operation (FlashQuant wiki "CUDA Kernels": flash_attention.cu "Online
+ * Softmax" and "GQA (Grouped Query Attention) Support"; paged_decode.cu "Page
+ * Table Addressing", "Partial Output", "Early Exit for Empty Splits";
+ * split_k_reduce.cu "Algorithm"):
+ *
+ *   for every sequence b < B and query head h < Hq, with G = Hq / Hkv and
+ *   kv = h / G (contiguous head groups), L = seq_lens[b]:
+ *     k_j = k_cache[block_table[b][j / page_size], j % page_size, kv, :]
+ *     v_j = v_cache[block_table[b][j / page_size], j % page_size, kv, :]
+ *     s_j = scale * <q[b, h, :], k_j>                      j = 0 .. L-1
+ *     out[b, h, :] = sum_j softmax(s)_j v_j                 (bf16, round to nearest even)
+ *     lse[b, h]    = ln sum_j exp(s_j)                      (f32, natural log)
+ *   L == 0 gives out = 0 and lse = -inf.
+ *
+ * The key range of every (b, kv head) is split over thread blocks (split-KV,
+ * "flash-decoding"); each split keeps an online softmax in f32 and the splits
+ * are merged by log-sum-exp.  The split count is a pure function of the shape
+ * and the SM count (OASR "Kernel Layer", "Fused attention": the split count
+ * must not depend on capture state because it changes the order the f32
+ * partials are summed).
+ *
+ * Conventions (OASR "Kernel Layer", "Fused attention"; Atlas "CUDA Kernel
+ * Engineering", "Conventions every Atlas kernel follows" and "CUDA graphs"):
+ *   - every pointer is a DEVICE pointer unless marked "host";
+ *   - every array is dense row-major, rightmost index contiguous;
+ *   - every device pointer must be 16-byte aligned;
+ *   - integers in tables are int32;
+ *   - the caller owns every buffer, including the workspace: the library
+ *     allocates no device memory, never synchronises inside a launch call, and
+ *     its launch calls can be captured into a CUDA graph (no allocation, no
+ *     synchronisation, no branch on capture state);
+ *   - launch calls are asynchronous on `stream`; a bad argument returns a
+ *     negative status BEFORE anything is launched; errors the device finds are
+ *     recorded in a sticky status word at the start of the workspace and read
+ *     back with pkv_check_status();
+ *   - bf16 buffers are typed pkv_bf16 (the raw 16-bit pattern), so this header
+ *     is valid C.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+typedef uint16_t pkv_bf16; /* bfloat16 bit pattern */
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = -1,         /* null pointer, non-positive size, Hq % Hkv != 0, seq bound */
+    PKV_ERR_UNSUPPORTED = -2,         /* D not in {64,128,256}, page_size not a power of two in
+                                         [8,256], group size Hq/Hkv > 32, no sm_103a device */
+    PKV_ERR_MISALIGNED = -3,          /* a device pointer is not 16-byte aligned */
+    PKV_ERR_WORKSPACE_TOO_SMALL = -4, /* workspace_bytes below the size query's answer */
+    PKV_ERR_CUDA = -5,                /* a CUDA runtime/driver call failed */
+    PKV_ERR_BAD_PAGE_INDEX = -6,      /* device: a used block_table entry outside [0, num_pages) */
+    PKV_ERR_DEVICE_TIMEOUT = -7,      /* device: a bounded wait for a copy ran out */
+    PKV_ERR_BAD_SEQ_LEN = -8          /* device: seq_lens[b] < 0 or > max_pages * page_size */
+} pkv_status;
+
+/* Human-readable name of a status code (static string; never NULL). */
+PKV_API const char *pkv_status_string(int status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+PKV_API int pkv_version(void);
+
+/* ------------------------------------------------------------------ planning */
+
+/*
+ * What a launch will do for a shape.  Returned by pkv_plan_query; the same
+ * function decides every launch, so a plan queried on the host is the plan the
+ * launch uses.
+ */
+typedef struct {
+    int num_splits;       /* S: key-range splits per (b, kv head) at full table width */
+    int chunk_tokens;     /* keys per split (a multiple of stage_tokens) */
+    int stage_tokens;     /* keys per pipeline stage (one TMA box row set) */
+    int warps;            /* consumer warps per thread block */
+    int ring_stages;      /* stages in flight per warp */
+    int blocks_per_sm;    /* resident thread blocks per SM the plan assumes */
+    int grid_blocks;      /* thread blocks of the split kernel (S * Hkv * B) */
+    int smem_bytes;       /* dynamic shared memory per block */
+    int merge_needed;     /* 1 when S > 1 (the merge kernel runs) */
+    size_t workspace_bytes;
+} pkv_plan;
+
+/*
+ * Pure host function: the plan for a shape on a device with `num_sms` SMs.
+ * num_splits > 0 forces that many splits (clamped to [1, ceil(max_pages *
+ * page_size / stage_tokens)]); 0 chooses automatically.  No CUDA call.
+ */
+PKV_API pkv_status pkv_plan_query(int B, int Hq, int Hkv, int D, int page_size, int max_pages,
+                          int num_sms, int num_splits, pkv_plan *plan /* host */);
+
+/*
+ * Workspace bytes that paged_decode_attn needs for this shape on `device`
+ * (queries the device's SM count).  The workspace holds a 256-byte header whose
+ * first int32 is the device status word, then the split partials.  Before its
+ * first use the header must be zero (allocate zeroed, or call
+ * pkv_reset_status).
+ */
+PKV_API pkv_status paged_decode_attn_workspace_size(int B, int Hq, int Hkv, int D, int page_size,
+                                            int max_pages, int device, size_t *bytes /* host */);
+
+/* Same, for a forced split count (see paged_decode_attn_ex). */
+PKV_API pkv_status paged_decode_attn_workspace_size_ex(int B, int Hq, int Hkv, int D, int page_size,
+                                               int max_pages, int device, int num_splits,
+                                               size_t *bytes /* host */);
+
+/* ------------------------------------------------------------------ decode */
+
+/*
+ * Paged GQA decode attention (one query token per sequence).
+ *
+ *   q           [B, Hq, D] bf16
+ *   k_cache     [num_pages, page_size, Hkv, D] bf16 (the page pool)
+ *   v_cache     [num_pages, page_size, Hkv, D] bf16
+ *   block_table [B, max_pages] int32: physical page of each logical page
+ *   seq_lens    [B] int32: keys per sequence
+ *   scale       multiplies q.k (the caller passes e.g. 1/sqrt(D))
+ *   out         [B, Hq, D] bf16 (written)
+ *   lse         [B, Hq] f32, natural log (written); may be NULL
+ *   workspace   caller-owned device buffer of workspace_bytes bytes
+ *
+ * Requirements checked on the host: pointers non-NULL (lse excepted) and
+ * 16-byte aligned; B >= 0 (B == 0 is a no-op); Hq, Hkv, num_pages, max_pages
+ * >= 1; Hq % Hkv == 0 and Hq / Hkv <= 32; D in {64, 128, 256}; page_size a
+ * power of two in [8, 256]; workspace large enough.
+ *
+ * Device-data preconditions (not checked on the host): 0 <= seq_lens[b] <=
+ * max_pages * page_size, and block_table[b][0 .. ceil(seq_lens[b]/page_size)-1]
+ * are page ids in [0, num_pages).  Entries past that are never read and may
+ * hold anything; key slots past seq_lens[b] in the last page are never used
+ * (they may hold NaN).  A violation is not a fault: a page id out of range is
+ * skipped (its keys contribute nothing) and the status word records
+ * PKV_ERR_BAD_PAGE_INDEX; a length out of range makes that sequence empty
+ * (out = 0, lse = -inf) and records PKV_ERR_BAD_SEQ_LEN.  The first error
+ * recorded since the last reset is kept.
+ */
+PKV_API pkv_status paged_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                             const int32_t *block_table, const int32_t *seq_lens,
+                             int B, int Hq, int Hkv, int D, int page_size, int num_pages,
+                             int max_pages, float scale, pkv_bf16 *out, float *lse,
+                             void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Same as paged_decode_attn with a forced split count (num_splits > 0), for
+ * tests and sweeps; 0 is the automatic choice.  Results for different split
+ * counts differ only by f32 summation order.
+ */
+PKV_API pkv_status paged_decode_attn_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                                const int32_t *block_table, const int32_t *seq_lens,
+                                int B, int Hq, int Hkv, int D, int page_size, int num_pages,
+                                int max_pages, float scale, pkv_bf16 *out, float *lse,
+                                void *workspace, size_t workspace_bytes, int num_splits,
+                                cudaStream_t stream);
+
+/* ------------------------------------------------------------------ merge */
+
+/*
+ * Log-sum-exp merge of S per-split partial results (FlashQuant wiki "CUDA
+ * Kernels", split_k_reduce.cu "Algorithm" and "Numerical Stability"), in the
+ * self-contained form: each split passes its softmax-normalised output and
+ * its natural-log LSE.
+ *
+ *   partial_out [S, B, Hq, D] f32   split s's output over its own keys
+ *   partial_lse [S, B, Hq] f32      split s's LSE; -inf marks an empty split
+ *   out         [B, Hq, D] bf16     sum_s w_s o_s / sum_s w_s,  w_s = exp(lse_s - max_s lse_s)
+ *   lse         [B, Hq] f32         max + ln sum_s w_s; may be NULL
+ * Every split empty gives out = 0 and lse = -inf.  S >= 1, D in {64,128,256}.
+ * This is also the combine step a caller would run after gathering partials
+ * produced elsewhere (for example by another device holding part of the keys).
+ */
+PKV_API pkv_status split_kv_merge(const float *partial_out, const float *partial_lse, int S, int B,
+                          int Hq, int D, pkv_bf16 *out, float *lse, cudaStream_t stream);
+
+/* ------------------------------------------------------------------ status */
+
+/*
+ * Synchronises `stream`, then copies the workspace's device status word into
+ * *device_status (host): PKV_OK or the first device-side error recorded since
+ * the last reset.  Returns PKV_ERR_CUDA if the synchronisation or copy fails.
+ */
+PKV_API pkv_status pkv_check_status(const void *workspace, cudaStream_t stream, int *device_status /* host */);
+
+/* Zeroes the workspace's status word, asynchronously on `stream`. */
+PKV_API pkv_status pkv_reset_status(void *workspace, cudaStream_t stream);
+
+/*
+ * Diagnostic: launches one block that waits, with the same bounded wait the
+ * decode kernel uses, on a barrier that nothing ever completes, for at most
+ * `timeout_us` microseconds, then records PKV_ERR_DEVICE_TIMEOUT in the
+ * workspace status word and returns.  Lets a test check that a stalled copy
+ * ends in a status code rather than a hang.
+ */
+PKV_API pkv_status pkv_selftest_wait_timeout(void *workspace, unsigned timeout_us, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

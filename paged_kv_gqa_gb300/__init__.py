@@ -1,0 +1,205 @@
+"""Paged GQA decode attention for GB300 (sm_103a): Python binding of the C library.
+
+Every function here only marshals arguments (device pointers, sizes, the
+current CUDA stream) into the C entry points of ``include/pkv.h`` with the same
+names; all of the work runs in the library's CUDA kernels.  There is no
+fallback: if the compiled library is missing, every call raises.
+
+Build the library with ``python -m paged_kv_gqa_gb300._build`` (or
+``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "PkvError", "load", "status_string", "plan_query", "paged_decode_attn_workspace_size",
+    "paged_decode_attn", "paged_decode_attn_ex", "split_kv_merge", "pkv_check_status",
+    "pkv_reset_status", "pkv_selftest_wait_timeout", "EXPORTED_SYMBOLS", "STATUS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libpkv.so")
+
+STATUS = {
+    0: "PKV_OK", -1: "PKV_ERR_INVALID_ARG", -2: "PKV_ERR_UNSUPPORTED", -3: "PKV_ERR_MISALIGNED",
+    -4: "PKV_ERR_WORKSPACE_TOO_SMALL", -5: "PKV_ERR_CUDA", -6: "PKV_ERR_BAD_PAGE_INDEX",
+    -7: "PKV_ERR_DEVICE_TIMEOUT", -8: "PKV_ERR_BAD_SEQ_LEN",
+}
+
+# Every symbol include/pkv.h declares.
+EXPORTED_SYMBOLS = [
+    "pkv_status_string", "pkv_version", "pkv_plan_query", "paged_decode_attn_workspace_size",
+    "paged_decode_attn_workspace_size_ex", "paged_decode_attn", "paged_decode_attn_ex", "split_kv_merge",
+    "pkv_check_status", "pkv_reset_status", "pkv_selftest_wait_timeout",
+]
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s returned %s (%d)" % (where, STATUS.get(status, "unknown"), status))
+
+
+class PkvPlan(ctypes.Structure):
+    _fields_ = [("num_splits", ctypes.c_int), ("chunk_tokens", ctypes.c_int), ("stage_tokens", ctypes.c_int),
+                ("warps", ctypes.c_int), ("ring_stages", ctypes.c_int), ("blocks_per_sm", ctypes.c_int),
+                ("grid_blocks", ctypes.c_int), ("smem_bytes", ctypes.c_int), ("merge_needed", ctypes.c_int),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Loads the compiled library (raises if it was not built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError("paged_kv_gqa_gb300: CUDA library %s is missing; build it with "
+                               "`python -m paged_kv_gqa_gb300._build`" % path)
+        lib = ctypes.CDLL(path)
+        P, I, F, S, U = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_uint
+        sig = {
+            "pkv_status_string": (ctypes.c_char_p, [I]),
+            "pkv_version": (I, []),
+            "pkv_plan_query": (I, [I, I, I, I, I, I, I, I, ctypes.POINTER(PkvPlan)]),
+            "paged_decode_attn_workspace_size": (I, [I, I, I, I, I, I, I, ctypes.POINTER(S)]),
+            "paged_decode_attn_workspace_size_ex": (I, [I, I, I, I, I, I, I, I, ctypes.POINTER(S)]),
+            "paged_decode_attn": (I, [P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, S, P]),
+            "paged_decode_attn_ex": (I, [P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, S, I, P]),
+            "split_kv_merge": (I, [P, P, I, I, I, I, P, P, P]),
+            "pkv_check_status": (I, [P, P, ctypes.POINTER(I)]),
+            "pkv_reset_status": (I, [P, P]),
+            "pkv_selftest_wait_timeout": (I, [P, U, P]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise PkvError(status, where)
+
+
+def status_string(status: int) -> str:
+    return load().pkv_status_string(int(status)).decode()
+
+
+def plan_query(B, Hq, Hkv, D, page_size, max_pages, num_sms, num_splits=0) -> dict:
+    plan = PkvPlan()
+    _check(load().pkv_plan_query(B, Hq, Hkv, D, page_size, max_pages, num_sms, num_splits, ctypes.byref(plan)),
+           "pkv_plan_query")
+    return plan.as_dict()
+
+
+# ----------------------------------------------------------------- tensor helpers (torch only for plumbing)
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dev_ptr(t, dtype, name, ndim=None):
+    torch = _torch()
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError("%s must have %d dimensions, got shape %s" % (name, ndim, tuple(t.shape)))
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def paged_decode_attn_workspace_size(B, Hq, Hkv, D, page_size, max_pages, device=None, num_splits=0) -> int:
+    torch = _torch()
+    dev = torch.cuda.current_device() if device is None else int(device)
+    n = ctypes.c_size_t(0)
+    _check(load().paged_decode_attn_workspace_size_ex(B, Hq, Hkv, D, page_size, max_pages, dev, num_splits,
+                                                      ctypes.byref(n)), "paged_decode_attn_workspace_size")
+    return n.value
+
+
+def paged_decode_attn_ex(q, k_cache, v_cache, block_table, seq_lens, scale, out, lse, workspace,
+                         num_splits=0, stream=None):
+    """Calls paged_decode_attn_ex on torch CUDA tensors (shapes as in include/pkv.h)."""
+    torch = _torch()
+    B, Hq, D = q.shape
+    num_pages, P, Hkv, Dk = k_cache.shape
+    if Dk != D or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("q/k_cache/v_cache shapes disagree")
+    if tuple(out.shape) != (B, Hq, D):
+        raise ValueError("out must be [B, Hq, D]")
+    if lse is not None and tuple(lse.shape) != (B, Hq):
+        raise ValueError("lse must be [B, Hq]")
+    max_pages = block_table.shape[1]
+    st = load().paged_decode_attn_ex(
+        _dev_ptr(q, torch.bfloat16, "q", 3), _dev_ptr(k_cache, torch.bfloat16, "k_cache", 4),
+        _dev_ptr(v_cache, torch.bfloat16, "v_cache", 4), _dev_ptr(block_table, torch.int32, "block_table", 2),
+        _dev_ptr(seq_lens, torch.int32, "seq_lens", 1), B, Hq, Hkv, D, P, num_pages, max_pages,
+        ctypes.c_float(scale), _dev_ptr(out, torch.bfloat16, "out", 3),
+        _dev_ptr(lse, torch.float32, "lse", 2) if lse is not None else None,
+        _dev_ptr(workspace, workspace.dtype, "workspace"), workspace.numel() * workspace.element_size(),
+        int(num_splits), _stream_handle(stream))
+    _check(st, "paged_decode_attn_ex")
+    return out, lse
+
+
+def paged_decode_attn(q, k_cache, v_cache, block_table, seq_lens, scale, out, lse, workspace, stream=None):
+    """Calls paged_decode_attn (automatic split count) on torch CUDA tensors."""
+    return paged_decode_attn_ex(q, k_cache, v_cache, block_table, seq_lens, scale, out, lse, workspace,
+                                num_splits=0, stream=stream)
+
+
+def split_kv_merge(partial_out, partial_lse, out, lse=None, stream=None):
+    """Calls split_kv_merge: partial_out [S,B,Hq,D] f32, partial_lse [S,B,Hq] f32 -> out bf16, lse f32."""
+    torch = _torch()
+    S, B, Hq, D = partial_out.shape
+    if tuple(partial_lse.shape) != (S, B, Hq):
+        raise ValueError("partial_lse must be [S, B, Hq]")
+    st = load().split_kv_merge(_dev_ptr(partial_out, torch.float32, "partial_out", 4),
+                               _dev_ptr(partial_lse, torch.float32, "partial_lse", 3), S, B, Hq, D,
+                               _dev_ptr(out, torch.bfloat16, "out", 3),
+                               _dev_ptr(lse, torch.float32, "lse", 2) if lse is not None else None,
+                               _stream_handle(stream))
+    _check(st, "split_kv_merge")
+    return out, lse
+
+
+def pkv_check_status(workspace, stream=None) -> int:
+    """Synchronises the stream and returns the workspace's device status word."""
+    v = ctypes.c_int(0)
+    _check(load().pkv_check_status(ctypes.c_void_p(workspace.data_ptr()), _stream_handle(stream), ctypes.byref(v)),
+           "pkv_check_status")
+    return v.value
+
+
+def pkv_reset_status(workspace, stream=None):
+    _check(load().pkv_reset_status(ctypes.c_void_p(workspace.data_ptr()), _stream_handle(stream)),
+           "pkv_reset_status")
+
+
+def pkv_selftest_wait_timeout(workspace, timeout_us=1000, stream=None):
+    _check(load().pkv_selftest_wait_timeout(ctypes.c_void_p(workspace.data_ptr()), int(timeout_us),
+                                            _stream_handle(stream)), "pkv_selftest_wait_timeout")

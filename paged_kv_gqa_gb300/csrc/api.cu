@@ -1,0 +1,368 @@
+// api.cu -- the C-ABI entry points declared in include/pkv.h.
+//
+// Host side of the library: argument checks (before any launch), the plan,
+// the TMA tensor-map cache, and the kernel launches.  Launch calls never
+// allocate device memory and never synchronise.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "decode_kernel.cuh"
+#include "merge_kernel.cuh"
+#include "pkv.h"
+#include "plan.h"
+
+namespace pkv {
+namespace {
+
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s: far above any healthy copy
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int log2_exact(int x)
+{
+    int r = 0;
+    while ((1 << r) < x) ++r;
+    return r;
+}
+
+// ---------------------------------------------------------------- tensor maps
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+struct MapKey {
+    const void *ptr;
+    int num_pages, P, Hkv, D, box_t, device;
+    bool operator==(const MapKey &o) const
+    {
+        return ptr == o.ptr && num_pages == o.num_pages && P == o.P && Hkv == o.Hkv && D == o.D &&
+               box_t == o.box_t && device == o.device;
+    }
+};
+
+struct MapCache {
+    static constexpr int N = 64;
+    MapKey keys[N];
+    CUtensorMap maps[N];
+    bool used[N] = {};
+    int next = 0;
+    std::mutex mu;
+};
+
+MapCache &map_cache()
+{
+    static MapCache c;
+    return c;
+}
+
+// View of the page pool [num_pages*P rows, Hkv, D] bf16, box (64 dims, 1 head,
+// box_t rows), 128-byte swizzle.  Cached per (pointer, shape, device).
+pkv_status get_pool_map(const void *pool, int num_pages, int P, int Hkv, int D, int box_t, int device,
+                        CUtensorMap *out)
+{
+    MapKey key{pool, num_pages, P, Hkv, D, box_t, device};
+    MapCache &c = map_cache();
+    std::lock_guard<std::mutex> lock(c.mu);
+    for (int i = 0; i < MapCache::N; ++i)
+        if (c.used[i] && c.keys[i] == key) {
+            *out = c.maps[i];
+            return PKV_OK;
+        }
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return PKV_ERR_CUDA;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)num_pages * (cuuint64_t)P};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
+    const cuuint32_t box[3] = {64u, 1u, (cuuint32_t)box_t};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUtensorMap m;
+    const CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return PKV_ERR_CUDA;
+    const int slot = c.next;
+    c.next = (c.next + 1) % MapCache::N;
+    c.keys[slot] = key;
+    c.maps[slot] = m;
+    c.used[slot] = true;
+    *out = m;
+    return PKV_OK;
+}
+
+// ---------------------------------------------------------------- device facts
+
+pkv_status current_device_sms(int *device, int *sms)
+{
+    if (cudaGetDevice(device) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, *device) != cudaSuccess) return PKV_ERR_CUDA;
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *device);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *device);
+    if (major != 10 || minor != 3) return PKV_ERR_UNSUPPORTED;  // built for sm_103a only
+    return PKV_OK;
+}
+
+// ---------------------------------------------------------------- launches
+
+template <int D, int NT>
+pkv_status launch_decode_variant(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
+                                 const pkv_plan &plan, int B, int Hkv, int device, cudaStream_t stream)
+{
+    static bool attr_set[64] = {};
+    static std::mutex mu;
+    auto kern = decode_split_kernel<D, NT>;
+    if (device < 0 || device >= 64) return PKV_ERR_UNSUPPORTED;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!attr_set[device]) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448) != cudaSuccess)
+                return PKV_ERR_CUDA;
+            attr_set[device] = true;
+        }
+    }
+    dim3 grid(plan.num_splits, Hkv, B);
+    dim3 block(plan.warps * 32);
+    kern<<<grid, block, plan.smem_bytes, stream>>>(mk, mv, p);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status launch_decode(int D, int NT, const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
+                         const pkv_plan &plan, int B, int Hkv, int device, cudaStream_t stream)
+{
+#define PKV_CASE(DD, NN) \
+    if (D == DD && NT == NN) return launch_decode_variant<DD, NN>(mk, mv, p, plan, B, Hkv, device, stream);
+    PKV_CASE(64, 1)
+    PKV_CASE(64, 2)
+    PKV_CASE(64, 4)
+    PKV_CASE(128, 1)
+    PKV_CASE(128, 2)
+    PKV_CASE(128, 4)
+    PKV_CASE(256, 1)
+    PKV_CASE(256, 2)
+    PKV_CASE(256, 4)
+#undef PKV_CASE
+    return PKV_ERR_UNSUPPORTED;
+}
+
+pkv_status launch_merge(int D, const MergeParams &mp, cudaStream_t stream)
+{
+    const int rows = mp.B * mp.Hq;
+    dim3 grid((rows + kMergeWarps - 1) / kMergeWarps), block(kMergeWarps * 32);
+    switch (D) {
+        case 64: merge_kernel<64><<<grid, block, 0, stream>>>(mp); break;
+        case 128: merge_kernel<128><<<grid, block, 0, stream>>>(mp); break;
+        case 256: merge_kernel<256><<<grid, block, 0, stream>>>(mp); break;
+        default: return PKV_ERR_UNSUPPORTED;
+    }
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status decode_impl(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                       const int32_t *block_table, const int32_t *seq_lens, int B, int Hq, int Hkv, int D,
+                       int page_size, int num_pages, int max_pages, float scale, pkv_bf16 *out, float *lse,
+                       void *workspace, size_t workspace_bytes_, int num_splits, cudaStream_t stream)
+{
+    if (num_pages <= 0 || num_splits < 0 || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+    const pkv_status shape_ok = validate_shape(B, Hq, Hkv, D, page_size, max_pages);
+    if (shape_ok != PKV_OK) return shape_ok;
+    if (B == 0) return PKV_OK;
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out || !workspace) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(block_table) ||
+        !aligned16(seq_lens) || !aligned16(out) || (lse && !aligned16(lse)) || !aligned16(workspace))
+        return PKV_ERR_MISALIGNED;
+    if ((long)num_pages * page_size >= (1l << 31)) return PKV_ERR_INVALID_ARG;
+
+    int device = 0, sms = 0;
+    pkv_status st = current_device_sms(&device, &sms);
+    if (st != PKV_OK) return st;
+    pkv_plan plan;
+    st = make_plan(B, Hq, Hkv, D, page_size, max_pages, sms, num_splits, &plan);
+    if (st != PKV_OK) return st;
+    if (workspace_bytes_ < plan.workspace_bytes) return PKV_ERR_WORKSPACE_TOO_SMALL;
+
+    const int box_t = plan.stage_tokens < page_size ? plan.stage_tokens : page_size;
+    CUtensorMap mk, mv;
+    st = get_pool_map(k_cache, num_pages, page_size, Hkv, D, box_t, device, &mk);
+    if (st != PKV_OK) return st;
+    st = get_pool_map(v_cache, num_pages, page_size, Hkv, D, box_t, device, &mv);
+    if (st != PKV_OK) return st;
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    DecodeParams p;
+    p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.lse = lse;
+    p.part_lse = reinterpret_cast<float *>(ws + workspace_lse_offset());
+    p.part_out = reinterpret_cast<float *>(ws + workspace_out_offset(plan.num_splits, B, Hq));
+    p.status = reinterpret_cast<int *>(ws);
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = Hq / Hkv;
+    p.P = page_size;
+    p.log2P = log2_exact(page_size);
+    p.num_pages = num_pages;
+    p.max_pages = max_pages;
+    p.chunk_tokens = plan.chunk_tokens;
+    p.num_splits = plan.num_splits;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+    p.wait_limit_ns = kWaitLimitNs;
+
+    st = launch_decode(D, head_tiles(p.G), mk, mv, p, plan, B, Hkv, device, stream);
+    if (st != PKV_OK || plan.num_splits <= 1) return st;
+
+    MergeParams mp;
+    mp.part_out = p.part_out;
+    mp.part_lse = p.part_lse;
+    mp.seq_lens = seq_lens;
+    mp.out = p.out;
+    mp.lse = lse;
+    mp.S = plan.num_splits;
+    mp.B = B;
+    mp.Hq = Hq;
+    mp.chunk_tokens = plan.chunk_tokens;
+    mp.max_tokens = max_pages * page_size;
+    return launch_merge(D, mp, stream);
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char *pkv_status_string(int status)
+{
+    switch (status) {
+        case PKV_OK: return "PKV_OK";
+        case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG";
+        case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+        case PKV_ERR_MISALIGNED: return "PKV_ERR_MISALIGNED";
+        case PKV_ERR_WORKSPACE_TOO_SMALL: return "PKV_ERR_WORKSPACE_TOO_SMALL";
+        case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+        case PKV_ERR_BAD_PAGE_INDEX: return "PKV_ERR_BAD_PAGE_INDEX";
+        case PKV_ERR_DEVICE_TIMEOUT: return "PKV_ERR_DEVICE_TIMEOUT";
+        case PKV_ERR_BAD_SEQ_LEN: return "PKV_ERR_BAD_SEQ_LEN";
+        default: return "PKV_UNKNOWN_STATUS";
+    }
+}
+
+int pkv_version(void) { return 100; }
+
+pkv_status pkv_plan_query(int B, int Hq, int Hkv, int D, int page_size, int max_pages, int num_sms, int num_splits,
+                          pkv_plan *plan)
+{
+    return make_plan(B, Hq, Hkv, D, page_size, max_pages, num_sms, num_splits, plan);
+}
+
+pkv_status paged_decode_attn_workspace_size_ex(int B, int Hq, int Hkv, int D, int page_size, int max_pages,
+                                               int device, int num_splits, size_t *bytes)
+{
+    if (!bytes) return PKV_ERR_INVALID_ARG;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return PKV_ERR_CUDA;
+    pkv_plan plan;
+    const pkv_status st = make_plan(B, Hq, Hkv, D, page_size, max_pages, sms, num_splits, &plan);
+    if (st != PKV_OK) return st;
+    *bytes = plan.workspace_bytes;
+    return PKV_OK;
+}
+
+pkv_status paged_decode_attn_workspace_size(int B, int Hq, int Hkv, int D, int page_size, int max_pages, int device,
+                                            size_t *bytes)
+{
+    return paged_decode_attn_workspace_size_ex(B, Hq, Hkv, D, page_size, max_pages, device, 0, bytes);
+}
+
+pkv_status paged_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                             const int32_t *block_table, const int32_t *seq_lens, int B, int Hq, int Hkv, int D,
+                             int page_size, int num_pages, int max_pages, float scale, pkv_bf16 *out, float *lse,
+                             void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    return decode_impl(q, k_cache, v_cache, block_table, seq_lens, B, Hq, Hkv, D, page_size, num_pages, max_pages,
+                       scale, out, lse, workspace, workspace_bytes, 0, stream);
+}
+
+pkv_status paged_decode_attn_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                                const int32_t *block_table, const int32_t *seq_lens, int B, int Hq, int Hkv, int D,
+                                int page_size, int num_pages, int max_pages, float scale, pkv_bf16 *out, float *lse,
+                                void *workspace, size_t workspace_bytes, int num_splits, cudaStream_t stream)
+{
+    return decode_impl(q, k_cache, v_cache, block_table, seq_lens, B, Hq, Hkv, D, page_size, num_pages, max_pages,
+                       scale, out, lse, workspace, workspace_bytes, num_splits, stream);
+}
+
+pkv_status split_kv_merge(const float *partial_out, const float *partial_lse, int S, int B, int Hq, int D,
+                          pkv_bf16 *out, float *lse, cudaStream_t stream)
+{
+    if (S <= 0 || B < 0 || Hq <= 0) return PKV_ERR_INVALID_ARG;
+    if (D != 64 && D != 128 && D != 256) return PKV_ERR_UNSUPPORTED;
+    if (B == 0) return PKV_OK;
+    if (!partial_out || !partial_lse || !out) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(partial_out) || !aligned16(partial_lse) || !aligned16(out) || (lse && !aligned16(lse)))
+        return PKV_ERR_MISALIGNED;
+    if ((long)S * B * Hq >= (1l << 31)) return PKV_ERR_INVALID_ARG;
+    MergeParams mp;
+    mp.part_out = partial_out;
+    mp.part_lse = partial_lse;
+    mp.seq_lens = nullptr;
+    mp.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    mp.lse = lse;
+    mp.S = S;
+    mp.B = B;
+    mp.Hq = Hq;
+    mp.chunk_tokens = 1;
+    mp.max_tokens = 0;
+    return launch_merge(D, mp, stream);
+}
+
+pkv_status pkv_check_status(const void *workspace, cudaStream_t stream, int *device_status)
+{
+    if (!workspace || !device_status) return PKV_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return PKV_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return PKV_ERR_CUDA;
+    *device_status = v;
+    return PKV_OK;
+}
+
+pkv_status pkv_reset_status(void *workspace, cudaStream_t stream)
+{
+    if (!workspace) return PKV_ERR_INVALID_ARG;
+    return cudaMemsetAsync(workspace, 0, sizeof(int), stream) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status pkv_selftest_wait_timeout(void *workspace, unsigned timeout_us, cudaStream_t stream)
+{
+    if (!workspace) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(workspace)) return PKV_ERR_MISALIGNED;
+    if (timeout_us == 0 || timeout_us > 10000000u) return PKV_ERR_INVALID_ARG;
+    wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(static_cast<int *>(workspace),
+                                                        (unsigned long long)timeout_us * 1000ull);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // extern "C"

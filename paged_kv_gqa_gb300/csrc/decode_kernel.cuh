@@ -1,0 +1,440 @@
+// decode_kernel.cuh -- split-KV paged GQA decode kernel for sm_103a.
+//
+// One thread block per (split c, kv head, sequence b).  The block owns the keys
+// [c*chunk, min((c+1)*chunk, L_b)) of that kv head and all G = Hq/Hkv query
+// heads that read it, so every K/V byte is fetched from HBM once per call
+// (AstrAI "CUDA Kernels", "Q Scheduling and KV Addressing": packing the query
+// heads of one kv-head group into a block streams K/V once per block rather
+// than once per query head).
+//
+// Data movement.  Each of the W warps streams its own sequence of stages
+// (stage s of the block goes to warp s % W).  A stage is T consecutive keys of
+// one kv head, fetched by TMA as 64-wide (128-byte) boxes straight out of the
+// page pool: the tensor map views k_cache/v_cache as [num_pages*P rows, Hkv,
+// D] and a box is (64 dims, 1 head, min(T,P) rows), so one copy moves a whole
+// page slice without any per-thread address arithmetic.  The physical row of a
+// key is block_table[b][j >> log2 P] * P + (j & (P-1)) (FlashQuant wiki "CUDA
+// Kernels", paged_decode.cu "Page Table Addressing": shift and mask instead of
+// divide and modulo).  The block's slice of the block table is staged in shared
+// memory first, so the page-id lookup is not a dependent global load in front
+// of every copy.  Each warp keeps R stages in flight on its own mbarriers; lane
+// 0 refills a slot as soon as the warp has consumed it.  Boxes land 128B-
+// swizzled so the ldmatrix reads below are free of bank conflicts.
+//
+// Math.  Keys sit on the mma M dimension and the query heads of the group on N
+// (8 per tile, padded), so G = 4, 8, 16 map onto m16n8k16 tiles without
+// wasting rows:
+//     S^T[key, head]  = K[key, :] . q^T[:, head]            (K via ldmatrix, q in registers)
+//     O^T[d, head]   += V^T[d, key] . P^T[key, head]        (V via ldmatrix.trans)
+// P^T comes out of the S accumulators as bf16 pairs and is turned into the B
+// operand with movmatrix.trans.  The softmax is the online recurrence in base 2
+// (FlashQuant wiki "CUDA Kernels", flash_attention.cu "Online Softmax"; the
+// "exp2/log2(e) prescaling" row of its optimisation summary): scores are
+// multiplied by scale*log2(e) in f32, the running max m, denominator l and the
+// accumulators are f32, and every exponential is one ex2.approx.  Row maxima
+// use warp shuffles; the denominators are summed per thread and reduced once at
+// the end.  The denominator sums the same bf16-rounded probabilities that feed
+// the PV product, so the output is an exact convex combination of V rows up to
+// f32 rounding.
+//
+// Masking.  Keys at or past L_b (the padded tail of the last page) and keys of
+// a page whose id is out of range get score -inf, and their V values are
+// zeroed in registers before the PV mma, so NaN or Inf left in unused slots
+// never reaches the result (0 * NaN would).
+//
+// Epilogue.  The W warps' states are merged through shared memory.  If the
+// sequence has a single split the block writes bf16 out and the natural-log
+// lse directly; otherwise it writes its normalised f32 output and lse to the
+// workspace for the merge kernel (FlashQuant wiki "CUDA Kernels", paged_decode.cu
+// "Partial Output"; here normalised and in natural log).  A split that starts
+// past L_b exits at once and is not merged ("Early Exit for Empty Splits").
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "plan.h"
+#include "ptx.cuh"
+
+namespace pkv {
+
+struct DecodeParams {
+    const __nv_bfloat16 *q;  // [B, Hq, D]
+    const int *block_table;  // [B, max_pages]
+    const int *seq_lens;     // [B]
+    __nv_bfloat16 *out;      // [B, Hq, D]
+    float *lse;              // [B, Hq] or nullptr
+    float *part_lse;         // [S, B, Hq]
+    float *part_out;         // [S, B, Hq, D]
+    int *status;             // workspace status word
+    int B, Hq, Hkv, G, P, log2P, num_pages, max_pages;
+    int chunk_tokens, num_splits;
+    float scale_log2;        // scale * log2(e)
+    unsigned long long wait_limit_ns;
+};
+
+__device__ __forceinline__ void record_status(int *status, int code)
+{
+    atomicCAS(status, 0, code);
+}
+
+constexpr float kLn2 = 0.693147180559945309f;
+
+template <int D, int NT>
+__global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
+    decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                        const DecodeParams p)
+{
+    constexpr int T = Tiling<D>::T;
+    constexpr int W = Tiling<D>::W;
+    constexpr int R = Tiling<D>::R;
+    constexpr int DC = D / 64;            // 128-byte box columns per key row
+    constexpr int KS = D / 16;            // k-steps of the score mma, d-tiles of the PV mma
+    constexpr int MT = T / 16;            // 16-key mma tiles per stage
+    constexpr int H8 = NT * 8;            // padded heads
+    constexpr int TILE = T * D * 2;       // bytes of one K (or V) stage tile
+    constexpr int STAGE = 2 * TILE;
+    constexpr int SUB = T * 128;          // bytes of one 64-dim column block of a tile
+    constexpr int RS = D + 4;             // f32 stride of the combine buffer rows
+
+    const int c = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, cc = lane & 3;
+    const int G = p.G;
+
+    // ---- length, split range ------------------------------------------------
+    const int Lmax = p.max_pages * p.P;
+    int L = p.seq_lens[b];
+    if (L < 0 || L > Lmax) {  // invalid length: the sequence is treated as empty
+        if (threadIdx.x == 0 && c == 0 && kvh == 0) record_status(p.status, PKV_ERR_BAD_SEQ_LEN);
+        L = 0;
+    }
+    const int tok_begin = c * p.chunk_tokens;
+    if (c > 0 && tok_begin >= L) return;  // empty split: the merge never reads it
+    if (L == 0) {                          // empty sequence: out = 0, lse = -inf
+        for (int i = threadIdx.x; i < G * D; i += W * 32)
+            p.out[((size_t)b * p.Hq + kvh * G + i / D) * D + (i % D)] = __float2bfloat16_rn(0.f);
+        if (p.lse)
+            for (int i = threadIdx.x; i < G; i += W * 32)
+                p.lse[(size_t)b * p.Hq + kvh * G + i] = -__int_as_float(0x7f800000);
+        return;
+    }
+    const int tok_end = min(tok_begin + p.chunk_tokens, L);
+    const int n_chunks = (L + p.chunk_tokens - 1) / p.chunk_tokens;
+    const int n_stages = (tok_end - tok_begin + T - 1) / T;
+    const int page_begin = tok_begin >> p.log2P;
+    const int page_end = ((tok_end - 1) >> p.log2P) + 1;
+    const int box_t = T < p.P ? T : p.P;   // keys per TMA box (one page slice)
+    const int nbox = T / box_t;
+
+    // ---- shared memory ------------------------------------------------------
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
+    uint8_t *base = smem_raw + (base_addr - raw_addr);
+    const SmemLayout lay = smem_layout(D, T, W, R, NT, p.chunk_tokens, p.P);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(base + lay.bars);
+    float *sm_m = reinterpret_cast<float *>(base + lay.m);
+    float *sm_l = reinterpret_cast<float *>(base + lay.l);
+    float *sm_f = reinterpret_cast<float *>(base + lay.f);
+    float *sm_lse = reinterpret_cast<float *>(base + lay.lse);
+    int *sm_tab = reinterpret_cast<int *>(base + lay.table);
+    float *red = reinterpret_cast<float *>(base);  // reuses the ring after the main loop
+
+    // Stage this split's block-table slice; out-of-range ids become -1.
+    int bad = 0;
+    for (int i = threadIdx.x; i < page_end - page_begin; i += W * 32) {
+        int pg = p.block_table[(size_t)b * p.max_pages + page_begin + i];
+        if ((unsigned)pg >= (unsigned)p.num_pages) {
+            record_status(p.status, PKV_ERR_BAD_PAGE_INDEX);
+            pg = -1;
+            bad = 1;
+        }
+        sm_tab[i] = pg;
+    }
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < W * R; ++i) mbar_init(smem_addr(&bars[i]), 1);
+        fence_barrier_init();
+    }
+    const bool any_bad = __syncthreads_or(bad) != 0;
+
+    // ---- query fragments (B operand of the score mma): q^T[d, head] --------------
+    uint32_t qf[KS][NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int head = nt * 8 + g;
+        const uint32_t *qp = reinterpret_cast<const uint32_t *>(
+            p.q + ((size_t)b * p.Hq + kvh * G + (head < G ? head : 0)) * D + 2 * cc);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            qf[ks][nt][0] = head < G ? __ldg(qp + ks * 8) : 0u;
+            qf[ks][nt][1] = head < G ? __ldg(qp + ks * 8 + 4) : 0u;
+        }
+    }
+
+    // ---- producer: lane 0 of each warp fills that warp's ring ----------------
+    const uint64_t policy = l2_policy_evict_first();
+    auto issue = [&](int s, int slot) {
+        const int t0 = tok_begin + s * T;
+        const uint32_t bar = smem_addr(&bars[warp * R + slot]);
+        const uint32_t kdst = base_addr + (uint32_t)((warp * R + slot) * STAGE);
+        const uint32_t vdst = kdst + TILE;
+        uint32_t bytes = 0;
+        for (int j = 0; j < nbox; ++j) {
+            const int t = t0 + j * box_t;
+            if (t < tok_end && sm_tab[(t >> p.log2P) - page_begin] >= 0) bytes += 2 * DC * box_t * 128;
+        }
+        mbar_arrive_expect_tx(bar, bytes);
+        for (int j = 0; j < nbox; ++j) {
+            const int t = t0 + j * box_t;
+            if (t >= tok_end) break;
+            const int pg = sm_tab[(t >> p.log2P) - page_begin];
+            if (pg < 0) continue;
+            const int row = pg * p.P + (t & (p.P - 1));
+#pragma unroll
+            for (int dc = 0; dc < DC; ++dc) {
+                const uint32_t off = (uint32_t)(dc * SUB + j * box_t * 128);
+                tma_load_3d(kdst + off, &tmK, dc * 64, kvh, row, bar, policy);
+                tma_load_3d(vdst + off, &tmV, dc * 64, kvh, row, bar, policy);
+            }
+        }
+    };
+    if (lane == 0) {
+        for (int r = 0; r < R; ++r) {
+            const int s = warp + r * W;
+            if (s < n_stages) issue(s, r);
+        }
+    }
+
+    // ---- consumer state -----------------------------------------------------
+    float acc[KS][NT][4];
+#pragma unroll
+    for (int i = 0; i < KS; ++i)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[i][nt][e] = 0.f;
+    float m_run[NT][2], l_run[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        m_run[nt][0] = m_run[nt][1] = -__int_as_float(0x7f800000);
+        l_run[nt][0] = l_run[nt][1] = 0.f;
+    }
+
+    auto key_valid = [&](int t) -> bool {
+        return t < tok_end && sm_tab[(t >> p.log2P) - page_begin] >= 0;
+    };
+
+    bool failed = false;
+    for (int it = 0;; ++it) {
+        const int s = warp + it * W;
+        if (s >= n_stages) break;
+        const int slot = it % R;
+        const uint32_t parity = (uint32_t)((it / R) & 1);
+        const bool ok = mbar_wait_bounded(smem_addr(&bars[warp * R + slot]), parity, p.wait_limit_ns);
+        if (!__all_sync(0xffffffffu, ok)) {
+            if (lane == 0) record_status(p.status, PKV_ERR_DEVICE_TIMEOUT);
+            failed = true;
+            break;
+        }
+        const int t0 = tok_begin + s * T;
+        const uint32_t kbase = base_addr + (uint32_t)((warp * R + slot) * STAGE);
+        const uint32_t vbase = kbase + TILE;
+        const bool masked = (t0 + T > tok_end) || any_bad;
+
+        // S^T = K q^T
+        float sc[MT][NT][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sc[mt][nt][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                const int row = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                const int chunk = (ks & 3) * 2 + (lane >> 4);
+                const uint32_t addr = kbase + (uint32_t)((ks >> 2) * SUB + row * 128 + ((chunk ^ (row & 7)) << 4));
+                uint32_t a0, a1, a2, a3;
+                ldmatrix_x4(addr, a0, a1, a2, a3);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[mt][nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
+            }
+        }
+
+        // scale to log2 units, mask, running max
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float v = sc[mt][nt][e] * p.scale_log2;
+                    if (masked) {
+                        const int t = t0 + mt * 16 + g + ((e >> 1) << 3);
+                        if (!key_valid(t)) v = -__int_as_float(0x7f800000);
+                    }
+                    sc[mt][nt][e] = v;
+                }
+        float alpha[NT][2], mref[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                float mx = -__int_as_float(0x7f800000);
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) mx = fmaxf(mx, fmaxf(sc[mt][nt][h2], sc[mt][nt][h2 + 2]));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                const float m_new = fmaxf(m_run[nt][h2], mx);
+                const float r = (m_new == -__int_as_float(0x7f800000)) ? 0.f : m_new;
+                alpha[nt][h2] = ex2(m_run[nt][h2] - r);
+                mref[nt][h2] = r;
+                m_run[nt][h2] = m_new;
+                l_run[nt][h2] *= alpha[nt][h2];
+            }
+#pragma unroll
+        for (int i = 0; i < KS; ++i)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                acc[i][nt][0] *= alpha[nt][0];
+                acc[i][nt][1] *= alpha[nt][1];
+                acc[i][nt][2] *= alpha[nt][0];
+                acc[i][nt][3] *= alpha[nt][1];
+            }
+
+        // O^T += V^T P^T, one 16-key tile at a time
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            uint32_t pb[NT][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const uint32_t x0 = pack_bf16x2(ex2(sc[mt][nt][0] - mref[nt][0]), ex2(sc[mt][nt][1] - mref[nt][1]));
+                const uint32_t x1 = pack_bf16x2(ex2(sc[mt][nt][2] - mref[nt][0]), ex2(sc[mt][nt][3] - mref[nt][1]));
+                l_run[nt][0] += bf16_lo(x0) + bf16_lo(x1);
+                l_run[nt][1] += bf16_hi(x0) + bf16_hi(x1);
+                pb[nt][0] = movmatrix_trans(x0);
+                pb[nt][1] = movmatrix_trans(x1);
+            }
+            uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+            if (masked) {
+                const int t = t0 + mt * 16 + 2 * cc;
+                vm0 = (key_valid(t) ? 0x0000ffffu : 0u) | (key_valid(t + 1) ? 0xffff0000u : 0u);
+                vm1 = (key_valid(t + 8) ? 0x0000ffffu : 0u) | (key_valid(t + 9) ? 0xffff0000u : 0u);
+            }
+#pragma unroll
+            for (int md = 0; md < KS; ++md) {
+                const int row = mt * 16 + (lane & 7) + (lane >> 4) * 8;
+                const int chunk = (md & 3) * 2 + ((lane >> 3) & 1);
+                const uint32_t addr = vbase + (uint32_t)((md >> 2) * SUB + row * 128 + ((chunk ^ (row & 7)) << 4));
+                uint32_t a0, a1, a2, a3;
+                ldmatrix_x4_trans(addr, a0, a1, a2, a3);
+                a0 &= vm0;
+                a1 &= vm0;
+                a2 &= vm1;
+                a3 &= vm1;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[md][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+            }
+        }
+
+        __syncwarp();
+        if (lane == 0) {
+            const int ns = s + R * W;
+            if (ns < n_stages) issue(ns, slot);
+        }
+    }
+    (void)failed;
+
+    // ---- per-warp finalisation: reduce the denominators over the key rows ----
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            float l = l_run[nt][h2];
+            l += __shfl_xor_sync(0xffffffffu, l, 4);
+            l += __shfl_xor_sync(0xffffffffu, l, 8);
+            l += __shfl_xor_sync(0xffffffffu, l, 16);
+            l_run[nt][h2] = l;
+        }
+    __syncthreads();  // every warp is done with the ring: reuse it as the combine buffer
+    if (g == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                sm_m[warp * H8 + nt * 8 + 2 * cc + h2] = m_run[nt][h2];
+                sm_l[warp * H8 + nt * 8 + 2 * cc + h2] = l_run[nt][h2];
+            }
+    }
+#pragma unroll
+    for (int md = 0; md < KS; ++md)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int h0 = nt * 8 + 2 * cc, d0 = md * 16 + g;
+            float *r0 = red + (warp * H8 + h0) * RS;
+            r0[d0] = acc[md][nt][0];
+            r0[RS + d0] = acc[md][nt][1];
+            r0[d0 + 8] = acc[md][nt][2];
+            r0[RS + d0 + 8] = acc[md][nt][3];
+        }
+    __syncthreads();
+
+    // ---- block combine: per-head factors, then the outputs ------------------
+    if (threadIdx.x < H8) {
+        const int h = threadIdx.x;
+        float M = -__int_as_float(0x7f800000);
+#pragma unroll
+        for (int w = 0; w < W; ++w) M = fmaxf(M, sm_m[w * H8 + h]);
+        if (M == -__int_as_float(0x7f800000)) {
+#pragma unroll
+            for (int w = 0; w < W; ++w) sm_f[w * H8 + h] = 0.f;
+            sm_lse[h] = -__int_as_float(0x7f800000);
+        } else {
+            float lsum = 0.f;
+#pragma unroll
+            for (int w = 0; w < W; ++w) lsum += sm_l[w * H8 + h] * ex2(sm_m[w * H8 + h] - M);
+            const float inv = 1.f / lsum;
+#pragma unroll
+            for (int w = 0; w < W; ++w) sm_f[w * H8 + h] = ex2(sm_m[w * H8 + h] - M) * inv;
+            sm_lse[h] = (M + __log2f(lsum)) * kLn2;
+        }
+    }
+    __syncthreads();
+
+    const bool direct = (n_chunks == 1);
+    for (int i = threadIdx.x; i < G * D; i += W * 32) {
+        const int h = i / D, d = i - h * D;
+        float o = 0.f;
+#pragma unroll
+        for (int w = 0; w < W; ++w) o += red[(w * H8 + h) * RS + d] * sm_f[w * H8 + h];
+        const size_t row = (size_t)b * p.Hq + kvh * G + h;
+        if (direct)
+            p.out[row * D + d] = __float2bfloat16_rn(o);
+        else
+            p.part_out[((size_t)c * p.B * p.Hq + row) * D + d] = o;
+    }
+    if (threadIdx.x < G) {
+        const size_t row = (size_t)b * p.Hq + kvh * G + threadIdx.x;
+        if (direct) {
+            if (p.lse) p.lse[row] = sm_lse[threadIdx.x];
+        } else {
+            p.part_lse[(size_t)c * p.B * p.Hq + row] = sm_lse[threadIdx.x];
+        }
+    }
+}
+
+// Bounded-wait self-test: waits on a barrier nothing completes.
+__global__ void wait_timeout_selftest_kernel(int *status, unsigned long long limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(smem_addr(&bar), 1);
+    fence_barrier_init();
+    if (!mbar_wait_bounded(smem_addr(&bar), 0, limit_ns)) record_status(status, PKV_ERR_DEVICE_TIMEOUT);
+}
+
+}  // namespace pkv

@@ -1,0 +1,137 @@
+// plan.cpp -- host planner for the split-KV decode launch.
+//
+// The split count is a pure function of the shape and the SM count (OASR
+// "Kernel Layer", "Fused attention": never of capture state, because it sets
+// the order the f32 partials are summed).  The device-side lengths are not
+// visible here, so the plan sizes splits for sequences of full table width:
+//   - a split never holds more than ~1 MiB of K+V (kMaxSplitBytes), so one
+//     long sequence cannot become a straggler;
+//   - above that bound, the split count is the one whose equal-sized splits
+//     fill the machine's last wave best, searched up to about kTargetWaves
+//     waves and never below kMinSplitTokens keys per split.
+// Splits that start past a sequence's length exit at once and are ignored by
+// the merge (FlashQuant wiki "CUDA Kernels", paged_decode.cu "Early Exit for
+// Empty Splits").
+#include "plan.h"
+
+#include <algorithm>
+#include <cmath>
+
+namespace pkv {
+
+namespace {
+constexpr long kMaxSplitBytes = 1l << 20;  // K+V bytes of one (b, kv head) split
+constexpr int kMinSplitTokens = 256;
+constexpr int kTargetWaves = 2;
+constexpr int kSmemPerSm = 233472;          // 228 KiB per SM on sm_100-class parts
+constexpr int kSmemPerBlockMax = 232448;    // 227 KiB opt-in maximum per block
+constexpr int kBlockReserve = 1024;         // shared memory the system reserves per block
+constexpr int kMaxTablePages = 4096;        // block_table slice a block stages in smem
+}  // namespace
+
+RuntimeTiling tiling_for(int D)
+{
+    switch (D) {
+        case 64: return {Tiling<64>::T, Tiling<64>::W, Tiling<64>::R};
+        case 128: return {Tiling<128>::T, Tiling<128>::W, Tiling<128>::R};
+        case 256: return {Tiling<256>::T, Tiling<256>::W, Tiling<256>::R};
+        default: return {0, 0, 0};
+    }
+}
+
+size_t workspace_lse_offset() { return kWorkspaceHeader; }
+
+size_t workspace_out_offset(int S, int B, int Hq)
+{
+    const size_t lse_bytes = (size_t)S * B * Hq * sizeof(float);
+    return kWorkspaceHeader + (lse_bytes + 255) / 256 * 256;
+}
+
+size_t workspace_bytes(int S, int B, int Hq, int D)
+{
+    if (S <= 1) return kWorkspaceHeader;
+    return workspace_out_offset(S, B, Hq) + (size_t)S * B * Hq * D * sizeof(float);
+}
+
+static bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+pkv_status validate_shape(int B, int Hq, int Hkv, int D, int page_size, int max_pages)
+{
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || max_pages <= 0) return PKV_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return PKV_ERR_INVALID_ARG;
+    if (D != 64 && D != 128 && D != 256) return PKV_ERR_UNSUPPORTED;
+    if (!is_pow2(page_size) || page_size < 8 || page_size > 256) return PKV_ERR_UNSUPPORTED;
+    if ((long)max_pages * page_size >= (1l << 30)) return PKV_ERR_INVALID_ARG;
+    if (Hq / Hkv > 32) return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
+pkv_status make_plan(int B, int Hq, int Hkv, int D, int page_size, int max_pages, int num_sms,
+                     int num_splits, pkv_plan *plan)
+{
+    if (!plan || num_sms <= 0 || num_splits < 0) return PKV_ERR_INVALID_ARG;
+    const pkv_status v = validate_shape(B, Hq, Hkv, D, page_size, max_pages);
+    if (v != PKV_OK) return v;
+    const int G = Hq / Hkv;
+
+    const RuntimeTiling t = tiling_for(D);
+    const int NT = head_tiles(G);
+    const int max_tokens = max_pages * page_size;
+    const int units = std::max(1, B * Hkv);
+
+    // Resident blocks per SM, sized with the largest table slice the auto plan uses.
+    const int cap_tokens = std::max(t.T, (int)(kMaxSplitBytes / (4l * D)) / t.T * t.T);
+    const SmemLayout ref = smem_layout(D, t.T, t.W, t.R, NT, cap_tokens, page_size);
+    int per_sm = std::max(1, kSmemPerSm / (ref.dynamic + kBlockReserve));
+    per_sm = std::min(per_sm, 2048 / (t.W * 32));
+    const int slots = num_sms * per_sm;
+
+    const int max_stage_splits = (max_tokens + t.T - 1) / t.T;
+    int S;
+    if (num_splits > 0) {
+        S = std::min(num_splits, max_stage_splits);
+    } else {
+        // Smallest S that bounds the bytes of one split, then the S in a window
+        // above it whose equal-sized splits fill the last wave of the machine
+        // best (assuming every sequence spans the full table width).
+        const int s_lo = std::max(1, (max_tokens + cap_tokens - 1) / cap_tokens);
+        const int s_thin = std::max(1, max_tokens / kMinSplitTokens);
+        const int s_fill = (kTargetWaves * slots + units - 1) / units;
+        const int s_hi = std::max(s_lo, std::min(s_thin, std::max(2 * s_lo, 2 * s_fill)));
+        S = s_lo;
+        double best = -1.0;
+        for (int s = s_lo; s <= s_hi; ++s) {
+            const double waves = (double)units * s / slots;
+            const double eff = waves / std::ceil(waves);
+            if (eff > best + 0.01) {
+                best = eff;
+                S = s;
+            }
+        }
+    }
+    S = std::max(1, S);
+    int chunk = (max_tokens + S - 1) / S;
+    chunk = (chunk + t.T - 1) / t.T * t.T;
+    // A block stages its block_table slice in shared memory: bound it.
+    const int max_chunk = (kMaxTablePages - 2) * page_size;
+    if (chunk > max_chunk) chunk = max_chunk / t.T * t.T;
+    S = (max_tokens + chunk - 1) / chunk;
+
+    const SmemLayout lay = smem_layout(D, t.T, t.W, t.R, NT, chunk, page_size);
+    if (lay.dynamic > kSmemPerBlockMax) return PKV_ERR_UNSUPPORTED;
+    per_sm = std::max(1, std::min(kSmemPerSm / (lay.dynamic + kBlockReserve), 2048 / (t.W * 32)));
+
+    plan->num_splits = S;
+    plan->chunk_tokens = chunk;
+    plan->stage_tokens = t.T;
+    plan->warps = t.W;
+    plan->ring_stages = t.R;
+    plan->blocks_per_sm = per_sm;
+    plan->grid_blocks = S * Hkv * B;
+    plan->smem_bytes = lay.dynamic;
+    plan->merge_needed = S > 1 ? 1 : 0;
+    plan->workspace_bytes = workspace_bytes(S, B, Hq, D);
+    return PKV_OK;
+}
+
+}  // namespace pkv

@@ -1,0 +1,88 @@
+// plan.h -- the host planner: split count, tiling and workspace layout as a
+// pure function of (shape, SM count).  No CUDA calls.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "pkv.h"
+
+namespace pkv {
+
+// Compile-time tiling of one decode-kernel variant, chosen by head dim D.
+//   T: keys per pipeline stage (a multiple of the 16-row mma tile)
+//   W: consumer warps per block, each streaming its own stages
+//   R: ring depth per warp (stages in flight)
+template <int D>
+struct Tiling;
+template <>
+struct Tiling<64> { static constexpr int T = 32, W = 4, R = 3; };
+template <>
+struct Tiling<128> { static constexpr int T = 16, W = 4, R = 3; };
+template <>
+struct Tiling<256> { static constexpr int T = 16, W = 4, R = 3; };
+
+struct RuntimeTiling {
+    int T, W, R;
+};
+RuntimeTiling tiling_for(int D);
+
+// Number of 8-wide head tiles (mma N tiles) for group size G.
+inline int head_tiles(int G) { return G <= 8 ? 1 : (G <= 16 ? 2 : 4); }
+
+#if defined(__CUDACC__)
+#define PKV_HD __host__ __device__ __forceinline__
+#else
+#define PKV_HD inline
+#endif
+
+// Shared-memory carve-up of one decode block (byte offsets from a 1024-aligned
+// base).  The kernel and the planner both use this, so they cannot disagree.
+struct SmemLayout {
+    int ring;      // W*R stages of [K tile | V tile], each tile T x D bf16, 128B-swizzled
+    int bars;      // W*R mbarriers (8 B each)
+    int m;         // [W][H8] f32 running max per warp (log2 units)
+    int l;         // [W][H8] f32 softmax denominator per warp
+    int f;         // [W][H8] f32 per-warp combine factor
+    int lse;       // [H8] f32 block result per head
+    int table;     // block_table slice (int32), `table_entries` of them
+    int table_entries;
+    int total;     // bytes from the aligned base
+    int dynamic;   // bytes to request (total + alignment slack)
+};
+
+PKV_HD int round_up_int(int x, int m) { return (x + m - 1) / m * m; }
+
+PKV_HD SmemLayout smem_layout(int D, int T, int W, int R, int NT, int chunk_tokens, int page_size)
+{
+    SmemLayout s;
+    const int H8 = NT * 8;
+    const int ring = W * R * 2 * T * D * 2;
+    const int red = W * H8 * (D + 4) * 4;  // per-warp f32 accumulators, reuses the ring
+    s.ring = 0;
+    s.bars = round_up_int(ring > red ? ring : red, 1024);
+    s.m = s.bars + W * R * 8;
+    s.l = s.m + W * H8 * 4;
+    s.f = s.l + W * H8 * 4;
+    s.lse = s.f + W * H8 * 4;
+    s.table = round_up_int(s.lse + H8 * 4, 16);
+    s.table_entries = chunk_tokens / page_size + 2;
+    s.total = round_up_int(s.table + s.table_entries * 4, 16);
+    s.dynamic = s.total + 1024;
+    return s;
+}
+
+// Workspace layout: [header 256 B][partial lse S*B*Hq f32, padded to 256 B][partial out S*B*Hq*D f32]
+constexpr size_t kWorkspaceHeader = 256;
+size_t workspace_bytes(int S, int B, int Hq, int D);
+size_t workspace_lse_offset();
+size_t workspace_out_offset(int S, int B, int Hq);
+
+// Shape checks shared by every entry point (no CUDA call).
+pkv_status validate_shape(int B, int Hq, int Hkv, int D, int page_size, int max_pages);
+
+// Validates the shape (not pointers) and fills `plan`.
+pkv_status make_plan(int B, int Hq, int Hkv, int D, int page_size, int max_pages, int num_sms,
+                     int num_splits, pkv_plan *plan);
+
+}  // namespace pkv

@@ -1,0 +1,61 @@
+"""Helpers shared by the GPU tests: run the CUDA path through the C-ABI binding
+and compare it with the CPU oracle."""
+import numpy as np
+import torch
+
+import oracle
+import paged_kv_gqa_gb300 as pkv
+
+OUT_TOL = 1.5e-2     # max |out_gpu - out_oracle| on bf16 outputs
+LSE_TOL = 1e-3       # max |lse_gpu - lse_oracle| on f32 LSE
+SPLIT_TOL = 2e-3     # max |out(S1) - out(S2)| between split counts
+
+
+def run_gpu(case, num_splits=0, with_lse=True, expect_status=0):
+    """One call of paged_decode_attn_ex on the case's tensors (moved to cuda:0)."""
+    c = case if case.q.is_cuda else case.to("cuda")
+    ws_bytes = pkv.paged_decode_attn_workspace_size(c.B, c.Hq, c.Hkv, c.D, c.P, c.max_pages,
+                                                    num_splits=num_splits)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    out = torch.full((c.B, c.Hq, c.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((c.B, c.Hq), float("nan"), dtype=torch.float32, device="cuda") if with_lse else None
+    pkv.paged_decode_attn_ex(c.q, c.k_cache, c.v_cache, c.block_table, c.seq_lens, c.scale, out, lse, ws,
+                             num_splits=num_splits)
+    status = pkv.pkv_check_status(ws)
+    assert status == expect_status, "device status %s" % pkv.STATUS.get(status, status)
+    return out, lse
+
+
+def max_abs_diff(a, b):
+    """max |a - b| where equal infinities count as 0."""
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    same_inf = np.isinf(a) & np.isinf(b) & (np.sign(a) == np.sign(b))
+    d = np.where(same_inf, 0.0, np.abs(a - b))
+    return float(np.max(d)) if d.size else 0.0
+
+
+def compare_with_oracle(case, out, lse, select=None, nthreads=0):
+    """Returns (max out error, max lse error) against the oracle (all rows or a sample)."""
+    q, k, v, bt, sl = case.host_bits()
+    ref_o, ref_l = oracle.paged_decode(q, k, v, bt, sl, case.scale, select=select, nthreads=nthreads)
+    o = out.float().cpu().numpy()
+    l = lse.cpu().numpy() if lse is not None else None
+    if select is not None:
+        idx = np.asarray(list(select))
+        o = o[idx[:, 0], idx[:, 1]]
+        l = l[idx[:, 0], idx[:, 1]] if l is not None else None
+    eo = max_abs_diff(o, ref_o)
+    el = max_abs_diff(l, ref_l) if l is not None else 0.0
+    return eo, el
+
+
+def sample_rows(case, n=24, seed=0):
+    """A seeded sample of (b, h) rows, always including the longest and the shortest sequence."""
+    rng = np.random.default_rng(seed)
+    lens = case.seq_lens.cpu().numpy()
+    rows = {(int(np.argmax(lens)), 0), (int(np.argmax(lens)), case.Hq - 1), (int(np.argmin(lens)), case.Hq // 2),
+            (0, 0), (case.B - 1, case.Hq - 1)}
+    while len(rows) < n:
+        rows.add((int(rng.integers(case.B)), int(rng.integers(case.Hq))))
+    return sorted(rows)

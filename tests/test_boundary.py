@@ -1,0 +1,140 @@
+"""The C-ABI boundary without a GPU: the library loads, exports every declared
+symbol, rejects bad arguments before touching CUDA, and plans deterministically."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_gqa_gb300 as pkv
+from paged_kv_gqa_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return pkv.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"PKV_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 11
+    assert sorted(pkv.EXPORTED_SYMBOLS) == names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_no_internal_symbols_leak():
+    _build.build()
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", pkv.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    ours = {n for n in exported if n.startswith(("pkv", "paged_decode", "split_kv"))}
+    assert ours == set(_declared())
+
+
+def test_status_strings(lib):
+    for code, name in pkv.STATUS.items():
+        assert pkv.status_string(code) == name
+    assert pkv.status_string(12345) == "PKV_UNKNOWN_STATUS"
+    assert lib.pkv_version() >= 100
+
+
+def _call_decode(lib, q=0x1000, k=0x2000, v=0x3000, bt=0x4000, sl=0x5000, B=2, Hq=8, Hkv=2, D=128, P=16,
+                 num_pages=64, max_pages=8, scale=0.125, out=0x6000, lse=0x7000, ws=0x8000, ws_bytes=1 << 20,
+                 splits=0):
+    """Fake (never dereferenced) pointers: every case below must be rejected on the host."""
+    V = ctypes.c_void_p
+    return lib.paged_decode_attn_ex(V(q), V(k), V(v), V(bt), V(sl), B, Hq, Hkv, D, P, num_pages, max_pages,
+                                    ctypes.c_float(scale), V(out), V(lse), V(ws), ws_bytes, splits, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=0), -1), (dict(k=0), -1), (dict(v=0), -1), (dict(bt=0), -1), (dict(sl=0), -1), (dict(out=0), -1),
+    (dict(ws=0), -1), (dict(Hq=0), -1), (dict(Hkv=0), -1), (dict(Hq=6, Hkv=4), -1), (dict(B=-1), -1),
+    (dict(num_pages=0), -1), (dict(max_pages=0), -1), (dict(splits=-2), -1), (dict(scale=float("nan")), -1),
+    (dict(D=96), -2), (dict(D=32), -2), (dict(P=12), -2), (dict(P=4), -2), (dict(P=512), -2),
+    (dict(Hq=66, Hkv=1), -2),
+    (dict(q=0x1008), -3), (dict(k=0x2004), -3), (dict(bt=0x4002), -3), (dict(lse=0x7001), -3), (dict(ws=0x8008), -3),
+])
+def test_host_rejects_bad_arguments(lib, kw, status):
+    assert _call_decode(lib, **kw) == status
+
+
+def test_batch_zero_is_a_noop(lib):
+    assert _call_decode(lib, B=0, q=0, k=0, v=0) == 0
+
+
+def test_merge_rejects_bad_arguments(lib):
+    V = ctypes.c_void_p
+    assert lib.split_kv_merge(V(0x1000), V(0x2000), 0, 1, 1, 128, V(0x3000), None, None) == -1
+    assert lib.split_kv_merge(V(0x1000), V(0x2000), 2, 1, 1, 96, V(0x3000), None, None) == -2
+    assert lib.split_kv_merge(V(0x1004), V(0x2000), 2, 1, 1, 128, V(0x3000), None, None) == -3
+    assert lib.split_kv_merge(V(0), V(0x2000), 2, 1, 1, 128, V(0x3000), None, None) == -1
+    assert lib.split_kv_merge(V(0x1000), V(0x2000), 2, 0, 1, 128, V(0x3000), None, None) == 0
+
+
+def test_status_calls_reject_null(lib):
+    v = ctypes.c_int(0)
+    assert lib.pkv_check_status(None, None, ctypes.byref(v)) == -1
+    assert lib.pkv_reset_status(None, None) == -1
+    assert lib.pkv_selftest_wait_timeout(None, 10, None) == -1
+    assert lib.pkv_selftest_wait_timeout(ctypes.c_void_p(0x1000), 0, None) == -1
+
+
+# ----------------------------------------------------------------- planner (pure host function)
+
+WORKLOADS = {
+    "tiny": (1, 8, 2, 64, 16, 16),
+    "batch": (8, 32, 8, 128, 16, 256),
+    "ragged": (64, 32, 8, 128, 16, 2048),
+    "long": (4, 64, 8, 128, 16, 8192),
+    "bigpage": (256, 32, 8, 128, 64, 32),
+    "bigpage_g16": (256, 32, 2, 256, 64, 32),
+}
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+@pytest.mark.parametrize("sms", [148, 152, 160])
+def test_plan_invariants(lib, name, sms):
+    B, Hq, Hkv, D, P, max_pages = WORKLOADS[name]
+    plan = pkv.plan_query(B, Hq, Hkv, D, P, max_pages, sms)
+    max_tokens = max_pages * P
+    assert plan["chunk_tokens"] % plan["stage_tokens"] == 0
+    assert plan["num_splits"] * plan["chunk_tokens"] >= max_tokens
+    assert (plan["num_splits"] - 1) * plan["chunk_tokens"] < max_tokens
+    assert plan["smem_bytes"] <= 232448
+    assert plan["grid_blocks"] == plan["num_splits"] * Hkv * B
+    assert plan["merge_needed"] == (1 if plan["num_splits"] > 1 else 0)
+    # K+V bytes of one split stay bounded so no split becomes a straggler
+    assert plan["chunk_tokens"] * 4 * D <= (1 << 20) or plan["num_splits"] == 1
+    if plan["num_splits"] > 1:
+        ws = 256 + ((plan["num_splits"] * B * Hq * 4 + 255) // 256) * 256 + plan["num_splits"] * B * Hq * D * 4
+        assert plan["workspace_bytes"] == ws
+    else:
+        assert plan["workspace_bytes"] == 256
+    # a pure function of (shape, SM count)
+    assert pkv.plan_query(B, Hq, Hkv, D, P, max_pages, sms) == plan
+
+
+def test_plan_splits_long_context_and_not_big_batches(lib):
+    assert pkv.plan_query(4, 64, 8, 128, 16, 8192, 152)["num_splits"] >= 32
+    assert pkv.plan_query(256, 32, 8, 128, 64, 32, 152)["num_splits"] == 1
+
+
+def test_plan_forced_splits(lib):
+    for s in (1, 2, 3, 7, 64):
+        plan = pkv.plan_query(8, 32, 8, 128, 16, 256, 152, s)
+        assert plan["num_splits"] == s
+    # clamped to one split per stage
+    assert pkv.plan_query(1, 8, 2, 64, 16, 2, 152, 1000)["num_splits"] == 1
+    with pytest.raises(pkv.PkvError):
+        pkv.plan_query(1, 8, 2, 64, 16, 2, 152, -1)

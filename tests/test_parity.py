@@ -1,0 +1,175 @@
+"""Parity of the CUDA path (through the C-ABI) with the CPU fp64 oracle.
+
+Bars: max |out - oracle| <= 1.5e-2 on bf16 outputs, max |lse - oracle| <= 1e-3
+on f32 LSE, and results at different split counts within 2e-3 of each other.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_gqa_gb300 as pkv
+from paged_kv_gqa_gb300 import _build
+from gpu_util import LSE_TOL, OUT_TOL, SPLIT_TOL, compare_with_oracle, max_abs_diff, run_gpu, sample_rows
+from workloads import CONFIG_ORDER, make_case
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    _build.build()
+    return pkv.load()
+
+
+def _spec(B, Hq, Hkv, D, P, seed=0, **kw):
+    return dict(B=B, Hq=Hq, Hkv=Hkv, D=D, P=P, lens=("fixed", 1), seed=seed, **kw)
+
+
+# Small cases the oracle checks in full: several stages and splits, ragged tails,
+# every head dim, group sizes 1..32, page sizes 8..256, NaN in every unused slot.
+SMALL = [
+    # B, Hq, Hkv, D, P, lens
+    (1, 8, 2, 64, 16, [256]),
+    (3, 8, 2, 64, 8, [1, 7, 8]),
+    (4, 8, 8, 64, 16, [9, 15, 16, 17]),
+    (3, 32, 8, 128, 16, [1, 300, 1000]),
+    (5, 32, 8, 128, 16, [0, 17, 15, 16, 2500]),
+    (2, 64, 8, 128, 16, [4097, 333]),
+    (2, 16, 4, 128, 64, [63, 200]),
+    (2, 16, 1, 128, 32, [130, 64]),
+    (2, 32, 2, 256, 64, [2048, 77]),
+    (3, 16, 2, 256, 16, [1, 500, 129]),
+    (2, 64, 2, 128, 16, [700, 45]),
+    (2, 32, 16, 64, 256, [600, 255]),
+    (1, 4, 1, 256, 8, [1000]),
+    (2, 24, 8, 128, 16, [100, 33]),   # G = 3 (padded head tile)
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,D,P,lens", SMALL, ids=lambda x: str(x).replace(" ", ""))
+def test_small_cases_full_oracle(B, Hq, Hkv, D, P, lens):
+    case = make_case(_spec(B, Hq, Hkv, D, P, seed=B * 7 + D), seq_lens=lens, poison=True)
+    out, lse = run_gpu(case)
+    eo, el = compare_with_oracle(case, out, lse)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+    assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("name", CONFIG_ORDER)
+def test_workloads_sampled_oracle(name):
+    """Every workload at full size, in the launch configuration the benchmark times."""
+    case = make_case(name, device="cuda")
+    out, lse = run_gpu(case)
+    rows = sample_rows(case, n=24, seed=1) if name != "tiny" else None
+    eo, el = compare_with_oracle(case, out, lse, select=rows)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (name, eo, el)
+    # properties that hold at every row: finite, and a convex combination of V rows
+    o = out.float()
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    assert o.abs().max().item() <= case.v_cache.float().abs().max().item() * (1 + 2 ** -7)
+    del case, out, lse
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("case_args", [
+    ("batch", None),
+    (_spec(3, 32, 8, 128, 16, seed=3), [1, 1000, 5000]),
+    (_spec(2, 32, 2, 256, 64, seed=4), [3000, 65]),
+])
+def test_split_count_invariance(case_args):
+    spec, lens = case_args
+    case = make_case(spec, seq_lens=lens, device="cuda") if lens else make_case(spec, device="cuda")
+    max_tokens = case.max_pages * case.P
+    counts = [1, 2, 0, max(3, max_tokens // 16)]
+    outs = [run_gpu(case, num_splits=s) for s in counts]
+    for i in range(len(outs)):
+        for j in range(i + 1, len(outs)):
+            d = max_abs_diff(outs[i][0].float().cpu().numpy(), outs[j][0].float().cpu().numpy())
+            dl = max_abs_diff(outs[i][1].cpu().numpy(), outs[j][1].cpu().numpy())
+            assert d <= SPLIT_TOL and dl <= LSE_TOL, (counts[i], counts[j], d, dl)
+    eo, el = compare_with_oracle(case, *outs[0], select=sample_rows(case, 12))
+    assert eo <= OUT_TOL and el <= LSE_TOL
+
+
+def test_reruns_are_bitwise_identical():
+    case = make_case("batch", device="cuda")
+    a = run_gpu(case)
+    b = run_gpu(case)
+    assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
+    assert torch.equal(a[1], b[1])
+
+
+def test_physical_page_placement_does_not_matter():
+    case = make_case(_spec(4, 32, 8, 128, 16, seed=9), seq_lens=[1000, 17, 333, 2049])
+    out_a, lse_a = run_gpu(case, num_splits=3)
+    rng = np.random.default_rng(3)
+    new_pool = case.num_pages + 40
+    perm = torch.from_numpy(rng.permutation(new_pool)[: case.num_pages].astype(np.int64))
+    k2 = torch.full((new_pool,) + tuple(case.k_cache.shape[1:]), float("nan"), dtype=torch.bfloat16)
+    v2 = k2.clone()
+    k2[perm] = case.k_cache
+    v2[perm] = case.v_cache
+    bt = case.block_table.long()
+    bt2 = torch.where(bt >= 0, perm[bt.clamp(min=0)], torch.full_like(bt, -1)).int()
+    moved = make_case(_spec(4, 32, 8, 128, 16, seed=9), seq_lens=[1000, 17, 333, 2049])
+    moved.k_cache, moved.v_cache, moved.block_table, moved.num_pages = k2, v2, bt2, new_pool
+    out_b, lse_b = run_gpu(moved, num_splits=3)
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16)) and torch.equal(lse_a, lse_b)
+
+
+def test_lse_may_be_null():
+    case = make_case(_spec(2, 8, 2, 64, 16, seed=1), seq_lens=[100, 3000])
+    out_a, _ = run_gpu(case, with_lse=False)
+    out_b, _ = run_gpu(case)
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+
+
+def test_single_token_returns_v_row_exactly():
+    """With one key the softmax weight is exactly 1: out is that V row, bit for bit."""
+    case = make_case(_spec(3, 16, 2, 128, 16, seed=5), seq_lens=[1, 1, 1], poison=True)
+    out, lse = run_gpu(case)
+    bt = case.block_table
+    for b in range(3):
+        for h in range(16):
+            assert torch.equal(out[b, h].cpu().view(torch.int16), case.v_cache[bt[b, 0], 0, h // 8].view(torch.int16))
+
+
+def test_graph_capture_replay():
+    case = make_case(_spec(4, 32, 8, 128, 16, seed=2), seq_lens=[500, 4000, 17, 1200]).to("cuda")
+    ws_bytes = pkv.paged_decode_attn_workspace_size(case.B, case.Hq, case.Hkv, case.D, case.P, case.max_pages)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    out = torch.empty((case.B, case.Hq, case.D), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((case.B, case.Hq), dtype=torch.float32, device="cuda")
+    args = (case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens, case.scale, out, lse, ws)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        pkv.paged_decode_attn(*args)  # warm-up outside capture (tensor maps, attributes)
+    torch.cuda.synchronize()
+    ref = out.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pkv.paged_decode_attn(*args, stream=s)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert pkv.pkv_check_status(ws) == 0
+
+
+def test_split_kv_merge_matches_oracle():
+    rng = np.random.default_rng(0)
+    S, B, Hq = 5, 3, 8
+    for D in (64, 128, 256):
+        po = rng.standard_normal((S, B, Hq, D)).astype(np.float32)
+        pl = (rng.standard_normal((S, B, Hq)) * 4).astype(np.float32)
+        pl[1, 0, :] = -np.inf          # an empty split
+        pl[:, 2, 3] = -np.inf          # a row whose splits are all empty
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+        pkv.split_kv_merge(torch.from_numpy(po).cuda(), torch.from_numpy(pl).cuda(), out, lse)
+        torch.cuda.synchronize()
+        ro, rl = oracle.merge(po.reshape(S, B * Hq, D).astype(np.float64), pl.reshape(S, B * Hq).astype(np.float64))
+        assert max_abs_diff(out.float().cpu().numpy().reshape(B * Hq, D), ro) <= 1e-2
+        assert max_abs_diff(lse.cpu().numpy().reshape(-1), rl) <= 1e-5
+        assert np.isneginf(lse[2, 3].item()) and out[2, 3].abs().max().item() == 0
