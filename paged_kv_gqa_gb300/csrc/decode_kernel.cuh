@@ -33,9 +33,10 @@
 // multiplied by scale*log2(e) in f32, the running max m, denominator l and the
 // accumulators are f32, and every exponential is one ex2.approx.  Row maxima
 // use warp shuffles; the denominators are summed per thread and reduced once at
-// the end.  The denominator sums the same bf16-rounded probabilities that feed
-// the PV product, so the output is an exact convex combination of V rows up to
-// f32 rounding.
+// the end.  Two denominators are kept: the sum of the f32 probabilities, which
+// gives the LSE, and the sum of the same bf16-rounded probabilities that feed
+// the PV product, which normalises the output so that it is a convex
+// combination of V rows up to f32 rounding (a constant V comes back unchanged).
 //
 // Masking.  Keys at or past L_b (the padded tail of the last page) and keys of
 // a page whose id is out of range get score -inf, and their V values are
@@ -136,6 +137,7 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + lay.bars);
     float *sm_m = reinterpret_cast<float *>(base + lay.m);
     float *sm_l = reinterpret_cast<float *>(base + lay.l);
+    float *sm_lt = reinterpret_cast<float *>(base + lay.lt);
     float *sm_f = reinterpret_cast<float *>(base + lay.f);
     float *sm_lse = reinterpret_cast<float *>(base + lay.lse);
     int *sm_tab = reinterpret_cast<int *>(base + lay.table);
@@ -214,11 +216,12 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[i][nt][e] = 0.f;
-    float m_run[NT][2], l_run[NT][2];
+    float m_run[NT][2], l_run[NT][2], lt_run[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         m_run[nt][0] = m_run[nt][1] = -__int_as_float(0x7f800000);
         l_run[nt][0] = l_run[nt][1] = 0.f;
+        lt_run[nt][0] = lt_run[nt][1] = 0.f;
     }
 
     auto key_valid = [&](int t) -> bool {
@@ -295,6 +298,7 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
                 mref[nt][h2] = r;
                 m_run[nt][h2] = m_new;
                 l_run[nt][h2] *= alpha[nt][h2];
+                lt_run[nt][h2] *= alpha[nt][h2];
             }
 #pragma unroll
         for (int i = 0; i < KS; ++i)
@@ -312,10 +316,14 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
             uint32_t pb[NT][2];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                const uint32_t x0 = pack_bf16x2(ex2(sc[mt][nt][0] - mref[nt][0]), ex2(sc[mt][nt][1] - mref[nt][1]));
-                const uint32_t x1 = pack_bf16x2(ex2(sc[mt][nt][2] - mref[nt][0]), ex2(sc[mt][nt][3] - mref[nt][1]));
-                l_run[nt][0] += bf16_lo(x0) + bf16_lo(x1);
-                l_run[nt][1] += bf16_hi(x0) + bf16_hi(x1);
+                const float p0 = ex2(sc[mt][nt][0] - mref[nt][0]), p1 = ex2(sc[mt][nt][1] - mref[nt][1]);
+                const float p2 = ex2(sc[mt][nt][2] - mref[nt][0]), p3 = ex2(sc[mt][nt][3] - mref[nt][1]);
+                const uint32_t x0 = pack_bf16x2(p0, p1);
+                const uint32_t x1 = pack_bf16x2(p2, p3);
+                l_run[nt][0] += p0 + p2;
+                l_run[nt][1] += p1 + p3;
+                lt_run[nt][0] += bf16_lo(x0) + bf16_lo(x1);
+                lt_run[nt][1] += bf16_hi(x0) + bf16_hi(x1);
                 pb[nt][0] = movmatrix_trans(x0);
                 pb[nt][1] = movmatrix_trans(x1);
             }
@@ -354,11 +362,15 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
-            float l = l_run[nt][h2];
+            float l = l_run[nt][h2], lt = lt_run[nt][h2];
             l += __shfl_xor_sync(0xffffffffu, l, 4);
             l += __shfl_xor_sync(0xffffffffu, l, 8);
             l += __shfl_xor_sync(0xffffffffu, l, 16);
+            lt += __shfl_xor_sync(0xffffffffu, lt, 4);
+            lt += __shfl_xor_sync(0xffffffffu, lt, 8);
+            lt += __shfl_xor_sync(0xffffffffu, lt, 16);
             l_run[nt][h2] = l;
+            lt_run[nt][h2] = lt;
         }
     __syncthreads();  // every warp is done with the ring: reuse it as the combine buffer
     if (g == 0) {
@@ -368,6 +380,7 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
             for (int h2 = 0; h2 < 2; ++h2) {
                 sm_m[warp * H8 + nt * 8 + 2 * cc + h2] = m_run[nt][h2];
                 sm_l[warp * H8 + nt * 8 + 2 * cc + h2] = l_run[nt][h2];
+                sm_lt[warp * H8 + nt * 8 + 2 * cc + h2] = lt_run[nt][h2];
             }
     }
 #pragma unroll
@@ -394,10 +407,14 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
             for (int w = 0; w < W; ++w) sm_f[w * H8 + h] = 0.f;
             sm_lse[h] = -__int_as_float(0x7f800000);
         } else {
-            float lsum = 0.f;
+            float lsum = 0.f, ltsum = 0.f;
 #pragma unroll
-            for (int w = 0; w < W; ++w) lsum += sm_l[w * H8 + h] * ex2(sm_m[w * H8 + h] - M);
-            const float inv = 1.f / lsum;
+            for (int w = 0; w < W; ++w) {
+                const float e = ex2(sm_m[w * H8 + h] - M);
+                lsum += sm_l[w * H8 + h] * e;
+                ltsum += sm_lt[w * H8 + h] * e;
+            }
+            const float inv = 1.f / ltsum;
 #pragma unroll
             for (int w = 0; w < W; ++w) sm_f[w * H8 + h] = ex2(sm_m[w * H8 + h] - M) * inv;
             sm_lse[h] = (M + __log2f(lsum)) * kLn2;

@@ -42,7 +42,8 @@ struct SmemLayout {
     int ring;      // W*R stages of [K tile | V tile], each tile T x D bf16, 128B-swizzled
     int bars;      // W*R mbarriers (8 B each)
     int m;         // [W][H8] f32 running max per warp (log2 units)
-    int l;         // [W][H8] f32 softmax denominator per warp
+    int l;         // [W][H8] f32 softmax denominator per warp (sum of the f32 probabilities)
+    int lt;        // [W][H8] f32 same, summed over the bf16-rounded probabilities the PV mma uses
     int f;         // [W][H8] f32 per-warp combine factor
     int lse;       // [H8] f32 block result per head
     int table;     // block_table slice (int32), `table_entries` of them
@@ -63,7 +64,8 @@ PKV_HD SmemLayout smem_layout(int D, int T, int W, int R, int NT, int chunk_toke
     s.bars = round_up_int(ring > red ? ring : red, 1024);
     s.m = s.bars + W * R * 8;
     s.l = s.m + W * H8 * 4;
-    s.f = s.l + W * H8 * 4;
+    s.lt = s.l + W * H8 * 4;
+    s.f = s.lt + W * H8 * 4;
     s.lse = s.f + W * H8 * 4;
     s.table = round_up_int(s.lse + H8 * 4, 16);
     s.table_entries = chunk_tokens / page_size + 2;

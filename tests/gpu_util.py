@@ -31,7 +31,8 @@ def max_abs_diff(a, b):
     a = np.asarray(a, np.float64)
     b = np.asarray(b, np.float64)
     same_inf = np.isinf(a) & np.isinf(b) & (np.sign(a) == np.sign(b))
-    d = np.where(same_inf, 0.0, np.abs(a - b))
+    with np.errstate(invalid="ignore"):
+        d = np.where(same_inf, 0.0, np.abs(a - b))
     return float(np.max(d)) if d.size else 0.0
 
 
@@ -59,3 +60,24 @@ def sample_rows(case, n=24, seed=0):
     while len(rows) < n:
         rows.add((int(rng.integers(case.B)), int(rng.integers(case.Hq))))
     return sorted(rows)
+
+
+def bf16_ulp(x):
+    """Spacing of bf16 numbers at |x| (8 significant bits)."""
+    x = np.maximum(np.abs(np.asarray(x, np.float64)), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(x)) - 7)
+
+
+def split_invariance_violation(a, b, tol=SPLIT_TOL):
+    """Largest excess of |a - b| over the split-count bar.
+
+    Different split counts only reorder f32 sums, so the f32 results agree to
+    far better than 2e-3; after rounding to bf16 two such values may still land
+    one rounding step apart when they straddle a rounding boundary.  An element
+    passes when it is within `tol` or within one bf16 step of the larger value.
+    Returns (max excess, fraction of elements that differ at all, max |a-b|)."""
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    d = np.abs(a - b)
+    allowed = np.maximum(tol, bf16_ulp(np.maximum(np.abs(a), np.abs(b))))
+    return float(np.max(d - allowed)), float(np.mean(d > 0)), float(np.max(d))
