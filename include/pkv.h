@@ -169,6 +169,37 @@ PKV_API pkv_status paged_decode_attn_ex(const pkv_bf16 *q, const pkv_bf16 *k_cac
                                 void *workspace, size_t workspace_bytes, int num_splits,
                                 cudaStream_t stream);
 
+/*
+ * Decode attention for callers that cannot allocate device memory.
+ *
+ * Same operation, arguments and results as paged_decode_attn, without the
+ * workspace: the split partials and the status word live in one fixed device
+ * array inside this library (32 MiB, held on every GPU that loads the
+ * library until the process exits).  It exists for callers that may not call
+ * cudaMalloc at decode time -- a serving loop whose device memory pool is
+ * sized and frozen at start-up, a plugin that is handed only one step's
+ * tensors, a host without the runtime's allocator -- and it allocates nothing
+ * itself.  The pages describe no such entry point; it is a library service.
+ *
+ *   device_status  device int (may be NULL): receives this call's device status
+ *                  word (PKV_OK or the first device-side error) once the
+ *                  kernels are done, in stream order.
+ *
+ * The first call on a device looks up the array's device address for that
+ * device (make that call before any stream capture).  A shape whose plan
+ * needs more than 32 MiB of partials returns PKV_ERR_WORKSPACE_TOO_SMALL
+ * before anything runs; use paged_decode_attn with a workspace for those.
+ * Every call clears the status word first.  All calls on a device share the
+ * array: calls that may overlap on the GPU (other streams, other host
+ * threads) race on it and must be ordered by the caller.
+ */
+PKV_API pkv_status paged_decode_attn_static_scratch(const pkv_bf16 *q, const pkv_bf16 *k_cache,
+                                                    const pkv_bf16 *v_cache, const int32_t *block_table,
+                                                    const int32_t *seq_lens, int B, int Hq, int Hkv, int D,
+                                                    int page_size, int num_pages, int max_pages, float scale,
+                                                    pkv_bf16 *out, float *lse, int *device_status,
+                                                    cudaStream_t stream);
+
 /* ------------------------------------------------------------------ merge */
 
 /*

@@ -17,7 +17,8 @@ import threading
 __all__ = [
     "PkvError", "load", "status_string", "plan_query", "paged_decode_attn_workspace_size",
     "paged_decode_attn", "paged_decode_attn_ex", "split_kv_merge", "pkv_check_status",
-    "pkv_reset_status", "pkv_selftest_wait_timeout", "EXPORTED_SYMBOLS", "STATUS",
+    "pkv_reset_status", "pkv_selftest_wait_timeout", "paged_decode_attn_static_scratch", "EXPORTED_SYMBOLS",
+    "STATUS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -33,7 +34,7 @@ STATUS = {
 EXPORTED_SYMBOLS = [
     "pkv_status_string", "pkv_version", "pkv_plan_query", "paged_decode_attn_workspace_size",
     "paged_decode_attn_workspace_size_ex", "paged_decode_attn", "paged_decode_attn_ex", "split_kv_merge",
-    "pkv_check_status", "pkv_reset_status", "pkv_selftest_wait_timeout",
+    "pkv_check_status", "pkv_reset_status", "pkv_selftest_wait_timeout", "paged_decode_attn_static_scratch",
 ]
 
 
@@ -80,6 +81,7 @@ def load(path: str = LIB_PATH):
             "pkv_check_status": (I, [P, P, ctypes.POINTER(I)]),
             "pkv_reset_status": (I, [P, P]),
             "pkv_selftest_wait_timeout": (I, [P, U, P]),
+            "paged_decode_attn_static_scratch": (I, [P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -203,3 +205,22 @@ def pkv_reset_status(workspace, stream=None):
 def pkv_selftest_wait_timeout(workspace, timeout_us=1000, stream=None):
     _check(load().pkv_selftest_wait_timeout(ctypes.c_void_p(workspace.data_ptr()), int(timeout_us),
                                             _stream_handle(stream)), "pkv_selftest_wait_timeout")
+
+
+def paged_decode_attn_static_scratch(q, k_cache, v_cache, block_table, seq_lens, scale, out, lse,
+                                     device_status=None, stream=None):
+    """Calls paged_decode_attn_static_scratch: decode without a caller workspace, for
+    callers that cannot allocate device memory (the library's fixed scratch is used)."""
+    torch = _torch()
+    B, Hq, D = q.shape
+    num_pages, P, Hkv, _ = k_cache.shape
+    st = load().paged_decode_attn_static_scratch(
+        _dev_ptr(q, torch.bfloat16, "q", 3), _dev_ptr(k_cache, torch.bfloat16, "k_cache", 4),
+        _dev_ptr(v_cache, torch.bfloat16, "v_cache", 4), _dev_ptr(block_table, torch.int32, "block_table", 2),
+        _dev_ptr(seq_lens, torch.int32, "seq_lens", 1), B, Hq, Hkv, D, P, num_pages, block_table.shape[1],
+        ctypes.c_float(scale), _dev_ptr(out, torch.bfloat16, "out", 3),
+        _dev_ptr(lse, torch.float32, "lse", 2) if lse is not None else None,
+        _dev_ptr(device_status, torch.int32, "device_status") if device_status is not None else None,
+        _stream_handle(stream))
+    _check(st, "paged_decode_attn_static_scratch")
+    return out, lse

@@ -366,3 +366,88 @@ pkv_status pkv_selftest_wait_timeout(void *workspace, unsigned timeout_us, cudaS
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode with library-owned scratch, for callers that cannot allocate device
+// memory.
+//
+// Some callers cannot call cudaMalloc at the point where they run attention:
+// code running under an allocator that forbids new device allocations (for
+// example a serving loop whose memory pool is sized and frozen at start-up),
+// plugins that are handed only the tensors of one step, or hosts that do not
+// link the CUDA runtime allocator at all.  For them the split partials and the
+// status word live in one fixed file-scope device array instead of a
+// caller-provided workspace.  Every GPU that loads this library holds that
+// array (kStaticScratchBytes) until the process exits.
+//
+// The array's name is only a host-side stand-in for the device variable, so
+// its device address is looked up with cudaGetSymbolAddress, once per device,
+// with that device current, on the first call on that device.  Make that
+// first call before any stream capture.  All calls share the array and it
+// keeps the previous call's contents: each call clears the status word before
+// its kernels run, and calls that overlap on the GPU (different streams, or
+// different host threads, without ordering) race on it.
+// ---------------------------------------------------------------------------
+
+namespace pkv {
+namespace {
+
+constexpr size_t kStaticScratchBytes = 32u << 20;  // 32 MiB per device
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+std::mutex g_scratch_mu;
+void *g_scratch_ptr[64] = {};
+
+pkv_status static_scratch_for_current_device(int *device, void **ptr)
+{
+    if (cudaGetDevice(device) != cudaSuccess) return PKV_ERR_CUDA;
+    if (*device < 0 || *device >= 64) return PKV_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[*device]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return PKV_ERR_CUDA;
+        g_scratch_ptr[*device] = p;
+    }
+    *ptr = g_scratch_ptr[*device];
+    return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" pkv_status paged_decode_attn_static_scratch(const pkv_bf16 *q, const pkv_bf16 *k_cache,
+                                                       const pkv_bf16 *v_cache, const int32_t *block_table,
+                                                       const int32_t *seq_lens, int B, int Hq, int Hkv, int D,
+                                                       int page_size, int num_pages, int max_pages, float scale,
+                                                       pkv_bf16 *out, float *lse, int *device_status,
+                                                       cudaStream_t stream)
+{
+    // Host-side checks first, so a rejected call touches neither the GPU nor the scratch.
+    if (num_pages <= 0 || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+    const pkv_status shape_ok = validate_shape(B, Hq, Hkv, D, page_size, max_pages);
+    if (shape_ok != PKV_OK) return shape_ok;
+    if (B == 0) return PKV_OK;
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out) return PKV_ERR_INVALID_ARG;
+    if (device_status && (reinterpret_cast<uintptr_t>(device_status) & 3u)) return PKV_ERR_MISALIGNED;
+
+    int device = 0, sms = 0;
+    pkv_status st = current_device_sms(&device, &sms);
+    if (st != PKV_OK) return st;
+    pkv_plan plan;
+    st = make_plan(B, Hq, Hkv, D, page_size, max_pages, sms, 0, &plan);
+    if (st != PKV_OK) return st;
+    if (plan.workspace_bytes > kStaticScratchBytes) return PKV_ERR_WORKSPACE_TOO_SMALL;
+
+    void *scratch = nullptr;
+    st = static_scratch_for_current_device(&device, &scratch);
+    if (st != PKV_OK) return st;
+    // The status word must start at zero; the partials are fully written before they are read.
+    if (cudaMemsetAsync(scratch, 0, sizeof(int), stream) != cudaSuccess) return PKV_ERR_CUDA;
+    st = paged_decode_attn(q, k_cache, v_cache, block_table, seq_lens, B, Hq, Hkv, D, page_size, num_pages,
+                           max_pages, scale, out, lse, scratch, kStaticScratchBytes, stream);
+    if (st != PKV_OK) return st;
+    if (device_status &&
+        cudaMemcpyAsync(device_status, scratch, sizeof(int), cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    return PKV_OK;
+}
