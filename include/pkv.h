@@ -94,7 +94,8 @@ typedef struct {
     int blocks_per_sm;    /* resident thread blocks per SM the plan assumes */
     int grid_blocks;      /* thread blocks of the split kernel (S * Hkv * B) */
     int smem_bytes;       /* dynamic shared memory per block */
-    int merge_needed;     /* 1 when S > 1 (the merge kernel runs) */
+    int merge_needed;     /* 1 when S > 1: the last split block of each (b, kv head) merges the
+                             partials inside the same kernel launch */
     size_t workspace_bytes;
 } pkv_plan;
 
@@ -109,9 +110,11 @@ PKV_API pkv_status pkv_plan_query(int B, int Hq, int Hkv, int D, int page_size, 
 /*
  * Workspace bytes that paged_decode_attn needs for this shape on `device`
  * (queries the device's SM count).  The workspace holds a 256-byte header whose
- * first int32 is the device status word, then the split partials.  Before its
- * first use the header must be zero (allocate zeroed, or call
- * pkv_reset_status).
+ * first int32 is the device status word, then (when the plan splits) one int32
+ * completion counter per (b, kv head) and the split partials.  Allocate it
+ * zeroed before its first use; the kernel returns every counter to zero, so a
+ * workspace can be reused call after call without clearing it again.  Calls
+ * that may overlap on the GPU must not share a workspace.
  */
 PKV_API pkv_status paged_decode_attn_workspace_size(int B, int Hq, int Hkv, int D, int page_size,
                                             int max_pages, int device, size_t *bytes /* host */);

@@ -214,8 +214,10 @@ pkv_status decode_impl(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf1
     p.seq_lens = seq_lens;
     p.out = reinterpret_cast<__nv_bfloat16 *>(out);
     p.lse = lse;
-    p.part_lse = reinterpret_cast<float *>(ws + workspace_lse_offset());
-    p.part_out = reinterpret_cast<float *>(ws + workspace_out_offset(plan.num_splits, B, Hq));
+    const WorkspaceLayout wl = workspace_layout(plan.num_splits, B, Hq, Hkv, D);
+    p.counters = reinterpret_cast<int *>(ws + wl.counters);
+    p.part_lse = reinterpret_cast<float *>(ws + wl.part_lse);
+    p.part_out = reinterpret_cast<float *>(ws + wl.part_out);
     p.status = reinterpret_cast<int *>(ws);
     p.B = B;
     p.Hq = Hq;
@@ -230,21 +232,7 @@ pkv_status decode_impl(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf1
     p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
     p.wait_limit_ns = kWaitLimitNs;
 
-    st = launch_decode(D, head_tiles(p.G), mk, mv, p, plan, B, Hkv, device, stream);
-    if (st != PKV_OK || plan.num_splits <= 1) return st;
-
-    MergeParams mp;
-    mp.part_out = p.part_out;
-    mp.part_lse = p.part_lse;
-    mp.seq_lens = seq_lens;
-    mp.out = p.out;
-    mp.lse = lse;
-    mp.S = plan.num_splits;
-    mp.B = B;
-    mp.Hq = Hq;
-    mp.chunk_tokens = plan.chunk_tokens;
-    mp.max_tokens = max_pages * page_size;
-    return launch_merge(D, mp, stream);
+    return launch_decode(D, head_tiles(p.G), mk, mv, p, plan, B, Hkv, device, stream);
 }
 
 }  // namespace

@@ -46,9 +46,11 @@
 // Epilogue.  The W warps' states are merged through shared memory.  If the
 // sequence has a single split the block writes bf16 out and the natural-log
 // lse directly; otherwise it writes its normalised f32 output and lse to the
-// workspace for the merge kernel (FlashQuant wiki "CUDA Kernels", paged_decode.cu
-// "Partial Output"; here normalised and in natural log).  A split that starts
-// past L_b exits at once and is not merged ("Early Exit for Empty Splits").
+// workspace (FlashQuant wiki "CUDA Kernels", paged_decode.cu "Partial Output";
+// here normalised and in natural log), and the last split of the (b, kv head)
+// group to finish merges the group's partials in the same launch, so no second
+// kernel and no launch gap sit on the critical path.  A split that starts past
+// L_b exits at once and is never merged ("Early Exit for Empty Splits").
 #pragma once
 
 #include <cuda_bf16.h>
@@ -67,6 +69,7 @@ struct DecodeParams {
     float *lse;              // [B, Hq] or nullptr
     float *part_lse;         // [S, B, Hq]
     float *part_out;         // [S, B, Hq, D]
+    int *counters;           // [B, Hkv] splits finished per group (wraps to 0 after the last)
     int *status;             // workspace status word
     int B, Hq, Hkv, G, P, log2P, num_pages, max_pages;
     int chunk_tokens, num_splits;
@@ -80,6 +83,7 @@ __device__ __forceinline__ void record_status(int *status, int code)
 }
 
 constexpr float kLn2 = 0.693147180559945309f;
+constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D, int NT>
 __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
@@ -423,24 +427,104 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
     __syncthreads();
 
     const bool direct = (n_chunks == 1);
-    for (int i = threadIdx.x; i < G * D; i += W * 32) {
-        const int h = i / D, d = i - h * D;
-        float o = 0.f;
+    if (direct) {  // the only split of this sequence: final bf16 output and lse
+        for (int i = threadIdx.x; i < G * D / 2; i += W * 32) {
+            const int h = (2 * i) / D, d = 2 * i - h * D;
+            float o0 = 0.f, o1 = 0.f;
 #pragma unroll
-        for (int w = 0; w < W; ++w) o += red[(w * H8 + h) * RS + d] * sm_f[w * H8 + h];
-        const size_t row = (size_t)b * p.Hq + kvh * G + h;
-        if (direct)
-            p.out[row * D + d] = __float2bfloat16_rn(o);
-        else
-            p.part_out[((size_t)c * p.B * p.Hq + row) * D + d] = o;
-    }
-    if (threadIdx.x < G) {
-        const size_t row = (size_t)b * p.Hq + kvh * G + threadIdx.x;
-        if (direct) {
-            if (p.lse) p.lse[row] = sm_lse[threadIdx.x];
-        } else {
-            p.part_lse[(size_t)c * p.B * p.Hq + row] = sm_lse[threadIdx.x];
+            for (int w = 0; w < W; ++w) {
+                const float f = sm_f[w * H8 + h];
+                o0 += red[(w * H8 + h) * RS + d] * f;
+                o1 += red[(w * H8 + h) * RS + d + 1] * f;
+            }
+            const size_t row = (size_t)b * p.Hq + kvh * G + h;
+            *reinterpret_cast<uint32_t *>(p.out + row * D + d) = pack_bf16x2(o0, o1);
         }
+        if (threadIdx.x < G && p.lse) p.lse[(size_t)b * p.Hq + kvh * G + threadIdx.x] = sm_lse[threadIdx.x];
+        return;
+    }
+
+    // ---- one of several splits: write this split's normalised output and lse ----
+    const size_t rows = (size_t)p.B * p.Hq;
+    const size_t row0 = (size_t)b * p.Hq + kvh * G;
+    for (int i = threadIdx.x; i < G * D / 4; i += W * 32) {
+        const int h = (4 * i) / D, d = 4 * i - h * D;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+            const float f = sm_f[w * H8 + h];
+            const float *r = red + (w * H8 + h) * RS + d;
+            o.x += r[0] * f;
+            o.y += r[1] * f;
+            o.z += r[2] * f;
+            o.w += r[3] * f;
+        }
+        *reinterpret_cast<float4 *>(p.part_out + ((size_t)c * rows + row0 + h) * D + d) = o;
+    }
+    if (threadIdx.x < G) p.part_lse[(size_t)c * rows + row0 + threadIdx.x] = sm_lse[threadIdx.x];
+
+    // ---- the last split of this (b, kv head) to finish merges all of them ----------
+    // Log-sum-exp merge (FlashQuant wiki "CUDA Kernels", split_k_reduce.cu
+    // "Algorithm"): the weight of split s is exp(lse_s - max_s lse_s).  The
+    // splits are combined in index order whichever block arrives last, so the
+    // result does not depend on scheduling.  atomicInc wraps the per-group
+    // counter back to 0 on the last arrival, ready for the next call.
+    __threadfence();
+    __syncthreads();
+    int *flag = reinterpret_cast<int *>(base + lay.flag);
+    if (threadIdx.x == 0)
+        *flag = atomicInc(reinterpret_cast<unsigned *>(p.counters + b * p.Hkv + kvh), (unsigned)(n_chunks - 1)) ==
+                (unsigned)(n_chunks - 1);
+    __syncthreads();
+    if (!*flag) return;
+    __threadfence();
+
+    const float ninf = -__int_as_float(0x7f800000);
+    for (int h = warp; h < G; h += W) {  // per-head max and weight sum over the splits
+        const float *lp = p.part_lse + row0 + h;
+        float mx = ninf;
+        for (int sidx = lane; sidx < n_chunks; sidx += 32) mx = fmaxf(mx, __ldcg(lp + sidx * rows));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        float wsum = 0.f;
+        if (mx != ninf)
+            for (int sidx = lane; sidx < n_chunks; sidx += 32) wsum += ex2((__ldcg(lp + sidx * rows) - mx) * kLog2e);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+        if (lane == 0) {
+            sm_m[h] = mx;
+            sm_l[h] = wsum;
+        }
+    }
+    __syncthreads();
+    constexpr int V4 = D / 4;
+    for (int e = threadIdx.x; e < G * V4; e += W * 32) {
+        const int h = e / V4, d4 = e - h * V4;
+        const float mx = sm_m[h];
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        float inv = 0.f;
+        if (mx != ninf) {
+            const float *lp = p.part_lse + row0 + h;
+            const float4 *op = reinterpret_cast<const float4 *>(p.part_out + (row0 + h) * D) + d4;
+#pragma unroll 4
+            for (int sidx = 0; sidx < n_chunks; ++sidx) {
+                const float w = ex2((__ldcg(lp + sidx * rows) - mx) * kLog2e);
+                const float4 v = __ldcg(op + sidx * rows * V4);
+                a.x += w * v.x;
+                a.y += w * v.y;
+                a.z += w * v.z;
+                a.w += w * v.w;
+            }
+            inv = 1.f / sm_l[h];
+        }
+        uint2 packed;
+        packed.x = pack_bf16x2(a.x * inv, a.y * inv);
+        packed.y = pack_bf16x2(a.z * inv, a.w * inv);
+        *reinterpret_cast<uint2 *>(p.out + (row0 + h) * D + 4 * d4) = packed;
+    }
+    if (threadIdx.x < G && p.lse) {
+        const float mx = sm_m[threadIdx.x];
+        p.lse[row0 + threadIdx.x] = mx == ninf ? ninf : mx + __logf(sm_l[threadIdx.x]);
     }
 }
 

@@ -33,7 +33,6 @@ struct MergeParams {
 };
 
 constexpr int kMergeWarps = 4;
-constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeParams p)

@@ -39,18 +39,16 @@ RuntimeTiling tiling_for(int D)
     }
 }
 
-size_t workspace_lse_offset() { return kWorkspaceHeader; }
+static size_t pad256(size_t x) { return (x + 255) / 256 * 256; }
 
-size_t workspace_out_offset(int S, int B, int Hq)
+WorkspaceLayout workspace_layout(int S, int B, int Hq, int Hkv, int D)
 {
-    const size_t lse_bytes = (size_t)S * B * Hq * sizeof(float);
-    return kWorkspaceHeader + (lse_bytes + 255) / 256 * 256;
-}
-
-size_t workspace_bytes(int S, int B, int Hq, int D)
-{
-    if (S <= 1) return kWorkspaceHeader;
-    return workspace_out_offset(S, B, Hq) + (size_t)S * B * Hq * D * sizeof(float);
+    WorkspaceLayout w;
+    w.counters = kWorkspaceHeader;
+    w.part_lse = w.counters + pad256((size_t)B * Hkv * sizeof(int));
+    w.part_out = w.part_lse + pad256((size_t)S * B * Hq * sizeof(float));
+    w.total = S <= 1 ? kWorkspaceHeader : w.part_out + (size_t)S * B * Hq * D * sizeof(float);
+    return w;
 }
 
 static bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
@@ -130,7 +128,7 @@ pkv_status make_plan(int B, int Hq, int Hkv, int D, int page_size, int max_pages
     plan->grid_blocks = S * Hkv * B;
     plan->smem_bytes = lay.dynamic;
     plan->merge_needed = S > 1 ? 1 : 0;
-    plan->workspace_bytes = workspace_bytes(S, B, Hq, D);
+    plan->workspace_bytes = workspace_layout(S, B, Hq, Hkv, D).total;
     return PKV_OK;
 }
 

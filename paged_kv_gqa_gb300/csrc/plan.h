@@ -46,6 +46,7 @@ struct SmemLayout {
     int lt;        // [W][H8] f32 same, summed over the bf16-rounded probabilities the PV mma uses
     int f;         // [W][H8] f32 per-warp combine factor
     int lse;       // [H8] f32 block result per head
+    int flag;      // one int: "this block merges its group"
     int table;     // block_table slice (int32), `table_entries` of them
     int table_entries;
     int total;     // bytes from the aligned base
@@ -67,18 +68,25 @@ PKV_HD SmemLayout smem_layout(int D, int T, int W, int R, int NT, int chunk_toke
     s.lt = s.l + W * H8 * 4;
     s.f = s.lt + W * H8 * 4;
     s.lse = s.f + W * H8 * 4;
-    s.table = round_up_int(s.lse + H8 * 4, 16);
+    s.flag = s.lse + H8 * 4;
+    s.table = round_up_int(s.flag + 4, 16);
     s.table_entries = chunk_tokens / page_size + 2;
     s.total = round_up_int(s.table + s.table_entries * 4, 16);
     s.dynamic = s.total + 1024;
     return s;
 }
 
-// Workspace layout: [header 256 B][partial lse S*B*Hq f32, padded to 256 B][partial out S*B*Hq*D f32]
+// Workspace layout (byte offsets), used only when S > 1:
+//   [0, 256)   header: int32 status word at 0
+//   counters   B*Hkv int32 split-completion counters (zero before first use; self-resetting)
+//   part_lse   S*B*Hq f32
+//   part_out   S*B*Hq*D f32
+// With S == 1 the workspace is the 256-byte header alone.
 constexpr size_t kWorkspaceHeader = 256;
-size_t workspace_bytes(int S, int B, int Hq, int D);
-size_t workspace_lse_offset();
-size_t workspace_out_offset(int S, int B, int Hq);
+struct WorkspaceLayout {
+    size_t counters, part_lse, part_out, total;
+};
+WorkspaceLayout workspace_layout(int S, int B, int Hq, int Hkv, int D);
 
 // Shape checks shared by every entry point (no CUDA call).
 pkv_status validate_shape(int B, int Hq, int Hkv, int D, int page_size, int max_pages);

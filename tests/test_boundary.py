@@ -117,7 +117,8 @@ def test_plan_invariants(lib, name, sms):
     # K+V bytes of one split stay bounded so no split becomes a straggler
     assert plan["chunk_tokens"] * 4 * D <= (1 << 20) or plan["num_splits"] == 1
     if plan["num_splits"] > 1:
-        ws = 256 + ((plan["num_splits"] * B * Hq * 4 + 255) // 256) * 256 + plan["num_splits"] * B * Hq * D * 4
+        pad = lambda x: (x + 255) // 256 * 256
+        ws = 256 + pad(B * Hkv * 4) + pad(plan["num_splits"] * B * Hq * 4) + plan["num_splits"] * B * Hq * D * 4
         assert plan["workspace_bytes"] == ws
     else:
         assert plan["workspace_bytes"] == 256
