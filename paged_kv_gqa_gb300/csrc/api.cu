@@ -53,11 +53,11 @@ EncodeTiledFn encode_fn()
 
 struct MapKey {
     const void *ptr;
-    int num_pages, P, Hkv, D, box_t, device;
+    int num_pages, P, Hkv, D, box_t, device, rank;
     bool operator==(const MapKey &o) const
     {
         return ptr == o.ptr && num_pages == o.num_pages && P == o.P && Hkv == o.Hkv && D == o.D &&
-               box_t == o.box_t && device == o.device;
+               box_t == o.box_t && device == o.device && rank == o.rank;
     }
 };
 
@@ -76,12 +76,17 @@ MapCache &map_cache()
     return c;
 }
 
-// View of the page pool [num_pages*P rows, Hkv, D] bf16, box (64 dims, 1 head,
-// box_t rows), 128-byte swizzle.  Cached per (pointer, shape, device).
-pkv_status get_pool_map(const void *pool, int num_pages, int P, int Hkv, int D, int box_t, int device,
+// Tensor maps over the page pool (bf16, 128-byte swizzle), cached per (pointer,
+// shape, device, rank):
+//   rank 4: dims (64 dims, num_pages*P rows, D/64 column blocks, Hkv heads) with
+//           strides (row: Hkv*D*2 B, column block: 128 B, head: D*2 B); one box
+//           (64, box_t, D/64, 1) lands a page slice of one head as [D/64][box_t][64];
+//   rank 3: dims (D, Hkv, num_pages*P rows), box (64, 1, box_t): one box per
+//           64-column block (the fallback when the driver refuses the rank-4 view).
+pkv_status get_pool_map(const void *pool, int num_pages, int P, int Hkv, int D, int box_t, int device, int rank,
                         CUtensorMap *out)
 {
-    MapKey key{pool, num_pages, P, Hkv, D, box_t, device};
+    MapKey key{pool, num_pages, P, Hkv, D, box_t, device, rank};
     MapCache &c = map_cache();
     std::lock_guard<std::mutex> lock(c.mu);
     for (int i = 0; i < MapCache::N; ++i)
@@ -91,14 +96,26 @@ pkv_status get_pool_map(const void *pool, int num_pages, int P, int Hkv, int D, 
         }
     EncodeTiledFn fn = encode_fn();
     if (!fn) return PKV_ERR_CUDA;
-    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)num_pages * (cuuint64_t)P};
-    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
-    const cuuint32_t box[3] = {64u, 1u, (cuuint32_t)box_t};
-    const cuuint32_t estr[3] = {1u, 1u, 1u};
     CUtensorMap m;
-    const CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides, box,
-                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r;
+    if (rank == 4) {
+        const cuuint64_t dims[4] = {64u, (cuuint64_t)num_pages * (cuuint64_t)P, (cuuint64_t)(D / 64),
+                                    (cuuint64_t)Hkv};
+        const cuuint64_t strides[3] = {(cuuint64_t)Hkv * D * 2, 128u, (cuuint64_t)D * 2};
+        const cuuint32_t box[4] = {64u, (cuuint32_t)box_t, (cuuint32_t)(D / 64), 1u};
+        const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+        r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(pool), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)num_pages * (cuuint64_t)P};
+        const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
+        const cuuint32_t box[3] = {64u, 1u, (cuuint32_t)box_t};
+        const cuuint32_t estr[3] = {1u, 1u, 1u};
+        r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     if (r != CUDA_SUCCESS) return PKV_ERR_CUDA;
     const int slot = c.next;
     c.next = (c.next + 1) % MapCache::N;
@@ -126,31 +143,34 @@ pkv_status current_device_sms(int *device, int *sms)
 
 template <int D, int NT>
 pkv_status launch_decode_variant(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
-                                 const pkv_plan &plan, int B, int Hkv, int device, cudaStream_t stream)
+                                 const pkv_plan &plan, int device, cudaStream_t stream)
 {
     static bool attr_set[64] = {};
     static std::mutex mu;
-    auto kern = decode_split_kernel<D, NT>;
+    auto kern = decode_kernel<D, NT>;
+    constexpr int smem = persist_layout<D, NT>().dynamic;
+    static_assert(smem <= kSmemPerBlockMax, "decode kernel shared memory over the per-block limit");
+    static_assert(sizeof(ItemDesc) == kDescBytes, "descriptor size");
     if (device < 0 || device >= 64) return PKV_ERR_UNSUPPORTED;
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!attr_set[device]) {
-            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448) != cudaSuccess)
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
                 return PKV_ERR_CUDA;
             attr_set[device] = true;
         }
     }
-    dim3 grid(plan.num_splits, Hkv, B);
-    dim3 block(plan.warps * 32);
-    kern<<<grid, block, plan.smem_bytes, stream>>>(mk, mv, p);
+    dim3 grid(plan.grid_blocks);
+    dim3 block((PTiling<D, NT>::W + 1) * 32);
+    kern<<<grid, block, smem, stream>>>(mk, mv, p);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 pkv_status launch_decode(int D, int NT, const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
-                         const pkv_plan &plan, int B, int Hkv, int device, cudaStream_t stream)
+                         const pkv_plan &plan, int device, cudaStream_t stream)
 {
 #define PKV_CASE(DD, NN) \
-    if (D == DD && NT == NN) return launch_decode_variant<DD, NN>(mk, mv, p, plan, B, Hkv, device, stream);
+    if (D == DD && NT == NN) return launch_decode_variant<DD, NN>(mk, mv, p, plan, device, stream);
     PKV_CASE(64, 1)
     PKV_CASE(64, 2)
     PKV_CASE(64, 4)
@@ -201,25 +221,29 @@ pkv_status decode_impl(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf1
     if (workspace_bytes_ < plan.workspace_bytes) return PKV_ERR_WORKSPACE_TOO_SMALL;
 
     const int box_t = plan.stage_tokens < page_size ? plan.stage_tokens : page_size;
+    // One box per tensor per stage when a stage lies in one page (rank-4 view);
+    // otherwise, or if the driver refuses that view, one box per 64 columns.
     CUtensorMap mk, mv;
-    st = get_pool_map(k_cache, num_pages, page_size, Hkv, D, box_t, device, &mk);
-    if (st != PKV_OK) return st;
-    st = get_pool_map(v_cache, num_pages, page_size, Hkv, D, box_t, device, &mv);
-    if (st != PKV_OK) return st;
+    int box4 = 0;
+    if (plan.stage_tokens <= page_size &&
+        get_pool_map(k_cache, num_pages, page_size, Hkv, D, box_t, device, 4, &mk) == PKV_OK &&
+        get_pool_map(v_cache, num_pages, page_size, Hkv, D, box_t, device, 4, &mv) == PKV_OK)
+        box4 = 1;
+    if (!box4) {
+        st = get_pool_map(k_cache, num_pages, page_size, Hkv, D, box_t, device, 3, &mk);
+        if (st != PKV_OK) return st;
+        st = get_pool_map(v_cache, num_pages, page_size, Hkv, D, box_t, device, 3, &mv);
+        if (st != PKV_OK) return st;
+    }
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const int Bl = B < kMaxBatchPerLaunch ? B : kMaxBatchPerLaunch;
+    const WorkspaceLayout wl = workspace_layout(plan.grid_blocks, Bl, Hq, Hkv, D);
     DecodeParams p;
-    p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
-    p.block_table = block_table;
-    p.seq_lens = seq_lens;
-    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
-    p.lse = lse;
-    const WorkspaceLayout wl = workspace_layout(plan.num_splits, B, Hq, Hkv, D);
     p.counters = reinterpret_cast<int *>(ws + wl.counters);
     p.part_lse = reinterpret_cast<float *>(ws + wl.part_lse);
     p.part_out = reinterpret_cast<float *>(ws + wl.part_out);
     p.status = reinterpret_cast<int *>(ws);
-    p.B = B;
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.G = Hq / Hkv;
@@ -227,12 +251,24 @@ pkv_status decode_impl(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf1
     p.log2P = log2_exact(page_size);
     p.num_pages = num_pages;
     p.max_pages = max_pages;
-    p.chunk_tokens = plan.chunk_tokens;
-    p.num_splits = plan.num_splits;
+    p.box4 = box4;
+    p.min_range_tiles = plan.chunk_tokens / plan.stage_tokens;
+    p.max_item_tiles = plan.max_item_tiles;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
     p.wait_limit_ns = kWaitLimitNs;
-
-    return launch_decode(D, head_tiles(p.G), mk, mv, p, plan, B, Hkv, device, stream);
+    // Batches above kMaxBatchPerLaunch run as several launches on the same stream.
+    for (int b0 = 0; b0 < B; b0 += kMaxBatchPerLaunch) {
+        const int Bs = B - b0 < kMaxBatchPerLaunch ? B - b0 : kMaxBatchPerLaunch;
+        p.q = reinterpret_cast<const __nv_bfloat16 *>(q) + (size_t)b0 * Hq * D;
+        p.block_table = block_table + (size_t)b0 * max_pages;
+        p.seq_lens = seq_lens + b0;
+        p.out = reinterpret_cast<__nv_bfloat16 *>(out) + (size_t)b0 * Hq * D;
+        p.lse = lse ? lse + (size_t)b0 * Hq : nullptr;
+        p.B = Bs;
+        st = launch_decode(D, head_tiles(p.G), mk, mv, p, plan, device, stream);
+        if (st != PKV_OK) return st;
+    }
+    return PKV_OK;
 }
 
 }  // namespace
@@ -380,7 +416,7 @@ pkv_status pkv_selftest_wait_timeout(void *workspace, unsigned timeout_us, cudaS
 namespace pkv {
 namespace {
 
-constexpr size_t kStaticScratchBytes = 32u << 20;  // 32 MiB per device
+constexpr size_t kStaticScratchBytes = 16u << 20;  // 16 MiB per device
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 std::mutex g_scratch_mu;
