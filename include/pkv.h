@@ -86,26 +86,23 @@ PKV_API int pkv_version(void);
  * launch uses.
  */
 typedef struct {
-    int num_splits;       /* most pieces one (b, kv head) key range is cut into, for sequences
-                             of full table width (the device cuts by the real lengths) */
-    int chunk_tokens;     /* fewest keys in one block's slice of the batch */
+    int num_splits;       /* S: key-range splits per (b, kv head) at full table width */
+    int chunk_tokens;     /* keys per split (a multiple of stage_tokens) */
     int stage_tokens;     /* keys per pipeline stage (one TMA box row set) */
-    int warps;            /* consumer warps per block; one more warp prepares work items */
-    int ring_stages;      /* stages in flight per consumer warp */
-    int blocks_per_sm;    /* 1: the grid is persistent, one block per SM */
-    int grid_blocks;      /* blocks of the decode kernel (the SM count) */
+    int warps;            /* consumer warps per thread block */
+    int ring_stages;      /* stages in flight per warp */
+    int blocks_per_sm;    /* resident thread blocks per SM the plan assumes */
+    int grid_blocks;      /* thread blocks of the split kernel (S * Hkv * B) */
     int smem_bytes;       /* dynamic shared memory per block */
-    int merge_needed;     /* 1 when a key range can be cut into pieces; the block that finishes a
-                             range's last piece merges the pieces inside the same launch */
-    int max_item_tiles;   /* stage tiles per work item (bounds its staged block-table slice) */
+    int merge_needed;     /* 1 when S > 1: the last split block of each (b, kv head) merges the
+                             partials inside the same kernel launch */
     size_t workspace_bytes;
 } pkv_plan;
 
 /*
  * Pure host function: the plan for a shape on a device with `num_sms` SMs.
- * num_splits > 0 sets the finest split: every block's slice then holds at
- * least ceil(max_pages * page_size / num_splits) keys; 0 chooses
- * automatically.  No CUDA call.
+ * num_splits > 0 forces that many splits (clamped to [1, ceil(max_pages *
+ * page_size / stage_tokens)]); 0 chooses automatically.  No CUDA call.
  */
 PKV_API pkv_status pkv_plan_query(int B, int Hq, int Hkv, int D, int page_size, int max_pages,
                           int num_sms, int num_splits, pkv_plan *plan /* host */);
@@ -164,10 +161,9 @@ PKV_API pkv_status paged_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache,
                              void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
- * Same as paged_decode_attn with a forced split granularity (num_splits > 0:
- * each block's slice of the batch holds at least ceil(max_pages * page_size /
- * num_splits) keys), for tests and sweeps; 0 is the automatic choice.  Results
- * for different settings differ only by f32 summation order.
+ * Same as paged_decode_attn with a forced split count (num_splits > 0), for
+ * tests and sweeps; 0 is the automatic choice.  Results for different split
+ * counts differ only by f32 summation order.
  */
 PKV_API pkv_status paged_decode_attn_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
                                 const int32_t *block_table, const int32_t *seq_lens,
@@ -181,7 +177,7 @@ PKV_API pkv_status paged_decode_attn_ex(const pkv_bf16 *q, const pkv_bf16 *k_cac
  *
  * Same operation, arguments and results as paged_decode_attn, without the
  * workspace: the split partials and the status word live in one fixed device
- * array inside this library (16 MiB, held on every GPU that loads the
+ * array inside this library (32 MiB, held on every GPU that loads the
  * library until the process exits).  It exists for callers that may not call
  * cudaMalloc at decode time -- a serving loop whose device memory pool is
  * sized and frozen at start-up, a plugin that is handed only one step's
@@ -194,7 +190,7 @@ PKV_API pkv_status paged_decode_attn_ex(const pkv_bf16 *q, const pkv_bf16 *k_cac
  *
  * The first call on a device looks up the array's device address for that
  * device (make that call before any stream capture).  A shape whose plan
- * needs more than 16 MiB of workspace returns PKV_ERR_WORKSPACE_TOO_SMALL
+ * needs more than 32 MiB of partials returns PKV_ERR_WORKSPACE_TOO_SMALL
  * before anything runs; use paged_decode_attn with a workspace for those.
  * Every call clears the status word first.  All calls on a device share the
  * array: calls that may overlap on the GPU (other streams, other host

@@ -48,7 +48,7 @@ class PkvPlan(ctypes.Structure):
     _fields_ = [("num_splits", ctypes.c_int), ("chunk_tokens", ctypes.c_int), ("stage_tokens", ctypes.c_int),
                 ("warps", ctypes.c_int), ("ring_stages", ctypes.c_int), ("blocks_per_sm", ctypes.c_int),
                 ("grid_blocks", ctypes.c_int), ("smem_bytes", ctypes.c_int), ("merge_needed", ctypes.c_int),
-                ("max_item_tiles", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace_bytes", ctypes.c_size_t)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -143,34 +143,31 @@ pkv_status current_device_sms(int *device, int *sms)
 
 template <int D, int NT>
 pkv_status launch_decode_variant(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
-                                 const pkv_plan &plan, int device, cudaStream_t stream)
+                                 const pkv_plan &plan, int B, int Hkv, int device, cudaStream_t stream)
 {
     static bool attr_set[64] = {};
     static std::mutex mu;
-    auto kern = decode_kernel<D, NT>;
-    constexpr int smem = persist_layout<D, NT>().dynamic;
-    static_assert(smem <= kSmemPerBlockMax, "decode kernel shared memory over the per-block limit");
-    static_assert(sizeof(ItemDesc) == kDescBytes, "descriptor size");
+    auto kern = decode_split_kernel<D, NT>;
     if (device < 0 || device >= 64) return PKV_ERR_UNSUPPORTED;
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!attr_set[device]) {
-            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448) != cudaSuccess)
                 return PKV_ERR_CUDA;
             attr_set[device] = true;
         }
     }
-    dim3 grid(plan.grid_blocks);
-    dim3 block((PTiling<D, NT>::W + 1) * 32);
-    kern<<<grid, block, smem, stream>>>(mk, mv, p);
+    dim3 grid(Hkv, plan.num_splits, B);
+    dim3 block(plan.warps * 32);
+    kern<<<grid, block, plan.smem_bytes, stream>>>(mk, mv, p);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 pkv_status launch_decode(int D, int NT, const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
-                         const pkv_plan &plan, int device, cudaStream_t stream)
+                         const pkv_plan &plan, int B, int Hkv, int device, cudaStream_t stream)
 {
 #define PKV_CASE(DD, NN) \
-    if (D == DD && NT == NN) return launch_decode_variant<DD, NN>(mk, mv, p, plan, device, stream);
+    if (D == DD && NT == NN) return launch_decode_variant<DD, NN>(mk, mv, p, plan, B, Hkv, device, stream);
     PKV_CASE(64, 1)
     PKV_CASE(64, 2)
     PKV_CASE(64, 4)
@@ -237,13 +234,18 @@ pkv_status decode_impl(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf1
     }
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    const int Bl = B < kMaxBatchPerLaunch ? B : kMaxBatchPerLaunch;
-    const WorkspaceLayout wl = workspace_layout(plan.grid_blocks, Bl, Hq, Hkv, D);
     DecodeParams p;
+    p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.lse = lse;
+    const WorkspaceLayout wl = workspace_layout(plan.num_splits, B, Hq, Hkv, D);
     p.counters = reinterpret_cast<int *>(ws + wl.counters);
     p.part_lse = reinterpret_cast<float *>(ws + wl.part_lse);
     p.part_out = reinterpret_cast<float *>(ws + wl.part_out);
     p.status = reinterpret_cast<int *>(ws);
+    p.B = B;
     p.Hq = Hq;
     p.Hkv = Hkv;
     p.G = Hq / Hkv;
@@ -251,24 +253,13 @@ pkv_status decode_impl(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf1
     p.log2P = log2_exact(page_size);
     p.num_pages = num_pages;
     p.max_pages = max_pages;
+    p.chunk_tokens = plan.chunk_tokens;
+    p.num_splits = plan.num_splits;
     p.box4 = box4;
-    p.min_range_tiles = plan.chunk_tokens / plan.stage_tokens;
-    p.max_item_tiles = plan.max_item_tiles;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
     p.wait_limit_ns = kWaitLimitNs;
-    // Batches above kMaxBatchPerLaunch run as several launches on the same stream.
-    for (int b0 = 0; b0 < B; b0 += kMaxBatchPerLaunch) {
-        const int Bs = B - b0 < kMaxBatchPerLaunch ? B - b0 : kMaxBatchPerLaunch;
-        p.q = reinterpret_cast<const __nv_bfloat16 *>(q) + (size_t)b0 * Hq * D;
-        p.block_table = block_table + (size_t)b0 * max_pages;
-        p.seq_lens = seq_lens + b0;
-        p.out = reinterpret_cast<__nv_bfloat16 *>(out) + (size_t)b0 * Hq * D;
-        p.lse = lse ? lse + (size_t)b0 * Hq : nullptr;
-        p.B = Bs;
-        st = launch_decode(D, head_tiles(p.G), mk, mv, p, plan, device, stream);
-        if (st != PKV_OK) return st;
-    }
-    return PKV_OK;
+
+    return launch_decode(D, head_tiles(p.G), mk, mv, p, plan, B, Hkv, device, stream);
 }
 
 }  // namespace
@@ -416,7 +407,7 @@ pkv_status pkv_selftest_wait_timeout(void *workspace, unsigned timeout_us, cudaS
 namespace pkv {
 namespace {
 
-constexpr size_t kStaticScratchBytes = 16u << 20;  // 16 MiB per device
+constexpr size_t kStaticScratchBytes = 32u << 20;  // 32 MiB per device
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 std::mutex g_scratch_mu;

@@ -1,16 +1,21 @@
-// plan.cpp -- host planner for the balanced persistent decode launch.
+// plan.cpp -- host planner for the split-KV decode launch.
 //
-// The grid is one block per SM.  The device splits the batch's key tiles into
-// equal slices, one per block, from seq_lens (a deterministic function of the
-// lengths and the SM count; OASR "Kernel Layer", "Fused attention": the split
-// must not depend on capture state, since it sets the order the f32 partials
-// are summed).  The host only fixes:
-//   - the minimum slice (kMinRangeTokens keys, or max_tokens / num_splits when a
-//     split count is forced), so that tiny batches are not cut into slivers whose
-//     partials cost more than they save;
-//   - the largest work item (kMaxItemPages pages of block table staged in shared
-//     memory);
-//   - the workspace: a header, one counter per (b, kv head), two partial slots per block.
+// The split count is a pure function of the shape and the SM count (OASR
+// "Kernel Layer", "Fused attention": never of capture state, because it sets
+// the order the f32 partials are summed).  The device-side lengths are not
+// visible here, so the plan sizes splits for sequences of full table width.
+// The rule (tuned on GB300 by sweeping the split count per workload):
+//   - about one wave of blocks: enough splits that every resident block slot
+//     gets one, since fewer, larger blocks amortise each block's start-up and
+//     epilogue; a batch that already fills the slots is not split;
+//   - a split holds at most ~1 MiB of K+V (kMaxSplitBytes) when the (b, kv
+//     head) units are fewer than the slots, ~2 MiB when they fill the slots, so
+//     that no split becomes a straggler;
+//   - never fewer than kMinSplitTokens keys per split;
+//   - with several waves, the count in [S, 1.5 S] that fills the last wave best.
+// Splits that start past a sequence's length exit at once and are ignored by
+// the merge (FlashQuant wiki "CUDA Kernels", paged_decode.cu "Early Exit for
+// Empty Splits").
 #include "plan.h"
 
 #include <algorithm>
@@ -19,37 +24,33 @@
 namespace pkv {
 
 namespace {
-constexpr int kMinRangeTokens = 256;
+constexpr long kMaxSplitBytes = 1l << 20;  // K+V bytes of one (b, kv head) split
+constexpr int kMinSplitTokens = 256;
+constexpr int kSmemPerSm = 233472;          // 228 KiB per SM on sm_100-class parts
+constexpr int kSmemPerBlockMax = 232448;    // 227 KiB opt-in maximum per block
+constexpr int kBlockReserve = 1024;         // shared memory the system reserves per block
+constexpr int kMaxTablePages = 4096;        // block_table slice a block stages in smem
 }  // namespace
 
-template <int D, int NT>
-static RuntimeTiling tiling_of()
+RuntimeTiling tiling_for(int D)
 {
-    using TL = PTiling<D, NT>;
-    return {TL::T, TL::W, TL::R, persist_layout<D, NT>().dynamic};
-}
-
-RuntimeTiling tiling_for(int D, int NT)
-{
-#define PKV_T(DD, NN) \
-    if (D == DD && NT == NN) return tiling_of<DD, NN>();
-    PKV_T(64, 1) PKV_T(64, 2) PKV_T(64, 4)
-    PKV_T(128, 1) PKV_T(128, 2) PKV_T(128, 4)
-    PKV_T(256, 1) PKV_T(256, 2) PKV_T(256, 4)
-#undef PKV_T
-    return {0, 0, 0, 0};
+    switch (D) {
+        case 64: return {Tiling<64>::T, Tiling<64>::W, Tiling<64>::R};
+        case 128: return {Tiling<128>::T, Tiling<128>::W, Tiling<128>::R};
+        case 256: return {Tiling<256>::T, Tiling<256>::W, Tiling<256>::R};
+        default: return {0, 0, 0};
+    }
 }
 
 static size_t pad256(size_t x) { return (x + 255) / 256 * 256; }
 
-WorkspaceLayout workspace_layout(int grid, int B, int Hq, int Hkv, int D)
+WorkspaceLayout workspace_layout(int S, int B, int Hq, int Hkv, int D)
 {
-    const size_t G = (size_t)(Hq / Hkv);
     WorkspaceLayout w;
     w.counters = kWorkspaceHeader;
     w.part_lse = w.counters + pad256((size_t)B * Hkv * sizeof(int));
-    w.part_out = w.part_lse + pad256(2 * (size_t)grid * G * sizeof(float));
-    w.total = w.part_out + 2 * (size_t)grid * G * D * sizeof(float);
+    w.part_out = w.part_lse + pad256((size_t)S * B * Hq * sizeof(float));
+    w.total = S <= 1 ? kWorkspaceHeader : w.part_out + (size_t)S * B * Hq * D * sizeof(float);
     return w;
 }
 
@@ -73,35 +74,72 @@ pkv_status make_plan(int B, int Hq, int Hkv, int D, int page_size, int max_pages
     const pkv_status v = validate_shape(B, Hq, Hkv, D, page_size, max_pages);
     if (v != PKV_OK) return v;
     const int G = Hq / Hkv;
+
+    const RuntimeTiling t = tiling_for(D);
     const int NT = head_tiles(G);
-    const RuntimeTiling t = tiling_for(D, NT);
-    if (t.smem > kSmemPerBlockMax) return PKV_ERR_UNSUPPORTED;
-    const int Bl = std::max(1, std::min(B, kMaxBatchPerLaunch));  // sequences per launch
     const int max_tokens = max_pages * page_size;
-    const int max_tiles = (max_tokens + t.T - 1) / t.T;
-    const int grid = num_sms;
-    if ((long)Bl * Hkv * max_tiles >= (1l << 31)) return PKV_ERR_INVALID_ARG;  // tile indices are int32
+    const int units = std::max(1, B * Hkv);
 
-    const int min_range = num_splits > 0 ? std::max(1, (max_tiles + num_splits - 1) / num_splits)
-                                         : std::max(1, (kMinRangeTokens + t.T - 1) / t.T);
-    const int max_item = std::max(1, (kMaxItemPages - 2) * page_size / t.T);
-    // Estimates for sequences of full table width (the device uses the real lengths).
-    const long total_full = (long)Bl * Hkv * max_tiles;
-    const long per_full = std::max((total_full + grid - 1) / grid, (long)min_range);
-    const int pieces = (int)std::min<long>((max_tiles + per_full - 1) / per_full + (max_tiles % per_full ? 1 : 0),
-                                           grid);
+    // Resident blocks per SM, sized with the largest table slice the auto plan uses.
+    const int cap_tokens = std::max(t.T, (int)(kMaxSplitBytes / (4l * D)) / t.T * t.T);
+    const SmemLayout ref = smem_layout(D, t.T, t.W, t.R, NT, cap_tokens, page_size);
+    int per_sm = std::max(1, kSmemPerSm / (ref.dynamic + kBlockReserve));
+    per_sm = std::min(per_sm, 2048 / (t.W * 32));
+    const int slots = num_sms * per_sm;
 
-    plan->num_splits = std::max(1, pieces);
-    plan->chunk_tokens = min_range * t.T;
+    const int max_stage_splits = (max_tokens + t.T - 1) / t.T;
+    int S;
+    if (num_splits > 0) {
+        S = std::min(num_splits, max_stage_splits);
+    } else {
+        // About one wave of blocks: enough splits that every resident slot gets one.
+        // Fewer (larger) blocks amortise each block's fixed start-up and epilogue cost;
+        // a batch that already has a block per slot is not split at all.
+        S = std::max(1, (slots + units - 1) / units);
+        // Bound the bytes of one split so that no split becomes a straggler: ~1 MiB
+        // when the units are fewer than the slots (long sequences), ~2 MiB when the
+        // units already fill the slots (a long split then shares the machine with many).
+        const int cap = units < slots ? cap_tokens : 2 * cap_tokens;
+        S = std::max(S, (max_tokens + cap - 1) / cap);
+        // Never thinner than kMinSplitTokens keys per split.
+        S = std::min(S, std::max(1, max_tokens / kMinSplitTokens));
+        // Several waves of equal splits: pick the count in [S, 1.5 S] that fills the
+        // last wave best.
+        if ((long)units * S >= 2l * slots) {
+            const int s_lo = S, s_hi = S + S / 2;
+            double best = -1.0;
+            for (int s = s_lo; s <= s_hi; ++s) {
+                const double waves = (double)units * s / slots;
+                const double eff = waves / std::ceil(waves);
+                if (eff > best + 0.005) {
+                    best = eff;
+                    S = s;
+                }
+            }
+        }
+    }
+    S = std::max(1, S);
+    int chunk = (max_tokens + S - 1) / S;
+    chunk = (chunk + t.T - 1) / t.T * t.T;
+    // A block stages its block_table slice in shared memory: bound it.
+    const int max_chunk = (kMaxTablePages - 2) * page_size;
+    if (chunk > max_chunk) chunk = max_chunk / t.T * t.T;
+    S = (max_tokens + chunk - 1) / chunk;
+
+    const SmemLayout lay = smem_layout(D, t.T, t.W, t.R, NT, chunk, page_size);
+    if (lay.dynamic > kSmemPerBlockMax) return PKV_ERR_UNSUPPORTED;
+    per_sm = std::max(1, std::min(kSmemPerSm / (lay.dynamic + kBlockReserve), 2048 / (t.W * 32)));
+
+    plan->num_splits = S;
+    plan->chunk_tokens = chunk;
     plan->stage_tokens = t.T;
     plan->warps = t.W;
     plan->ring_stages = t.R;
-    plan->blocks_per_sm = 1;
-    plan->grid_blocks = grid;
-    plan->smem_bytes = t.smem;
-    plan->merge_needed = pieces > 1 ? 1 : 0;
-    plan->max_item_tiles = max_item;
-    plan->workspace_bytes = workspace_layout(grid, Bl, Hq, Hkv, D).total;
+    plan->blocks_per_sm = per_sm;
+    plan->grid_blocks = S * Hkv * B;
+    plan->smem_bytes = lay.dynamic;
+    plan->merge_needed = S > 1 ? 1 : 0;
+    plan->workspace_bytes = workspace_layout(S, B, Hq, Hkv, D).total;
     return PKV_OK;
 }
 

@@ -107,35 +107,38 @@ WORKLOADS = {
 def test_plan_invariants(lib, name, sms):
     B, Hq, Hkv, D, P, max_pages = WORKLOADS[name]
     plan = pkv.plan_query(B, Hq, Hkv, D, P, max_pages, sms)
-    assert plan["chunk_tokens"] % plan["stage_tokens"] == 0 and plan["chunk_tokens"] >= 256
+    max_tokens = max_pages * P
+    assert plan["chunk_tokens"] % plan["stage_tokens"] == 0
+    assert plan["num_splits"] * plan["chunk_tokens"] >= max_tokens
+    assert (plan["num_splits"] - 1) * plan["chunk_tokens"] < max_tokens
     assert plan["smem_bytes"] <= 232448
-    assert plan["grid_blocks"] == sms and plan["blocks_per_sm"] == 1   # persistent: one block per SM
-    assert plan["ring_stages"] >= 2 and plan["warps"] in (2, 4, 8)
-    assert 1 <= plan["num_splits"] <= sms
+    assert plan["grid_blocks"] == plan["num_splits"] * Hkv * B
     assert plan["merge_needed"] == (1 if plan["num_splits"] > 1 else 0)
-    # a work item stages at most 256 pages of block table
-    assert (plan["max_item_tiles"] * plan["stage_tokens"] + P - 1) // P + 2 <= 256
-    # workspace: header, one counter per (b, kv head), two partial slots (G heads) per block
-    pad = lambda x: (x + 255) // 256 * 256
-    G = Hq // Hkv
-    ws = 256 + pad(min(B, 1024) * Hkv * 4) + pad(2 * sms * G * 4) + 2 * sms * G * D * 4
-    assert plan["workspace_bytes"] == ws
+    # K+V bytes of one split stay bounded (<= 2 MiB) so no split becomes a straggler
+    assert plan["chunk_tokens"] * 4 * D <= (2 << 20) or plan["num_splits"] == 1
+    if plan["num_splits"] > 1:
+        pad = lambda x: (x + 255) // 256 * 256
+        ws = 256 + pad(B * Hkv * 4) + pad(plan["num_splits"] * B * Hq * 4) + plan["num_splits"] * B * Hq * D * 4
+        assert plan["workspace_bytes"] == ws
+    else:
+        assert plan["workspace_bytes"] == 256
     # a pure function of (shape, SM count)
     assert pkv.plan_query(B, Hq, Hkv, D, P, max_pages, sms) == plan
 
 
-def test_plan_cuts_long_context_and_not_big_batches(lib):
-    # four 131072-key sequences over 152 SMs: each key range is cut into several pieces
-    assert pkv.plan_query(4, 64, 8, 128, 16, 8192, 152)["num_splits"] >= 4
-    # 256 x 8 ranges of 2048 keys: about 13 whole ranges per block, at most two cut
-    assert pkv.plan_query(256, 32, 8, 128, 64, 32, 152)["num_splits"] <= 2
+def test_plan_splits_long_context_and_not_big_batches(lib):
+    assert pkv.plan_query(4, 64, 8, 128, 16, 8192, 152)["num_splits"] >= 32
+    assert pkv.plan_query(256, 32, 8, 128, 64, 32, 152)["num_splits"] == 1
+    # a small batch is split into about one wave of blocks
+    p = pkv.plan_query(8, 32, 8, 128, 16, 247, 152)
+    assert 3 <= p["num_splits"] <= 8 and p["grid_blocks"] <= 2 * 2 * 152
 
 
 def test_plan_forced_splits(lib):
-    # a forced split count sets the smallest slice: max_tokens / num_splits keys
-    for n in (1, 2, 3, 7, 64):
-        plan = pkv.plan_query(8, 32, 8, 128, 16, 200, 152, n)
-        assert plan["chunk_tokens"] == -(-(200 * 16 // 16) // n) * 16
-    assert pkv.plan_query(1, 8, 2, 64, 16, 2, 152, 1000)["chunk_tokens"] == 32
+    for s in (1, 2, 3, 7, 64):
+        plan = pkv.plan_query(8, 32, 8, 128, 16, 256, 152, s)
+        assert plan["num_splits"] == s
+    # clamped to one split per stage
+    assert pkv.plan_query(1, 8, 2, 64, 16, 2, 152, 1000)["num_splits"] == 1
     with pytest.raises(pkv.PkvError):
         pkv.plan_query(1, 8, 2, 64, 16, 2, 152, -1)

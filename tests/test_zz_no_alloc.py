@@ -85,13 +85,13 @@ def test_static_scratch_clears_status_between_calls(lib):
 
 
 def test_static_scratch_rejects_shapes_beyond_its_size(lib):
-    # 1024 sequences x 4096 kv heads need 16 MiB of per-head counters alone: more than the array holds.
+    # 64 sequences x 64 query heads of D=256 over 131072 keys need far more than 32 MiB of partials.
     V = ctypes.c_void_p
-    plan = pkv.plan_query(1024, 4096, 4096, 64, 16, 1, torch.cuda.get_device_properties(0).multi_processor_count)
-    assert plan["workspace_bytes"] > 16 << 20
+    plan = pkv.plan_query(64, 64, 2, 256, 16, 8192, torch.cuda.get_device_properties(0).multi_processor_count)
+    assert plan["workspace_bytes"] > 32 << 20
     dummy = torch.zeros(16, dtype=torch.uint8, device="cuda")
     p = V(dummy.data_ptr())
-    st = lib.paged_decode_attn_static_scratch(p, p, p, p, p, 1024, 4096, 4096, 64, 16, 1024, 1,
-                                              ctypes.c_float(0.125), p, None, None,
+    st = lib.paged_decode_attn_static_scratch(p, p, p, p, p, 64, 64, 2, 256, 16, 8192 * 64, 8192,
+                                              ctypes.c_float(0.0625), p, None, None,
                                               V(torch.cuda.current_stream().cuda_stream))
     assert st == -4
