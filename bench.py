@@ -30,7 +30,7 @@ sys.path.insert(0, ROOT)
 METRIC = "paged GQA decode attn: µs/call, achieved HBM GB/s and % of GB300 peak"
 NOMINAL_HBM_GBS = 8000.0
 KERNEL_SOURCES = ["paged_kv_gqa_gb300/csrc/decode_kernel.cuh", "paged_kv_gqa_gb300/csrc/ptx.cuh",
-                  "paged_kv_gqa_gb300/csrc/plan.h"]
+                  "paged_kv_gqa_gb300/csrc/plan.h", "paged_kv_gqa_gb300/csrc/plan.cpp"]
 
 
 def kernel_source_hash() -> str:
@@ -131,6 +131,21 @@ def dist_setup(n_gpus: int):
         dist.init_process_group(backend)
         return dist, rank, world, local
     return None, rank, world, local
+
+
+def max_over_ranks(value: float, dist, device) -> float:
+    """The slowest rank's time: every rank contributes its value, all get the max."""
+    if not dist:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_gbs(bytes_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank processed bytes_per_rank in the slowest rank's time."""
+    return bytes_per_rank * world / (ms_per_step * 1e-3) / 1e9
 
 
 def run_reference(args) -> None:
@@ -273,10 +288,7 @@ def run_pkv(args) -> None:
     clocks = sampler.stop()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     mean_ms = sum(step_ms) / len(step_ms)
-    if dist:
-        t = torch.tensor([mean_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        mean_ms = float(t.item())
+    mean_ms = max_over_ranks(mean_ms, dist, dev)
     status = pkv.pkv_check_status(ws)
 
     # ---- end to end through the public API with host buffers -------------------
@@ -293,7 +305,7 @@ def run_pkv(args) -> None:
             dist.destroy_process_group()
         return
     peaks = measured_peaks()
-    gbs = ab["total"] / (mean_ms * 1e-3) / 1e9
+    gbs = weak_scaling_gbs(ab["total"], 1, mean_ms)
     traffic = profiled_traffic(args.workload)
     line = {
         "metric": METRIC, "value": round(gbs * world, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -357,12 +369,9 @@ def _e2e(args, case, ab, pkv, torch, dev, stream, flush, plan, dist):
         e.record(stream)
     torch.cuda.synchronize()
     ms = sum(s.elapsed_time(e) for s, e in ev) / steps
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
     world = dist.get_world_size() if dist else 1
-    return {"value": round(ab["total"] * world / (ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+    return {"value": round(weak_scaling_gbs(ab["total"], world, ms), 3), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4), "steps": steps}
 
 

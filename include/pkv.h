@@ -192,9 +192,10 @@ PKV_API pkv_status paged_decode_attn_ex(const pkv_bf16 *q, const pkv_bf16 *k_cac
  * device (make that call before any stream capture).  A shape whose plan
  * needs more than 32 MiB of partials returns PKV_ERR_WORKSPACE_TOO_SMALL
  * before anything runs; use paged_decode_attn with a workspace for those.
- * Every call clears the status word first.  All calls on a device share the
- * array: calls that may overlap on the GPU (other streams, other host
- * threads) race on it and must be ordered by the caller.
+ * Every call first clears the status word and the split-completion
+ * counters.  All calls on a device share the array: calls that may overlap
+ * on the GPU (other streams, other host threads) race on it and must be
+ * ordered by the caller.
  */
 PKV_API pkv_status paged_decode_attn_static_scratch(const pkv_bf16 *q, const pkv_bf16 *k_cache,
                                                     const pkv_bf16 *v_cache, const int32_t *block_table,

@@ -456,8 +456,11 @@ extern "C" pkv_status paged_decode_attn_static_scratch(const pkv_bf16 *q, const 
     void *scratch = nullptr;
     st = static_scratch_for_current_device(&device, &scratch);
     if (st != PKV_OK) return st;
-    // The status word must start at zero; the partials are fully written before they are read.
-    if (cudaMemsetAsync(scratch, 0, sizeof(int), stream) != cudaSuccess) return PKV_ERR_CUDA;
+    // The status word and the split-completion counters must start at zero (a previous
+    // call that gave up part-way could have left a counter raised); the partials are
+    // fully written before they are read.
+    const size_t zero_bytes = workspace_layout(plan.num_splits, B, Hq, Hkv, D).part_lse;
+    if (cudaMemsetAsync(scratch, 0, zero_bytes, stream) != cudaSuccess) return PKV_ERR_CUDA;
     st = paged_decode_attn(q, k_cache, v_cache, block_table, seq_lens, B, Hq, Hkv, D, page_size, num_pages,
                            max_pages, scale, out, lse, scratch, kStaticScratchBytes, stream);
     if (st != PKV_OK) return st;
