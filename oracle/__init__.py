@@ -8,6 +8,9 @@ The arithmetic lives in ``oracle.c`` (plain C, double precision), compiled with
 gcc into ``oracle/_build/liboracle.so`` on first use.  This module only marshals
 numpy arrays into that library.
 
+Functions: ``paged_decode`` (decode attention by the definition), ``merge`` (the
+log-sum-exp combine of split partials), ``kv_append`` (the paged cache write).
+
 Pins (see ``tests/test_oracle.py``): single-token rows, constant V, all-equal K,
 hand-derived golden cases, physical-page and page-size invariance, a brute-force
 comparison with torch's float64 scaled-dot-product attention, merge
@@ -56,6 +59,8 @@ def _load():
                                                 ctypes.c_double, p, i, p, p, i]
             lib.oracle_merge.restype = None
             lib.oracle_merge.argtypes = [p, p, i, i, i, p, p]
+            lib.oracle_kv_append.restype = i
+            lib.oracle_kv_append.argtypes = [p, p, p, p, i, i, i, i, i, i, p, p]
             _lib = lib
     return _lib
 
@@ -132,3 +137,27 @@ def merge(partial_out, partial_lse):
     lse = np.empty((N,), np.float64)
     lib.oracle_merge(_ptr(po), _ptr(pl), S, N, D, _ptr(out), _ptr(lse))
     return out, lse
+
+
+def kv_append(k_new_bits, v_new_bits, block_table, positions, k_bits, v_bits):
+    """Paged KV append on host copies: returns (k_cache, v_cache, rejected).
+
+    k_new_bits, v_new_bits uint16 [B, Hkv, D]; positions int32 [B] (the key index to
+    write; < 0 skips the sequence); k_bits, v_bits uint16 [num_pages, P, Hkv, D] are
+    copied, not modified.  `rejected` counts sequences whose position or page id was
+    out of range (nothing written for them).
+    """
+    lib = _load()
+    kn = _as_bits(k_new_bits)
+    vn = _as_bits(v_new_bits)
+    k = np.array(_as_bits(k_bits), copy=True)
+    v = np.array(_as_bits(v_bits), copy=True)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    pos = np.ascontiguousarray(positions, dtype=np.int32)
+    B, Hkv, D = kn.shape
+    num_pages, P, Hkv2, D2 = k.shape
+    if (Hkv2, D2) != (Hkv, D) or vn.shape != kn.shape or v.shape != k.shape:
+        raise ValueError("shape mismatch")
+    rej = lib.oracle_kv_append(_ptr(kn), _ptr(vn), _ptr(bt), _ptr(pos), B, Hkv, D, P, num_pages, bt.shape[1],
+                               _ptr(k), _ptr(v))
+    return k, v, rej

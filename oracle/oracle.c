@@ -229,3 +229,37 @@ void oracle_merge(const double *partial_out, const double *partial_lse,
         lse[n] = M + log(W);
     }
 }
+
+/*
+ * oracle_kv_append: write one new key row and value row per (sequence, kv head)
+ * into the page pool, at logical key position positions[b]: physical page
+ * block_table[b][positions[b] / P], slot positions[b] mod P (the page-table
+ * addressing of FlashQuant wiki "CUDA Kernels", paged_decode.cu "Page Table
+ * Addressing"; the per-token cache write of Atlas "CUDA Kernel Engineering",
+ * "The kernel inventory", KV append).
+ *   k_new, v_new [B, Hkv, D] bf16 bits; k_cache, v_cache [num_pages, P, Hkv, D] (updated in place)
+ * positions[b] < 0 skips sequence b.  Returns the number of sequences skipped because
+ * the position is past max_pages*P or the page id is outside [0, num_pages); their
+ * rows are not written.
+ */
+int oracle_kv_append(const uint16_t *k_new, const uint16_t *v_new, const int32_t *block_table,
+                     const int32_t *positions, int B, int Hkv, int D, int P, int num_pages, int max_pages,
+                     uint16_t *k_cache, uint16_t *v_cache)
+{
+    int rejected = 0;
+    for (int b = 0; b < B; ++b) {
+        const int pos = positions[b];
+        if (pos < 0) continue;
+        if (pos >= max_pages * P) { ++rejected; continue; }
+        const int page = block_table[(size_t)b * max_pages + pos / P];
+        if (page < 0 || page >= num_pages) { ++rejected; continue; }
+        const int slot = pos % P;
+        for (int g = 0; g < Hkv; ++g) {
+            const size_t dst = (((size_t)page * P + slot) * Hkv + g) * D;
+            const size_t src = ((size_t)b * Hkv + g) * D;
+            memcpy(k_cache + dst, k_new + src, sizeof(uint16_t) * (size_t)D);
+            memcpy(v_cache + dst, v_new + src, sizeof(uint16_t) * (size_t)D);
+        }
+    }
+    return rejected;
+}

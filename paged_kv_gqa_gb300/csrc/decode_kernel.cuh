@@ -151,6 +151,25 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
     int *sm_tab = reinterpret_cast<int *>(base + lay.table);
     float *red = reinterpret_cast<float *>(base);  // reuses the ring after the main loop
 
+    if (threadIdx.x == 0) {  // the first copies need the tensor maps: fetch them early
+        prefetch_tensor_map(&tmK);
+        prefetch_tensor_map(&tmV);
+    }
+    // ---- query fragments (B operand of the score mma): q^T[d, head] --------------
+    // Loaded first, so that their latency overlaps the block-table staging below.
+    uint32_t qf[KS][NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int head = nt * 8 + g;
+        const uint32_t *qp = reinterpret_cast<const uint32_t *>(
+            p.q + ((size_t)b * p.Hq + kvh * G + (head < G ? head : 0)) * D + 2 * cc);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            qf[ks][nt][0] = head < G ? __ldg(qp + ks * 8) : 0u;
+            qf[ks][nt][1] = head < G ? __ldg(qp + ks * 8 + 4) : 0u;
+        }
+    }
+
     // Stage this split's block-table slice; out-of-range ids become -1.
     int bad = 0;
     for (int i = threadIdx.x; i < page_end - page_begin; i += W * 32) {
@@ -167,20 +186,6 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
         fence_barrier_init();
     }
     const bool any_bad = __syncthreads_or(bad) != 0;
-
-    // ---- query fragments (B operand of the score mma): q^T[d, head] --------------
-    uint32_t qf[KS][NT][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int head = nt * 8 + g;
-        const uint32_t *qp = reinterpret_cast<const uint32_t *>(
-            p.q + ((size_t)b * p.Hq + kvh * G + (head < G ? head : 0)) * D + 2 * cc);
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            qf[ks][nt][0] = head < G ? __ldg(qp + ks * 8) : 0u;
-            qf[ks][nt][1] = head < G ? __ldg(qp + ks * 8 + 4) : 0u;
-        }
-    }
 
     // ---- producer: lane 0 of each warp fills that warp's ring ----------------
     const uint64_t policy = l2_policy_evict_first();

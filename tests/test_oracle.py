@@ -331,3 +331,64 @@ def test_merge_single_split_is_identity():
     pl = rng.standard_normal((1, 5)) * 10
     o, l = oracle.merge(po, pl)
     assert np.array_equal(o, po[0]) and np.allclose(l, pl[0], rtol=0, atol=1e-15)
+
+
+# --------------------------------------------------------------------------- kv append
+
+
+def test_kv_append_hand_case():
+    # P=4, two kv heads, D=2.  Sequence 0 appends key 5 -> logical page 1 (physical 1), slot 1;
+    # sequence 1 appends key 0 -> logical page 0 (physical 0), slot 0.
+    P, Hkv, D = 4, 2, 2
+    k = np.zeros((4, P, Hkv, D), np.uint16)
+    v = np.zeros_like(k)
+    kn = np.arange(1, 9, dtype=np.uint16).reshape(2, Hkv, D)
+    vn = kn + 100
+    bt = np.array([[3, 1], [0, 2]], np.int32)
+    k2, v2, rej = oracle.kv_append(kn, vn, bt, np.array([5, 0], np.int32), k, v)
+    assert rej == 0
+    want_k = np.zeros_like(k)
+    want_k[1, 1] = kn[0]
+    want_k[0, 0] = kn[1]
+    assert np.array_equal(k2, want_k) and np.array_equal(v2, np.where(want_k > 0, want_k + 100, 0))
+    assert np.array_equal(k, 0 * k)  # inputs untouched
+
+
+def test_kv_append_skips_and_rejects():
+    P, Hkv, D = 4, 1, 2
+    k = np.full((3, P, Hkv, D), 7, np.uint16)
+    kn = np.ones((3, Hkv, D), np.uint16)
+    bt = np.array([[0, 1], [2, -1], [1, 0]], np.int32)
+    k2, v2, rej = oracle.kv_append(kn, kn, bt, np.array([-1, 5, 8], np.int32), k, k)
+    # -1: skipped silently; 5 -> logical page 1 holds -1 (bad id); 8 >= max_pages * P
+    assert rej == 2 and np.array_equal(k2, k) and np.array_equal(v2, k)
+
+
+def test_append_then_decode_matches_brute_force():
+    # The appended key joins the softmax exactly as a key that was always there.
+    c = make_case(_spec(B=3, Hq=8, Hkv=2, D=64, P=16), seq_lens=[16, 37, 0], seed=17)
+    q, k, v, bt, sl = c.host_bits()
+    g = torch.Generator().manual_seed(3)
+    kn = bf16_bits(torch.randn(c.B, c.Hkv, c.D, generator=g).to(torch.bfloat16))
+    vn = bf16_bits(torch.randn(c.B, c.Hkv, c.D, generator=g).to(torch.bfloat16))
+    # sequence 0 is page-aligned (16 keys): its new key opens a new page
+    bt = np.concatenate([bt, np.full((c.B, 1), -1, np.int32)], axis=1)
+    spare = [c.num_pages, c.num_pages + 1, c.num_pages + 2]
+    k = np.concatenate([k, np.zeros((3,) + k.shape[1:], np.uint16)])
+    v = np.concatenate([v, np.zeros((3,) + v.shape[1:], np.uint16)])
+    for b in range(c.B):
+        bt[b, int(sl[b]) // c.P] = spare[b] if int(sl[b]) % c.P == 0 else bt[b, int(sl[b]) // c.P]
+    k2, v2, rej = oracle.kv_append(kn, vn, bt, sl, k, v)
+    assert rej == 0
+    out, lse = oracle.paged_decode(q, k2, v2, bt, sl + 1, c.scale)
+    qf = bits_to_bf16(q).double()
+    kf = bits_to_bf16(k2).double().numpy()
+    vf = bits_to_bf16(v2).double().numpy()
+    for b in range(c.B):
+        idx = np.arange(int(sl[b]) + 1)
+        kd = torch.from_numpy(kf[bt[b, idx // c.P], idx % c.P]).permute(1, 0, 2).repeat_interleave(c.G, 0)
+        vd = torch.from_numpy(vf[bt[b, idx // c.P], idx % c.P]).permute(1, 0, 2).repeat_interleave(c.G, 0)
+        # the last key/value rows are the appended ones
+        assert np.array_equal(kd[:, -1].numpy(), bits_to_bf16(kn[b]).double().numpy().repeat(c.G, 0))
+        ref = torch.nn.functional.scaled_dot_product_attention(qf[b].unsqueeze(1), kd, vd, scale=c.scale)[:, 0]
+        assert np.max(np.abs(out[b] - ref.numpy())) <= 1e-12
