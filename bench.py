@@ -375,13 +375,55 @@ def _e2e(args, case, ab, pkv, torch, dev, stream, flush, plan, dist):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4), "steps": steps}
 
 
+def run_append(args) -> None:
+    """The paged KV append (the cache write before a decode step) on the large-batch shape:
+    B=256 sequences, Hkv=8, D=128, 64-key pages; each step writes one K row and one V row
+    per (sequence, kv head) into the last slot of the sequence's last page."""
+    import torch
+    import paged_kv_gqa_gb300 as pkv
+    from workloads import make_case
+
+    if args.impl == "reference" or int(os.environ.get("RANK", "0")) != 0:
+        return
+    dev = torch.device("cuda", 0)
+    case = make_case("bigpage", device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(77)
+    kn = torch.randn(case.B, case.Hkv, case.D, generator=g, device=dev).to(torch.bfloat16)
+    vn = torch.randn(case.B, case.Hkv, case.D, generator=g, device=dev).to(torch.bfloat16)
+    pos = (case.seq_lens - 1).to(torch.int32)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    call = lambda: pkv.paged_kv_append(kn, vn, case.block_table, pos, case.k_cache, case.v_cache, status=status,
+                                       stream=stream)
+    for _ in range(args.warmup):
+        call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for s_, e_ in ev:
+        flush.fill_(3)
+        s_.record(stream)
+        call()
+        e_.record(stream)
+    torch.cuda.synchronize()
+    ms = sum(s_.elapsed_time(e_) for s_, e_ in ev) / len(ev)
+    assert int(status.item()) == 0
+    rows = case.B * case.Hkv
+    moved = 2 * 2 * rows * case.D * 2 + case.B * 4 * 2  # K and V rows read and written, positions, table entries
+    print(json.dumps({"metric": "paged KV append: us/call and achieved HBM GB/s", "value": round(moved / (ms * 1e-3) / 1e9, 2),
+                      "unit": "GB/s", "us_per_call": round(ms * 1e3, 3), "steps": args.steps, "warmup": args.warmup,
+                      "config": {"workload": "append", "B": case.B, "Hkv": case.Hkv, "D": case.D, "page_size": case.P},
+                      "bytes_per_call": moved, "gpu_launches": args.steps}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="batch",
-                    choices=["tiny", "batch", "ragged", "long", "bigpage", "bigpage_g16"])
+                    choices=["tiny", "batch", "ragged", "long", "bigpage", "bigpage_g16", "append"])
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
@@ -391,7 +433,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.impl == "reference":
+    if args.workload == "append":
+        run_append(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_pkv(args)

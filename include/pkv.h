@@ -204,6 +204,36 @@ PKV_API pkv_status paged_decode_attn_static_scratch(const pkv_bf16 *q, const pkv
                                                     pkv_bf16 *out, float *lse, int *device_status,
                                                     cudaStream_t stream);
 
+/* ------------------------------------------------------------------ append */
+
+/*
+ * Paged KV append: the per-token cache write that precedes a decode step
+ * (Atlas "CUDA Kernel Engineering", "The kernel inventory": KV append, a
+ * per-token K/V write into the paged cache).  For every sequence b and kv head
+ * g, copies k_new[b, g, :] and v_new[b, g, :] into
+ *   k_cache / v_cache[block_table[b][pos / page_size], pos % page_size, g, :]
+ * with pos = positions[b] (normally the sequence's length before the step; the
+ * caller then passes seq_lens + 1 to the decode call).  One launch, K and V
+ * together, asynchronous on `stream`.
+ *
+ *   k_new, v_new  [B, Hkv, D] bf16
+ *   block_table   [B, max_pages] int32 (the same table the decode call reads)
+ *   positions     [B] int32; a negative position skips that sequence
+ *   k_cache, v_cache [num_pages, page_size, Hkv, D] bf16 (written in place)
+ *   status        device int32 or NULL; the first device-side error is
+ *                 recorded there when it holds 0 -- the decode workspace
+ *                 pointer can be passed (its first int32 is the status word)
+ * Host checks as for paged_decode_attn (D in {64,128,256}, power-of-two
+ * page_size in [8,256], 16-byte alignment).  Device: a position >=
+ * max_pages * page_size records PKV_ERR_BAD_SEQ_LEN, a page id outside
+ * [0, num_pages) records PKV_ERR_BAD_PAGE_INDEX; that sequence is not written.
+ * Every other byte of the pools is left untouched.
+ */
+PKV_API pkv_status paged_kv_append(const pkv_bf16 *k_new, const pkv_bf16 *v_new, const int32_t *block_table,
+                                   const int32_t *positions, int B, int Hkv, int D, int page_size, int num_pages,
+                                   int max_pages, pkv_bf16 *k_cache, pkv_bf16 *v_cache, int *status,
+                                   cudaStream_t stream);
+
 /* ------------------------------------------------------------------ merge */
 
 /*

@@ -17,7 +17,8 @@ import threading
 __all__ = [
     "PkvError", "load", "status_string", "plan_query", "paged_decode_attn_workspace_size",
     "paged_decode_attn", "paged_decode_attn_ex", "split_kv_merge", "pkv_check_status",
-    "pkv_reset_status", "pkv_selftest_wait_timeout", "paged_decode_attn_static_scratch", "EXPORTED_SYMBOLS",
+    "pkv_reset_status", "pkv_selftest_wait_timeout", "paged_decode_attn_static_scratch", "paged_kv_append",
+    "EXPORTED_SYMBOLS",
     "STATUS",
 ]
 
@@ -35,6 +36,7 @@ EXPORTED_SYMBOLS = [
     "pkv_status_string", "pkv_version", "pkv_plan_query", "paged_decode_attn_workspace_size",
     "paged_decode_attn_workspace_size_ex", "paged_decode_attn", "paged_decode_attn_ex", "split_kv_merge",
     "pkv_check_status", "pkv_reset_status", "pkv_selftest_wait_timeout", "paged_decode_attn_static_scratch",
+    "paged_kv_append",
 ]
 
 
@@ -82,6 +84,7 @@ def load(path: str = LIB_PATH):
             "pkv_reset_status": (I, [P, P]),
             "pkv_selftest_wait_timeout": (I, [P, U, P]),
             "paged_decode_attn_static_scratch": (I, [P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, P]),
+            "paged_kv_append": (I, [P, P, P, P, I, I, I, I, I, I, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -224,3 +227,19 @@ def paged_decode_attn_static_scratch(q, k_cache, v_cache, block_table, seq_lens,
         _stream_handle(stream))
     _check(st, "paged_decode_attn_static_scratch")
     return out, lse
+
+
+def paged_kv_append(k_new, v_new, block_table, positions, k_cache, v_cache, status=None, stream=None):
+    """Calls paged_kv_append: writes k_new/v_new [B, Hkv, D] into the page pools at positions[b]."""
+    torch = _torch()
+    B, Hkv, D = k_new.shape
+    num_pages, P, Hkv2, D2 = k_cache.shape
+    if (Hkv2, D2) != (Hkv, D) or tuple(v_new.shape) != tuple(k_new.shape) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_new/v_new/k_cache/v_cache shapes disagree")
+    st = load().paged_kv_append(
+        _dev_ptr(k_new, torch.bfloat16, "k_new", 3), _dev_ptr(v_new, torch.bfloat16, "v_new", 3),
+        _dev_ptr(block_table, torch.int32, "block_table", 2), _dev_ptr(positions, torch.int32, "positions", 1),
+        B, Hkv, D, P, num_pages, block_table.shape[1], _dev_ptr(k_cache, torch.bfloat16, "k_cache", 4),
+        _dev_ptr(v_cache, torch.bfloat16, "v_cache", 4),
+        ctypes.c_void_p(status.data_ptr()) if status is not None else None, _stream_handle(stream))
+    _check(st, "paged_kv_append")

@@ -22,7 +22,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libpkv.so")
 
 SOURCES = ["api.cu", "plan.cpp"]
-HEADERS = ["decode_kernel.cuh", "merge_kernel.cuh", "ptx.cuh", "plan.h"]
+HEADERS = ["decode_kernel.cuh", "merge_kernel.cuh", "append_kernel.cuh", "ptx.cuh", "plan.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

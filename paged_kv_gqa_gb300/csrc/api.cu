@@ -11,6 +11,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "append_kernel.cuh"
 #include "decode_kernel.cuh"
 #include "merge_kernel.cuh"
 #include "pkv.h"
@@ -352,6 +353,39 @@ pkv_status split_kv_merge(const float *partial_out, const float *partial_lse, in
     mp.chunk_tokens = 1;
     mp.max_tokens = 0;
     return launch_merge(D, mp, stream);
+}
+
+pkv_status paged_kv_append(const pkv_bf16 *k_new, const pkv_bf16 *v_new, const int32_t *block_table,
+                           const int32_t *positions, int B, int Hkv, int D, int page_size, int num_pages,
+                           int max_pages, pkv_bf16 *k_cache, pkv_bf16 *v_cache, int *status, cudaStream_t stream)
+{
+    if (num_pages <= 0) return PKV_ERR_INVALID_ARG;
+    const pkv_status shape_ok = validate_shape(B, Hkv, Hkv, D, page_size, max_pages);
+    if (shape_ok != PKV_OK) return shape_ok;
+    if (B == 0) return PKV_OK;
+    if (!k_new || !v_new || !block_table || !positions || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(block_table) || !aligned16(positions) ||
+        !aligned16(k_cache) || !aligned16(v_cache) || (status && (reinterpret_cast<uintptr_t>(status) & 3u)))
+        return PKV_ERR_MISALIGNED;
+    if ((long)num_pages * page_size >= (1l << 31) || (long)B * Hkv >= (1l << 31)) return PKV_ERR_INVALID_ARG;
+    AppendParams ap;
+    ap.k_new = reinterpret_cast<const uint4 *>(k_new);
+    ap.v_new = reinterpret_cast<const uint4 *>(v_new);
+    ap.block_table = block_table;
+    ap.positions = positions;
+    ap.k_cache = reinterpret_cast<uint4 *>(k_cache);
+    ap.v_cache = reinterpret_cast<uint4 *>(v_cache);
+    ap.status = status;
+    ap.B = B;
+    ap.Hkv = Hkv;
+    ap.D = D;
+    ap.P = page_size;
+    ap.log2P = log2_exact(page_size);
+    ap.num_pages = num_pages;
+    ap.max_pages = max_pages;
+    const long units = (long)B * Hkv;
+    kv_append_kernel<<<(unsigned)((units + kAppendWarps - 1) / kAppendWarps), kAppendWarps * 32, 0, stream>>>(ap);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 pkv_status pkv_check_status(const void *workspace, cudaStream_t stream, int *device_status)

@@ -37,7 +37,7 @@ def test_no_internal_symbols_leak():
     import subprocess
     out = subprocess.run(["nm", "-D", "--defined-only", pkv.LIB_PATH], capture_output=True, text=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
-    ours = {n for n in exported if n.startswith(("pkv", "paged_decode", "split_kv"))}
+    ours = {n for n in exported if n.startswith(("pkv", "paged_decode", "paged_kv", "split_kv"))}
     assert ours == set(_declared())
 
 
@@ -142,3 +142,17 @@ def test_plan_forced_splits(lib):
     assert pkv.plan_query(1, 8, 2, 64, 16, 2, 152, 1000)["num_splits"] == 1
     with pytest.raises(pkv.PkvError):
         pkv.plan_query(1, 8, 2, 64, 16, 2, 152, -1)
+
+
+def test_append_rejects_bad_arguments(lib):
+    V = ctypes.c_void_p
+
+    def call(kn=0x1000, vn=0x2000, bt=0x3000, pos=0x4000, B=2, Hkv=2, D=128, P=16, npg=8, mp=4,
+             kc=0x5000, vc=0x6000, st=None):
+        return lib.paged_kv_append(V(kn), V(vn), V(bt), V(pos), B, Hkv, D, P, npg, mp, V(kc), V(vc),
+                                   V(st) if st else None, None)
+
+    assert call(kn=0) == -1 and call(kc=0) == -1 and call(npg=0) == -1 and call(Hkv=0) == -1
+    assert call(D=96) == -2 and call(P=12) == -2
+    assert call(vn=0x2008) == -3 and call(pos=0x4004) == -3 and call(st=0x7002) == -3
+    assert call(B=0, kn=0, vn=0) == 0
