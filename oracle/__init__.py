@@ -9,12 +9,17 @@ gcc into ``oracle/_build/liboracle.so`` on first use.  This module only marshals
 numpy arrays into that library.
 
 Functions: ``paged_decode`` (decode attention by the definition), ``merge`` (the
-log-sum-exp combine of split partials), ``kv_append`` (the paged cache write).
+log-sum-exp combine of split partials), ``kv_append`` (the paged cache write), and
+the FP8 KV variant: ``e4m3_value`` / ``e4m3_encode`` (the codec), ``fp8_quantize_rows``
+(power-of-two row scales), ``quantize_pool`` / ``dequantize_pool``,
+``paged_decode_fp8`` and ``kv_append_fp8``.
 
 Pins (see ``tests/test_oracle.py``): single-token rows, constant V, all-equal K,
 hand-derived golden cases, physical-page and page-size invariance, a brute-force
 comparison with torch's float64 scaled-dot-product attention, merge
-associativity, scale -> 0, the GQA head mapping, and poisoned padding.
+associativity, scale -> 0, the GQA head mapping, and poisoned padding; for FP8,
+code values from the format's definition, torch's float8_e4m3fn codec, rounding
+ties, the quantiser's scale rule and error bound, and hand-placed scales.
 """
 from __future__ import annotations
 
@@ -61,6 +66,17 @@ def _load():
             lib.oracle_merge.argtypes = [p, p, i, i, i, p, p]
             lib.oracle_kv_append.restype = i
             lib.oracle_kv_append.argtypes = [p, p, p, p, i, i, i, i, i, i, p, p]
+            lib.oracle_e4m3_value.restype = ctypes.c_double
+            lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+            lib.oracle_e4m3_encode.argtypes = [ctypes.c_double]
+            lib.oracle_fp8_quantize_rows.restype = None
+            lib.oracle_fp8_quantize_rows.argtypes = [p, i, i, p, p]
+            lib.oracle_paged_decode_fp8.restype = i
+            lib.oracle_paged_decode_fp8.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, i, i,
+                                                    ctypes.c_double, p, i, p, p, i]
+            lib.oracle_kv_append_fp8.restype = i
+            lib.oracle_kv_append_fp8.argtypes = [p, p, p, p, i, i, i, i, i, i, p, p, p, p]
             _lib = lib
     return _lib
 
@@ -75,6 +91,22 @@ def _as_bits(x) -> np.ndarray:
     if a.dtype != np.uint16:
         raise TypeError("bf16 operands must be passed as uint16 bit patterns, got %s" % a.dtype)
     return a
+
+
+def _select(select, B, Hq, D):
+    if select is None:
+        return None, 0, np.empty((B, Hq, D), np.float64), np.empty((B, Hq), np.float64)
+    pairs = np.asarray(list(select), dtype=np.int64).reshape(-1, 2)
+    sel = np.ascontiguousarray(pairs[:, 0] * Hq + pairs[:, 1], dtype=np.int32)
+    nsel = sel.shape[0]
+    return sel, nsel, np.empty((nsel, D), np.float64), np.empty((nsel,), np.float64)
+
+
+def _check_rc(rc, name):
+    if rc == 1:
+        raise ValueError("a used block_table entry is outside [0, num_pages)")
+    if rc != 0:
+        raise ValueError("%s rejected its arguments (rc=%d)" % (name, rc))
 
 
 def paged_decode(q_bits, k_bits, v_bits, block_table, seq_lens, scale, select=None, nthreads=0):
@@ -99,25 +131,12 @@ def paged_decode(q_bits, k_bits, v_bits, block_table, seq_lens, scale, select=No
     if Dk != D or v.shape != k.shape:
         raise ValueError("shape mismatch between q, k and v")
     max_pages = bt.shape[1] if bt.ndim == 2 else 0
-    if select is None:
-        sel = None
-        out = np.empty((B, Hq, D), np.float64)
-        lse = np.empty((B, Hq), np.float64)
-        nsel = 0
-    else:
-        pairs = np.asarray(list(select), dtype=np.int64).reshape(-1, 2)
-        sel = np.ascontiguousarray(pairs[:, 0] * Hq + pairs[:, 1], dtype=np.int32)
-        nsel = sel.shape[0]
-        out = np.empty((nsel, D), np.float64)
-        lse = np.empty((nsel,), np.float64)
+    sel, nsel, out, lse = _select(select, B, Hq, D)
     rc = lib.oracle_paged_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(bt), _ptr(sl),
                                  B, Hq, Hkv, D, P, num_pages, max_pages, float(scale),
                                  _ptr(sel) if sel is not None else None, nsel,
                                  _ptr(out), _ptr(lse), int(nthreads))
-    if rc == 1:
-        raise ValueError("a used block_table entry is outside [0, num_pages)")
-    if rc != 0:
-        raise ValueError("oracle_paged_decode rejected its arguments (rc=%d)" % rc)
+    _check_rc(rc, "oracle_paged_decode")
     return out, lse
 
 
@@ -161,3 +180,101 @@ def kv_append(k_new_bits, v_new_bits, block_table, positions, k_bits, v_bits):
     rej = lib.oracle_kv_append(_ptr(kn), _ptr(vn), _ptr(bt), _ptr(pos), B, Hkv, D, P, num_pages, bt.shape[1],
                                _ptr(k), _ptr(v))
     return k, v, rej
+
+
+# ------------------------------------------------------------------ FP8 (e4m3) KV variant
+
+def e4m3_value(codes) -> np.ndarray:
+    """Exact value (float64) of each e4m3 code (uint8 array); NaN for 0x7F / 0xFF."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8)
+    table = np.array([lib.oracle_e4m3_value(i) for i in range(256)], np.float64)
+    return table[c]
+
+
+def e4m3_encode(values) -> np.ndarray:
+    """Nearest e4m3 code of each value (ties to even, saturating at +-448)."""
+    lib = _load()
+    v = np.asarray(values, dtype=np.float64)
+    flat = [lib.oracle_e4m3_encode(float(x)) for x in v.reshape(-1)]
+    return np.asarray(flat, dtype=np.uint8).reshape(v.shape)
+
+
+def fp8_quantize_rows(x_bits):
+    """Quantise rows of bf16 values: x_bits uint16 [..., D] -> (codes uint8 [..., D],
+    scales float32 [...]) with one power-of-two scale per row."""
+    lib = _load()
+    x = _as_bits(x_bits)
+    D = x.shape[-1]
+    N = int(np.prod(x.shape[:-1]))
+    codes = np.empty(x.shape, np.uint8)
+    scales = np.empty(x.shape[:-1], np.float32)
+    lib.oracle_fp8_quantize_rows(_ptr(x), N, D, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def quantize_pool(pool_bits):
+    """bf16 pool uint16 [num_pages, P, Hkv, D] -> (codes uint8 [num_pages, P, Hkv, D],
+    scales float32 [num_pages, Hkv, P]): the scale layout is head-major within a page."""
+    codes, scales = fp8_quantize_rows(pool_bits)
+    return codes, np.ascontiguousarray(scales.transpose(0, 2, 1))
+
+
+def dequantize_pool(codes, scales) -> np.ndarray:
+    """codes uint8 [num_pages, P, Hkv, D], scales [num_pages, Hkv, P] -> float64 values
+    code value * scale, in the pool layout."""
+    vals = e4m3_value(codes)
+    s = np.asarray(scales, dtype=np.float64).transpose(0, 2, 1)[..., None]
+    return vals * s
+
+
+def paged_decode_fp8(q_bits, k8, v8, k_scale, v_scale, block_table, seq_lens, scale, select=None, nthreads=0):
+    """Decode attention over an fp8 cache: key/value elements are code value * scale.
+
+    k8, v8 uint8 [num_pages, P, Hkv, D]; k_scale, v_scale float32 [num_pages, Hkv, P];
+    the other arguments and the result are those of ``paged_decode``.
+    """
+    lib = _load()
+    q = _as_bits(q_bits)
+    k = np.ascontiguousarray(k8, dtype=np.uint8)
+    v = np.ascontiguousarray(v8, dtype=np.uint8)
+    ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+    vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B, Hq, D = q.shape
+    num_pages, P, Hkv, Dk = k.shape
+    if Dk != D or v.shape != k.shape or ks.shape != (num_pages, Hkv, P) or vs.shape != ks.shape:
+        raise ValueError("shape mismatch between q, the fp8 pools and their scales")
+    max_pages = bt.shape[1] if bt.ndim == 2 else 0
+    sel, nsel, out, lse = _select(select, B, Hq, D)
+    rc = lib.oracle_paged_decode_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(ks), _ptr(vs), _ptr(bt), _ptr(sl),
+                                     B, Hq, Hkv, D, P, num_pages, max_pages, float(scale),
+                                     _ptr(sel) if sel is not None else None, nsel,
+                                     _ptr(out), _ptr(lse), int(nthreads))
+    _check_rc(rc, "oracle_paged_decode_fp8")
+    return out, lse
+
+
+def kv_append_fp8(k_new_bits, v_new_bits, block_table, positions, k8, v8, k_scale, v_scale):
+    """Quantise-and-append on host copies: returns (k8, v8, k_scale, v_scale, rejected).
+
+    k_new_bits, v_new_bits uint16 [B, Hkv, D]; k8, v8 uint8 [num_pages, P, Hkv, D];
+    k_scale, v_scale float32 [num_pages, Hkv, P].  Inputs are copied, not modified.
+    """
+    lib = _load()
+    kn = _as_bits(k_new_bits)
+    vn = _as_bits(v_new_bits)
+    k = np.array(k8, dtype=np.uint8, copy=True)
+    v = np.array(v8, dtype=np.uint8, copy=True)
+    ks = np.array(k_scale, dtype=np.float32, copy=True)
+    vs = np.array(v_scale, dtype=np.float32, copy=True)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    pos = np.ascontiguousarray(positions, dtype=np.int32)
+    B, Hkv, D = kn.shape
+    num_pages, P, Hkv2, D2 = k.shape
+    if (Hkv2, D2) != (Hkv, D) or vn.shape != kn.shape or v.shape != k.shape or ks.shape != (num_pages, Hkv, P):
+        raise ValueError("shape mismatch")
+    rej = lib.oracle_kv_append_fp8(_ptr(kn), _ptr(vn), _ptr(bt), _ptr(pos), B, Hkv, D, P, num_pages,
+                                   bt.shape[1], _ptr(k), _ptr(v), _ptr(ks), _ptr(vs))
+    return k, v, ks, vs, rej

@@ -38,6 +38,12 @@
  * out = 0 and lse = -inf; slots past L_b and table entries past the used pages
  * are never read.
  *
+ * FP8 KV variant (OASR "Kernel Layer", "FP8 KV variants"): the cache may hold
+ * float8 e4m3 codes with one f32 scale per (token, kv head); the key/value used
+ * is then code value * scale, exact in double.  The codec (e4m3_value,
+ * oracle_e4m3_encode) is written from the format's definition, and the
+ * quantiser (oracle_fp8_quantize_rows) picks a power-of-two scale per row.
+ *
  * Parallelism: (b, h) outputs are independent; worker threads take them by a
  * fixed stride, so results do not depend on the thread count.
  */
@@ -56,10 +62,88 @@ static double bf16_bits_to_double(uint16_t bits)
     return (double)f;
 }
 
+/*
+ * float8 e4m3, the "fn" variant the pages name (float8_e4m3fn): bit 7 sign,
+ * bits 6..3 exponent E with bias 7, bits 2..0 mantissa M, no infinities.
+ *   E == 0:            (M / 8) * 2^-6            (subnormal; M == 0 is +-0)
+ *   E == 15 && M == 7: NaN
+ *   otherwise:         (1 + M / 8) * 2^(E - 7)   (largest finite: 448)
+ */
+static double e4m3_value(uint8_t code)
+{
+    const int neg = code >> 7, E = (code >> 3) & 15, M = code & 7;
+    if (E == 15 && M == 7) return NAN;
+    const double mag = E == 0 ? ldexp((double)M, -9) : ldexp(1.0 + M / 8.0, E - 7);
+    return neg ? -mag : mag;
+}
+
+double oracle_e4m3_value(uint8_t code) { return e4m3_value(code); }
+
+/*
+ * Round to the nearest finite e4m3 value, ties to the even code (the one whose
+ * mantissa's last bit is 0), saturating at +-448; NaN gives the NaN code 0x7F.
+ * The non-negative finite codes 0x00..0x7E are in increasing order of value,
+ * so the neighbours of |x| are found by bisection over the codes.
+ */
+uint8_t oracle_e4m3_encode(double x)
+{
+    if (isnan(x)) return 0x7F;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    const double ax = fabs(x);
+    int code;
+    if (ax >= 448.0) {
+        code = 0x7E;
+    } else {
+        int lo = 0, hi = 0x7E;  /* value(lo) <= ax < value(hi) */
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) / 2;
+            if (e4m3_value((uint8_t)mid) <= ax) lo = mid; else hi = mid;
+        }
+        const double dlo = ax - e4m3_value((uint8_t)lo), dhi = e4m3_value((uint8_t)hi) - ax;
+        if (dlo < dhi) code = lo;
+        else if (dhi < dlo) code = hi;
+        else code = (lo % 2 == 0) ? lo : hi;
+    }
+    return (uint8_t)(sign | code);
+}
+
+/*
+ * Quantise N rows of D bf16 values (one row = one token of one kv head): the
+ * row's scale is s = 2^k with k the smallest integer in [-64, 64] such that
+ * max_d |x_d| <= 448 * 2^k (NaN values are left out of the maximum), and code_d
+ * = encode(x_d / s).  A power of two makes x / s exact and code * s exactly
+ * representable in bf16 (OASR "Kernel Layer", "FP8 KV variants": power-of-two
+ * scales make the dequantised product exact).  Reading: the pages fix the
+ * scale to a power of two but not which one; this is the smallest that does not
+ * saturate the row, and the exponent clamp keeps every dequantised value an
+ * exact bf16 normal.  An all-zero row gets 2^-64.
+ */
+void oracle_fp8_quantize_rows(const uint16_t *x, int N, int D, uint8_t *codes, float *scales)
+{
+    for (int n = 0; n < N; ++n) {
+        const uint16_t *row = x + (size_t)n * D;
+        double amax = 0.0;
+        for (int d = 0; d < D; ++d) {
+            const double a = fabs(bf16_bits_to_double(row[d]));
+            if (a > amax) amax = a;  /* NaN compares false and is skipped */
+        }
+        int k = -64;
+        while (k < 64 && amax > ldexp(448.0, k)) ++k;
+        const double s = ldexp(1.0, k);
+        scales[n] = (float)s;
+        for (int d = 0; d < D; ++d)
+            codes[(size_t)n * D + d] = oracle_e4m3_encode(bf16_bits_to_double(row[d]) / s);
+    }
+}
+
 typedef struct {
     const uint16_t *q;           /* [B, Hq, D] bf16 bits */
-    const uint16_t *k;           /* [num_pages, P, Hkv, D] bf16 bits */
+    const uint16_t *k;           /* [num_pages, P, Hkv, D] bf16 bits (bf16 cache) */
     const uint16_t *v;           /* same */
+    const uint8_t *k8;           /* [num_pages, P, Hkv, D] e4m3 codes (fp8 cache), else NULL */
+    const uint8_t *v8;           /* same */
+    const float *k_scale;        /* [num_pages, Hkv, P] f32 per (token, kv head) (fp8 cache) */
+    const float *v_scale;        /* same */
     const int32_t *block_table;  /* [B, max_pages] */
     const int32_t *seq_lens;     /* [B] */
     int B, Hq, Hkv, D, P, num_pages, max_pages;
@@ -77,6 +161,17 @@ typedef struct {
     int tid;
 } worker_arg;
 
+/* Element d of the key (is_v == 0) or value (is_v == 1) of slot `slot` in page
+ * `page`, kv head g, as an exact double: a bf16 value, or code value * scale. */
+static double kv_elem(const decode_args *a, int is_v, int page, int slot, int g, int d)
+{
+    const size_t off = (((size_t)page * a->P + slot) * a->Hkv + g) * a->D + d;
+    if (!a->k8) return bf16_bits_to_double((is_v ? a->v : a->k)[off]);
+    const uint8_t code = (is_v ? a->v8 : a->k8)[off];
+    const float s = (is_v ? a->v_scale : a->k_scale)[((size_t)page * a->Hkv + g) * a->P + slot];
+    return e4m3_value(code) * (double)s;
+}
+
 /* One output row: the definition above, written out. */
 static int decode_one(const decode_args *a, int b, int h, double *o, double *lse_out)
 {
@@ -93,20 +188,18 @@ static int decode_one(const decode_args *a, int b, int h, double *o, double *lse
     }
 
     double *s = (double *)malloc(sizeof(double) * (size_t)L);
-    const uint16_t **vrow = (const uint16_t **)malloc(sizeof(*vrow) * (size_t)L);
-    if (!s || !vrow) { free(s); free(vrow); return 1; }
+    int *jpage = (int *)malloc(sizeof(int) * (size_t)L);
+    if (!s || !jpage) { free(s); free(jpage); return 1; }
 
     for (int j = 0; j < L; ++j) {
         const int page = a->block_table[(size_t)b * a->max_pages + j / a->P];
         const int slot = j % a->P;
-        if (page < 0 || page >= a->num_pages) { free(s); free(vrow); return 1; }
-        const size_t row = (((size_t)page * a->P + slot) * a->Hkv + g) * D;
-        const uint16_t *kj = a->k + row;
+        if (page < 0 || page >= a->num_pages) { free(s); free(jpage); return 1; }
         double dot = 0.0;
         for (int d = 0; d < D; ++d)
-            dot += bf16_bits_to_double(qh[d]) * bf16_bits_to_double(kj[d]);
+            dot += bf16_bits_to_double(qh[d]) * kv_elem(a, 0, page, slot, g, d);
         s[j] = a->scale * dot;
-        vrow[j] = a->v + row;
+        jpage[j] = page;
     }
 
     double M = s[0];
@@ -121,13 +214,13 @@ static int decode_one(const decode_args *a, int b, int h, double *o, double *lse
     for (int d = 0; d < D; ++d) {
         double acc = 0.0;
         for (int j = 0; j < L; ++j)
-            acc += s[j] * bf16_bits_to_double(vrow[j][d]);
+            acc += s[j] * kv_elem(a, 1, jpage[j], j % a->P, g, d);
         o[d] = acc / Z;
     }
     *lse_out = M + log(Z);
 
     free(s);
-    free(vrow);
+    free(jpage);
     return 0;
 }
 
@@ -152,6 +245,28 @@ static int resolve_threads(int nthreads)
     return n > 0 ? (int)n : 1;
 }
 
+static int run_decode(decode_args *a, int nthreads)
+{
+    if (a->B < 0 || a->Hq <= 0 || a->Hkv <= 0 || a->D <= 0 || a->P <= 0 || a->Hq % a->Hkv != 0)
+        return 2;
+    for (int b = 0; b < a->B; ++b)
+        if (a->seq_lens[b] > (long)a->max_pages * a->P) return 2;
+    a->nthreads = resolve_threads(nthreads);
+
+    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)a->nthreads);
+    worker_arg *wa = (worker_arg *)malloc(sizeof(worker_arg) * (size_t)a->nthreads);
+    if (!th || !wa) { free(th); free(wa); return 2; }
+    for (int t = 0; t < a->nthreads; ++t) {
+        wa[t].a = a;
+        wa[t].tid = t;
+        pthread_create(&th[t], NULL, decode_worker, &wa[t]);
+    }
+    for (int t = 0; t < a->nthreads; ++t) pthread_join(th[t], NULL);
+    free(th);
+    free(wa);
+    return a->error ? 1 : 0;
+}
+
 /*
  * oracle_paged_decode: returns 0 on success, 1 if a used block_table entry is
  * outside [0, num_pages), 2 on bad arguments.  `sel` (may be NULL) restricts
@@ -164,31 +279,35 @@ int oracle_paged_decode(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                         int max_pages, double scale, const int32_t *sel, int nsel,
                         double *out, double *lse, int nthreads)
 {
-    if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || P <= 0 || Hq % Hkv != 0)
-        return 2;
-    for (int b = 0; b < B; ++b)
-        if (seq_lens[b] > (long)max_pages * P) return 2;
-
     decode_args a;
     memset(&a, 0, sizeof a);
     a.q = q; a.k = k; a.v = v; a.block_table = block_table; a.seq_lens = seq_lens;
     a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.D = D; a.P = P;
     a.num_pages = num_pages; a.max_pages = max_pages; a.scale = scale;
     a.sel = sel; a.nsel = nsel; a.out = out; a.lse = lse;
-    a.nthreads = resolve_threads(nthreads);
+    return run_decode(&a, nthreads);
+}
 
-    pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)a.nthreads);
-    worker_arg *wa = (worker_arg *)malloc(sizeof(worker_arg) * (size_t)a.nthreads);
-    if (!th || !wa) { free(th); free(wa); return 2; }
-    for (int t = 0; t < a.nthreads; ++t) {
-        wa[t].a = &a;
-        wa[t].tid = t;
-        pthread_create(&th[t], NULL, decode_worker, &wa[t]);
-    }
-    for (int t = 0; t < a.nthreads; ++t) pthread_join(th[t], NULL);
-    free(th);
-    free(wa);
-    return a.error ? 1 : 0;
+/*
+ * oracle_paged_decode_fp8: the same definition over an fp8 cache.  k8, v8 are
+ * e4m3 codes [num_pages, P, Hkv, D]; k_scale, v_scale are f32 [num_pages, Hkv, P];
+ * key/value element = code value * scale.  Return codes as above.
+ */
+int oracle_paged_decode_fp8(const uint16_t *q, const uint8_t *k8, const uint8_t *v8,
+                            const float *k_scale, const float *v_scale,
+                            const int32_t *block_table, const int32_t *seq_lens,
+                            int B, int Hq, int Hkv, int D, int P, int num_pages,
+                            int max_pages, double scale, const int32_t *sel, int nsel,
+                            double *out, double *lse, int nthreads)
+{
+    decode_args a;
+    memset(&a, 0, sizeof a);
+    a.q = q; a.k8 = k8; a.v8 = v8; a.k_scale = k_scale; a.v_scale = v_scale;
+    a.block_table = block_table; a.seq_lens = seq_lens;
+    a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.D = D; a.P = P;
+    a.num_pages = num_pages; a.max_pages = max_pages; a.scale = scale;
+    a.sel = sel; a.nsel = nsel; a.out = out; a.lse = lse;
+    return run_decode(&a, nthreads);
 }
 
 /*
@@ -259,6 +378,37 @@ int oracle_kv_append(const uint16_t *k_new, const uint16_t *v_new, const int32_t
             const size_t src = ((size_t)b * Hkv + g) * D;
             memcpy(k_cache + dst, k_new + src, sizeof(uint16_t) * (size_t)D);
             memcpy(v_cache + dst, v_new + src, sizeof(uint16_t) * (size_t)D);
+        }
+    }
+    return rejected;
+}
+
+/*
+ * oracle_kv_append_fp8: the append above into an fp8 cache, quantising on the
+ * way (OASR "Kernel Layer", "FP8 KV variants": one quantise-and-scatter launch
+ * writes K and V).  Each new (sequence, kv head) row is quantised by
+ * oracle_fp8_quantize_rows; its codes go to k8/v8 [num_pages, P, Hkv, D] and its
+ * scale to k_scale/v_scale [num_pages, Hkv, P].  Skip and reject rules and the
+ * return value are those of oracle_kv_append.
+ */
+int oracle_kv_append_fp8(const uint16_t *k_new, const uint16_t *v_new, const int32_t *block_table,
+                         const int32_t *positions, int B, int Hkv, int D, int P, int num_pages, int max_pages,
+                         uint8_t *k8, uint8_t *v8, float *k_scale, float *v_scale)
+{
+    int rejected = 0;
+    for (int b = 0; b < B; ++b) {
+        const int pos = positions[b];
+        if (pos < 0) continue;
+        if (pos >= max_pages * P) { ++rejected; continue; }
+        const int page = block_table[(size_t)b * max_pages + pos / P];
+        if (page < 0 || page >= num_pages) { ++rejected; continue; }
+        const int slot = pos % P;
+        for (int g = 0; g < Hkv; ++g) {
+            const size_t dst = (((size_t)page * P + slot) * Hkv + g) * D;
+            const size_t src = ((size_t)b * Hkv + g) * D;
+            const size_t sdst = ((size_t)page * Hkv + g) * P + slot;
+            oracle_fp8_quantize_rows(k_new + src, 1, D, k8 + dst, k_scale + sdst);
+            oracle_fp8_quantize_rows(v_new + src, 1, D, v8 + dst, v_scale + sdst);
         }
     }
     return rejected;
