@@ -5,11 +5,15 @@ gather, scores, online softmax, PV, split epilogue, merge) over one batch of
 seeded synthetic inputs resident in HBM.  L2 is flushed (a 2 x L2-size buffer
 is rewritten) before every timed step, outside the step's event pair.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl pkv|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--cache bf16|fp8]
+                    [--impl pkv|reference]
 
 Prints one JSON line (rank 0).  `value` is achieved GB/s of algorithmic bytes
 (K and V of the valid keys, q, out, lse, used block-table entries, lengths)
 summed over all ranks, divided by the max over ranks of the time per step.
+`--cache fp8` runs the same workload over an fp8 (e4m3) cache with per-(token, kv
+head) power-of-two scales, quantised on the device before timing; its algorithmic
+bytes count one byte per K/V element plus the scales.
 `--impl reference` times the CPU fp64 oracle on the host cores instead.
 """
 from __future__ import annotations
@@ -31,6 +35,10 @@ METRIC = "paged GQA decode attn: µs/call, achieved HBM GB/s and % of GB300 peak
 NOMINAL_HBM_GBS = 8000.0
 KERNEL_SOURCES = ["paged_kv_gqa_gb300/csrc/decode_kernel.cuh", "paged_kv_gqa_gb300/csrc/ptx.cuh",
                   "paged_kv_gqa_gb300/csrc/plan.h", "paged_kv_gqa_gb300/csrc/plan.cpp"]
+
+
+def profile_name(workload: str, cache: str = "bf16") -> str:
+    return workload if cache == "bf16" else "%s_%s" % (workload, cache)
 
 
 def kernel_source_hash() -> str:
@@ -160,17 +168,24 @@ def run_reference(args) -> None:
         return
     case = make_case(args.workload)
     q, k, v, bt, sl = case.host_bits()
+    cache = getattr(args, "cache", "bf16")
+    if cache == "fp8":  # the oracle's own quantiser makes its fp8 cache
+        k8, ks = oracle.quantize_pool(k)
+        v8, vs = oracle.quantize_pool(v)
+        one = lambda: oracle.paged_decode_fp8(q, k8, v8, ks, vs, bt, sl, case.scale, select=rows)
+    else:
+        one = lambda: oracle.paged_decode(q, k, v, bt, sl, case.scale, select=rows)
     rows, sample = _reference_sample(case, args.ref_seconds)
-    ab = algorithmic_bytes(case)
+    ab = algorithmic_bytes(case, cache=cache)
     frac = len(rows) / (case.B * case.Hq)
     step_bytes = ab["total"] * frac
     cores = os.cpu_count() or 1
     for _ in range(args.warmup):
-        oracle.paged_decode(q, k, v, bt, sl, case.scale, select=rows)
+        one()
     t = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle.paged_decode(q, k, v, bt, sl, case.scale, select=rows)
+        one()
         t.append(time.perf_counter() - t0)
     sec = sum(t) / len(t)
     value = step_bytes / sec / 1e9
@@ -204,7 +219,7 @@ def _reference_sample(case, seconds_hint):
 
 def _config_block(case, args, plan):
     lens = case.seq_lens.cpu().numpy()
-    cfg = {"workload": args.workload, "B": case.B, "Hq": case.Hq, "Hkv": case.Hkv, "D": case.D,
+    cfg = {"workload": args.workload, "cache": getattr(args, "cache", "bf16"), "B": case.B, "Hq": case.Hq, "Hkv": case.Hkv, "D": case.D,
            "page_size": case.P, "num_pages": case.num_pages, "max_pages": case.max_pages,
            "seq_lens": {"min": int(lens.min()), "max": int(lens.max()), "sum": int(lens.sum())},
            "seed": case.meta["seed"], "l2": "flushed before every timed step (2 x L2 bytes rewritten)"}
@@ -214,19 +229,23 @@ def _config_block(case, args, plan):
     return cfg
 
 
-def _cpu_baseline(case, seconds: float) -> dict:
-    """The oracle as it stands on the host cores, on a bounded sample of the workload."""
+def _cpu_baseline(case, seconds: float, fp8=None) -> dict:
+    """The oracle as it stands on the host cores, on a bounded sample of the workload.
+    fp8: optional host (k8, v8, k_scale, v_scale) numpy arrays of an fp8 cache."""
     import oracle
     from workloads import algorithmic_bytes
     q, k, v, bt, sl = case.host_bits()
     rows, sample = _reference_sample(case, 1.0)
     frac = len(rows) / (case.B * case.Hq)
-    step_bytes = algorithmic_bytes(case)["total"] * frac
+    step_bytes = algorithmic_bytes(case, cache="fp8" if fp8 else "bf16")["total"] * frac
     n, t_total = 0, 0.0
     t_end = time.perf_counter() + seconds
     while time.perf_counter() < t_end or n == 0:
         t0 = time.perf_counter()
-        oracle.paged_decode(q, k, v, bt, sl, case.scale, select=rows)
+        if fp8:
+            oracle.paged_decode_fp8(q, *fp8, bt, sl, case.scale, select=rows)
+        else:
+            oracle.paged_decode(q, k, v, bt, sl, case.scale, select=rows)
         t_total += time.perf_counter() - t0
         n += 1
     return {"value": round(step_bytes * n / t_total / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count() or 1,
@@ -244,7 +263,14 @@ def run_pkv(args) -> None:
     pkv.load()
 
     case = make_case(args.workload, device=dev)
-    ab = algorithmic_bytes(case)
+    fp8 = args.cache == "fp8"
+    pools8 = None
+    if fp8:  # quantise the pools on the device, then drop the bf16 copies
+        pools8 = pkv.quantize_pool_fp8(case.k_cache, case.v_cache)
+        torch.cuda.synchronize()
+        case.k_cache = case.v_cache = None
+        torch.cuda.empty_cache()
+    ab = algorithmic_bytes(case, cache=args.cache)
     props = torch.cuda.get_device_properties(dev)
     plan = pkv.plan_query(case.B, case.Hq, case.Hkv, case.D, case.P, case.max_pages, props.multi_processor_count)
     ws_bytes = pkv.paged_decode_attn_workspace_size(case.B, case.Hq, case.Hkv, case.D, case.P, case.max_pages)
@@ -257,8 +283,12 @@ def run_pkv(args) -> None:
     launches_per_call = 1  # the split merge runs inside the decode kernel
 
     def call():
-        pkv.paged_decode_attn(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens, case.scale,
-                              out, lse, ws, stream=stream)
+        if fp8:
+            pkv.paged_decode_attn_fp8(case.q, *pools8, case.block_table, case.seq_lens, case.scale, out, lse, ws,
+                                      stream=stream)
+        else:
+            pkv.paged_decode_attn(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens, case.scale,
+                                  out, lse, ws, stream=stream)
 
     for _ in range(args.warmup):
         flush.fill_(1)
@@ -294,11 +324,15 @@ def run_pkv(args) -> None:
     # ---- end to end through the public API with host buffers -------------------
     e2e = None
     if not args.no_e2e:
-        e2e = _e2e(args, case, ab, pkv, torch, dev, stream, flush, plan, dist)
+        e2e = _e2e(args, case, ab, pkv, torch, dev, stream, flush, plan, dist, pools8)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = _cpu_baseline(case.to("cpu"), args.cpu_seconds)
+        if fp8:
+            hc = _host_case(case)
+            cpu = _cpu_baseline(hc, args.cpu_seconds, fp8=tuple(t.cpu().numpy() for t in pools8))
+        else:
+            cpu = _cpu_baseline(case.to("cpu"), args.cpu_seconds)
 
     if rank != 0:
         if dist:
@@ -306,11 +340,13 @@ def run_pkv(args) -> None:
         return
     peaks = measured_peaks()
     gbs = weak_scaling_gbs(ab["total"], 1, mean_ms)
-    traffic = profiled_traffic(args.workload)
+    traffic = profiled_traffic(profile_name(args.workload, args.cache))
     line = {
         "metric": METRIC, "value": round(gbs * world, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(mean_ms, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16, shuffled page pool)",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, shuffled page pool)" + (
+            "; K/V quantised on the device to e4m3 with per-(token, kv head) power-of-two scales" if fp8 else ""),
         "config": _config_block(case, args, plan),
         "us_per_call": round(mean_ms * 1e3, 3),
         "us_per_call_p10_p50_p90": [round(x * 1e3, 3) for x in _quantiles(step_ms)],
@@ -319,7 +355,8 @@ def run_pkv(args) -> None:
         "algorithmic_bytes": ab["total"], "tail_bytes_touched": ab["tail_bytes"],
         "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": traffic,
-                     "kernel": "decode_split_kernel (one launch per call; split merge fused)",
+                     "kernel": "decode_split_kernel%s (one launch per call; split merge fused)" % (
+                         "<fp8 cache>" if fp8 else ""),
                      "peak_source": peaks["source"]},
         "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_call * args.steps,
@@ -335,11 +372,28 @@ def _quantiles(xs):
     return [s[int(0.1 * (len(s) - 1))], s[int(0.5 * (len(s) - 1))], s[int(0.9 * (len(s) - 1))]]
 
 
-def _e2e(args, case, ab, pkv, torch, dev, stream, flush, plan, dist):
+def _host_case(case):
+    """A host copy of a case whose bf16 pools were dropped (fp8 runs): q, table, lengths."""
+    from workloads import Case
+    c = Case(**case.__dict__)
+    for n in ("q", "block_table", "seq_lens"):
+        setattr(c, n, getattr(case, n).cpu())
+    import torch
+    c.k_cache = c.v_cache = torch.empty(0, dtype=torch.bfloat16)
+    return c
+
+
+def _e2e(args, case, ab, pkv, torch, dev, stream, flush, plan, dist, pools8=None):
     """Same metric, through the public call with host buffers: each step copies the
     step's inputs host -> device from pinned memory, runs the call, and reads the
     result back."""
-    host = {n: getattr(case, n).cpu().pin_memory() for n in ("q", "k_cache", "v_cache", "block_table", "seq_lens")}
+    if pools8 is not None:
+        host = {n: getattr(case, n).cpu().pin_memory() for n in ("q", "block_table", "seq_lens")}
+        for n, t in zip(("k8", "v8", "ks", "vs"), pools8):
+            host[n] = t.cpu().pin_memory()
+    else:
+        host = {n: getattr(case, n).cpu().pin_memory() for n in ("q", "k_cache", "v_cache", "block_table",
+                                                                   "seq_lens")}
     devb = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
     out_h = torch.empty((case.B, case.Hq, case.D), dtype=torch.bfloat16).pin_memory()
     lse_h = torch.empty((case.B, case.Hq), dtype=torch.float32).pin_memory()
@@ -353,8 +407,12 @@ def _e2e(args, case, ab, pkv, torch, dev, stream, flush, plan, dist):
     def step():
         for n in host:
             devb[n].copy_(host[n], non_blocking=True)
-        pkv.paged_decode_attn(devb["q"], devb["k_cache"], devb["v_cache"], devb["block_table"], devb["seq_lens"],
-                              case.scale, out, lse, ws, stream=stream)
+        if pools8 is not None:
+            pkv.paged_decode_attn_fp8(devb["q"], devb["k8"], devb["v8"], devb["ks"], devb["vs"], devb["block_table"],
+                                      devb["seq_lens"], case.scale, out, lse, ws, stream=stream)
+        else:
+            pkv.paged_decode_attn(devb["q"], devb["k_cache"], devb["v_cache"], devb["block_table"],
+                                  devb["seq_lens"], case.scale, out, lse, ws, stream=stream)
         out_h.copy_(out, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
 
@@ -424,6 +482,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="batch",
                     choices=["tiny", "batch", "ragged", "long", "bigpage", "bigpage_g16", "append"])
+    ap.add_argument("--cache", default="bf16", choices=["bf16", "fp8"])
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)

@@ -234,6 +234,58 @@ PKV_API pkv_status paged_kv_append(const pkv_bf16 *k_new, const pkv_bf16 *v_new,
                                    int max_pages, pkv_bf16 *k_cache, pkv_bf16 *v_cache, int *status,
                                    cudaStream_t stream);
 
+/* ------------------------------------------------------------------ fp8 cache */
+
+/*
+ * FP8 KV cache (OASR "Kernel Layer", "FP8 KV variants"): the pools hold float8
+ * e4m3 codes ("fn" variant: sign, 4 exponent bits with bias 7, 3 mantissa bits,
+ * no infinities, S.1111.111 = NaN, largest finite 448) with one f32 scale per
+ * (token, kv head).  The key (value) element used for slot t of page p, kv head
+ * g, dim d is
+ *     bf16( code(k_cache[p, t, g, d]) * k_scale[p, g, t] )
+ * (the product in f32, rounded to bf16).  With power-of-two scales, as
+ * paged_kv_append_fp8 writes them, the product is exact, and the result is
+ * bit-identical to paged_decode_attn_ex with the same num_splits on a bf16 cache
+ * holding those values: the kernel dequantises each stage into the same bf16
+ * tile and runs the same code after it, with the same plan (split count, chunk,
+ * workspace size) as paged_decode_attn for the shape.
+ *
+ *   k_cache, v_cache  [num_pages, page_size, Hkv, D] uint8 e4m3 codes
+ *   k_scale, v_scale  [num_pages, Hkv, page_size] f32 (head-major within a page,
+ *                     so one head's scales for a page are contiguous), 16-byte
+ *                     aligned
+ * Every other argument, the workspace (size from
+ * paged_decode_attn_workspace_size_ex with the same num_splits), the status
+ * word and the error behaviour are those of paged_decode_attn_ex.  NaN codes
+ * or scales in slots past seq_lens[b] are never used.
+ */
+PKV_API pkv_status paged_decode_attn_fp8(const pkv_bf16 *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                                         const float *k_scale, const float *v_scale, const int32_t *block_table,
+                                         const int32_t *seq_lens, int B, int Hq, int Hkv, int D, int page_size,
+                                         int num_pages, int max_pages, float scale, pkv_bf16 *out, float *lse,
+                                         void *workspace, size_t workspace_bytes, int num_splits,
+                                         cudaStream_t stream);
+
+/*
+ * Quantise-and-append into an fp8 cache: paged_kv_append's write, quantising
+ * each new (sequence, kv head) row of K and of V on the way, K and V in one
+ * launch (OASR "Kernel Layer", "FP8 KV variants": one quantise-and-scatter
+ * launch writes the cache).  A row x of D values gets
+ *     scale = 2^k, k the smallest integer in [-64, 64] with max_d |x_d| <= 448 * 2^k
+ *     code_d = e4m3(x_d / scale), round to nearest even, saturating at +-448
+ * (NaN values are left out of the maximum and give a NaN code).  The codes go to
+ * k_cache/v_cache[page, slot, g, :] and the scale to k_scale/v_scale[page, g,
+ * slot], with page and slot from positions[b] as in paged_kv_append.  Every
+ * other argument and the error behaviour are those of paged_kv_append; the
+ * scale tensors are [num_pages, Hkv, page_size] f32, 16-byte aligned.  Calling
+ * it with B = num_pages * page_size rows, a one-page table per row and
+ * positions = slot quantises a whole pool in one launch.
+ */
+PKV_API pkv_status paged_kv_append_fp8(const pkv_bf16 *k_new, const pkv_bf16 *v_new, const int32_t *block_table,
+                                       const int32_t *positions, int B, int Hkv, int D, int page_size,
+                                       int num_pages, int max_pages, uint8_t *k_cache, uint8_t *v_cache,
+                                       float *k_scale, float *v_scale, int *status, cudaStream_t stream);
+
 /* ------------------------------------------------------------------ merge */
 
 /*

@@ -200,16 +200,32 @@ def e4m3_encode(values) -> np.ndarray:
     return np.asarray(flat, dtype=np.uint8).reshape(v.shape)
 
 
-def fp8_quantize_rows(x_bits):
+def fp8_quantize_rows(x_bits, nthreads=0):
     """Quantise rows of bf16 values: x_bits uint16 [..., D] -> (codes uint8 [..., D],
-    scales float32 [...]) with one power-of-two scale per row."""
+    scales float32 [...]) with one power-of-two scale per row.  Rows are independent;
+    large inputs are cut into contiguous row ranges quantised on parallel threads."""
     lib = _load()
     x = _as_bits(x_bits)
     D = x.shape[-1]
     N = int(np.prod(x.shape[:-1]))
     codes = np.empty(x.shape, np.uint8)
     scales = np.empty(x.shape[:-1], np.float32)
-    lib.oracle_fp8_quantize_rows(_ptr(x), N, D, _ptr(codes), _ptr(scales))
+    xf, cf, sf = x.reshape(N, D), codes.reshape(N, D), scales.reshape(N)
+    n_th = nthreads if nthreads > 0 else (os.cpu_count() or 1)
+    step = max(1 << 14, -(-N // n_th))
+    ranges = [(a, min(N, a + step)) for a in range(0, N, step)]
+
+    def run(r):
+        a, b = r
+        lib.oracle_fp8_quantize_rows(_ptr(xf[a:b]), b - a, D, _ptr(cf[a:b]), _ptr(sf[a:b]))
+
+    if len(ranges) <= 1:
+        for r in ranges:
+            run(r)
+    else:
+        from concurrent.futures import ThreadPoolExecutor
+        with ThreadPoolExecutor(max_workers=len(ranges)) as ex:
+            list(ex.map(run, ranges))
     return codes, scales
 
 

@@ -18,6 +18,7 @@ __all__ = [
     "PkvError", "load", "status_string", "plan_query", "paged_decode_attn_workspace_size",
     "paged_decode_attn", "paged_decode_attn_ex", "split_kv_merge", "pkv_check_status",
     "pkv_reset_status", "pkv_selftest_wait_timeout", "paged_decode_attn_static_scratch", "paged_kv_append",
+    "paged_decode_attn_fp8", "paged_kv_append_fp8", "quantize_pool_fp8",
     "EXPORTED_SYMBOLS",
     "STATUS",
 ]
@@ -36,7 +37,7 @@ EXPORTED_SYMBOLS = [
     "pkv_status_string", "pkv_version", "pkv_plan_query", "paged_decode_attn_workspace_size",
     "paged_decode_attn_workspace_size_ex", "paged_decode_attn", "paged_decode_attn_ex", "split_kv_merge",
     "pkv_check_status", "pkv_reset_status", "pkv_selftest_wait_timeout", "paged_decode_attn_static_scratch",
-    "paged_kv_append",
+    "paged_kv_append", "paged_decode_attn_fp8", "paged_kv_append_fp8",
 ]
 
 
@@ -85,6 +86,8 @@ def load(path: str = LIB_PATH):
             "pkv_selftest_wait_timeout": (I, [P, U, P]),
             "paged_decode_attn_static_scratch": (I, [P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, P]),
             "paged_kv_append": (I, [P, P, P, P, I, I, I, I, I, I, P, P, P, P]),
+            "paged_decode_attn_fp8": (I, [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, S, I, P]),
+            "paged_kv_append_fp8": (I, [P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -243,3 +246,73 @@ def paged_kv_append(k_new, v_new, block_table, positions, k_cache, v_cache, stat
         _dev_ptr(v_cache, torch.bfloat16, "v_cache", 4),
         ctypes.c_void_p(status.data_ptr()) if status is not None else None, _stream_handle(stream))
     _check(st, "paged_kv_append")
+
+
+# ----------------------------------------------------------------- fp8 (e4m3) cache
+
+def paged_decode_attn_fp8(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, scale, out, lse, workspace,
+                          num_splits=0, stream=None):
+    """Calls paged_decode_attn_fp8: k_cache/v_cache uint8 e4m3 codes [num_pages, P, Hkv, D],
+    k_scale/v_scale float32 [num_pages, Hkv, P]; the rest as for paged_decode_attn_ex."""
+    torch = _torch()
+    B, Hq, D = q.shape
+    num_pages, P, Hkv, Dk = k_cache.shape
+    if Dk != D or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("q/k_cache/v_cache shapes disagree")
+    if tuple(k_scale.shape) != (num_pages, Hkv, P) or tuple(v_scale.shape) != (num_pages, Hkv, P):
+        raise ValueError("k_scale/v_scale must be [num_pages, Hkv, page_size]")
+    if tuple(out.shape) != (B, Hq, D):
+        raise ValueError("out must be [B, Hq, D]")
+    if lse is not None and tuple(lse.shape) != (B, Hq):
+        raise ValueError("lse must be [B, Hq]")
+    st = load().paged_decode_attn_fp8(
+        _dev_ptr(q, torch.bfloat16, "q", 3), _dev_ptr(k_cache, torch.uint8, "k_cache", 4),
+        _dev_ptr(v_cache, torch.uint8, "v_cache", 4), _dev_ptr(k_scale, torch.float32, "k_scale", 3),
+        _dev_ptr(v_scale, torch.float32, "v_scale", 3), _dev_ptr(block_table, torch.int32, "block_table", 2),
+        _dev_ptr(seq_lens, torch.int32, "seq_lens", 1), B, Hq, Hkv, D, P, num_pages, block_table.shape[1],
+        ctypes.c_float(scale), _dev_ptr(out, torch.bfloat16, "out", 3),
+        _dev_ptr(lse, torch.float32, "lse", 2) if lse is not None else None,
+        _dev_ptr(workspace, workspace.dtype, "workspace"), workspace.numel() * workspace.element_size(),
+        int(num_splits), _stream_handle(stream))
+    _check(st, "paged_decode_attn_fp8")
+    return out, lse
+
+
+def paged_kv_append_fp8(k_new, v_new, block_table, positions, k_cache, v_cache, k_scale, v_scale, status=None,
+                        stream=None):
+    """Calls paged_kv_append_fp8: quantises k_new/v_new [B, Hkv, D] (bf16) into the fp8 pools
+    (uint8 [num_pages, P, Hkv, D]) and their scales (float32 [num_pages, Hkv, P]) at positions[b]."""
+    torch = _torch()
+    B, Hkv, D = k_new.shape
+    num_pages, P, Hkv2, D2 = k_cache.shape
+    if (Hkv2, D2) != (Hkv, D) or tuple(v_new.shape) != tuple(k_new.shape) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_new/v_new/k_cache/v_cache shapes disagree")
+    if tuple(k_scale.shape) != (num_pages, Hkv, P) or tuple(v_scale.shape) != (num_pages, Hkv, P):
+        raise ValueError("k_scale/v_scale must be [num_pages, Hkv, page_size]")
+    st = load().paged_kv_append_fp8(
+        _dev_ptr(k_new, torch.bfloat16, "k_new", 3), _dev_ptr(v_new, torch.bfloat16, "v_new", 3),
+        _dev_ptr(block_table, torch.int32, "block_table", 2), _dev_ptr(positions, torch.int32, "positions", 1),
+        B, Hkv, D, P, num_pages, block_table.shape[1], _dev_ptr(k_cache, torch.uint8, "k_cache", 4),
+        _dev_ptr(v_cache, torch.uint8, "v_cache", 4), _dev_ptr(k_scale, torch.float32, "k_scale", 3),
+        _dev_ptr(v_scale, torch.float32, "v_scale", 3),
+        ctypes.c_void_p(status.data_ptr()) if status is not None else None, _stream_handle(stream))
+    _check(st, "paged_kv_append_fp8")
+
+
+def quantize_pool_fp8(k_cache, v_cache, stream=None):
+    """Quantises whole bf16 pools [num_pages, P, Hkv, D] into new fp8 pools and scales with one
+    paged_kv_append_fp8 launch (one row per (page, slot), a one-page table per row)."""
+    torch = _torch()
+    num_pages, P, Hkv, D = k_cache.shape
+    dev = k_cache.device
+    n = num_pages * P
+    rows = torch.arange(n, device=dev, dtype=torch.int32)
+    table = (rows // P).reshape(n, 1).contiguous()
+    pos = (rows % P).contiguous()
+    k8 = torch.empty((num_pages, P, Hkv, D), dtype=torch.uint8, device=dev)
+    v8 = torch.empty_like(k8)
+    ks = torch.empty((num_pages, Hkv, P), dtype=torch.float32, device=dev)
+    vs = torch.empty_like(ks)
+    paged_kv_append_fp8(k_cache.reshape(n, Hkv, D), v_cache.reshape(n, Hkv, D), table, pos, k8, v8, ks, vs,
+                        stream=stream)
+    return k8, v8, ks, vs

@@ -12,7 +12,7 @@
 #include <mutex>
 
 #include "append_kernel.cuh"
-#include "decode_kernel.cuh"
+#include "decode_launch.cuh"
 #include "merge_kernel.cuh"
 #include "pkv.h"
 #include "plan.h"
@@ -54,7 +54,7 @@ EncodeTiledFn encode_fn()
 
 struct MapKey {
     const void *ptr;
-    int num_pages, P, Hkv, D, box_t, device, rank;
+    int num_pages, P, Hkv, D, box_t, device, rank;  // rank 8: the fp8 (byte) view
     bool operator==(const MapKey &o) const
     {
         return ptr == o.ptr && num_pages == o.num_pages && P == o.P && Hkv == o.Hkv && D == o.D &&
@@ -83,7 +83,10 @@ MapCache &map_cache()
 //           strides (row: Hkv*D*2 B, column block: 128 B, head: D*2 B); one box
 //           (64, box_t, D/64, 1) lands a page slice of one head as [D/64][box_t][64];
 //   rank 3: dims (D, Hkv, num_pages*P rows), box (64, 1, box_t): one box per
-//           64-column block (the fallback when the driver refuses the rank-4 view).
+//           64-column block (the fallback when the driver refuses the rank-4 view);
+//   rank 8 (fp8 pool, bytes, no swizzle): dims (D, Hkv, num_pages*P rows) with
+//           strides (D B, Hkv*D B), box (D, 1, box_t): a page slice of one head
+//           lands as [box_t][D] codes.
 pkv_status get_pool_map(const void *pool, int num_pages, int P, int Hkv, int D, int box_t, int device, int rank,
                         CUtensorMap *out)
 {
@@ -99,7 +102,15 @@ pkv_status get_pool_map(const void *pool, int num_pages, int P, int Hkv, int D, 
     if (!fn) return PKV_ERR_CUDA;
     CUtensorMap m;
     CUresult r;
-    if (rank == 4) {
+    if (rank == 8) {
+        const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)num_pages * (cuuint64_t)P};
+        const cuuint64_t strides[2] = {(cuuint64_t)D, (cuuint64_t)Hkv * D};
+        const cuuint32_t box[3] = {(cuuint32_t)D, 1u, (cuuint32_t)box_t};
+        const cuuint32_t estr[3] = {1u, 1u, 1u};
+        r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(pool), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else if (rank == 4) {
         const cuuint64_t dims[4] = {64u, (cuuint64_t)num_pages * (cuuint64_t)P, (cuuint64_t)(D / 64),
                                     (cuuint64_t)Hkv};
         const cuuint64_t strides[3] = {(cuuint64_t)Hkv * D * 2, 128u, (cuuint64_t)D * 2};
@@ -142,45 +153,16 @@ pkv_status current_device_sms(int *device, int *sms)
 
 // ---------------------------------------------------------------- launches
 
-template <int D, int NT>
-pkv_status launch_decode_variant(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
-                                 const pkv_plan &plan, int B, int Hkv, int device, cudaStream_t stream)
+// Bounded-wait self-test: waits on a barrier nothing completes.
+__global__ void wait_timeout_selftest_kernel(int *status, unsigned long long limit_ns)
 {
-    static bool attr_set[64] = {};
-    static std::mutex mu;
-    auto kern = decode_split_kernel<D, NT>;
-    if (device < 0 || device >= 64) return PKV_ERR_UNSUPPORTED;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (!attr_set[device]) {
-            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448) != cudaSuccess)
-                return PKV_ERR_CUDA;
-            attr_set[device] = true;
-        }
-    }
-    dim3 grid(Hkv, plan.num_splits, B);
-    dim3 block(plan.warps * 32);
-    kern<<<grid, block, plan.smem_bytes, stream>>>(mk, mv, p);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(smem_addr(&bar), 1);
+    fence_barrier_init();
+    if (!mbar_wait_bounded(smem_addr(&bar), 0, limit_ns)) record_status(status, PKV_ERR_DEVICE_TIMEOUT);
 }
 
-pkv_status launch_decode(int D, int NT, const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
-                         const pkv_plan &plan, int B, int Hkv, int device, cudaStream_t stream)
-{
-#define PKV_CASE(DD, NN) \
-    if (D == DD && NT == NN) return launch_decode_variant<DD, NN>(mk, mv, p, plan, B, Hkv, device, stream);
-    PKV_CASE(64, 1)
-    PKV_CASE(64, 2)
-    PKV_CASE(64, 4)
-    PKV_CASE(128, 1)
-    PKV_CASE(128, 2)
-    PKV_CASE(128, 4)
-    PKV_CASE(256, 1)
-    PKV_CASE(256, 2)
-    PKV_CASE(256, 4)
-#undef PKV_CASE
-    return PKV_ERR_UNSUPPORTED;
-}
 
 pkv_status launch_merge(int D, const MergeParams &mp, cudaStream_t stream)
 {
@@ -195,43 +177,59 @@ pkv_status launch_merge(int D, const MergeParams &mp, cudaStream_t stream)
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-pkv_status decode_impl(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+// The fp8 cache's scale tensors (on == false: a bf16 cache).
+struct Fp8Scales {
+    bool on = false;
+    const float *k_scale = nullptr, *v_scale = nullptr;
+};
+
+pkv_status decode_impl(const pkv_bf16 *q, const void *k_cache, const void *v_cache, Fp8Scales fp8,
                        const int32_t *block_table, const int32_t *seq_lens, int B, int Hq, int Hkv, int D,
                        int page_size, int num_pages, int max_pages, float scale, pkv_bf16 *out, float *lse,
                        void *workspace, size_t workspace_bytes_, int num_splits, cudaStream_t stream)
 {
+    const bool kv8 = fp8.on;
     if (num_pages <= 0 || num_splits < 0 || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
     const pkv_status shape_ok = validate_shape(B, Hq, Hkv, D, page_size, max_pages);
     if (shape_ok != PKV_OK) return shape_ok;
     if (B == 0) return PKV_OK;
     if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out || !workspace) return PKV_ERR_INVALID_ARG;
+    if (kv8 && (!fp8.k_scale || !fp8.v_scale)) return PKV_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(block_table) ||
         !aligned16(seq_lens) || !aligned16(out) || (lse && !aligned16(lse)) || !aligned16(workspace))
         return PKV_ERR_MISALIGNED;
+    if (kv8 && (!aligned16(fp8.k_scale) || !aligned16(fp8.v_scale))) return PKV_ERR_MISALIGNED;
     if ((long)num_pages * page_size >= (1l << 31)) return PKV_ERR_INVALID_ARG;
 
     int device = 0, sms = 0;
     pkv_status st = current_device_sms(&device, &sms);
     if (st != PKV_OK) return st;
     pkv_plan plan;
-    st = make_plan(B, Hq, Hkv, D, page_size, max_pages, sms, num_splits, &plan);
+    st = make_plan(B, Hq, Hkv, D, page_size, max_pages, sms, num_splits, &plan, kv8);
     if (st != PKV_OK) return st;
     if (workspace_bytes_ < plan.workspace_bytes) return PKV_ERR_WORKSPACE_TOO_SMALL;
 
     const int box_t = plan.stage_tokens < page_size ? plan.stage_tokens : page_size;
-    // One box per tensor per stage when a stage lies in one page (rank-4 view);
-    // otherwise, or if the driver refuses that view, one box per 64 columns.
     CUtensorMap mk, mv;
     int box4 = 0;
-    if (plan.stage_tokens <= page_size &&
-        get_pool_map(k_cache, num_pages, page_size, Hkv, D, box_t, device, 4, &mk) == PKV_OK &&
-        get_pool_map(v_cache, num_pages, page_size, Hkv, D, box_t, device, 4, &mv) == PKV_OK)
-        box4 = 1;
-    if (!box4) {
-        st = get_pool_map(k_cache, num_pages, page_size, Hkv, D, box_t, device, 3, &mk);
+    if (kv8) {
+        st = get_pool_map(k_cache, num_pages, page_size, Hkv, D, box_t, device, 8, &mk);
         if (st != PKV_OK) return st;
-        st = get_pool_map(v_cache, num_pages, page_size, Hkv, D, box_t, device, 3, &mv);
+        st = get_pool_map(v_cache, num_pages, page_size, Hkv, D, box_t, device, 8, &mv);
         if (st != PKV_OK) return st;
+    } else {
+        // One box per tensor per stage when a stage lies in one page (rank-4 view);
+        // otherwise, or if the driver refuses that view, one box per 64 columns.
+        if (plan.stage_tokens <= page_size &&
+            get_pool_map(k_cache, num_pages, page_size, Hkv, D, box_t, device, 4, &mk) == PKV_OK &&
+            get_pool_map(v_cache, num_pages, page_size, Hkv, D, box_t, device, 4, &mv) == PKV_OK)
+            box4 = 1;
+        if (!box4) {
+            st = get_pool_map(k_cache, num_pages, page_size, Hkv, D, box_t, device, 3, &mk);
+            if (st != PKV_OK) return st;
+            st = get_pool_map(v_cache, num_pages, page_size, Hkv, D, box_t, device, 3, &mv);
+            if (st != PKV_OK) return st;
+        }
     }
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -246,6 +244,8 @@ pkv_status decode_impl(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf1
     p.part_lse = reinterpret_cast<float *>(ws + wl.part_lse);
     p.part_out = reinterpret_cast<float *>(ws + wl.part_out);
     p.status = reinterpret_cast<int *>(ws);
+    p.k_scale = fp8.k_scale;
+    p.v_scale = fp8.v_scale;
     p.B = B;
     p.Hq = Hq;
     p.Hkv = Hkv;
@@ -260,7 +260,30 @@ pkv_status decode_impl(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf1
     p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
     p.wait_limit_ns = kWaitLimitNs;
 
-    return launch_decode(D, head_tiles(p.G), mk, mv, p, plan, B, Hkv, device, stream);
+    const int NT = head_tiles(p.G);
+    return kv8 ? launch_decode_fp8(D, NT, mk, mv, p, plan, B, Hkv, device, stream)
+               : launch_decode_bf16(D, NT, mk, mv, p, plan, B, Hkv, device, stream);
+}
+
+// Shared checks of the two append entry points; returns PKV_OK with *skip set when B == 0.
+pkv_status append_checks(const void *k_new, const void *v_new, const int32_t *block_table, const int32_t *positions,
+                         int B, int Hkv, int D, int page_size, int num_pages, int max_pages, const void *k_cache,
+                         const void *v_cache, const int *status, bool *skip)
+{
+    *skip = false;
+    if (num_pages <= 0) return PKV_ERR_INVALID_ARG;
+    const pkv_status shape_ok = validate_shape(B, Hkv, Hkv, D, page_size, max_pages);
+    if (shape_ok != PKV_OK) return shape_ok;
+    if (B == 0) {
+        *skip = true;
+        return PKV_OK;
+    }
+    if (!k_new || !v_new || !block_table || !positions || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(block_table) || !aligned16(positions) ||
+        !aligned16(k_cache) || !aligned16(v_cache) || (status && (reinterpret_cast<uintptr_t>(status) & 3u)))
+        return PKV_ERR_MISALIGNED;
+    if ((long)num_pages * page_size >= (1l << 31) || (long)B * Hkv >= (1l << 31)) return PKV_ERR_INVALID_ARG;
+    return PKV_OK;
 }
 
 }  // namespace
@@ -318,8 +341,8 @@ pkv_status paged_decode_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache, const p
                              int page_size, int num_pages, int max_pages, float scale, pkv_bf16 *out, float *lse,
                              void *workspace, size_t workspace_bytes, cudaStream_t stream)
 {
-    return decode_impl(q, k_cache, v_cache, block_table, seq_lens, B, Hq, Hkv, D, page_size, num_pages, max_pages,
-                       scale, out, lse, workspace, workspace_bytes, 0, stream);
+    return decode_impl(q, k_cache, v_cache, Fp8Scales{}, block_table, seq_lens, B, Hq, Hkv, D, page_size,
+                       num_pages, max_pages, scale, out, lse, workspace, workspace_bytes, 0, stream);
 }
 
 pkv_status paged_decode_attn_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
@@ -327,8 +350,22 @@ pkv_status paged_decode_attn_ex(const pkv_bf16 *q, const pkv_bf16 *k_cache, cons
                                 int page_size, int num_pages, int max_pages, float scale, pkv_bf16 *out, float *lse,
                                 void *workspace, size_t workspace_bytes, int num_splits, cudaStream_t stream)
 {
-    return decode_impl(q, k_cache, v_cache, block_table, seq_lens, B, Hq, Hkv, D, page_size, num_pages, max_pages,
-                       scale, out, lse, workspace, workspace_bytes, num_splits, stream);
+    return decode_impl(q, k_cache, v_cache, Fp8Scales{}, block_table, seq_lens, B, Hq, Hkv, D, page_size,
+                       num_pages, max_pages, scale, out, lse, workspace, workspace_bytes, num_splits, stream);
+}
+
+pkv_status paged_decode_attn_fp8(const pkv_bf16 *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                                 const float *k_scale, const float *v_scale, const int32_t *block_table,
+                                 const int32_t *seq_lens, int B, int Hq, int Hkv, int D, int page_size,
+                                 int num_pages, int max_pages, float scale, pkv_bf16 *out, float *lse,
+                                 void *workspace, size_t workspace_bytes, int num_splits, cudaStream_t stream)
+{
+    Fp8Scales f;
+    f.on = true;
+    f.k_scale = k_scale;
+    f.v_scale = v_scale;
+    return decode_impl(q, k_cache, v_cache, f, block_table, seq_lens, B, Hq, Hkv, D, page_size, num_pages,
+                       max_pages, scale, out, lse, workspace, workspace_bytes, num_splits, stream);
 }
 
 pkv_status split_kv_merge(const float *partial_out, const float *partial_lse, int S, int B, int Hq, int D,
@@ -359,15 +396,10 @@ pkv_status paged_kv_append(const pkv_bf16 *k_new, const pkv_bf16 *v_new, const i
                            const int32_t *positions, int B, int Hkv, int D, int page_size, int num_pages,
                            int max_pages, pkv_bf16 *k_cache, pkv_bf16 *v_cache, int *status, cudaStream_t stream)
 {
-    if (num_pages <= 0) return PKV_ERR_INVALID_ARG;
-    const pkv_status shape_ok = validate_shape(B, Hkv, Hkv, D, page_size, max_pages);
-    if (shape_ok != PKV_OK) return shape_ok;
-    if (B == 0) return PKV_OK;
-    if (!k_new || !v_new || !block_table || !positions || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
-    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(block_table) || !aligned16(positions) ||
-        !aligned16(k_cache) || !aligned16(v_cache) || (status && (reinterpret_cast<uintptr_t>(status) & 3u)))
-        return PKV_ERR_MISALIGNED;
-    if ((long)num_pages * page_size >= (1l << 31) || (long)B * Hkv >= (1l << 31)) return PKV_ERR_INVALID_ARG;
+    bool skip = false;
+    const pkv_status st = append_checks(k_new, v_new, block_table, positions, B, Hkv, D, page_size, num_pages,
+                                        max_pages, k_cache, v_cache, status, &skip);
+    if (st != PKV_OK || skip) return st;
     AppendParams ap;
     ap.k_new = reinterpret_cast<const uint4 *>(k_new);
     ap.v_new = reinterpret_cast<const uint4 *>(v_new);
@@ -385,6 +417,44 @@ pkv_status paged_kv_append(const pkv_bf16 *k_new, const pkv_bf16 *v_new, const i
     ap.max_pages = max_pages;
     const long units = (long)B * Hkv;
     kv_append_kernel<<<(unsigned)((units + kAppendWarps - 1) / kAppendWarps), kAppendWarps * 32, 0, stream>>>(ap);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+pkv_status paged_kv_append_fp8(const pkv_bf16 *k_new, const pkv_bf16 *v_new, const int32_t *block_table,
+                               const int32_t *positions, int B, int Hkv, int D, int page_size, int num_pages,
+                               int max_pages, uint8_t *k_cache, uint8_t *v_cache, float *k_scale, float *v_scale,
+                               int *status, cudaStream_t stream)
+{
+    bool skip = false;
+    const pkv_status st = append_checks(k_new, v_new, block_table, positions, B, Hkv, D, page_size, num_pages,
+                                        max_pages, k_cache, v_cache, status, &skip);
+    if (st != PKV_OK || skip) return st;
+    if (!k_scale || !v_scale) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(k_scale) || !aligned16(v_scale)) return PKV_ERR_MISALIGNED;
+    Fp8AppendParams ap;
+    ap.k_new = reinterpret_cast<const uint16_t *>(k_new);
+    ap.v_new = reinterpret_cast<const uint16_t *>(v_new);
+    ap.block_table = block_table;
+    ap.positions = positions;
+    ap.k_cache = k_cache;
+    ap.v_cache = v_cache;
+    ap.k_scale = k_scale;
+    ap.v_scale = v_scale;
+    ap.status = status;
+    ap.B = B;
+    ap.Hkv = Hkv;
+    ap.P = page_size;
+    ap.log2P = log2_exact(page_size);
+    ap.num_pages = num_pages;
+    ap.max_pages = max_pages;
+    const long units = (long)B * Hkv;
+    const unsigned grid = (unsigned)((units + kAppendWarps - 1) / kAppendWarps);
+    switch (D) {
+        case 64: kv_append_fp8_kernel<64><<<grid, kAppendWarps * 32, 0, stream>>>(ap); break;
+        case 128: kv_append_fp8_kernel<128><<<grid, kAppendWarps * 32, 0, stream>>>(ap); break;
+        case 256: kv_append_fp8_kernel<256><<<grid, kAppendWarps * 32, 0, stream>>>(ap); break;
+        default: return PKV_ERR_UNSUPPORTED;
+    }
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -44,6 +44,17 @@
 // zeroed in registers before the PV mma, so NaN or Inf left in unused slots
 // never reaches the result (0 * NaN would).
 //
+// FP8 cache (KV8).  The pool may instead hold float8 e4m3 codes with one f32
+// scale per (token, kv head), the scales stored [page][kv head][slot] so that a
+// page slice of one head's scales is contiguous (OASR "Kernel Layer", "FP8 KV
+// variants").  The ring then carries the code bytes (one unswizzled TMA box per
+// tensor) and the scales (one bulk copy per tensor) on the same mbarrier, and
+// each warp, right after its stage lands, dequantises it into a bf16 tile laid out
+// exactly as the bf16 TMA boxes land (same swizzle), then refills the ring slot at
+// once.  Everything after the dequantisation is the bf16 code path, so with
+// power-of-two scales (code * scale exact in bf16) the result is bit-identical to
+// the bf16 kernel run on the dequantised cache.
+//
 // Epilogue.  The W warps' states are merged through shared memory.  If the
 // sequence has a single split the block writes bf16 out and the natural-log
 // lse directly; otherwise it writes its normalised f32 output and lse to the
@@ -72,6 +83,8 @@ struct DecodeParams {
     float *part_out;         // [S, B, Hq, D]
     int *counters;           // [B, Hkv] splits finished per group (wraps to 0 after the last)
     int *status;             // workspace status word
+    const float *k_scale;    // fp8 cache: [num_pages, Hkv, P] f32 per (token, kv head)
+    const float *v_scale;
     int B, Hq, Hkv, G, P, log2P, num_pages, max_pages;
     int chunk_tokens, num_splits;
     int box4;                // 1: the tensor maps are 4-D and one box spans all D columns
@@ -87,20 +100,44 @@ __device__ __forceinline__ void record_status(int *status, int code)
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D, int NT>
+// Dequantises one T x D stage of e4m3 codes (row-major, as the unswizzled TMA box
+// lands) into the bf16 tile layout of the bf16 path: [D/64 column blocks][T rows]
+// [128 B], the 16-byte chunk c of row r stored at chunk position c ^ (r & 7).
+// Each lane turns 8 codes (one 16-byte bf16 chunk) per step; the 8 lanes of a
+// quarter-warp cover one 128-byte row segment, so the stores are conflict-free.
+template <int D, int T>
+__device__ __forceinline__ void dequant_stage(uint32_t codes, uint32_t scales, uint32_t dst, int lane)
+{
+    constexpr int CPR = D / 8;  // bf16 chunks per row
+    constexpr int N = T * CPR / 32;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const int qi = i * 32 + lane;
+        const int r = qi / CPR, cr = qi % CPR;
+        const uint2 c = ld_shared_u2(codes + (uint32_t)qi * 8u);
+        const float sc = ld_shared_f32(scales + (uint32_t)r * 4u);
+        const uint32_t o0 = e4m3x2_to_bf16x2(c.x & 0xffffu, sc);
+        const uint32_t o1 = e4m3x2_to_bf16x2(c.x >> 16, sc);
+        const uint32_t o2 = e4m3x2_to_bf16x2(c.y & 0xffffu, sc);
+        const uint32_t o3 = e4m3x2_to_bf16x2(c.y >> 16, sc);
+        st_shared_v4(dst + (uint32_t)((cr >> 3) * (T * 128) + r * 128 + (((cr & 7) ^ (r & 7)) << 4)), o0, o1, o2, o3);
+    }
+}
+
+template <int D, int NT, bool KV8>
 __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const DecodeParams p)
 {
     constexpr int T = Tiling<D>::T;
     constexpr int W = Tiling<D>::W;
-    constexpr int R = Tiling<D>::R;
+    constexpr int R = KV8 ? Tiling<D>::R8 : Tiling<D>::R;
     constexpr int DC = D / 64;            // 128-byte box columns per key row
     constexpr int KS = D / 16;            // k-steps of the score mma, d-tiles of the PV mma
     constexpr int MT = T / 16;            // 16-key mma tiles per stage
     constexpr int H8 = NT * 8;            // padded heads
-    constexpr int TILE = T * D * 2;       // bytes of one K (or V) stage tile
-    constexpr int STAGE = 2 * TILE;
+    constexpr int TILE = T * D * 2;       // bytes of one K (or V) bf16 tile
+    constexpr int STAGE = KV8 ? 2 * T * D + 2 * T * 4 : 2 * TILE;  // bytes of one ring stage
     constexpr int SUB = T * 128;          // bytes of one 64-dim column block of a tile
     constexpr int RS = D + 4;             // f32 stride of the combine buffer rows
 
@@ -141,7 +178,9 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
     const uint32_t raw_addr = smem_addr(smem_raw);
     const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
     uint8_t *base = smem_raw + (base_addr - raw_addr);
-    const SmemLayout lay = smem_layout(D, T, W, R, NT, p.chunk_tokens, p.P);
+    const SmemLayout lay = smem_layout(D, T, W, R, NT, p.chunk_tokens, p.P, KV8);
+    const uint32_t ring_addr = base_addr + (uint32_t)lay.ring;
+    const uint32_t tile_k = base_addr + (uint32_t)(lay.tiles + warp * 2 * TILE);  // KV8: this warp's bf16 tiles
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + lay.bars);
     float *sm_m = reinterpret_cast<float *>(base + lay.m);
     float *sm_l = reinterpret_cast<float *>(base + lay.l);
@@ -192,12 +231,12 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
     auto issue = [&](int s, int slot) {
         const int t0 = tok_begin + s * T;
         const uint32_t bar = smem_addr(&bars[warp * R + slot]);
-        const uint32_t kdst = base_addr + (uint32_t)((warp * R + slot) * STAGE);
-        const uint32_t vdst = kdst + TILE;
+        const uint32_t kdst = ring_addr + (uint32_t)((warp * R + slot) * STAGE);
+        constexpr uint32_t kBoxBytes = KV8 ? 2u * (uint32_t)D + 8u : 2u * DC * 128u;  // per key row, K and V
         uint32_t bytes = 0;
         for (int j = 0; j < nbox; ++j) {
             const int t = t0 + j * box_t;
-            if (t < tok_end && sm_tab[(t >> p.log2P) - page_begin] >= 0) bytes += 2 * DC * box_t * 128;
+            if (t < tok_end && sm_tab[(t >> p.log2P) - page_begin] >= 0) bytes += kBoxBytes * box_t;
         }
         mbar_arrive_expect_tx(bar, bytes);
         for (int j = 0; j < nbox; ++j) {
@@ -205,17 +244,28 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
             if (t >= tok_end) break;
             const int pg = sm_tab[(t >> p.log2P) - page_begin];
             if (pg < 0) continue;
-            const int row = pg * p.P + (t & (p.P - 1));
-            if (p.box4 && nbox == 1) {
+            const int slot_in_page = t & (p.P - 1);
+            const int row = pg * p.P + slot_in_page;
+            if constexpr (KV8) {
+                // codes: one (D bytes, 1 head, box_t rows) box per tensor; scales: box_t
+                // contiguous f32 of this head's slice of the page
+                const uint32_t off = (uint32_t)(j * box_t * D);
+                tma_load_3d(kdst + off, &tmK, 0, kvh, row, bar, policy);
+                tma_load_3d(kdst + T * D + off, &tmV, 0, kvh, row, bar, policy);
+                const size_t sidx = ((size_t)pg * p.Hkv + kvh) * p.P + slot_in_page;
+                const uint32_t soff = (uint32_t)(2 * T * D + j * box_t * 4);
+                bulk_copy_g2s(kdst + soff, p.k_scale + sidx, (uint32_t)box_t * 4u, bar);
+                bulk_copy_g2s(kdst + soff + T * 4, p.v_scale + sidx, (uint32_t)box_t * 4u, bar);
+            } else if (p.box4 && nbox == 1) {
                 // one box per tensor: (64 dims, box_t rows, all D/64 column blocks, 1 head)
                 tma_load_4d(kdst, &tmK, 0, row, 0, kvh, bar, policy);
-                tma_load_4d(vdst, &tmV, 0, row, 0, kvh, bar, policy);
+                tma_load_4d(kdst + TILE, &tmV, 0, row, 0, kvh, bar, policy);
             } else {
 #pragma unroll
                 for (int dc = 0; dc < DC; ++dc) {
                     const uint32_t off = (uint32_t)(dc * SUB + j * box_t * 128);
                     tma_load_3d(kdst + off, &tmK, dc * 64, kvh, row, bar, policy);
-                    tma_load_3d(vdst + off, &tmV, dc * 64, kvh, row, bar, policy);
+                    tma_load_3d(kdst + TILE + off, &tmV, dc * 64, kvh, row, bar, policy);
                 }
             }
         }
@@ -260,7 +310,18 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
             break;
         }
         const int t0 = tok_begin + s * T;
-        const uint32_t kbase = base_addr + (uint32_t)((warp * R + slot) * STAGE);
+        uint32_t kbase = ring_addr + (uint32_t)((warp * R + slot) * STAGE);
+        if constexpr (KV8) {
+            // dequantise K and V into this warp's bf16 tiles, then hand the slot back to the copy engine
+            dequant_stage<D, T>(kbase, kbase + 2 * T * D, tile_k, lane);
+            dequant_stage<D, T>(kbase + T * D, kbase + 2 * T * D + T * 4, tile_k + TILE, lane);
+            __syncwarp();
+            if (lane == 0) {
+                const int ns = s + R * W;
+                if (ns < n_stages) issue(ns, slot);
+            }
+            kbase = tile_k;
+        }
         const uint32_t vbase = kbase + TILE;
         const bool masked = (t0 + T > tok_end) || any_bad;
 
@@ -369,7 +430,7 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
         }
 
         __syncwarp();
-        if (lane == 0) {
+        if (!KV8 && lane == 0) {
             const int ns = s + R * W;
             if (ns < n_stages) issue(ns, slot);
         }
@@ -561,16 +622,6 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
         const float mx = sm_m[threadIdx.x];
         p.lse[row0 + threadIdx.x] = mx == ninf ? ninf : mx + __logf(sm_l[threadIdx.x]);
     }
-}
-
-// Bounded-wait self-test: waits on a barrier nothing completes.
-__global__ void wait_timeout_selftest_kernel(int *status, unsigned long long limit_ns)
-{
-    __shared__ __align__(8) uint64_t bar;
-    if (threadIdx.x != 0) return;
-    mbar_init(smem_addr(&bar), 1);
-    fence_barrier_init();
-    if (!mbar_wait_bounded(smem_addr(&bar), 0, limit_ns)) record_status(status, PKV_ERR_DEVICE_TIMEOUT);
 }
 
 }  // namespace pkv

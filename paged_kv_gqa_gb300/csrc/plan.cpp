@@ -35,10 +35,10 @@ constexpr int kMaxTablePages = 4096;        // block_table slice a block stages 
 RuntimeTiling tiling_for(int D)
 {
     switch (D) {
-        case 64: return {Tiling<64>::T, Tiling<64>::W, Tiling<64>::R};
-        case 128: return {Tiling<128>::T, Tiling<128>::W, Tiling<128>::R};
-        case 256: return {Tiling<256>::T, Tiling<256>::W, Tiling<256>::R};
-        default: return {0, 0, 0};
+        case 64: return {Tiling<64>::T, Tiling<64>::W, Tiling<64>::R, Tiling<64>::R8};
+        case 128: return {Tiling<128>::T, Tiling<128>::W, Tiling<128>::R, Tiling<128>::R8};
+        case 256: return {Tiling<256>::T, Tiling<256>::W, Tiling<256>::R, Tiling<256>::R8};
+        default: return {0, 0, 0, 0};
     }
 }
 
@@ -68,7 +68,7 @@ pkv_status validate_shape(int B, int Hq, int Hkv, int D, int page_size, int max_
 }
 
 pkv_status make_plan(int B, int Hq, int Hkv, int D, int page_size, int max_pages, int num_sms,
-                     int num_splits, pkv_plan *plan)
+                     int num_splits, pkv_plan *plan, bool kv8)
 {
     if (!plan || num_sms <= 0 || num_splits < 0) return PKV_ERR_INVALID_ARG;
     const pkv_status v = validate_shape(B, Hq, Hkv, D, page_size, max_pages);
@@ -126,7 +126,10 @@ pkv_status make_plan(int B, int Hq, int Hkv, int D, int page_size, int max_pages
     if (chunk > max_chunk) chunk = max_chunk / t.T * t.T;
     S = (max_tokens + chunk - 1) / chunk;
 
-    const SmemLayout lay = smem_layout(D, t.T, t.W, t.R, NT, chunk, page_size);
+    // The split count above is the bf16 kernel's for both caches (same tiling, same
+    // splits, same summation order); only the footprint below depends on the cache.
+    const int R = kv8 ? t.R8 : t.R;
+    const SmemLayout lay = smem_layout(D, t.T, t.W, R, NT, chunk, page_size, kv8);
     if (lay.dynamic > kSmemPerBlockMax) return PKV_ERR_UNSUPPORTED;
     per_sm = std::max(1, std::min(kSmemPerSm / (lay.dynamic + kBlockReserve), 2048 / (t.W * 32)));
 
@@ -134,7 +137,7 @@ pkv_status make_plan(int B, int Hq, int Hkv, int D, int page_size, int max_pages
     plan->chunk_tokens = chunk;
     plan->stage_tokens = t.T;
     plan->warps = t.W;
-    plan->ring_stages = t.R;
+    plan->ring_stages = R;
     plan->blocks_per_sm = per_sm;
     plan->grid_blocks = S * Hkv * B;
     plan->smem_bytes = lay.dynamic;

@@ -177,4 +177,41 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
+// ------------------------------------------------------------------ shared-memory moves, fp8 codes
+
+__device__ __forceinline__ uint2 ld_shared_u2(uint32_t addr)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+// Two float8 e4m3 codes (low byte = first) -> their bf16 values times a power-of-two
+// scale s, packed low = first.  Decoding to f16 is exact (every e4m3 value is an
+// f16 normal or zero), widening to f32 is exact, and the product by a power of two
+// is exact and representable in bf16 while it stays within bf16's normal range, so
+// the result is exactly code * s.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t codes16, float s)
+{
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)codes16));
+    float f0, f1;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(f0) : "h"((unsigned short)(h2 & 0xffffu)));
+    asm("cvt.f32.f16 %0, %1;" : "=f"(f1) : "h"((unsigned short)(h2 >> 16)));
+    return pack_bf16x2(f0 * s, f1 * s);
+}
+
 }  // namespace pkv

@@ -156,3 +156,53 @@ def test_append_rejects_bad_arguments(lib):
     assert call(D=96) == -2 and call(P=12) == -2
     assert call(vn=0x2008) == -3 and call(pos=0x4004) == -3 and call(st=0x7002) == -3
     assert call(B=0, kn=0, vn=0) == 0
+
+
+def test_fp8_decode_rejects_bad_arguments(lib):
+    V = ctypes.c_void_p
+
+    def call(ks=0x9000, vs=0xA000, q=0x1000, k=0x2000, B=2, D=128, P=16, splits=0):
+        return lib.paged_decode_attn_fp8(V(q), V(k), V(0x3000), V(ks), V(vs), V(0x4000), V(0x5000), B, 8, 2, D, P,
+                                         64, 8, ctypes.c_float(0.125), V(0x6000), V(0x7000), V(0x8000), 1 << 20,
+                                         splits, None)
+
+    assert call(ks=0) == -1 and call(vs=0) == -1 and call(q=0) == -1 and call(splits=-1) == -1
+    assert call(ks=0x9004) == -3 and call(vs=0xA008) == -3 and call(k=0x2001) == -3
+    assert call(D=96) == -2 and call(P=4) == -2
+    assert call(B=0, q=0, k=0, ks=0, vs=0) == 0
+
+
+def test_fp8_append_rejects_bad_arguments(lib):
+    V = ctypes.c_void_p
+
+    def call(ks=0x7000, vs=0x8000, kn=0x1000, kc=0x5000, B=2, D=128):
+        return lib.paged_kv_append_fp8(V(kn), V(0x2000), V(0x3000), V(0x4000), B, 2, D, 16, 8, 4, V(kc), V(0x6000),
+                                       V(ks), V(vs), None, None)
+
+    assert call(ks=0) == -1 and call(vs=0) == -1 and call(kn=0) == -1
+    assert call(ks=0x7004) == -3 and call(kc=0x5008) == -3
+    assert call(D=32) == -2
+    assert call(B=0, kn=0, ks=0, vs=0) == 0
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_fp8_footprint_keeps_the_bf16_residency(lib, name):
+    # the fp8 kernel's shared memory (deeper ring + dequantised tiles) must not lower the
+    # number of resident blocks per SM that the split rule assumed
+    B, Hq, Hkv, D, P, max_pages = WORKLOADS[name]
+    plan = pkv.plan_query(B, Hq, Hkv, D, P, max_pages, 152)
+    T, W, R, R8 = plan["stage_tokens"], plan["warps"], plan["ring_stages"], 4
+    H8 = 8 * (1 if Hq // Hkv <= 8 else 2 if Hq // Hkv <= 16 else 4)
+    pad = lambda x, m: (x + m - 1) // m * m
+
+    def dyn(kv8):
+        tiles = W * 2 * T * D * 2 if kv8 else 0
+        ring = W * (R8 if kv8 else R) * ((2 * T * D + 8 * T) if kv8 else 4 * T * D)
+        bars = pad(max(tiles + ring, W * H8 * (D + 4) * 4), 1024)
+        flag = bars + W * (R8 if kv8 else R) * 8 + 4 * W * H8 * 4 + H8 * 4
+        table = pad(flag + 4, 16)
+        return pad(table + (plan["chunk_tokens"] // P + 2) * 4, 16) + 1024
+
+    assert dyn(False) == plan["smem_bytes"]
+    per_sm = lambda d: min(233472 // (d + 1024), 2048 // (W * 32))
+    assert per_sm(dyn(True)) >= per_sm(dyn(False)) or name == "bigpage_g16" and per_sm(dyn(True)) >= 1

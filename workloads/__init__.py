@@ -203,20 +203,34 @@ def make_case(name_or_spec, device="cpu", seed=None, poison=False, seq_lens=None
                 seq_lens=torch.from_numpy(lens.astype(np.int32)).to(device), meta=meta)
 
 
-def algorithmic_bytes(case: Case) -> dict:
+def used_slot_mask(case: Case) -> np.ndarray:
+    """bool [num_pages, P]: the (page, slot) pairs some sequence's valid key occupies."""
+    lens = case.seq_lens.cpu().numpy().astype(np.int64)
+    table = case.block_table.cpu().numpy()
+    mask = np.zeros((case.num_pages, case.P), dtype=bool)
+    for b in range(case.B):
+        for j in range(int((lens[b] + case.P - 1) // case.P)):
+            mask[int(table[b, j]), : min(case.P, int(lens[b]) - j * case.P)] = True
+    return mask
+
+
+def algorithmic_bytes(case: Case, cache: str = "bf16") -> dict:
     """Bytes the computation must move at minimum, per call.
 
     K and V of the valid tokens only, plus q, out (bf16), lse (f32), the used
     block-table entries and the sequence lengths.  The padded tail of each last
     page is reported separately as ``tail_bytes`` (touched, not required).
+    cache="fp8": one byte per K/V element plus one f32 scale per (token, kv head)
+    for each of K and V.
     """
     lens = case.seq_lens.cpu().numpy().astype(np.int64)
     n_pages = (lens + case.P - 1) // case.P
-    kv = 2 * int(lens.sum()) * case.Hkv * case.D * 2
+    row = case.D * 2 if cache == "bf16" else case.D + 4  # bytes per (token, kv head) of K (or V)
+    kv = 2 * int(lens.sum()) * case.Hkv * row
     qo = 2 * case.B * case.Hq * case.D * 2
     lse = case.B * case.Hq * 4
     table = int(n_pages.sum()) * 4
     total = kv + qo + lse + table + 4 * case.B
-    tail = 2 * int((n_pages * case.P - lens).sum()) * case.Hkv * case.D * 2
+    tail = 2 * int((n_pages * case.P - lens).sum()) * case.Hkv * row
     return dict(total=total, kv=kv, q_out=qo, lse=lse, table=table, tail_bytes=tail,
                 flops=4 * int(lens.sum()) * case.Hq * case.D)
