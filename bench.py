@@ -272,8 +272,10 @@ def run_pkv(args) -> None:
         torch.cuda.empty_cache()
     ab = algorithmic_bytes(case, cache=args.cache)
     props = torch.cuda.get_device_properties(dev)
-    plan = pkv.plan_query(case.B, case.Hq, case.Hkv, case.D, case.P, case.max_pages, props.multi_processor_count)
-    ws_bytes = pkv.paged_decode_attn_workspace_size(case.B, case.Hq, case.Hkv, case.D, case.P, case.max_pages)
+    plan = pkv.plan_query(case.B, case.Hq, case.Hkv, case.D, case.P, case.max_pages, props.multi_processor_count,
+                          cache=args.cache)
+    ws_bytes = pkv.paged_decode_attn_workspace_size(case.B, case.Hq, case.Hkv, case.D, case.P, case.max_pages,
+                                                    cache=args.cache)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
     out = torch.empty((case.B, case.Hq, case.D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((case.B, case.Hq), dtype=torch.float32, device=dev)

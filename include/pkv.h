@@ -107,6 +107,20 @@ typedef struct {
 PKV_API pkv_status pkv_plan_query(int B, int Hq, int Hkv, int D, int page_size, int max_pages,
                           int num_sms, int num_splits, pkv_plan *plan /* host */);
 
+/* KV cache element types. */
+enum pkv_kv_dtype {
+    PKV_KV_BF16 = 0,      /* bf16 pools (paged_decode_attn*) */
+    PKV_KV_FP8_E4M3 = 1   /* e4m3 codes + f32 scales (paged_decode_attn_fp8) */
+};
+
+/*
+ * pkv_plan_query for either cache type: the fp8-cache kernel has its own
+ * shared-memory footprint and residency, hence its own split count and
+ * workspace size.  kv_dtype other than the two above: PKV_ERR_INVALID_ARG.
+ */
+PKV_API pkv_status pkv_plan_query_kv(int B, int Hq, int Hkv, int D, int page_size, int max_pages, int num_sms,
+                                     int num_splits, int kv_dtype, pkv_plan *plan);
+
 /*
  * Workspace bytes that paged_decode_attn needs for this shape on `device`
  * (queries the device's SM count).  The workspace holds a 256-byte header whose
@@ -123,6 +137,12 @@ PKV_API pkv_status paged_decode_attn_workspace_size(int B, int Hq, int Hkv, int 
 PKV_API pkv_status paged_decode_attn_workspace_size_ex(int B, int Hq, int Hkv, int D, int page_size,
                                                int max_pages, int device, int num_splits,
                                                size_t *bytes /* host */);
+
+/* Workspace bytes for either cache type (see pkv_plan_query_kv); the fp8 call needs
+ * the PKV_KV_FP8_E4M3 size. */
+PKV_API pkv_status paged_decode_attn_workspace_size_kv(int B, int Hq, int Hkv, int D, int page_size,
+                                                       int max_pages, int device, int num_splits, int kv_dtype,
+                                                       size_t *bytes);
 
 /* ------------------------------------------------------------------ decode */
 
@@ -242,21 +262,24 @@ PKV_API pkv_status paged_kv_append(const pkv_bf16 *k_new, const pkv_bf16 *v_new,
  * no infinities, S.1111.111 = NaN, largest finite 448) with one f32 scale per
  * (token, kv head).  The key (value) element used for slot t of page p, kv head
  * g, dim d is
- *     bf16( code(k_cache[p, t, g, d]) * k_scale[p, g, t] )
- * (the product in f32, rounded to bf16).  With power-of-two scales, as
- * paged_kv_append_fp8 writes them, the product is exact, and the result is
- * bit-identical to paged_decode_attn_ex with the same num_splits on a bf16 cache
- * holding those values: the kernel dequantises each stage into the same bf16
- * tile and runs the same code after it, with the same plan (split count, chunk,
- * workspace size) as paged_decode_attn for the shape.
+ *     code(k_cache[p, t, g, d]) * k_scale[p, g, t]
+ * The kernel decodes the codes exactly into f16 and runs the f16 tensor-core
+ * mma with f32 accumulation; the key scale multiplies the score, the value scale
+ * the probability, so any positive finite scale is honoured (the power-of-two
+ * scales paged_kv_append_fp8 writes make code * scale exactly representable in
+ * bf16 as well).  The plan (split count, chunk, workspace size) is
+ * pkv_plan_query_kv's with PKV_KV_FP8_E4M3.  Results match the bf16 kernel run
+ * on a bf16 cache holding code * scale up to the rounding of the probabilities
+ * and the f32 summation order.
  *
  *   k_cache, v_cache  [num_pages, page_size, Hkv, D] uint8 e4m3 codes
  *   k_scale, v_scale  [num_pages, Hkv, page_size] f32 (head-major within a page,
  *                     so one head's scales for a page are contiguous), 16-byte
  *                     aligned
  * Every other argument, the workspace (size from
- * paged_decode_attn_workspace_size_ex with the same num_splits), the status
- * word and the error behaviour are those of paged_decode_attn_ex.  NaN codes
+ * paged_decode_attn_workspace_size_kv with PKV_KV_FP8_E4M3 and the same
+ * num_splits), the status word and the error behaviour are those of
+ * paged_decode_attn_ex.  NaN codes
  * or scales in slots past seq_lens[b] are never used.
  */
 PKV_API pkv_status paged_decode_attn_fp8(const pkv_bf16 *q, const uint8_t *k_cache, const uint8_t *v_cache,

@@ -37,8 +37,11 @@ EXPORTED_SYMBOLS = [
     "pkv_status_string", "pkv_version", "pkv_plan_query", "paged_decode_attn_workspace_size",
     "paged_decode_attn_workspace_size_ex", "paged_decode_attn", "paged_decode_attn_ex", "split_kv_merge",
     "pkv_check_status", "pkv_reset_status", "pkv_selftest_wait_timeout", "paged_decode_attn_static_scratch",
-    "paged_kv_append", "paged_decode_attn_fp8", "paged_kv_append_fp8",
+    "paged_kv_append", "paged_decode_attn_fp8", "paged_kv_append_fp8", "pkv_plan_query_kv",
+    "paged_decode_attn_workspace_size_kv",
 ]
+
+KV_DTYPES = {"bf16": 0, "fp8": 1}
 
 
 class PkvError(RuntimeError):
@@ -87,6 +90,8 @@ def load(path: str = LIB_PATH):
             "paged_decode_attn_static_scratch": (I, [P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, P]),
             "paged_kv_append": (I, [P, P, P, P, I, I, I, I, I, I, P, P, P, P]),
             "paged_decode_attn_fp8": (I, [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, S, I, P]),
+            "pkv_plan_query_kv": (I, [I, I, I, I, I, I, I, I, I, ctypes.POINTER(PkvPlan)]),
+            "paged_decode_attn_workspace_size_kv": (I, [I, I, I, I, I, I, I, I, I, ctypes.POINTER(S)]),
             "paged_kv_append_fp8": (I, [P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
@@ -106,10 +111,10 @@ def status_string(status: int) -> str:
     return load().pkv_status_string(int(status)).decode()
 
 
-def plan_query(B, Hq, Hkv, D, page_size, max_pages, num_sms, num_splits=0) -> dict:
+def plan_query(B, Hq, Hkv, D, page_size, max_pages, num_sms, num_splits=0, cache="bf16") -> dict:
     plan = PkvPlan()
-    _check(load().pkv_plan_query(B, Hq, Hkv, D, page_size, max_pages, num_sms, num_splits, ctypes.byref(plan)),
-           "pkv_plan_query")
+    _check(load().pkv_plan_query_kv(B, Hq, Hkv, D, page_size, max_pages, num_sms, num_splits, KV_DTYPES[cache],
+                                    ctypes.byref(plan)), "pkv_plan_query_kv")
     return plan.as_dict()
 
 
@@ -140,12 +145,14 @@ def _dev_ptr(t, dtype, name, ndim=None):
     return ctypes.c_void_p(t.data_ptr())
 
 
-def paged_decode_attn_workspace_size(B, Hq, Hkv, D, page_size, max_pages, device=None, num_splits=0) -> int:
+def paged_decode_attn_workspace_size(B, Hq, Hkv, D, page_size, max_pages, device=None, num_splits=0,
+                                     cache="bf16") -> int:
     torch = _torch()
     dev = torch.cuda.current_device() if device is None else int(device)
     n = ctypes.c_size_t(0)
-    _check(load().paged_decode_attn_workspace_size_ex(B, Hq, Hkv, D, page_size, max_pages, dev, num_splits,
-                                                      ctypes.byref(n)), "paged_decode_attn_workspace_size")
+    _check(load().paged_decode_attn_workspace_size_kv(B, Hq, Hkv, D, page_size, max_pages, dev, num_splits,
+                                                      KV_DTYPES[cache], ctypes.byref(n)),
+           "paged_decode_attn_workspace_size_kv")
     return n.value
 
 

@@ -84,9 +84,11 @@ MapCache &map_cache()
 //           (64, box_t, D/64, 1) lands a page slice of one head as [D/64][box_t][64];
 //   rank 3: dims (D, Hkv, num_pages*P rows), box (64, 1, box_t): one box per
 //           64-column block (the fallback when the driver refuses the rank-4 view);
-//   rank 8 (fp8 pool, bytes, no swizzle): dims (D, Hkv, num_pages*P rows) with
-//           strides (D B, Hkv*D B), box (D, 1, box_t): a page slice of one head
-//           lands as [box_t][D] codes.
+//   rank 8 (the fp8 pool, bytes): the rank-4 view with INNER = min(D, 128) bytes
+//           per column block: dims (INNER, num_pages*P rows, D/INNER, Hkv), strides
+//           (Hkv*D B, INNER B, D B), box (INNER, box_t, D/INNER, 1), 128-byte
+//           swizzle (64-byte for D = 64): a page slice of one head lands as
+//           [D/INNER][box_t][INNER] codes.
 pkv_status get_pool_map(const void *pool, int num_pages, int P, int Hkv, int D, int box_t, int device, int rank,
                         CUtensorMap *out)
 {
@@ -103,13 +105,15 @@ pkv_status get_pool_map(const void *pool, int num_pages, int P, int Hkv, int D, 
     CUtensorMap m;
     CUresult r;
     if (rank == 8) {
-        const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)num_pages * (cuuint64_t)P};
-        const cuuint64_t strides[2] = {(cuuint64_t)D, (cuuint64_t)Hkv * D};
-        const cuuint32_t box[3] = {(cuuint32_t)D, 1u, (cuuint32_t)box_t};
-        const cuuint32_t estr[3] = {1u, 1u, 1u};
-        r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(pool), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        const int inner = D < 128 ? D : 128;
+        const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)num_pages * (cuuint64_t)P,
+                                    (cuuint64_t)(D / inner), (cuuint64_t)Hkv};
+        const cuuint64_t strides[3] = {(cuuint64_t)Hkv * D, (cuuint64_t)inner, (cuuint64_t)D};
+        const cuuint32_t box[4] = {(cuuint32_t)inner, (cuuint32_t)box_t, (cuuint32_t)(D / inner), 1u};
+        const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+        r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(pool), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, inner == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     } else if (rank == 4) {
         const cuuint64_t dims[4] = {64u, (cuuint64_t)num_pages * (cuuint64_t)P, (cuuint64_t)(D / 64),
                                     (cuuint64_t)Hkv};
@@ -325,6 +329,27 @@ pkv_status paged_decode_attn_workspace_size_ex(int B, int Hq, int Hkv, int D, in
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return PKV_ERR_CUDA;
     pkv_plan plan;
     const pkv_status st = make_plan(B, Hq, Hkv, D, page_size, max_pages, sms, num_splits, &plan);
+    if (st != PKV_OK) return st;
+    *bytes = plan.workspace_bytes;
+    return PKV_OK;
+}
+
+pkv_status pkv_plan_query_kv(int B, int Hq, int Hkv, int D, int page_size, int max_pages, int num_sms,
+                             int num_splits, int kv_dtype, pkv_plan *plan)
+{
+    if (kv_dtype != PKV_KV_BF16 && kv_dtype != PKV_KV_FP8_E4M3) return PKV_ERR_INVALID_ARG;
+    return make_plan(B, Hq, Hkv, D, page_size, max_pages, num_sms, num_splits, plan, kv_dtype == PKV_KV_FP8_E4M3);
+}
+
+pkv_status paged_decode_attn_workspace_size_kv(int B, int Hq, int Hkv, int D, int page_size, int max_pages,
+                                               int device, int num_splits, int kv_dtype, size_t *bytes)
+{
+    if (!bytes || (kv_dtype != PKV_KV_BF16 && kv_dtype != PKV_KV_FP8_E4M3)) return PKV_ERR_INVALID_ARG;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return PKV_ERR_CUDA;
+    pkv_plan plan;
+    const pkv_status st = make_plan(B, Hq, Hkv, D, page_size, max_pages, sms, num_splits, &plan,
+                                    kv_dtype == PKV_KV_FP8_E4M3);
     if (st != PKV_OK) return st;
     *bytes = plan.workspace_bytes;
     return PKV_OK;

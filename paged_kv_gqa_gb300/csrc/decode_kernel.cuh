@@ -47,13 +47,29 @@
 // FP8 cache (KV8).  The pool may instead hold float8 e4m3 codes with one f32
 // scale per (token, kv head), the scales stored [page][kv head][slot] so that a
 // page slice of one head's scales is contiguous (OASR "Kernel Layer", "FP8 KV
-// variants").  The ring then carries the code bytes (one unswizzled TMA box per
-// tensor) and the scales (one bulk copy per tensor) on the same mbarrier, and
-// each warp, right after its stage lands, dequantises it into a bf16 tile laid out
-// exactly as the bf16 TMA boxes land (same swizzle), then refills the ring slot at
-// once.  Everything after the dequantisation is the bf16 code path, so with
-// power-of-two scales (code * scale exact in bf16) the result is bit-identical to
-// the bf16 kernel run on the dequantised cache.
+// variants").  The ring carries the code bytes (one TMA box per tensor, 128B-
+// swizzled like the bf16 tiles; 64B for D = 64) and the scales (one bulk copy per
+// tensor) on the same mbarrier.  The codes go straight from shared memory into the
+// mma fragments: ldmatrix on the code bytes (a b16 view: four codes per lane per
+// 8x8 matrix), one cvt.rn.f16x2.e4m3x2 per code pair (exact: every e4m3 value is an
+// f16), and the f16 mma.  No dequantised copy is written back to shared memory.
+//   - Scores: a lane's four codes from one 16-byte chunk are its k slots
+//     {2t, 2t+1, 2t+8, 2t+9}, so the query columns are permuted the same way within
+//     each 16-wide k step (the same products, in other k slots).  q is held as f16
+//     scaled by 2^eq, eq chosen per block so the group's largest |q| lands in
+//     [2^14, 2^15) (exact for every element within 2^28 of it); the per-key K
+//     scale and 2^-eq fold into the factor that turns scores into log2 units.
+//   - Values: ldmatrix.trans on the code bytes gives a lane two keys x two
+//     adjacent dims; one byte permute makes key pairs per dim, so the PV tile's
+//     rows {g, g+8} are dims {2g, 2g+1} of each 16-dim chunk (only the output
+//     rows' order changes).  The per-key V scale folds into the probabilities:
+//     p * vscale * 2^-Ev, with Ev the running maximum of the scale exponents; a
+//     rise of Ev rescales the accumulators along with the softmax correction, and
+//     the warp's result is multiplied by 2^Ev at the end.  The f32 denominator
+//     normalises the output.
+// The pages' own design dequantises each stage into a served-dtype tile in shared
+// memory; on this part that round trip through shared memory made the fp8 kernel
+// slower than the bf16 one, so the fp8 path reads the codes in place instead.
 //
 // Epilogue.  The W warps' states are merged through shared memory.  If the
 // sequence has a single split the block writes bf16 out and the natural-log
@@ -67,6 +83,7 @@
 
 #include <cuda_bf16.h>
 #include <cstdint>
+#include <type_traits>
 
 #include "plan.h"
 #include "ptx.cuh"
@@ -100,44 +117,42 @@ __device__ __forceinline__ void record_status(int *status, int code)
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Dequantises one T x D stage of e4m3 codes (row-major, as the unswizzled TMA box
-// lands) into the bf16 tile layout of the bf16 path: [D/64 column blocks][T rows]
-// [128 B], the 16-byte chunk c of row r stored at chunk position c ^ (r & 7).
-// Each lane turns 8 codes (one 16-byte bf16 chunk) per step; the 8 lanes of a
-// quarter-warp cover one 128-byte row segment, so the stores are conflict-free.
-template <int D, int T>
-__device__ __forceinline__ void dequant_stage(uint32_t codes, uint32_t scales, uint32_t dst, int lane)
+// Byte offset of 16-byte chunk c (0 .. D/16-1) of row r in one fp8 code tile as the
+// TMA box lands it: [box j][column block][box_t rows][INNER bytes] with INNER =
+// min(D, 128), swizzled like the TMA's 128B (64B when INNER == 64) mode.
+template <int D>
+__device__ __forceinline__ uint32_t code_offset(int r, int c, int log2_box_t)
 {
-    constexpr int CPR = D / 8;  // bf16 chunks per row
-    constexpr int N = T * CPR / 32;
-#pragma unroll
-    for (int i = 0; i < N; ++i) {
-        const int qi = i * 32 + lane;
-        const int r = qi / CPR, cr = qi % CPR;
-        const uint2 c = ld_shared_u2(codes + (uint32_t)qi * 8u);
-        const float sc = ld_shared_f32(scales + (uint32_t)r * 4u);
-        const uint32_t o0 = e4m3x2_to_bf16x2(c.x & 0xffffu, sc);
-        const uint32_t o1 = e4m3x2_to_bf16x2(c.x >> 16, sc);
-        const uint32_t o2 = e4m3x2_to_bf16x2(c.y & 0xffffu, sc);
-        const uint32_t o3 = e4m3x2_to_bf16x2(c.y >> 16, sc);
-        st_shared_v4(dst + (uint32_t)((cr >> 3) * (T * 128) + r * 128 + (((cr & 7) ^ (r & 7)) << 4)), o0, o1, o2, o3);
+    constexpr int INNER = D < 128 ? D : 128;
+    constexpr int CB = D / INNER;
+    constexpr int CPI = INNER / 16;
+    const int cb = c / CPI, cc = c % CPI;
+    int row;
+    if constexpr (CB == 1) {
+        row = r;
+    } else {
+        const int j = r >> log2_box_t, rr = r & ((1 << log2_box_t) - 1);
+        row = ((j * CB + cb) << log2_box_t) + rr;
     }
+    const uint32_t lin = (uint32_t)(row * INNER + cc * 16);
+    constexpr uint32_t kMask = INNER == 128 ? 7u : 3u;
+    return lin ^ (((lin >> 7) & kMask) << 4);
 }
 
 template <int D, int NT, bool KV8>
-__global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
+__global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
     decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const DecodeParams p)
 {
     constexpr int T = Tiling<D>::T;
     constexpr int W = Tiling<D>::W;
-    constexpr int R = KV8 ? Tiling<D>::R8 : Tiling<D>::R;
+    constexpr int R = ring_depth(D, NT, KV8);
     constexpr int DC = D / 64;            // 128-byte box columns per key row
     constexpr int KS = D / 16;            // k-steps of the score mma, d-tiles of the PV mma
     constexpr int MT = T / 16;            // 16-key mma tiles per stage
     constexpr int H8 = NT * 8;            // padded heads
-    constexpr int TILE = T * D * 2;       // bytes of one K (or V) bf16 tile
-    constexpr int STAGE = KV8 ? 2 * T * D + 2 * T * 4 : 2 * TILE;  // bytes of one ring stage
+    constexpr int TILE = KV8 ? T * D : T * D * 2;  // bytes of one K (or V) tile in the ring
+    constexpr int STAGE = 2 * TILE;
     constexpr int SUB = T * 128;          // bytes of one 64-dim column block of a tile
     constexpr int RS = D + 4;             // f32 stride of the combine buffer rows
 
@@ -180,7 +195,7 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
     uint8_t *base = smem_raw + (base_addr - raw_addr);
     const SmemLayout lay = smem_layout(D, T, W, R, NT, p.chunk_tokens, p.P, KV8);
     const uint32_t ring_addr = base_addr + (uint32_t)lay.ring;
-    const uint32_t tile_k = base_addr + (uint32_t)(lay.tiles + warp * 2 * TILE);  // KV8: this warp's bf16 tiles
+    const uint32_t scale_addr = base_addr + (uint32_t)lay.scales;  // KV8: [W*R][K scales T | V scales T]
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + lay.bars);
     float *sm_m = reinterpret_cast<float *>(base + lay.m);
     float *sm_l = reinterpret_cast<float *>(base + lay.l);
@@ -197,16 +212,48 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
     // ---- query fragments (B operand of the score mma): q^T[d, head] --------------
     // Loaded first, so that their latency overlaps the block-table staging below.
     uint32_t qf[KS][NT][2];
+    float score_mul = p.scale_log2;  // KV8: times 2^-eq
+    if constexpr (!KV8) {
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-        const int head = nt * 8 + g;
-        const uint32_t *qp = reinterpret_cast<const uint32_t *>(
-            p.q + ((size_t)b * p.Hq + kvh * G + (head < G ? head : 0)) * D + 2 * cc);
+        for (int nt = 0; nt < NT; ++nt) {
+            const int head = nt * 8 + g;
+            const uint32_t *qp = reinterpret_cast<const uint32_t *>(
+                p.q + ((size_t)b * p.Hq + kvh * G + (head < G ? head : 0)) * D + 2 * cc);
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            qf[ks][nt][0] = head < G ? __ldg(qp + ks * 8) : 0u;
-            qf[ks][nt][1] = head < G ? __ldg(qp + ks * 8 + 4) : 0u;
+            for (int ks = 0; ks < KS; ++ks) {
+                qf[ks][nt][0] = head < G ? __ldg(qp + ks * 8) : 0u;
+                qf[ks][nt][1] = head < G ? __ldg(qp + ks * 8 + 4) : 0u;
+            }
         }
+    } else {
+        // f16, scaled by 2^eq, columns 16ks + 4cc .. +3 in the lane's k slots (see above)
+        uint2 raw[KS][NT];
+        float qmax = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int head = nt * 8 + g;
+            const uint2 *qp = reinterpret_cast<const uint2 *>(
+                p.q + ((size_t)b * p.Hq + kvh * G + (head < G ? head : 0)) * D + 4 * cc);
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                raw[ks][nt] = head < G ? __ldg(qp + ks * 4) : make_uint2(0u, 0u);
+                qmax = fmaxf(qmax, fmaxf(fmaxf(fabsf(bf16_lo(raw[ks][nt].x)), fabsf(bf16_hi(raw[ks][nt].x))),
+                                         fmaxf(fabsf(bf16_lo(raw[ks][nt].y)), fabsf(bf16_hi(raw[ks][nt].y)))));
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, o));
+        const int eq = qmax > 0.f ? max(-126, min(126, 14 - ilog2f(qmax))) : 0;
+        const float qs = exp2i(eq);
+        score_mul = p.scale_log2 * exp2i(-eq);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                const uint2 r = raw[ks][nt];
+                qf[ks][nt][0] = pack_f16x2(bf16_lo(r.x) * qs, bf16_hi(r.x) * qs);
+                qf[ks][nt][1] = pack_f16x2(bf16_lo(r.y) * qs, bf16_hi(r.y) * qs);
+            }
     }
 
     // Stage this split's block-table slice; out-of-range ids become -1.
@@ -232,7 +279,7 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
         const int t0 = tok_begin + s * T;
         const uint32_t bar = smem_addr(&bars[warp * R + slot]);
         const uint32_t kdst = ring_addr + (uint32_t)((warp * R + slot) * STAGE);
-        constexpr uint32_t kBoxBytes = KV8 ? 2u * (uint32_t)D + 8u : 2u * DC * 128u;  // per key row, K and V
+        constexpr uint32_t kBoxBytes = KV8 ? 2u * (uint32_t)D + 8u : 2u * DC * 128u;  // per key row: K, V (+ scales)
         uint32_t bytes = 0;
         for (int j = 0; j < nbox; ++j) {
             const int t = t0 + j * box_t;
@@ -247,15 +294,15 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
             const int slot_in_page = t & (p.P - 1);
             const int row = pg * p.P + slot_in_page;
             if constexpr (KV8) {
-                // codes: one (D bytes, 1 head, box_t rows) box per tensor; scales: box_t
-                // contiguous f32 of this head's slice of the page
+                // codes: one (INNER bytes, box_t rows, D/INNER column blocks, 1 head) box per
+                // tensor; scales: box_t contiguous f32 of this head's slice of the page
                 const uint32_t off = (uint32_t)(j * box_t * D);
-                tma_load_3d(kdst + off, &tmK, 0, kvh, row, bar, policy);
-                tma_load_3d(kdst + T * D + off, &tmV, 0, kvh, row, bar, policy);
+                tma_load_4d(kdst + off, &tmK, 0, row, 0, kvh, bar, policy);
+                tma_load_4d(kdst + TILE + off, &tmV, 0, row, 0, kvh, bar, policy);
                 const size_t sidx = ((size_t)pg * p.Hkv + kvh) * p.P + slot_in_page;
-                const uint32_t soff = (uint32_t)(2 * T * D + j * box_t * 4);
-                bulk_copy_g2s(kdst + soff, p.k_scale + sidx, (uint32_t)box_t * 4u, bar);
-                bulk_copy_g2s(kdst + soff + T * 4, p.v_scale + sidx, (uint32_t)box_t * 4u, bar);
+                const uint32_t sdst = scale_addr + (uint32_t)((warp * R + slot) * (2 * T * 4) + j * box_t * 4);
+                bulk_copy_g2s(sdst, p.k_scale + sidx, (uint32_t)box_t * 4u, bar);
+                bulk_copy_g2s(sdst + T * 4, p.v_scale + sidx, (uint32_t)box_t * 4u, bar);
             } else if (p.box4 && nbox == 1) {
                 // one box per tensor: (64 dims, box_t rows, all D/64 column blocks, 1 head)
                 tma_load_4d(kdst, &tmK, 0, row, 0, kvh, bar, policy);
@@ -297,71 +344,124 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
         return t < tok_end && sm_tab[(t >> p.log2P) - page_begin] >= 0;
     };
 
-    bool failed = false;
-    for (int it = 0;; ++it) {
-        const int s = warp + it * W;
-        if (s >= n_stages) break;
-        const int slot = it % R;
-        const uint32_t parity = (uint32_t)((it / R) & 1);
-        const bool ok = mbar_wait_bounded(smem_addr(&bars[warp * R + slot]), parity, p.wait_limit_ns);
-        if (!__all_sync(0xffffffffu, ok)) {
-            if (lane == 0) record_status(p.status, PKV_ERR_DEVICE_TIMEOUT);
-            failed = true;
-            break;
-        }
-        const int t0 = tok_begin + s * T;
-        uint32_t kbase = ring_addr + (uint32_t)((warp * R + slot) * STAGE);
-        if constexpr (KV8) {
-            // dequantise K and V into this warp's bf16 tiles, then hand the slot back to the copy engine
-            dequant_stage<D, T>(kbase, kbase + 2 * T * D, tile_k, lane);
-            dequant_stage<D, T>(kbase + T * D, kbase + 2 * T * D + T * 4, tile_k + TILE, lane);
-            __syncwarp();
-            if (lane == 0) {
-                const int ns = s + R * W;
-                if (ns < n_stages) issue(ns, slot);
-            }
-            kbase = tile_k;
-        }
-        const uint32_t vbase = kbase + TILE;
-        const bool masked = (t0 + T > tok_end) || any_bad;
+    int ev_run = -126;  // KV8: running maximum of this warp's V-scale exponents
+    // KV8: per-lane ldmatrix offsets within a code tile (the same for K and V and for every
+    // stage): matrix (lane >> 3) of each x4 load covers keys 0-7 / 8-15 of chunks 2kp, 2kp+1
+    uint32_t coff[MT][KS / 2];
+    if constexpr (KV8) {
+        const int log2_box_t = box_t == 8 ? 3 : box_t == 16 ? 4 : 5;  // used for D = 256 only
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int kp = 0; kp < KS / 2; ++kp)
+                coff[mt][kp] = code_offset<D>(mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, 2 * kp + (lane >> 4),
+                                              log2_box_t);
+    }
 
-        // S^T = K q^T
-        float sc[MT][NT][4];
+    // One stage of T keys; MASKED (a compile-time flag) adds the key-validity checks that
+    // only the stages holding a split's tail, or a bad page, need.
+    auto run_stage = [&](auto masked_tag, const int t0, const uint32_t kbase, const int slot) {
+        constexpr bool MASKED = decltype(masked_tag)::value;
+        const uint32_t vbase = kbase + TILE;
+
+        // S^T = K q^T; with few independent tiles the k steps alternate between two
+        // accumulators (two shorter mma chains), otherwise the tiles give the parallelism
+        constexpr bool kTwoChains = MT * NT <= 2;
+        float sc[MT][NT][4], sc2[MT][NT][4];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) sc[mt][nt][e] = 0.f;
+                for (int e = 0; e < 4; ++e) sc[mt][nt][e] = sc2[mt][nt][e] = 0.f;
+        if constexpr (!KV8) {
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
+            for (int ks = 0; ks < KS; ++ks) {
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                const int row = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                const int chunk = (ks & 3) * 2 + (lane >> 4);
-                const uint32_t addr = kbase + (uint32_t)((ks >> 2) * SUB + row * 128 + ((chunk ^ (row & 7)) << 4));
-                uint32_t a0, a1, a2, a3;
-                ldmatrix_x4(addr, a0, a1, a2, a3);
+                for (int mt = 0; mt < MT; ++mt) {
+                    const int row = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                    const int chunk = (ks & 3) * 2 + (lane >> 4);
+                    const uint32_t addr = kbase + (uint32_t)((ks >> 2) * SUB + row * 128 + ((chunk ^ (row & 7)) << 4));
+                    uint32_t a0, a1, a2, a3;
+                    ldmatrix_x4(addr, a0, a1, a2, a3);
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(sc[mt][nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma_bf16_16816((kTwoChains && (ks & 1)) ? sc2[mt][nt] : sc[mt][nt], a0, a1, a2, a3,
+                                       qf[ks][nt][0], qf[ks][nt][1]);
+                }
+            }
+        } else {
+            // each register of an x4 load holds a lane's 4 codes of one chunk: the low pair
+            // goes to k slots 2t, 2t+1, the high pair to 2t+8, 2t+9
+#pragma unroll
+            for (int kp = 0; kp < KS / 2; ++kp) {
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    uint32_t r0, r1, r2, r3;
+                    ldmatrix_x4(kbase + coff[mt][kp], r0, r1, r2, r3);
+                    uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+                    e4m3x4_to_f16x2x2(r0, a0, a2);
+                    e4m3x4_to_f16x2x2(r1, a1, a3);
+                    e4m3x4_to_f16x2x2(r2, c0, c2);
+                    e4m3x4_to_f16x2x2(r3, c1, c3);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        mma_f16_16816(sc[mt][nt], a0, a1, a2, a3, qf[2 * kp][nt][0], qf[2 * kp][nt][1]);
+                        mma_f16_16816(kTwoChains ? sc2[mt][nt] : sc[mt][nt], c0, c1, c2, c3, qf[2 * kp + 1][nt][0],
+                                      qf[2 * kp + 1][nt][1]);
+                    }
+                }
             }
         }
 
-        // scale to log2 units, mask, running max
+        // scale to log2 units (KV8: times the key's scale), mask, running max
+        float kmul[MT][2], vmul[MT][2];
+        float vfac = 1.f;  // KV8: rescale of the accumulators when the V-scale exponent rises
+        if constexpr (KV8) {
+            const uint32_t sb = scale_addr + (uint32_t)((warp * R + slot) * (2 * T * 4));
+            int ev = -126;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int r = mt * 16 + g + 8 * h;
+                    kmul[mt][h] = ld_shared_f32(sb + (uint32_t)r * 4u) * score_mul;
+                    vmul[mt][h] = ld_shared_f32(sb + (uint32_t)(T + r) * 4u);
+                    if (MASKED && !key_valid(t0 + r)) vmul[mt][h] = 0.f;
+                    else ev = max(ev, min(126, ilog2f(vmul[mt][h])));
+                }
+            ev = max(ev, __shfl_xor_sync(0xffffffffu, ev, 4));
+            ev = max(ev, __shfl_xor_sync(0xffffffffu, ev, 8));
+            ev = max(ev, __shfl_xor_sync(0xffffffffu, ev, 16));
+            if (ev > ev_run) {
+                vfac = exp2i(ev_run - ev);
+                ev_run = ev;
+            }
+            const float inv = exp2i(-ev_run);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                vmul[mt][0] *= inv;
+                vmul[mt][1] *= inv;
+            }
+        } else {
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) kmul[mt][0] = kmul[mt][1] = vmul[mt][0] = vmul[mt][1] = p.scale_log2;
+        }
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    float v = sc[mt][nt][e] * p.scale_log2;
-                    if (masked) {
+                    float v = (kTwoChains ? sc[mt][nt][e] + sc2[mt][nt][e] : sc[mt][nt][e]) * kmul[mt][e >> 1];
+                    if (MASKED) {
                         const int t = t0 + mt * 16 + g + ((e >> 1) << 3);
                         if (!key_valid(t)) v = -__int_as_float(0x7f800000);
                     }
                     sc[mt][nt][e] = v;
                 }
         float alpha[NT][2], mref[NT][2];
+        bool rescale = vfac != 1.f;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -379,16 +479,22 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
                 m_run[nt][h2] = m_new;
                 l_run[nt][h2] *= alpha[nt][h2];
                 lt_run[nt][h2] *= alpha[nt][h2];
+                rescale |= alpha[nt][h2] != 1.f;
             }
-#pragma unroll
-        for (int i = 0; i < KS; ++i)
+        // the accumulators change only when a running maximum moved (multiplying by 1 is exact)
+        if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                acc[i][nt][0] *= alpha[nt][0];
-                acc[i][nt][1] *= alpha[nt][1];
-                acc[i][nt][2] *= alpha[nt][0];
-                acc[i][nt][3] *= alpha[nt][1];
+                const float f0 = alpha[nt][0] * vfac, f1 = alpha[nt][1] * vfac;
+#pragma unroll
+                for (int i = 0; i < KS; ++i) {
+                    acc[i][nt][0] *= f0;
+                    acc[i][nt][1] *= f1;
+                    acc[i][nt][2] *= f0;
+                    acc[i][nt][3] *= f1;
+                }
             }
+        }
 
         // O^T += V^T P^T, one 16-key tile at a time
 #pragma unroll
@@ -398,44 +504,116 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
             for (int nt = 0; nt < NT; ++nt) {
                 const float p0 = ex2(sc[mt][nt][0] - mref[nt][0]), p1 = ex2(sc[mt][nt][1] - mref[nt][1]);
                 const float p2 = ex2(sc[mt][nt][2] - mref[nt][0]), p3 = ex2(sc[mt][nt][3] - mref[nt][1]);
-                const uint32_t x0 = pack_bf16x2(p0, p1);
-                const uint32_t x1 = pack_bf16x2(p2, p3);
                 l_run[nt][0] += p0 + p2;
                 l_run[nt][1] += p1 + p3;
-                lt_run[nt][0] += bf16_lo(x0) + bf16_lo(x1);
-                lt_run[nt][1] += bf16_hi(x0) + bf16_hi(x1);
+                uint32_t x0, x1;
+                if constexpr (KV8) {
+                    x0 = pack_f16x2(p0 * vmul[mt][0], p1 * vmul[mt][0]);
+                    x1 = pack_f16x2(p2 * vmul[mt][1], p3 * vmul[mt][1]);
+                } else {
+                    x0 = pack_bf16x2(p0, p1);
+                    x1 = pack_bf16x2(p2, p3);
+                    lt_run[nt][0] += bf16_lo(x0) + bf16_lo(x1);
+                    lt_run[nt][1] += bf16_hi(x0) + bf16_hi(x1);
+                }
                 pb[nt][0] = movmatrix_trans(x0);
                 pb[nt][1] = movmatrix_trans(x1);
             }
+            // invalid keys' V values are zeroed in registers (their probability is 0, and 0 * NaN is NaN)
             uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
-            if (masked) {
+            if (MASKED) {
                 const int t = t0 + mt * 16 + 2 * cc;
                 vm0 = (key_valid(t) ? 0x0000ffffu : 0u) | (key_valid(t + 1) ? 0xffff0000u : 0u);
                 vm1 = (key_valid(t + 8) ? 0x0000ffffu : 0u) | (key_valid(t + 9) ? 0xffff0000u : 0u);
             }
+            if constexpr (!KV8) {
 #pragma unroll
-            for (int md = 0; md < KS; ++md) {
-                const int row = mt * 16 + (lane & 7) + (lane >> 4) * 8;
-                const int chunk = (md & 3) * 2 + ((lane >> 3) & 1);
-                const uint32_t addr = vbase + (uint32_t)((md >> 2) * SUB + row * 128 + ((chunk ^ (row & 7)) << 4));
-                uint32_t a0, a1, a2, a3;
-                ldmatrix_x4_trans(addr, a0, a1, a2, a3);
-                a0 &= vm0;
-                a1 &= vm0;
-                a2 &= vm1;
-                a3 &= vm1;
+                for (int md = 0; md < KS; ++md) {
+                    const int row = mt * 16 + (lane & 7) + (lane >> 4) * 8;
+                    const int chunk = (md & 3) * 2 + ((lane >> 3) & 1);
+                    const uint32_t addr = vbase + (uint32_t)((md >> 2) * SUB + row * 128 + ((chunk ^ (row & 7)) << 4));
+                    uint32_t a0, a1, a2, a3;
+                    ldmatrix_x4_trans(addr, a0, a1, a2, a3);
+                    if (MASKED) {
+                        a0 &= vm0;
+                        a1 &= vm0;
+                        a2 &= vm1;
+                        a3 &= vm1;
+                    }
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[md][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+                    for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(acc[md][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+                }
+            } else {
+                // ldmatrix.trans of the code bytes: a register holds keys (2t, 2t+1) x dims
+                // (2g, 2g+1) of a 16-dim chunk; the byte permute pairs the keys per dim, so
+                // PV rows g, g+8 are dims 2g, 2g+1 of the chunk
+#pragma unroll
+                for (int mp = 0; mp < KS / 2; ++mp) {
+                    uint32_t r0, r1, r2, r3;
+                    ldmatrix_x4_trans(vbase + coff[mt][mp], r0, r1, r2, r3);
+                    uint32_t a0, a1, a2, a3, c0, c1, c2, c3;
+                    e4m3x4_to_f16x2x2(__byte_perm(r0, 0u, 0x3120), a0, a1);
+                    e4m3x4_to_f16x2x2(__byte_perm(r1, 0u, 0x3120), a2, a3);
+                    e4m3x4_to_f16x2x2(__byte_perm(r2, 0u, 0x3120), c0, c1);
+                    e4m3x4_to_f16x2x2(__byte_perm(r3, 0u, 0x3120), c2, c3);
+                    if (MASKED) {
+                        a0 &= vm0;
+                        a1 &= vm0;
+                        a2 &= vm1;
+                        a3 &= vm1;
+                        c0 &= vm0;
+                        c1 &= vm0;
+                        c2 &= vm1;
+                        c3 &= vm1;
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        mma_f16_16816(acc[2 * mp][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+                        mma_f16_16816(acc[2 * mp + 1][nt], c0, c1, c2, c3, pb[nt][0], pb[nt][1]);
+                    }
+                }
             }
         }
+    };
+
+    bool failed = false;
+    for (int it = 0;; ++it) {
+        const int s = warp + it * W;
+        if (s >= n_stages) break;
+        const int slot = it % R;
+        const uint32_t parity = (uint32_t)((it / R) & 1);
+        const bool ok = mbar_wait_bounded(smem_addr(&bars[warp * R + slot]), parity, p.wait_limit_ns);
+        if (!__all_sync(0xffffffffu, ok)) {
+            if (lane == 0) record_status(p.status, PKV_ERR_DEVICE_TIMEOUT);
+            failed = true;
+            break;
+        }
+        const int t0 = tok_begin + s * T;
+        const uint32_t kbase = ring_addr + (uint32_t)((warp * R + slot) * STAGE);
+        if ((t0 + T > tok_end) || any_bad)
+            run_stage(std::true_type{}, t0, kbase, slot);
+        else
+            run_stage(std::false_type{}, t0, kbase, slot);
 
         __syncwarp();
-        if (!KV8 && lane == 0) {
+        if (lane == 0) {
             const int ns = s + R * W;
             if (ns < n_stages) issue(ns, slot);
         }
     }
     (void)failed;
+
+    if constexpr (KV8) {  // back to value units; the f32 denominator normalises
+        const float f = exp2i(ev_run);
+#pragma unroll
+        for (int i = 0; i < KS; ++i)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[i][nt][e] *= f;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) lt_run[nt][0] = l_run[nt][0], lt_run[nt][1] = l_run[nt][1];
+    }
 
     // ---- per-warp finalisation: reduce the denominators over the key rows ----
 #pragma unroll
@@ -467,12 +645,14 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, 1)
     for (int md = 0; md < KS; ++md)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            const int h0 = nt * 8 + 2 * cc, d0 = md * 16 + g;
+            // PV rows g, g+8 are dims g, g+8 of the chunk (bf16) or 2g, 2g+1 (fp8)
+            const int h0 = nt * 8 + 2 * cc;
+            const int d0 = KV8 ? md * 16 + 2 * g : md * 16 + g, d1 = KV8 ? d0 + 1 : d0 + 8;
             float *r0 = red + (warp * H8 + h0) * RS;
             r0[d0] = acc[md][nt][0];
             r0[RS + d0] = acc[md][nt][1];
-            r0[d0 + 8] = acc[md][nt][2];
-            r0[RS + d0 + 8] = acc[md][nt][3];
+            r0[d1] = acc[md][nt][2];
+            r0[RS + d1] = acc[md][nt][3];
         }
     __syncthreads();
 

@@ -13,6 +13,7 @@
 //     that no split becomes a straggler;
 //   - never fewer than kMinSplitTokens keys per split;
 //   - with several waves, the count in [S, 1.5 S] that fills the last wave best.
+// The fp8-cache kernel has its own footprint and residency, so its own split count.
 // Splits that start past a sequence's length exit at once and are ignored by
 // the merge (FlashQuant wiki "CUDA Kernels", paged_decode.cu "Early Exit for
 // Empty Splits").
@@ -35,10 +36,10 @@ constexpr int kMaxTablePages = 4096;        // block_table slice a block stages 
 RuntimeTiling tiling_for(int D)
 {
     switch (D) {
-        case 64: return {Tiling<64>::T, Tiling<64>::W, Tiling<64>::R, Tiling<64>::R8};
-        case 128: return {Tiling<128>::T, Tiling<128>::W, Tiling<128>::R, Tiling<128>::R8};
-        case 256: return {Tiling<256>::T, Tiling<256>::W, Tiling<256>::R, Tiling<256>::R8};
-        default: return {0, 0, 0, 0};
+        case 64: return {Tiling<64>::T, Tiling<64>::W};
+        case 128: return {Tiling<128>::T, Tiling<128>::W};
+        case 256: return {Tiling<256>::T, Tiling<256>::W};
+        default: return {0, 0};
     }
 }
 
@@ -80,11 +81,13 @@ pkv_status make_plan(int B, int Hq, int Hkv, int D, int page_size, int max_pages
     const int max_tokens = max_pages * page_size;
     const int units = std::max(1, B * Hkv);
 
-    // Resident blocks per SM, sized with the largest table slice the auto plan uses.
+    // Resident blocks per SM: the shared-memory limit (sized with the largest table slice
+    // the auto plan uses) or the variant's register budget, whichever is lower.
+    const int R = ring_depth(D, NT, kv8);
     const int cap_tokens = std::max(t.T, (int)(kMaxSplitBytes / (4l * D)) / t.T * t.T);
-    const SmemLayout ref = smem_layout(D, t.T, t.W, t.R, NT, cap_tokens, page_size);
+    const SmemLayout ref = smem_layout(D, t.T, t.W, R, NT, cap_tokens, page_size, kv8);
     int per_sm = std::max(1, kSmemPerSm / (ref.dynamic + kBlockReserve));
-    per_sm = std::min(per_sm, 2048 / (t.W * 32));
+    per_sm = std::min(per_sm, target_blocks(D, NT, kv8));
     const int slots = num_sms * per_sm;
 
     const int max_stage_splits = (max_tokens + t.T - 1) / t.T;
@@ -126,12 +129,9 @@ pkv_status make_plan(int B, int Hq, int Hkv, int D, int page_size, int max_pages
     if (chunk > max_chunk) chunk = max_chunk / t.T * t.T;
     S = (max_tokens + chunk - 1) / chunk;
 
-    // The split count above is the bf16 kernel's for both caches (same tiling, same
-    // splits, same summation order); only the footprint below depends on the cache.
-    const int R = kv8 ? t.R8 : t.R;
     const SmemLayout lay = smem_layout(D, t.T, t.W, R, NT, chunk, page_size, kv8);
     if (lay.dynamic > kSmemPerBlockMax) return PKV_ERR_UNSUPPORTED;
-    per_sm = std::max(1, std::min(kSmemPerSm / (lay.dynamic + kBlockReserve), 2048 / (t.W * 32)));
+    per_sm = std::max(1, std::min(kSmemPerSm / (lay.dynamic + kBlockReserve), target_blocks(D, NT, kv8)));
 
     plan->num_splits = S;
     plan->chunk_tokens = chunk;

@@ -9,42 +9,50 @@
 
 namespace pkv {
 
-// Compile-time tiling of one decode-kernel variant, chosen by head dim D.
-//   T: keys per pipeline stage (a multiple of the 16-row mma tile)
-//   W: consumer warps per block, each streaming its own stages
-//   R: ring depth per warp (stages in flight), bf16 cache
-//   R8: the same for an fp8 cache (stages are half the bytes, so the ring is deeper)
-// The fp8 variant keeps T and W, so that a shape gets the same split count and the
-// same online-softmax tiling with either cache.
-template <int D>
-struct Tiling;
-template <>
-struct Tiling<64> { static constexpr int T = 32, W = 4, R = 3, R8 = 4; };
-template <>
-struct Tiling<128> { static constexpr int T = 16, W = 4, R = 3, R8 = 4; };
-template <>
-struct Tiling<256> { static constexpr int T = 16, W = 4, R = 3, R8 = 4; };
-
-struct RuntimeTiling {
-    int T, W, R, R8;
-};
-RuntimeTiling tiling_for(int D);
-
-// Number of 8-wide head tiles (mma N tiles) for group size G.
-inline int head_tiles(int G) { return G <= 8 ? 1 : (G <= 16 ? 2 : 4); }
-
 #if defined(__CUDACC__)
 #define PKV_HD __host__ __device__ __forceinline__
 #else
 #define PKV_HD inline
 #endif
 
+// Compile-time tiling of one decode-kernel variant, chosen by head dim D.
+//   T: keys per pipeline stage (a multiple of the 16-row mma tile)
+//   W: consumer warps per block, each streaming its own stages
+template <int D>
+struct Tiling;
+template <>
+struct Tiling<64> { static constexpr int T = 32, W = 4; };
+template <>
+struct Tiling<128> { static constexpr int T = 16, W = 4; };
+template <>
+struct Tiling<256> { static constexpr int T = 16, W = 4; };
+
+struct RuntimeTiling {
+    int T, W;
+};
+RuntimeTiling tiling_for(int D);
+
+// Number of 8-wide head tiles (mma N tiles) for group size G.
+inline int head_tiles(int G) { return G <= 8 ? 1 : (G <= 16 ? 2 : 4); }
+
+// Resident blocks per SM a variant is compiled for (its launch bound, so its register
+// budget): the fp8 kernel with one head tile is light enough for three, which hides
+// more latency; D = 256 tiles fill shared memory with one.
+PKV_HD constexpr int target_blocks(int D, int NT, bool kv8) { return D == 256 ? 1 : (kv8 && NT == 1) ? 3 : 2; }
+
+// Ring depth per warp (stages in flight): an fp8 stage is half the bytes of a bf16
+// one, so its ring is twice as deep unless three blocks share the SM.
+PKV_HD constexpr int ring_depth(int D, int NT, bool kv8)
+{
+    return !kv8 ? 3 : target_blocks(D, NT, kv8) >= 3 ? 4 : 6;
+}
+
 // Shared-memory carve-up of one decode block (byte offsets from a 1024-aligned
 // base).  The kernel and the planner both use this, so they cannot disagree.
 struct SmemLayout {
-    int tiles;     // fp8 cache only: W x [K tile | V tile] bf16, the dequantised stage each warp reads
-    int ring;      // W*R stages; bf16: [K tile | V tile], each tile T x D bf16, 128B-swizzled;
-                   // fp8: [K codes T x D | V codes T x D | K scales T f32 | V scales T f32]
+    int ring;      // W*R stages of [K tile | V tile]; bf16: T x D bf16 per tile, 128B-swizzled;
+                   // fp8: T x D e4m3 codes per tile, 128B-swizzled (64B for D = 64)
+    int scales;    // fp8 only: W*R stages of [K scales | V scales], T f32 each
     int bars;      // W*R mbarriers (8 B each)
     int m;         // [W][H8] f32 running max per warp (log2 units)
     int l;         // [W][H8] f32 softmax denominator per warp (sum of the f32 probabilities)
@@ -60,20 +68,20 @@ struct SmemLayout {
 
 PKV_HD int round_up_int(int x, int m) { return (x + m - 1) / m * m; }
 
-// Bytes of one ring stage.
-PKV_HD int stage_bytes(int D, int T, bool kv8) { return kv8 ? 2 * T * D + 2 * T * 4 : 2 * T * D * 2; }
+// Bytes of one ring stage (K and V tiles; a multiple of 1024 for every tiling).
+PKV_HD int stage_bytes(int D, int T, bool kv8) { return kv8 ? 2 * T * D : 2 * T * D * 2; }
 
 PKV_HD SmemLayout smem_layout(int D, int T, int W, int R, int NT, int chunk_tokens, int page_size,
                               bool kv8 = false)
 {
     SmemLayout s;
     const int H8 = NT * 8;
-    const int tiles = kv8 ? W * 2 * T * D * 2 : 0;
     const int ring = W * R * stage_bytes(D, T, kv8);
-    const int red = W * H8 * (D + 4) * 4;  // per-warp f32 accumulators, reuses tiles and ring
-    s.tiles = 0;
-    s.ring = tiles;
-    s.bars = round_up_int(tiles + ring > red ? tiles + ring : red, 1024);
+    const int scales = kv8 ? W * R * 2 * T * 4 : 0;
+    const int red = W * H8 * (D + 4) * 4;  // per-warp f32 accumulators, reuses the ring
+    s.ring = 0;
+    s.scales = ring;
+    s.bars = round_up_int(ring + scales > red ? ring + scales : red, 1024);
     s.m = s.bars + W * R * 8;
     s.l = s.m + W * H8 * 4;
     s.lt = s.l + W * H8 * 4;
@@ -102,8 +110,8 @@ WorkspaceLayout workspace_layout(int S, int B, int Hq, int Hkv, int D);
 // Shape checks shared by every entry point (no CUDA call).
 pkv_status validate_shape(int B, int Hq, int Hkv, int D, int page_size, int max_pages);
 
-// Validates the shape (not pointers) and fills `plan`.  kv8 selects the fp8-cache
-// kernel's footprint; the split count does not depend on it.
+// Validates the shape (not pointers) and fills `plan` for the bf16-cache kernel or,
+// with kv8, the fp8-cache one.
 pkv_status make_plan(int B, int Hq, int Hkv, int D, int page_size, int max_pages, int num_sms,
                      int num_splits, pkv_plan *plan, bool kv8 = false);
 

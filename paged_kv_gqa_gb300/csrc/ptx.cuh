@@ -177,14 +177,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
-// ------------------------------------------------------------------ shared-memory moves, fp8 codes
-
-__device__ __forceinline__ uint2 ld_shared_u2(uint32_t addr)
-{
-    uint2 v;
-    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
-    return v;
-}
+// ------------------------------------------------------------------ fp8 codes, f16 operands
 
 __device__ __forceinline__ float ld_shared_f32(uint32_t addr)
 {
@@ -193,25 +186,48 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr)
     return v;
 }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+// D (16x8 f32) += A (16x16 f16, row) * B (16x8 f16, col)
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1)
 {
-    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Two float8 e4m3 codes (low byte = first) -> their bf16 values times a power-of-two
-// scale s, packed low = first.  Decoding to f16 is exact (every e4m3 value is an
-// f16 normal or zero), widening to f32 is exact, and the product by a power of two
-// is exact and representable in bf16 while it stays within bf16's normal range, so
-// the result is exactly code * s.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t codes16, float s)
+// Four float8 e4m3 codes (byte 0 first) -> their exact values as two f16x2: lo holds
+// codes 0, 1 and hi codes 2, 3 (every e4m3 value is an f16 normal or zero; NaN stays
+// NaN).  The register is split into its halves inside the asm, so no shift is needed.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t x, uint32_t &lo, uint32_t &hi)
 {
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)codes16));
-    float f0, f1;
-    asm("cvt.f32.f16 %0, %1;" : "=f"(f0) : "h"((unsigned short)(h2 & 0xffffu)));
-    asm("cvt.f32.f16 %0, %1;" : "=f"(f1) : "h"((unsigned short)(h2 >> 16)));
-    return pack_bf16x2(f0 * s, f1 * s);
+    asm("{\n\t.reg .b16 c01, c23;\n\t"
+        "mov.b32 {c01, c23}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, c01;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, c23;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(x));
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+{
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// 2^n as a float for n in [-126, 127] (exact); smaller n gives 0.
+__device__ __forceinline__ float exp2i(int n)
+{
+    return n < -126 ? 0.f : __uint_as_float((uint32_t)(n + 127) << 23);
+}
+
+// floor(log2 |x|) for a normal x; 0, subnormals -> -126; Inf/NaN -> 128.
+__device__ __forceinline__ int ilog2f(float x)
+{
+    const int e = (int)((__float_as_uint(x) >> 23) & 0xffu);
+    return e == 0 ? -126 : e - 127;
 }
 
 }  // namespace pkv

@@ -102,11 +102,12 @@ WORKLOADS = {
 }
 
 
+@pytest.mark.parametrize("cache", ["bf16", "fp8"])
 @pytest.mark.parametrize("name", list(WORKLOADS))
 @pytest.mark.parametrize("sms", [148, 152, 160])
-def test_plan_invariants(lib, name, sms):
+def test_plan_invariants(lib, name, sms, cache):
     B, Hq, Hkv, D, P, max_pages = WORKLOADS[name]
-    plan = pkv.plan_query(B, Hq, Hkv, D, P, max_pages, sms)
+    plan = pkv.plan_query(B, Hq, Hkv, D, P, max_pages, sms, cache=cache)
     max_tokens = max_pages * P
     assert plan["chunk_tokens"] % plan["stage_tokens"] == 0
     assert plan["num_splits"] * plan["chunk_tokens"] >= max_tokens
@@ -122,8 +123,8 @@ def test_plan_invariants(lib, name, sms):
         assert plan["workspace_bytes"] == ws
     else:
         assert plan["workspace_bytes"] == 256
-    # a pure function of (shape, SM count)
-    assert pkv.plan_query(B, Hq, Hkv, D, P, max_pages, sms) == plan
+    # a pure function of (shape, SM count, cache type)
+    assert pkv.plan_query(B, Hq, Hkv, D, P, max_pages, sms, cache=cache) == plan
 
 
 def test_plan_splits_long_context_and_not_big_batches(lib):
@@ -186,23 +187,22 @@ def test_fp8_append_rejects_bad_arguments(lib):
 
 
 @pytest.mark.parametrize("name", list(WORKLOADS))
-def test_fp8_footprint_keeps_the_bf16_residency(lib, name):
-    # the fp8 kernel's shared memory (deeper ring + dequantised tiles) must not lower the
-    # number of resident blocks per SM that the split rule assumed
+def test_residency_and_ring_per_cache(lib, name):
+    # bf16: two blocks per SM (one for D = 256), a 3-deep ring; fp8 with one head tile:
+    # three lighter blocks with a 4-deep ring, else two (one) with a 6-deep ring
     B, Hq, Hkv, D, P, max_pages = WORKLOADS[name]
-    plan = pkv.plan_query(B, Hq, Hkv, D, P, max_pages, 152)
-    T, W, R, R8 = plan["stage_tokens"], plan["warps"], plan["ring_stages"], 4
-    H8 = 8 * (1 if Hq // Hkv <= 8 else 2 if Hq // Hkv <= 16 else 4)
-    pad = lambda x, m: (x + m - 1) // m * m
+    b = pkv.plan_query(B, Hq, Hkv, D, P, max_pages, 152)
+    f = pkv.plan_query(B, Hq, Hkv, D, P, max_pages, 152, cache="fp8")
+    one_tile = Hq // Hkv <= 8
+    assert b["blocks_per_sm"] == (1 if D == 256 else 2) and b["ring_stages"] == 3
+    assert f["blocks_per_sm"] == (1 if D == 256 else 3 if one_tile else 2)
+    assert f["ring_stages"] == (4 if f["blocks_per_sm"] == 3 else 6)
+    assert f["blocks_per_sm"] * (f["smem_bytes"] + 1024) <= 233472
+    assert f["stage_tokens"] == b["stage_tokens"] and f["warps"] == b["warps"]
 
-    def dyn(kv8):
-        tiles = W * 2 * T * D * 2 if kv8 else 0
-        ring = W * (R8 if kv8 else R) * ((2 * T * D + 8 * T) if kv8 else 4 * T * D)
-        bars = pad(max(tiles + ring, W * H8 * (D + 4) * 4), 1024)
-        flag = bars + W * (R8 if kv8 else R) * 8 + 4 * W * H8 * 4 + H8 * 4
-        table = pad(flag + 4, 16)
-        return pad(table + (plan["chunk_tokens"] // P + 2) * 4, 16) + 1024
 
-    assert dyn(False) == plan["smem_bytes"]
-    per_sm = lambda d: min(233472 // (d + 1024), 2048 // (W * 32))
-    assert per_sm(dyn(True)) >= per_sm(dyn(False)) or name == "bigpage_g16" and per_sm(dyn(True)) >= 1
+def test_plan_rejects_unknown_kv_dtype(lib):
+    plan = pkv.PkvPlan()
+    assert lib.pkv_plan_query_kv(8, 32, 8, 128, 16, 64, 152, 0, 2, ctypes.byref(plan)) == -1
+    n = ctypes.c_size_t(0)
+    assert lib.paged_decode_attn_workspace_size_kv(8, 32, 8, 128, 16, 64, 0, 0, 7, ctypes.byref(n)) == -1
