@@ -36,15 +36,19 @@ RuntimeTiling tiling_for(int D);
 inline int head_tiles(int G) { return G <= 8 ? 1 : (G <= 16 ? 2 : 4); }
 
 // Resident blocks per SM a variant is compiled for (its launch bound, so its register
-// budget): the fp8 kernel with one head tile is light enough for three, which hides
-// more latency; D = 256 tiles fill shared memory with one.
-PKV_HD constexpr int target_blocks(int D, int NT, bool kv8) { return D == 256 ? 1 : (kv8 && NT == 1) ? 3 : 2; }
+// budget).  Variants with one head tile are light enough for three, which hides more
+// latency; D = 256 bf16 tiles fill shared memory with one block, fp8 ones with two.
+PKV_HD constexpr int target_blocks(int D, int NT, bool kv8)
+{
+    return D == 256 ? ((kv8 && NT <= 2) ? 2 : 1) : NT == 1 ? 3 : 2;
+}
 
-// Ring depth per warp (stages in flight): an fp8 stage is half the bytes of a bf16
-// one, so its ring is twice as deep unless three blocks share the SM.
+// Ring depth per warp (stages in flight), sized so a block's ring fits its share of
+// shared memory: an fp8 stage is half the bytes of a bf16 one.
 PKV_HD constexpr int ring_depth(int D, int NT, bool kv8)
 {
-    return !kv8 ? 3 : target_blocks(D, NT, kv8) >= 3 ? 4 : 6;
+    return D == 256 ? (kv8 ? (target_blocks(D, NT, kv8) == 2 ? 3 : 6) : 3)
+                    : target_blocks(D, NT, kv8) >= 3 ? (kv8 ? 4 : 2) : (kv8 ? 6 : 3);
 }
 
 // Shared-memory carve-up of one decode block (byte offsets from a 1024-aligned

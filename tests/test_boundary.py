@@ -188,16 +188,21 @@ def test_fp8_append_rejects_bad_arguments(lib):
 
 @pytest.mark.parametrize("name", list(WORKLOADS))
 def test_residency_and_ring_per_cache(lib, name):
-    # bf16: two blocks per SM (one for D = 256), a 3-deep ring; fp8 with one head tile:
-    # three lighter blocks with a 4-deep ring, else two (one) with a 6-deep ring
+    # one head tile (G <= 8): three blocks per SM for either cache (bf16 with a 2-deep
+    # ring, fp8 with a 4-deep one); otherwise two; D = 256: one bf16 block (3-deep ring),
+    # two fp8 blocks (3-deep) up to 16 heads per group
     B, Hq, Hkv, D, P, max_pages = WORKLOADS[name]
     b = pkv.plan_query(B, Hq, Hkv, D, P, max_pages, 152)
     f = pkv.plan_query(B, Hq, Hkv, D, P, max_pages, 152, cache="fp8")
-    one_tile = Hq // Hkv <= 8
-    assert b["blocks_per_sm"] == (1 if D == 256 else 2) and b["ring_stages"] == 3
-    assert f["blocks_per_sm"] == (1 if D == 256 else 3 if one_tile else 2)
-    assert f["ring_stages"] == (4 if f["blocks_per_sm"] == 3 else 6)
-    assert f["blocks_per_sm"] * (f["smem_bytes"] + 1024) <= 233472
+    G = Hq // Hkv
+    if D == 256:
+        assert (b["blocks_per_sm"], b["ring_stages"]) == (1, 3)
+        assert (f["blocks_per_sm"], f["ring_stages"]) == ((2, 3) if G <= 16 else (1, 6))
+    else:
+        assert (b["blocks_per_sm"], b["ring_stages"]) == ((3, 2) if G <= 8 else (2, 3))
+        assert (f["blocks_per_sm"], f["ring_stages"]) == ((3, 4) if G <= 8 else (2, 6))
+    for p in (b, f):
+        assert p["blocks_per_sm"] * (p["smem_bytes"] + 1024) <= 233472
     assert f["stage_tokens"] == b["stage_tokens"] and f["warps"] == b["warps"]
 
 
