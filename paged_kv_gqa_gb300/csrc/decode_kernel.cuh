@@ -209,8 +209,22 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
         prefetch_tensor_map(&tmK);
         prefetch_tensor_map(&tmV);
     }
+    // ---- page ids of this warp's first R stages, one per lane, straight from the block
+    // table: the first copies then wait for one table read instead of the whole staging
+    constexpr int kMaxBoxes = T / 8;  // boxes per stage at the smallest page size
+    int first_id = -1;
+    {
+        const int r = lane / nbox, j = lane - r * nbox;
+        const int s0 = warp + r * W;
+        const int t = tok_begin + s0 * T + j * box_t;
+        if (r < R && s0 < n_stages && t < tok_end) {
+            const int pg = p.block_table[(size_t)b * p.max_pages + (t >> p.log2P)];
+            first_id = (unsigned)pg < (unsigned)p.num_pages ? pg : -1;
+        }
+    }
+
     // ---- query fragments (B operand of the score mma): q^T[d, head] --------------
-    // Loaded first, so that their latency overlaps the block-table staging below.
+    // Loaded early, so that their latency overlaps the first copies and the table staging.
     uint32_t qf[KS][NT][2];
     float score_mul = p.scale_log2;  // KV8: times 2^-eq
     if constexpr (!KV8) {
@@ -256,41 +270,24 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
             }
     }
 
-    // Stage this split's block-table slice; out-of-range ids become -1.
-    int bad = 0;
-    for (int i = threadIdx.x; i < page_end - page_begin; i += W * 32) {
-        int pg = p.block_table[(size_t)b * p.max_pages + page_begin + i];
-        if ((unsigned)pg >= (unsigned)p.num_pages) {
-            record_status(p.status, PKV_ERR_BAD_PAGE_INDEX);
-            pg = -1;
-            bad = 1;
-        }
-        sm_tab[i] = pg;
-    }
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < W * R; ++i) mbar_init(smem_addr(&bars[i]), 1);
-        fence_barrier_init();
-    }
-    const bool any_bad = __syncthreads_or(bad) != 0;
-
     // ---- producer: lane 0 of each warp fills that warp's ring ----------------
     const uint64_t policy = l2_policy_evict_first();
-    auto issue = [&](int s, int slot) {
+    // Copies of stage s into ring slot `slot`; ids[j] is the page of box j (-1: not loaded).
+    auto issue_ids = [&](int s, int slot, const int (&ids)[kMaxBoxes]) {
         const int t0 = tok_begin + s * T;
         const uint32_t bar = smem_addr(&bars[warp * R + slot]);
         const uint32_t kdst = ring_addr + (uint32_t)((warp * R + slot) * STAGE);
         constexpr uint32_t kBoxBytes = KV8 ? 2u * (uint32_t)D + 8u : 2u * DC * 128u;  // per key row: K, V (+ scales)
         uint32_t bytes = 0;
-        for (int j = 0; j < nbox; ++j) {
-            const int t = t0 + j * box_t;
-            if (t < tok_end && sm_tab[(t >> p.log2P) - page_begin] >= 0) bytes += kBoxBytes * box_t;
-        }
+#pragma unroll
+        for (int j = 0; j < kMaxBoxes; ++j)
+            if (j < nbox && ids[j] >= 0) bytes += kBoxBytes * box_t;
         mbar_arrive_expect_tx(bar, bytes);
-        for (int j = 0; j < nbox; ++j) {
+#pragma unroll
+        for (int j = 0; j < kMaxBoxes; ++j) {
+            if (j >= nbox || ids[j] < 0) continue;
+            const int pg = ids[j];
             const int t = t0 + j * box_t;
-            if (t >= tok_end) break;
-            const int pg = sm_tab[(t >> p.log2P) - page_begin];
-            if (pg < 0) continue;
             const int slot_in_page = t & (p.P - 1);
             const int row = pg * p.P + slot_in_page;
             if constexpr (KV8) {
@@ -317,12 +314,51 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
             }
         }
     };
-    if (lane == 0) {
-        for (int r = 0; r < R; ++r) {
-            const int s = warp + r * W;
-            if (s < n_stages) issue(s, r);
+    // Later stages take their page ids from the staged table slice.
+    auto issue = [&](int s, int slot) {
+        int ids[kMaxBoxes];
+#pragma unroll
+        for (int j = 0; j < kMaxBoxes; ++j) {
+            const int t = tok_begin + s * T + j * box_t;
+            ids[j] = (j < nbox && t < tok_end) ? sm_tab[(t >> p.log2P) - page_begin] : -1;
+        }
+        issue_ids(s, slot, ids);
+    };
+
+    // Lane 0 of each warp initialises the warp's own barriers and issues its first R stages.
+    {
+        int ids[R][kMaxBoxes];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int j = 0; j < kMaxBoxes; ++j) {
+                const int v = __shfl_sync(0xffffffffu, first_id, (r * nbox + j) & 31);
+                ids[r][j] = j < nbox ? v : -1;
+            }
+        if (lane == 0) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) mbar_init(smem_addr(&bars[warp * R + r]), 1);
+            fence_barrier_init();
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int s0 = warp + r * W;
+                if (s0 < n_stages) issue_ids(s0, r, ids[r]);
+            }
         }
     }
+
+    // Stage this split's block-table slice for the later stages; out-of-range ids become -1.
+    int bad = 0;
+    for (int i = threadIdx.x; i < page_end - page_begin; i += W * 32) {
+        int pg = p.block_table[(size_t)b * p.max_pages + page_begin + i];
+        if ((unsigned)pg >= (unsigned)p.num_pages) {
+            record_status(p.status, PKV_ERR_BAD_PAGE_INDEX);
+            pg = -1;
+            bad = 1;
+        }
+        sm_tab[i] = pg;
+    }
+    const bool any_bad = __syncthreads_or(bad) != 0;
 
     // ---- consumer state -----------------------------------------------------
     float acc[KS][NT][4];
@@ -721,10 +757,9 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
 
     // ---- the last split of this (b, kv head) to finish merges all of them ----------
     // Log-sum-exp merge (FlashQuant wiki "CUDA Kernels", split_k_reduce.cu
-    // "Algorithm"): the weight of split s is exp(lse_s - max_s lse_s).  The
-    // splits are combined in index order whichever block arrives last, so the
-    // result does not depend on scheduling.  atomicInc wraps the per-group
-    // counter back to 0 on the last arrival, ready for the next call.
+    // "Algorithm"): split s is weighted by exp(lse_s - max_s lse_s), reached below by
+    // an online recurrence.  atomicInc wraps the per-group counter back to 0 on the
+    // last arrival, ready for the next call.
     __threadfence();
     __syncthreads();
     int *flag = reinterpret_cast<int *>(base + lay.flag);
@@ -735,33 +770,18 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
     if (!*flag) return;
     __threadfence();
 
+    // One pass over the splits per output element with the online log-sum-exp recurrence
+    // (running maximum m, weight sum w, accumulator a, all rescaled when m rises), so every
+    // split's lse and output loads are in flight together: this merge runs at the tail of
+    // the kernel and is latency-bound.  The splits are combined in index order whichever
+    // block arrives last, so the result does not depend on scheduling.
     const float ninf = -__int_as_float(0x7f800000);
-    for (int h = warp; h < G; h += W) {  // per-head max and weight sum over the splits
-        const float *lp = p.part_lse + row0 + h;
-        float mx = ninf;
-        for (int sidx = lane; sidx < n_chunks; sidx += 32) mx = fmaxf(mx, __ldcg(lp + sidx * rows));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        float wsum = 0.f;
-        if (mx != ninf)
-            for (int sidx = lane; sidx < n_chunks; sidx += 32) wsum += ex2((__ldcg(lp + sidx * rows) - mx) * kLog2e);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
-        if (lane == 0) {
-            sm_m[h] = mx;
-            sm_l[h] = wsum;
-        }
-    }
-    __syncthreads();
-    // Each thread accumulates two float4 columns at once over the splits, eight splits
-    // per unrolled step, so many independent loads are in flight: this merge runs at the
-    // tail of the kernel and is latency-bound.
     constexpr int V4 = D / 4;
     constexpr int NE = 2;
     const int nvec = G * V4;
     for (int e0 = threadIdx.x; e0 < nvec; e0 += NE * W * 32) {
         float4 a[NE];
-        float mxk[NE];
+        float m[NE], wsum[NE];
         const float *lp[NE];
         const float4 *op[NE];
 #pragma unroll
@@ -769,7 +789,8 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
             const int e = e0 + k * W * 32;
             const int h = (e < nvec ? e : 0) / V4, d4 = (e < nvec ? e : 0) - h * V4;
             a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-            mxk[k] = e < nvec ? sm_m[h] : ninf;
+            m[k] = ninf;
+            wsum[k] = 0.f;
             lp[k] = p.part_lse + row0 + h;
             op[k] = reinterpret_cast<const float4 *>(p.part_out + (row0 + h) * D) + d4;
         }
@@ -777,13 +798,17 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
         for (int sidx = 0; sidx < n_chunks; ++sidx) {
 #pragma unroll
             for (int k = 0; k < NE; ++k) {
-                if (mxk[k] == ninf) continue;
-                const float w = ex2((__ldcg(lp[k] + sidx * rows) - mxk[k]) * kLog2e);
+                const float l = __ldcg(lp[k] + sidx * rows);
                 const float4 v = __ldcg(op[k] + sidx * rows * V4);
-                a[k].x += w * v.x;
-                a[k].y += w * v.y;
-                a[k].z += w * v.z;
-                a[k].w += w * v.w;
+                const float m_new = fmaxf(m[k], l);
+                const float mr = m_new == ninf ? 0.f : m_new;  // every split so far empty
+                const float f_old = ex2((m[k] - mr) * kLog2e), f_new = ex2((l - mr) * kLog2e);
+                a[k].x = a[k].x * f_old + v.x * f_new;
+                a[k].y = a[k].y * f_old + v.y * f_new;
+                a[k].z = a[k].z * f_old + v.z * f_new;
+                a[k].w = a[k].w * f_old + v.w * f_new;
+                wsum[k] = wsum[k] * f_old + f_new;
+                m[k] = m_new;
             }
         }
 #pragma unroll
@@ -791,16 +816,13 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
             const int e = e0 + k * W * 32;
             if (e >= nvec) continue;
             const int h = e / V4, d4 = e - h * V4;
-            const float inv = mxk[k] == ninf ? 0.f : 1.f / sm_l[h];
+            const float inv = m[k] == ninf ? 0.f : 1.f / wsum[k];
             uint2 packed;
             packed.x = pack_bf16x2(a[k].x * inv, a[k].y * inv);
             packed.y = pack_bf16x2(a[k].z * inv, a[k].w * inv);
             *reinterpret_cast<uint2 *>(p.out + (row0 + h) * D + 4 * d4) = packed;
+            if (d4 == 0 && p.lse) p.lse[row0 + h] = m[k] == ninf ? ninf : m[k] + __logf(wsum[k]);
         }
-    }
-    if (threadIdx.x < G && p.lse) {
-        const float mx = sm_m[threadIdx.x];
-        p.lse[row0 + threadIdx.x] = mx == ninf ? ninf : mx + __logf(sm_l[threadIdx.x]);
     }
 }
 
