@@ -2,8 +2,11 @@
 
 One step = one call of the whole hot path (plan, page-table walk, TMA page
 gather, scores, online softmax, PV, split epilogue, merge) over one batch of
-seeded synthetic inputs resident in HBM.  L2 is flushed (a 2 x L2-size buffer
-is rewritten) before every timed step, outside the step's event pair.
+seeded synthetic inputs resident in HBM.  L2 is flushed before every timed step,
+outside the step's event pair: a 2 x L2-size buffer is rewritten, then a second
+2 x L2-size buffer is read, so that the step starts with a cold L2 holding clean
+lines only (the flush's own dirty lines are written back before the step, not
+inside it).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--cache bf16|fp8]
                     [--impl pkv|reference]
@@ -76,6 +79,21 @@ def profiled_traffic(workload: str):
         return int(fields["dram_bytes_per_launch"])
     except (KeyError, ValueError):
         return None
+
+
+class L2Flush:
+    """Evicts L2 before a timed step: rewrites a 2 x L2 buffer, then reads a second one,
+    so that no dirty line of the flush is left to be written back inside the step."""
+
+    def __init__(self, torch, dev, l2_bytes):
+        self.torch = torch
+        self.wbuf = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev)
+        self.rbuf = torch.ones(2 * l2_bytes // 4, dtype=torch.float32, device=dev)
+        self.sink = torch.empty(1, dtype=torch.float32, device=dev)
+
+    def fill_(self, v):
+        self.wbuf.fill_(v)
+        self.torch.sum(self.rbuf, dim=0, keepdim=True, out=self.sink)
 
 
 class ClockSampler:
@@ -222,7 +240,8 @@ def _config_block(case, args, plan):
     cfg = {"workload": args.workload, "cache": getattr(args, "cache", "bf16"), "B": case.B, "Hq": case.Hq, "Hkv": case.Hkv, "D": case.D,
            "page_size": case.P, "num_pages": case.num_pages, "max_pages": case.max_pages,
            "seq_lens": {"min": int(lens.min()), "max": int(lens.max()), "sum": int(lens.sum())},
-           "seed": case.meta["seed"], "l2": "flushed before every timed step (2 x L2 bytes rewritten)"}
+           "seed": case.meta["seed"], "l2": "flushed before every timed step: 2 x L2 bytes rewritten, then another 2 x L2 bytes read "
+                 "(cold and clean L2 at the start of the step)"}
     if plan is not None:
         cfg.update({"num_splits": plan["num_splits"], "chunk_tokens": plan["chunk_tokens"],
                     "grid_blocks": plan["grid_blocks"], "blocks_per_sm": plan["blocks_per_sm"]})
@@ -280,7 +299,7 @@ def run_pkv(args) -> None:
     out = torch.empty((case.B, case.Hq, case.D), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((case.B, case.Hq), dtype=torch.float32, device=dev)
     l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
-    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev, l2)
     stream = torch.cuda.current_stream(dev)
     launches_per_call = 1  # the split merge runs inside the decode kernel
 
@@ -453,7 +472,7 @@ def run_append(args) -> None:
     vn = torch.randn(case.B, case.Hkv, case.D, generator=g, device=dev).to(torch.bfloat16)
     pos = (case.seq_lens - 1).to(torch.int32)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev, 128 << 20)
     stream = torch.cuda.current_stream(dev)
     call = lambda: pkv.paged_kv_append(kn, vn, case.block_table, pos, case.k_cache, case.v_cache, status=status,
                                        stream=stream)
