@@ -8,7 +8,8 @@ The arithmetic lives in ``oracle.c`` (plain C, double precision), compiled with
 gcc into ``oracle/_build/liboracle.so`` on first use.  This module only marshals
 numpy arrays into that library.
 
-Functions: ``paged_decode`` (decode attention by the definition), ``merge`` (the
+Functions: ``paged_decode`` (decode attention by the definition), ``paged_prefill``
+(several query rows per request, ragged by ``qo_indptr``, causal or not), ``merge`` (the
 log-sum-exp combine of split partials), ``kv_append`` (the paged cache write), and
 the FP8 KV variant: ``e4m3_value`` / ``e4m3_encode`` (the codec), ``fp8_quantize_rows``
 (power-of-two row scales), ``quantize_pool`` / ``dequantize_pool``,
@@ -75,6 +76,9 @@ def _load():
             lib.oracle_paged_decode_fp8.restype = i
             lib.oracle_paged_decode_fp8.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, i, i,
                                                     ctypes.c_double, p, i, p, p, i]
+            lib.oracle_paged_prefill.restype = i
+            lib.oracle_paged_prefill.argtypes = [p, p, p, p, p, p, p, p, p, p, i, i, i, i, i, i, i, i,
+                                                 ctypes.c_double, i, p, i, p, p, i]
             lib.oracle_kv_append_fp8.restype = i
             lib.oracle_kv_append_fp8.argtypes = [p, p, p, p, i, i, i, i, i, i, p, p, p, p]
             _lib = lib
@@ -294,3 +298,54 @@ def kv_append_fp8(k_new_bits, v_new_bits, block_table, positions, k8, v8, k_scal
     rej = lib.oracle_kv_append_fp8(_ptr(kn), _ptr(vn), _ptr(bt), _ptr(pos), B, Hkv, D, P, num_pages,
                                    bt.shape[1], _ptr(k), _ptr(v), _ptr(ks), _ptr(vs))
     return k, v, ks, vs, rej
+
+
+# ------------------------------------------------------------------ multi-token rows
+
+def paged_prefill(q_bits, qo_indptr, block_table, seq_lens, scale, causal=True, k_bits=None, v_bits=None,
+                  fp8=None, select=None, nthreads=0):
+    """Attention for several query rows per request (ragged by qo_indptr), by the definition.
+
+    q_bits uint16 [total_q, Hq, D]; qo_indptr int32 [B+1]; block_table int32 [B, max_pages];
+    seq_lens int32 [B] (keys per request, the new tokens included).  The cache is either
+    k_bits/v_bits (uint16 bf16 [num_pages, P, Hkv, D]) or fp8 = (k8, v8, k_scale, v_scale).
+    causal: row i of request b (n_b rows, L_b keys) sees keys j <= L_b - n_b + i.
+    select: optional (t, h) pairs.  Returns (out [total_q, Hq, D] or [n, D], lse).
+    """
+    lib = _load()
+    q = _as_bits(q_bits)
+    qo = np.ascontiguousarray(qo_indptr, dtype=np.int32)
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    total_q, Hq, D = q.shape
+    B = sl.shape[0]
+    if qo.shape != (B + 1,):
+        raise ValueError("qo_indptr must be [B+1]")
+    if fp8 is not None:
+        k8, v8, ks, vs = (np.ascontiguousarray(fp8[0], dtype=np.uint8), np.ascontiguousarray(fp8[1], dtype=np.uint8),
+                          np.ascontiguousarray(fp8[2], dtype=np.float32), np.ascontiguousarray(fp8[3], dtype=np.float32))
+        num_pages, P, Hkv, Dk = k8.shape
+        ptrs = (None, None, _ptr(k8), _ptr(v8), _ptr(ks), _ptr(vs))
+    else:
+        k, v = _as_bits(k_bits), _as_bits(v_bits)
+        num_pages, P, Hkv, Dk = k.shape
+        ptrs = (_ptr(k), _ptr(v), None, None, None, None)
+    if Dk != D:
+        raise ValueError("head dims of q and the cache disagree")
+    max_pages = bt.shape[1] if bt.ndim == 2 else 0
+    if select is None:
+        sel, nsel = None, 0
+        out = np.empty((total_q, Hq, D), np.float64)
+        lse = np.empty((total_q, Hq), np.float64)
+    else:
+        pairs = np.asarray(list(select), dtype=np.int64).reshape(-1, 2)
+        sel = np.ascontiguousarray(pairs[:, 0] * Hq + pairs[:, 1], dtype=np.int32)
+        nsel = sel.shape[0]
+        out = np.empty((nsel, D), np.float64)
+        lse = np.empty((nsel,), np.float64)
+    rc = lib.oracle_paged_prefill(_ptr(q), *ptrs, _ptr(qo), _ptr(bt), _ptr(sl), B, Hq, Hkv, D, P, num_pages,
+                                  max_pages, total_q, float(scale), int(bool(causal)),
+                                  _ptr(sel) if sel is not None else None, nsel, _ptr(out), _ptr(lse),
+                                  int(nthreads))
+    _check_rc(rc, "oracle_paged_prefill")
+    return out, lse

@@ -38,6 +38,14 @@
  * out = 0 and lse = -inf; slots past L_b and table entries past the used pages
  * are never read.
  *
+ * Multi-token rows (AstrAI "CUDA Kernels", "Q Scheduling and KV Addressing":
+ * a packed [total_q, Hq, D] query tensor with qo_indptr): request b owns query
+ * rows qo_indptr[b] .. qo_indptr[b+1]-1, n_b of them, and L_b keys.  Reading:
+ * the new tokens are the last n_b positions of the request, so under the causal
+ * mask query row i (0-based within the request) sees keys j <= L_b - n_b + i,
+ * and without the mask all L_b keys; a row that sees no key gives 0 and -inf.
+ * Decode is the case n_b = 1, qo_indptr[b] = b.
+ *
  * FP8 KV variant (OASR "Kernel Layer", "FP8 KV variants"): the cache may hold
  * float8 e4m3 codes with one f32 scale per (token, kv head); the key/value used
  * is then code value * scale, exact in double.  The codec (e4m3_value,
@@ -146,12 +154,15 @@ typedef struct {
     const float *v_scale;        /* same */
     const int32_t *block_table;  /* [B, max_pages] */
     const int32_t *seq_lens;     /* [B] */
+    const int32_t *qo_indptr;    /* [B+1] query rows per request, or NULL: one row per request */
+    int total_q;                 /* query rows (B when qo_indptr is NULL) */
+    int causal;                  /* 1: row i of a request sees keys j <= L - n + i */
     int B, Hq, Hkv, D, P, num_pages, max_pages;
     double scale;
-    const int32_t *sel;          /* optional list of flattened b*Hq+h indices */
+    const int32_t *sel;          /* optional list of flattened row*Hq+h indices */
     int nsel;
-    double *out;                 /* [B, Hq, D] or [nsel, D] when sel != NULL */
-    double *lse;                 /* [B, Hq]    or [nsel]    when sel != NULL */
+    double *out;                 /* [total_q, Hq, D] or [nsel, D] when sel != NULL */
+    double *lse;                 /* [total_q, Hq]    or [nsel]    when sel != NULL */
     int nthreads;
     int error;                   /* set to 1 when a used page id is out of range */
 } decode_args;
@@ -172,14 +183,30 @@ static double kv_elem(const decode_args *a, int is_v, int page, int slot, int g,
     return e4m3_value(code) * (double)s;
 }
 
-/* One output row: the definition above, written out. */
-static int decode_one(const decode_args *a, int b, int h, double *o, double *lse_out)
+/* The request that owns query row t (a linear scan of qo_indptr). */
+static int request_of(const decode_args *a, int t)
+{
+    if (!a->qo_indptr) return t;
+    for (int b = 0; b < a->B; ++b)
+        if (t >= a->qo_indptr[b] && t < a->qo_indptr[b + 1]) return b;
+    return -1;
+}
+
+/* One output row (query row t, head h): the definition above, written out. */
+static int decode_one(const decode_args *a, int t, int h, double *o, double *lse_out)
 {
     const int G = a->Hq / a->Hkv;
     const int g = h / G;
-    const int L = a->seq_lens[b];
+    const int b = request_of(a, t);
     const int D = a->D;
-    const uint16_t *qh = a->q + ((size_t)b * a->Hq + h) * D;
+    const uint16_t *qh = a->q + ((size_t)t * a->Hq + h) * D;
+    if (b < 0) return 1;
+    int L = a->seq_lens[b];
+    if (a->qo_indptr && a->causal) {
+        const int n = a->qo_indptr[b + 1] - a->qo_indptr[b];
+        const int i = t - a->qo_indptr[b];
+        if (L - n + i + 1 < L) L = L - n + i + 1;  /* keys j <= L - n + i */
+    }
 
     if (L <= 0) {
         for (int d = 0; d < D; ++d) o[d] = 0.0;
@@ -228,11 +255,11 @@ static void *decode_worker(void *p)
 {
     worker_arg *w = (worker_arg *)p;
     decode_args *a = w->a;
-    const int n = a->sel ? a->nsel : a->B * a->Hq;
+    const int n = a->sel ? a->nsel : a->total_q * a->Hq;
     for (int i = w->tid; i < n; i += a->nthreads) {
         const int flat = a->sel ? a->sel[i] : i;
-        const int b = flat / a->Hq, h = flat % a->Hq;
-        if (decode_one(a, b, h, a->out + (size_t)i * a->D, a->lse + i))
+        const int t = flat / a->Hq, h = flat % a->Hq;
+        if (decode_one(a, t, h, a->out + (size_t)i * a->D, a->lse + i))
             a->error = 1;  /* benign race: any writer stores 1 */
     }
     return NULL;
@@ -251,6 +278,13 @@ static int run_decode(decode_args *a, int nthreads)
         return 2;
     for (int b = 0; b < a->B; ++b)
         if (a->seq_lens[b] > (long)a->max_pages * a->P) return 2;
+    if (!a->qo_indptr) {
+        a->total_q = a->B;
+    } else {
+        if (a->qo_indptr[0] != 0 || a->qo_indptr[a->B] != a->total_q) return 2;
+        for (int b = 0; b < a->B; ++b)
+            if (a->qo_indptr[b + 1] < a->qo_indptr[b]) return 2;
+    }
     a->nthreads = resolve_threads(nthreads);
 
     pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)a->nthreads);
@@ -307,6 +341,32 @@ int oracle_paged_decode_fp8(const uint16_t *q, const uint8_t *k8, const uint8_t 
     a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.D = D; a.P = P;
     a.num_pages = num_pages; a.max_pages = max_pages; a.scale = scale;
     a.sel = sel; a.nsel = nsel; a.out = out; a.lse = lse;
+    return run_decode(&a, nthreads);
+}
+
+/*
+ * oracle_paged_prefill: several query rows per request (see the header), over a
+ * bf16 cache (k, v non-NULL) or an fp8 one (k8, v8, k_scale, v_scale non-NULL).
+ *   q [total_q, Hq, D] bf16 bits; qo_indptr [B+1] with qo_indptr[0] = 0 and
+ *   qo_indptr[B] = total_q; out [total_q, Hq, D], lse [total_q, Hq] (or the
+ *   selected rows, flattened t*Hq + h).  Return codes as oracle_paged_decode.
+ */
+int oracle_paged_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                         const uint8_t *k8, const uint8_t *v8, const float *k_scale, const float *v_scale,
+                         const int32_t *qo_indptr, const int32_t *block_table, const int32_t *seq_lens,
+                         int B, int Hq, int Hkv, int D, int P, int num_pages, int max_pages, int total_q,
+                         double scale, int causal, const int32_t *sel, int nsel,
+                         double *out, double *lse, int nthreads)
+{
+    decode_args a;
+    memset(&a, 0, sizeof a);
+    a.q = q; a.k = k; a.v = v; a.k8 = k8; a.v8 = v8; a.k_scale = k_scale; a.v_scale = v_scale;
+    a.qo_indptr = qo_indptr; a.total_q = total_q; a.causal = causal;
+    a.block_table = block_table; a.seq_lens = seq_lens;
+    a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.D = D; a.P = P;
+    a.num_pages = num_pages; a.max_pages = max_pages; a.scale = scale;
+    a.sel = sel; a.nsel = nsel; a.out = out; a.lse = lse;
+    if (!qo_indptr) return 2;
     return run_decode(&a, nthreads);
 }
 

@@ -89,6 +89,7 @@ class Case:
     block_table: torch.Tensor  # [B, max_pages] int32
     seq_lens: torch.Tensor     # [B] int32
     meta: dict = field(default_factory=dict)
+    qo_indptr: torch.Tensor = None  # [B+1] int32 for multi-token cases (q is then [total_q, Hq, D])
 
     @property
     def G(self) -> int:
@@ -96,8 +97,9 @@ class Case:
 
     def to(self, device) -> "Case":
         c = Case(**{**self.__dict__})
-        for name in ("q", "k_cache", "v_cache", "block_table", "seq_lens"):
-            setattr(c, name, getattr(self, name).to(device))
+        for name in ("q", "k_cache", "v_cache", "block_table", "seq_lens", "qo_indptr"):
+            if getattr(self, name) is not None:
+                setattr(c, name, getattr(self, name).to(device))
         return c
 
     def host_bits(self):
@@ -234,3 +236,19 @@ def algorithmic_bytes(case: Case, cache: str = "bf16") -> dict:
     tail = 2 * int((n_pages * case.P - lens).sum()) * case.Hkv * row
     return dict(total=total, kv=kv, q_out=qo, lse=lse, table=table, tail_bytes=tail,
                 flops=4 * int(lens.sum()) * case.Hq * case.D)
+
+
+def make_prefill_case(name_or_spec, q_lens, kv_lens=None, device="cpu", seed=None, poison=False, scale=None) -> Case:
+    """A multi-token case: request b has q_lens[b] query rows (packed into q [total_q, Hq, D],
+    qo_indptr [B+1]) over kv_lens[b] cached keys (default: the spec's length rule; the new
+    tokens are counted in kv_lens).  Pool, table and K/V as in make_case."""
+    c = make_case(name_or_spec, device=device, seed=seed, poison=poison, seq_lens=kv_lens, scale=scale)
+    q_lens = np.asarray(q_lens, dtype=np.int64)
+    assert q_lens.shape == (c.B,) and (q_lens >= 0).all()
+    qo = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(c.meta["seed"] + 7919)
+    c.q = _randn_bf16((int(qo[-1]), c.Hq, c.D), gen, device)
+    c.qo_indptr = torch.from_numpy(qo).to(device)
+    c.meta["q_lens"] = q_lens.tolist()
+    return c
