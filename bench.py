@@ -237,14 +237,16 @@ def _reference_sample(case, seconds_hint):
 
 def _config_block(case, args, plan):
     lens = case.seq_lens.cpu().numpy()
-    cfg = {"workload": args.workload, "cache": getattr(args, "cache", "bf16"), "B": case.B, "Hq": case.Hq, "Hkv": case.Hkv, "D": case.D,
+    cfg = {"workload": args.workload, "cache": getattr(args, "cache", "bf16"), "q_len": getattr(args, "q_len", 1),
+           "B": case.B, "Hq": case.Hq, "Hkv": case.Hkv, "D": case.D,
            "page_size": case.P, "num_pages": case.num_pages, "max_pages": case.max_pages,
            "seq_lens": {"min": int(lens.min()), "max": int(lens.max()), "sum": int(lens.sum())},
            "seed": case.meta["seed"], "l2": "flushed before every timed step: 2 x L2 bytes rewritten, then another 2 x L2 bytes read "
                  "(cold and clean L2 at the start of the step)"}
     if plan is not None:
         cfg.update({"num_splits": plan["num_splits"], "chunk_tokens": plan["chunk_tokens"],
-                    "grid_blocks": plan["grid_blocks"], "blocks_per_sm": plan["blocks_per_sm"]})
+                    "grid_blocks": plan["grid_blocks"], "blocks_per_sm": plan["blocks_per_sm"],
+                    "rows_per_block": plan["rows_per_block"], "q_tiles": plan["q_tiles"]})
     return cfg
 
 
@@ -281,7 +283,14 @@ def run_pkv(args) -> None:
     dev = torch.device("cuda", local)
     pkv.load()
 
-    case = make_case(args.workload, device=dev)
+    q_len = getattr(args, "q_len", 1)
+    if q_len > 1:  # several new tokens per sequence (a multi-token decode step)
+        from workloads import CONFIGS, draw_seq_lens, make_prefill_case
+        spec = CONFIGS[args.workload]
+        kv_lens = draw_seq_lens(spec["lens"], spec["B"], spec["P"], spec["seed"])
+        case = make_prefill_case(args.workload, [q_len] * spec["B"], kv_lens, device=dev)
+    else:
+        case = make_case(args.workload, device=dev)
     fp8 = args.cache == "fp8"
     pools8 = None
     if fp8:  # quantise the pools on the device, then drop the bf16 copies
@@ -291,20 +300,32 @@ def run_pkv(args) -> None:
         torch.cuda.empty_cache()
     ab = algorithmic_bytes(case, cache=args.cache)
     props = torch.cuda.get_device_properties(dev)
-    plan = pkv.plan_query(case.B, case.Hq, case.Hkv, case.D, case.P, case.max_pages, props.multi_processor_count,
-                          cache=args.cache)
-    ws_bytes = pkv.paged_decode_attn_workspace_size(case.B, case.Hq, case.Hkv, case.D, case.P, case.max_pages,
-                                                    cache=args.cache)
+    if q_len > 1:
+        total_q = int(case.q.shape[0])
+        plan = pkv.prefill_plan_query(case.B, case.Hq, case.Hkv, case.D, case.P, case.max_pages, total_q, q_len,
+                                      props.multi_processor_count, cache=args.cache)
+        ws_bytes = plan["workspace_bytes"]
+    else:
+        plan = pkv.plan_query(case.B, case.Hq, case.Hkv, case.D, case.P, case.max_pages, props.multi_processor_count,
+                              cache=args.cache)
+        ws_bytes = pkv.paged_decode_attn_workspace_size(case.B, case.Hq, case.Hkv, case.D, case.P, case.max_pages,
+                                                        cache=args.cache)
     ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
-    out = torch.empty((case.B, case.Hq, case.D), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((case.B, case.Hq), dtype=torch.float32, device=dev)
+    rows_q = case.q.shape[0]
+    out = torch.empty((rows_q, case.Hq, case.D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((rows_q, case.Hq), dtype=torch.float32, device=dev)
     l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
     flush = L2Flush(torch, dev, l2)
     stream = torch.cuda.current_stream(dev)
     launches_per_call = 1  # the split merge runs inside the decode kernel
 
     def call():
-        if fp8:
+        if q_len > 1:
+            kc, vc = (pools8[0], pools8[1]) if fp8 else (case.k_cache, case.v_cache)
+            pkv.paged_prefill_attn(case.q, kc, vc, case.qo_indptr, case.block_table, case.seq_lens, q_len, case.scale,
+                                   out, lse, ws, causal=True, stream=stream,
+                                   fp8_scales=(pools8[2], pools8[3]) if fp8 else None)
+        elif fp8:
             pkv.paged_decode_attn_fp8(case.q, *pools8, case.block_table, case.seq_lens, case.scale, out, lse, ws,
                                       stream=stream)
         else:
@@ -344,11 +365,11 @@ def run_pkv(args) -> None:
 
     # ---- end to end through the public API with host buffers -------------------
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and q_len == 1:
         e2e = _e2e(args, case, ab, pkv, torch, dev, stream, flush, plan, dist, pools8)
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and q_len == 1:
         if fp8:
             hc = _host_case(case)
             cpu = _cpu_baseline(hc, args.cpu_seconds, fp8=tuple(t.cpu().numpy() for t in pools8))
@@ -504,6 +525,8 @@ def main():
     ap.add_argument("--workload", default="batch",
                     choices=["tiny", "batch", "ragged", "long", "bigpage", "bigpage_g16", "append"])
     ap.add_argument("--cache", default="bf16", choices=["bf16", "fp8"])
+    ap.add_argument("--q-len", type=int, default=1,
+                    help="new tokens per sequence (causal multi-token step); 1 = decode")
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)

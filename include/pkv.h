@@ -69,7 +69,9 @@ typedef enum {
     PKV_ERR_CUDA = -5,                /* a CUDA runtime/driver call failed */
     PKV_ERR_BAD_PAGE_INDEX = -6,      /* device: a used block_table entry outside [0, num_pages) */
     PKV_ERR_DEVICE_TIMEOUT = -7,      /* device: a bounded wait for a copy ran out */
-    PKV_ERR_BAD_SEQ_LEN = -8          /* device: seq_lens[b] < 0 or > max_pages * page_size */
+    PKV_ERR_BAD_SEQ_LEN = -8,         /* device: seq_lens[b] < 0 or > max_pages * page_size */
+    PKV_ERR_BAD_QO_INDPTR = -9        /* device: a request's query rows outside [0, total_q) or more
+                                         than max_q_len of them */
 } pkv_status;
 
 /* Human-readable name of a status code (static string; never NULL). */
@@ -97,6 +99,8 @@ typedef struct {
     int merge_needed;     /* 1 when S > 1: the last split block of each (b, kv head) merges the
                              partials inside the same kernel launch */
     size_t workspace_bytes;
+    int q_tiles;          /* blocks per (b, kv head) along its query rows (1 for decode) */
+    int rows_per_block;   /* (token, query head) rows one block serves: 8, 16 or 32 */
 } pkv_plan;
 
 /*
@@ -308,6 +312,58 @@ PKV_API pkv_status paged_kv_append_fp8(const pkv_bf16 *k_new, const pkv_bf16 *v_
                                        const int32_t *positions, int B, int Hkv, int D, int page_size,
                                        int num_pages, int max_pages, uint8_t *k_cache, uint8_t *v_cache,
                                        float *k_scale, float *v_scale, int *status, cudaStream_t stream);
+
+/* ------------------------------------------------------------------ several query rows */
+
+/*
+ * Several query rows per sequence: multi-token decode (speculative or
+ * multi-token prediction steps) and chunked paged prefill (AstrAI "CUDA Kernels",
+ * "Q Scheduling and KV Addressing": a packed [total_q, Hq, D] query tensor,
+ * qo_indptr, paged KV, the query heads of one kv-head group sharing each K/V
+ * tile).  Request b owns query rows qo_indptr[b] .. qo_indptr[b+1]-1 (n_b rows)
+ * and seq_lens[b] = L_b keys, the new tokens' keys included (append them first).
+ * The new tokens are the request's last n_b positions: with causal = 1, row i
+ * (0-based within the request) attends to keys j <= L_b - n_b + i; with
+ * causal = 0 to all L_b keys.  A row that sees no key gives out = 0, lse = -inf.
+ *
+ *   q, out      [total_q, Hq, D] bf16;  lse [total_q, Hq] f32 (may be NULL)
+ *   qo_indptr   [B+1] int32 device, qo_indptr[0] = 0, non-decreasing,
+ *               qo_indptr[B] = total_q, every n_b <= max_q_len
+ *   max_q_len   the most rows a request has (sizes the grid: a block serves up to
+ *               32 (token, query head) rows of one kv-head group; see
+ *               pkv_plan_query_prefill's q_tiles)
+ * Everything else as paged_decode_attn_ex (the fp8 form as paged_decode_attn_fp8).
+ * Workspace: paged_prefill_attn_workspace_size.  A request whose row range breaks
+ * the contract is skipped (nothing read or written for it) and
+ * PKV_ERR_BAD_QO_INDPTR is recorded.  Decode is the case qo_indptr[b] = b,
+ * max_q_len = 1.  The K/V stream is read once per query tile, so the path suits
+ * short row counts (decode-like steps, short chunks); long prefills are correct
+ * but re-read K/V once per 32 rows.
+ */
+PKV_API pkv_status paged_prefill_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                                      const int32_t *qo_indptr, const int32_t *block_table,
+                                      const int32_t *seq_lens, int B, int Hq, int Hkv, int D, int page_size,
+                                      int num_pages, int max_pages, int total_q, int max_q_len, int causal,
+                                      float scale, pkv_bf16 *out, float *lse, void *workspace,
+                                      size_t workspace_bytes, int num_splits, cudaStream_t stream);
+
+PKV_API pkv_status paged_prefill_attn_fp8(const pkv_bf16 *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                                          const float *k_scale, const float *v_scale, const int32_t *qo_indptr,
+                                          const int32_t *block_table, const int32_t *seq_lens, int B, int Hq,
+                                          int Hkv, int D, int page_size, int num_pages, int max_pages,
+                                          int total_q, int max_q_len, int causal, float scale, pkv_bf16 *out,
+                                          float *lse, void *workspace, size_t workspace_bytes, int num_splits,
+                                          cudaStream_t stream);
+
+/* The plan of a several-rows call (kv_dtype as pkv_plan_query_kv). */
+PKV_API pkv_status pkv_plan_query_prefill(int B, int Hq, int Hkv, int D, int page_size, int max_pages, int total_q,
+                                          int max_q_len, int num_sms, int num_splits, int kv_dtype,
+                                          pkv_plan *plan);
+
+/* Workspace bytes of a several-rows call on `device`. */
+PKV_API pkv_status paged_prefill_attn_workspace_size(int B, int Hq, int Hkv, int D, int page_size, int max_pages,
+                                                     int total_q, int max_q_len, int device, int num_splits,
+                                                     int kv_dtype, size_t *bytes);
 
 /* ------------------------------------------------------------------ merge */
 

@@ -18,7 +18,8 @@ __all__ = [
     "PkvError", "load", "status_string", "plan_query", "paged_decode_attn_workspace_size",
     "paged_decode_attn", "paged_decode_attn_ex", "split_kv_merge", "pkv_check_status",
     "pkv_reset_status", "pkv_selftest_wait_timeout", "paged_decode_attn_static_scratch", "paged_kv_append",
-    "paged_decode_attn_fp8", "paged_kv_append_fp8", "quantize_pool_fp8",
+    "paged_decode_attn_fp8", "paged_kv_append_fp8", "quantize_pool_fp8", "paged_prefill_attn",
+    "paged_prefill_attn_workspace_size", "prefill_plan_query",
     "EXPORTED_SYMBOLS",
     "STATUS",
 ]
@@ -29,7 +30,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libpkv.so")
 STATUS = {
     0: "PKV_OK", -1: "PKV_ERR_INVALID_ARG", -2: "PKV_ERR_UNSUPPORTED", -3: "PKV_ERR_MISALIGNED",
     -4: "PKV_ERR_WORKSPACE_TOO_SMALL", -5: "PKV_ERR_CUDA", -6: "PKV_ERR_BAD_PAGE_INDEX",
-    -7: "PKV_ERR_DEVICE_TIMEOUT", -8: "PKV_ERR_BAD_SEQ_LEN",
+    -7: "PKV_ERR_DEVICE_TIMEOUT", -8: "PKV_ERR_BAD_SEQ_LEN", -9: "PKV_ERR_BAD_QO_INDPTR",
 }
 
 # Every symbol include/pkv.h declares.
@@ -38,7 +39,8 @@ EXPORTED_SYMBOLS = [
     "paged_decode_attn_workspace_size_ex", "paged_decode_attn", "paged_decode_attn_ex", "split_kv_merge",
     "pkv_check_status", "pkv_reset_status", "pkv_selftest_wait_timeout", "paged_decode_attn_static_scratch",
     "paged_kv_append", "paged_decode_attn_fp8", "paged_kv_append_fp8", "pkv_plan_query_kv",
-    "paged_decode_attn_workspace_size_kv",
+    "paged_decode_attn_workspace_size_kv", "paged_prefill_attn", "paged_prefill_attn_fp8",
+    "pkv_plan_query_prefill", "paged_prefill_attn_workspace_size",
 ]
 
 KV_DTYPES = {"bf16": 0, "fp8": 1}
@@ -54,7 +56,7 @@ class PkvPlan(ctypes.Structure):
     _fields_ = [("num_splits", ctypes.c_int), ("chunk_tokens", ctypes.c_int), ("stage_tokens", ctypes.c_int),
                 ("warps", ctypes.c_int), ("ring_stages", ctypes.c_int), ("blocks_per_sm", ctypes.c_int),
                 ("grid_blocks", ctypes.c_int), ("smem_bytes", ctypes.c_int), ("merge_needed", ctypes.c_int),
-                ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace_bytes", ctypes.c_size_t), ("q_tiles", ctypes.c_int), ("rows_per_block", ctypes.c_int)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -92,6 +94,11 @@ def load(path: str = LIB_PATH):
             "paged_decode_attn_fp8": (I, [P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P, P, P, S, I, P]),
             "pkv_plan_query_kv": (I, [I, I, I, I, I, I, I, I, I, ctypes.POINTER(PkvPlan)]),
             "paged_decode_attn_workspace_size_kv": (I, [I, I, I, I, I, I, I, I, I, ctypes.POINTER(S)]),
+            "paged_prefill_attn": (I, [P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, F, P, P, P, S, I, P]),
+            "paged_prefill_attn_fp8": (I, [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, F, P, P, P, S, I,
+                                           P]),
+            "pkv_plan_query_prefill": (I, [I, I, I, I, I, I, I, I, I, I, I, ctypes.POINTER(PkvPlan)]),
+            "paged_prefill_attn_workspace_size": (I, [I, I, I, I, I, I, I, I, I, I, I, ctypes.POINTER(S)]),
             "paged_kv_append_fp8": (I, [P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
@@ -323,3 +330,57 @@ def quantize_pool_fp8(k_cache, v_cache, stream=None):
     paged_kv_append_fp8(k_cache.reshape(n, Hkv, D), v_cache.reshape(n, Hkv, D), table, pos, k8, v8, ks, vs,
                         stream=stream)
     return k8, v8, ks, vs
+
+
+# ----------------------------------------------------------------- several query rows per sequence
+
+def prefill_plan_query(B, Hq, Hkv, D, page_size, max_pages, total_q, max_q_len, num_sms, num_splits=0,
+                       cache="bf16") -> dict:
+    plan = PkvPlan()
+    _check(load().pkv_plan_query_prefill(B, Hq, Hkv, D, page_size, max_pages, total_q, max_q_len, num_sms,
+                                         num_splits, KV_DTYPES[cache], ctypes.byref(plan)), "pkv_plan_query_prefill")
+    return plan.as_dict()
+
+
+def paged_prefill_attn_workspace_size(B, Hq, Hkv, D, page_size, max_pages, total_q, max_q_len, device=None,
+                                      num_splits=0, cache="bf16") -> int:
+    torch = _torch()
+    dev = torch.cuda.current_device() if device is None else int(device)
+    n = ctypes.c_size_t(0)
+    _check(load().paged_prefill_attn_workspace_size(B, Hq, Hkv, D, page_size, max_pages, total_q, max_q_len, dev,
+                                                    num_splits, KV_DTYPES[cache], ctypes.byref(n)),
+           "paged_prefill_attn_workspace_size")
+    return n.value
+
+
+def paged_prefill_attn(q, k_cache, v_cache, qo_indptr, block_table, seq_lens, max_q_len, scale, out, lse, workspace,
+                       causal=True, num_splits=0, stream=None, fp8_scales=None):
+    """Calls paged_prefill_attn (or paged_prefill_attn_fp8 when fp8_scales = (k_scale, v_scale)):
+    q/out [total_q, Hq, D], qo_indptr [B+1], the cache and table as for decode."""
+    torch = _torch()
+    total_q, Hq, D = q.shape
+    num_pages, P, Hkv, Dk = k_cache.shape
+    B = seq_lens.shape[0]
+    if Dk != D or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("q/k_cache/v_cache shapes disagree")
+    if tuple(out.shape) != (total_q, Hq, D) or (lse is not None and tuple(lse.shape) != (total_q, Hq)):
+        raise ValueError("out must be [total_q, Hq, D] and lse [total_q, Hq]")
+    if tuple(qo_indptr.shape) != (B + 1,):
+        raise ValueError("qo_indptr must be [B+1]")
+    common = (_dev_ptr(qo_indptr, torch.int32, "qo_indptr", 1), _dev_ptr(block_table, torch.int32, "block_table", 2),
+              _dev_ptr(seq_lens, torch.int32, "seq_lens", 1), B, Hq, Hkv, D, P, num_pages, block_table.shape[1],
+              total_q, int(max_q_len), int(bool(causal)), ctypes.c_float(scale),
+              _dev_ptr(out, torch.bfloat16, "out", 3), _dev_ptr(lse, torch.float32, "lse", 2) if lse is not None else None,
+              _dev_ptr(workspace, workspace.dtype, "workspace"), workspace.numel() * workspace.element_size(),
+              int(num_splits), _stream_handle(stream))
+    if fp8_scales is None:
+        st = load().paged_prefill_attn(_dev_ptr(q, torch.bfloat16, "q", 3), _dev_ptr(k_cache, torch.bfloat16, "k_cache", 4),
+                                       _dev_ptr(v_cache, torch.bfloat16, "v_cache", 4), *common)
+    else:
+        ks, vs = fp8_scales
+        st = load().paged_prefill_attn_fp8(_dev_ptr(q, torch.bfloat16, "q", 3), _dev_ptr(k_cache, torch.uint8, "k_cache", 4),
+                                           _dev_ptr(v_cache, torch.uint8, "v_cache", 4),
+                                           _dev_ptr(ks, torch.float32, "k_scale", 3), _dev_ptr(vs, torch.float32, "v_scale", 3),
+                                           *common)
+    _check(st, "paged_prefill_attn")
+    return out, lse

@@ -187,12 +187,20 @@ struct Fp8Scales {
     const float *k_scale = nullptr, *v_scale = nullptr;
 };
 
+// Several query rows per sequence (qo_indptr == nullptr: decode, one row each).
+struct MultiRows {
+    const int32_t *qo_indptr = nullptr;
+    int total_q = 0, max_q_len = 0, causal = 0;
+};
+
 pkv_status decode_impl(const pkv_bf16 *q, const void *k_cache, const void *v_cache, Fp8Scales fp8,
                        const int32_t *block_table, const int32_t *seq_lens, int B, int Hq, int Hkv, int D,
                        int page_size, int num_pages, int max_pages, float scale, pkv_bf16 *out, float *lse,
-                       void *workspace, size_t workspace_bytes_, int num_splits, cudaStream_t stream)
+                       void *workspace, size_t workspace_bytes_, int num_splits, cudaStream_t stream,
+                       MultiRows mr = MultiRows{})
 {
     const bool kv8 = fp8.on;
+    const bool mq = mr.qo_indptr != nullptr;
     if (num_pages <= 0 || num_splits < 0 || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
     const pkv_status shape_ok = validate_shape(B, Hq, Hkv, D, page_size, max_pages);
     if (shape_ok != PKV_OK) return shape_ok;
@@ -204,12 +212,15 @@ pkv_status decode_impl(const pkv_bf16 *q, const void *k_cache, const void *v_cac
         return PKV_ERR_MISALIGNED;
     if (kv8 && (!aligned16(fp8.k_scale) || !aligned16(fp8.v_scale))) return PKV_ERR_MISALIGNED;
     if ((long)num_pages * page_size >= (1l << 31)) return PKV_ERR_INVALID_ARG;
+    if (mq && !aligned16(mr.qo_indptr)) return PKV_ERR_MISALIGNED;
+    const long group_rows = mq ? (long)mr.max_q_len * (Hq / Hkv) : 0;
+    const long total_rows = mq ? (long)mr.total_q * Hq : (long)B * Hq;
 
     int device = 0, sms = 0;
     pkv_status st = current_device_sms(&device, &sms);
     if (st != PKV_OK) return st;
     pkv_plan plan;
-    st = make_plan(B, Hq, Hkv, D, page_size, max_pages, sms, num_splits, &plan, kv8);
+    st = make_plan(B, Hq, Hkv, D, page_size, max_pages, sms, num_splits, &plan, kv8, group_rows, total_rows);
     if (st != PKV_OK) return st;
     if (workspace_bytes_ < plan.workspace_bytes) return PKV_ERR_WORKSPACE_TOO_SMALL;
 
@@ -243,13 +254,20 @@ pkv_status decode_impl(const pkv_bf16 *q, const void *k_cache, const void *v_cac
     p.seq_lens = seq_lens;
     p.out = reinterpret_cast<__nv_bfloat16 *>(out);
     p.lse = lse;
-    const WorkspaceLayout wl = workspace_layout(plan.num_splits, B, Hq, Hkv, D);
+    const WorkspaceLayout wl =
+        workspace_layout(plan.num_splits, (size_t)B * Hkv * plan.q_tiles, (size_t)total_rows, D);
     p.counters = reinterpret_cast<int *>(ws + wl.counters);
     p.part_lse = reinterpret_cast<float *>(ws + wl.part_lse);
     p.part_out = reinterpret_cast<float *>(ws + wl.part_out);
     p.status = reinterpret_cast<int *>(ws);
     p.k_scale = fp8.k_scale;
     p.v_scale = fp8.v_scale;
+    p.qo_indptr = mr.qo_indptr;
+    p.total_rows = (size_t)total_rows;
+    p.q_tiles = plan.q_tiles;
+    p.causal = mr.causal;
+    p.total_q = mr.total_q;
+    p.max_q_len = mr.max_q_len;
     p.B = B;
     p.Hq = Hq;
     p.Hkv = Hkv;
@@ -264,7 +282,10 @@ pkv_status decode_impl(const pkv_bf16 *q, const void *k_cache, const void *v_cac
     p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
     p.wait_limit_ns = kWaitLimitNs;
 
-    const int NT = head_tiles(p.G);
+    const int NT = plan.rows_per_block / 8;
+    if (mq)
+        return kv8 ? launch_prefill_fp8(D, NT, mk, mv, p, plan, B, Hkv, device, stream)
+                   : launch_prefill_bf16(D, NT, mk, mv, p, plan, B, Hkv, device, stream);
     return kv8 ? launch_decode_fp8(D, NT, mk, mv, p, plan, B, Hkv, device, stream)
                : launch_decode_bf16(D, NT, mk, mv, p, plan, B, Hkv, device, stream);
 }
@@ -309,6 +330,7 @@ const char *pkv_status_string(int status)
         case PKV_ERR_BAD_PAGE_INDEX: return "PKV_ERR_BAD_PAGE_INDEX";
         case PKV_ERR_DEVICE_TIMEOUT: return "PKV_ERR_DEVICE_TIMEOUT";
         case PKV_ERR_BAD_SEQ_LEN: return "PKV_ERR_BAD_SEQ_LEN";
+        case PKV_ERR_BAD_QO_INDPTR: return "PKV_ERR_BAD_QO_INDPTR";
         default: return "PKV_UNKNOWN_STATUS";
     }
 }
@@ -391,6 +413,76 @@ pkv_status paged_decode_attn_fp8(const pkv_bf16 *q, const uint8_t *k_cache, cons
     f.v_scale = v_scale;
     return decode_impl(q, k_cache, v_cache, f, block_table, seq_lens, B, Hq, Hkv, D, page_size, num_pages,
                        max_pages, scale, out, lse, workspace, workspace_bytes, num_splits, stream);
+}
+
+static pkv_status multi_rows(const int32_t *qo_indptr, int B, int total_q, int max_q_len, int causal,
+                             MultiRows *mr)
+{
+    if (!qo_indptr && B > 0) return PKV_ERR_INVALID_ARG;
+    if (total_q < 0 || max_q_len < 1 || (causal != 0 && causal != 1)) return PKV_ERR_INVALID_ARG;
+    mr->qo_indptr = qo_indptr;
+    mr->total_q = total_q;
+    mr->max_q_len = max_q_len;
+    mr->causal = causal;
+    return PKV_OK;
+}
+
+pkv_status paged_prefill_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
+                              const int32_t *qo_indptr, const int32_t *block_table, const int32_t *seq_lens, int B,
+                              int Hq, int Hkv, int D, int page_size, int num_pages, int max_pages, int total_q,
+                              int max_q_len, int causal, float scale, pkv_bf16 *out, float *lse, void *workspace,
+                              size_t workspace_bytes, int num_splits, cudaStream_t stream)
+{
+    MultiRows mr;
+    const pkv_status st = multi_rows(qo_indptr, B, total_q, max_q_len, causal, &mr);
+    if (st != PKV_OK) return st;
+    if (total_q == 0) return PKV_OK;
+    return decode_impl(q, k_cache, v_cache, Fp8Scales{}, block_table, seq_lens, B, Hq, Hkv, D, page_size,
+                       num_pages, max_pages, scale, out, lse, workspace, workspace_bytes, num_splits, stream, mr);
+}
+
+pkv_status paged_prefill_attn_fp8(const pkv_bf16 *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                                  const float *k_scale, const float *v_scale, const int32_t *qo_indptr,
+                                  const int32_t *block_table, const int32_t *seq_lens, int B, int Hq, int Hkv, int D,
+                                  int page_size, int num_pages, int max_pages, int total_q, int max_q_len,
+                                  int causal, float scale, pkv_bf16 *out, float *lse, void *workspace,
+                                  size_t workspace_bytes, int num_splits, cudaStream_t stream)
+{
+    MultiRows mr;
+    const pkv_status st = multi_rows(qo_indptr, B, total_q, max_q_len, causal, &mr);
+    if (st != PKV_OK) return st;
+    if (total_q == 0) return PKV_OK;
+    Fp8Scales f;
+    f.on = true;
+    f.k_scale = k_scale;
+    f.v_scale = v_scale;
+    return decode_impl(q, k_cache, v_cache, f, block_table, seq_lens, B, Hq, Hkv, D, page_size, num_pages,
+                       max_pages, scale, out, lse, workspace, workspace_bytes, num_splits, stream, mr);
+}
+
+pkv_status pkv_plan_query_prefill(int B, int Hq, int Hkv, int D, int page_size, int max_pages, int total_q,
+                                  int max_q_len, int num_sms, int num_splits, int kv_dtype, pkv_plan *plan)
+{
+    if (kv_dtype != PKV_KV_BF16 && kv_dtype != PKV_KV_FP8_E4M3) return PKV_ERR_INVALID_ARG;
+    if (total_q < 0 || max_q_len < 1 || Hkv <= 0) return PKV_ERR_INVALID_ARG;
+    return make_plan(B, Hq, Hkv, D, page_size, max_pages, num_sms, num_splits, plan, kv_dtype == PKV_KV_FP8_E4M3,
+                     (long)max_q_len * (Hkv > 0 ? Hq / Hkv : 1), (long)total_q * Hq);
+}
+
+pkv_status paged_prefill_attn_workspace_size(int B, int Hq, int Hkv, int D, int page_size, int max_pages,
+                                             int total_q, int max_q_len, int device, int num_splits, int kv_dtype,
+                                             size_t *bytes)
+{
+    if (!bytes) return PKV_ERR_INVALID_ARG;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return PKV_ERR_CUDA;
+    pkv_plan plan;
+    const pkv_status st =
+        pkv_plan_query_prefill(B, Hq, Hkv, D, page_size, max_pages, total_q, max_q_len, sms, num_splits, kv_dtype,
+                               &plan);
+    if (st != PKV_OK) return st;
+    *bytes = plan.workspace_bytes;
+    return PKV_OK;
 }
 
 pkv_status split_kv_merge(const float *partial_out, const float *partial_lse, int S, int B, int Hq, int D,
@@ -588,7 +680,7 @@ extern "C" pkv_status paged_decode_attn_static_scratch(const pkv_bf16 *q, const 
     // The status word and the split-completion counters must start at zero (a previous
     // call that gave up part-way could have left a counter raised); the partials are
     // fully written before they are read.
-    const size_t zero_bytes = workspace_layout(plan.num_splits, B, Hq, Hkv, D).part_lse;
+    const size_t zero_bytes = workspace_layout(plan.num_splits, (size_t)B * Hkv, (size_t)B * Hq, D).part_lse;
     if (cudaMemsetAsync(scratch, 0, zero_bytes, stream) != cudaSuccess) return PKV_ERR_CUDA;
     st = paged_decode_attn(q, k_cache, v_cache, block_table, seq_lens, B, Hq, Hkv, D, page_size, num_pages,
                            max_pages, scale, out, lse, scratch, kStaticScratchBytes, stream);

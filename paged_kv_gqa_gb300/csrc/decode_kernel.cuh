@@ -102,6 +102,11 @@ struct DecodeParams {
     int *status;             // workspace status word
     const float *k_scale;    // fp8 cache: [num_pages, Hkv, P] f32 per (token, kv head)
     const float *v_scale;
+    const int *qo_indptr;    // multi-token rows: [B+1] query rows per request (q, out: [total_q, Hq, D])
+    size_t total_rows;       // rows of out / lse / the partials: B*Hq, or total_q*Hq
+    int q_tiles;             // multi-token rows: blocks per (request, kv head) along its rows
+    int total_q, max_q_len;  // multi-token rows: rows of q, and the most rows one request may have
+    int causal;              // multi-token rows: row i of a request with n rows and L keys sees keys <= L-n+i
     int B, Hq, Hkv, G, P, log2P, num_pages, max_pages;
     int chunk_tokens, num_splits;
     int box4;                // 1: the tensor maps are 4-D and one box spans all D columns
@@ -139,7 +144,7 @@ __device__ __forceinline__ uint32_t code_offset(int r, int c, int log2_box_t)
     return lin ^ (((lin >> 7) & kMask) << 4);
 }
 
-template <int D, int NT, bool KV8>
+template <int D, int NT, bool KV8, bool MQ>
 __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
     decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const DecodeParams p)
@@ -157,8 +162,11 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
     constexpr int RS = D + 4;             // f32 stride of the combine buffer rows
 
     // kv head fastest: the blocks of one (split, sequence) start together and read the
-    // same pages' head slices, which share DRAM rows
-    const int kvh = blockIdx.x, c = blockIdx.y, b = blockIdx.z;
+    // same pages' head slices, which share DRAM rows.  MQ: blockIdx.x also carries the
+    // tile qt of the (token, head) rows of the group.
+    const int kvh = MQ ? (int)(blockIdx.x % (unsigned)p.Hkv) : (int)blockIdx.x;
+    const int qt = MQ ? (int)(blockIdx.x / (unsigned)p.Hkv) : 0;
+    const int c = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, cc = lane & 3;
     const int G = p.G;
@@ -170,14 +178,40 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
         if (threadIdx.x == 0 && c == 0 && kvh == 0) record_status(p.status, PKV_ERR_BAD_SEQ_LEN);
         L = 0;
     }
+    // The block's rows: decode, the G query heads of the group (one query row per
+    // sequence); MQ, rows rr = qt*H8 + r of the group's (token i, head h) rows, rr = i*G + h.
+    int n_q = 1, q_base = b, row_begin = 0, nrows = G;
+    if constexpr (MQ) {
+        q_base = p.qo_indptr[b];
+        n_q = p.qo_indptr[b + 1] - q_base;
+        if (q_base < 0 || n_q < 0 || n_q > p.max_q_len || q_base + n_q > p.total_q) {
+            // a malformed row range: nothing of this request is read or written
+            if (threadIdx.x == 0 && c == 0 && kvh == 0 && qt == 0) record_status(p.status, PKV_ERR_BAD_QO_INDPTR);
+            return;
+        }
+        row_begin = qt * H8;
+        nrows = min(H8, n_q * G - row_begin);
+        if (nrows <= 0) return;  // this tile of the group is past the request's rows
+    }
+    // global row (query row * Hq + query head) of block row r < nrows
+    auto grow = [&](int r) -> size_t {
+        if constexpr (MQ) {
+            const int rr = row_begin + r, i = rr / G;
+            return (size_t)(q_base + i) * p.Hq + kvh * G + (rr - i * G);
+        } else {
+            return (size_t)b * p.Hq + kvh * G + r;
+        }
+    };
+    // MQ with the causal mask: the last key block row r sees (keys past it get -inf)
+    auto key_limit = [&](int r) -> int { return (MQ && p.causal) ? L - n_q + (row_begin + r) / G : L - 1; };
+
     const int tok_begin = c * p.chunk_tokens;
     if (c > 0 && tok_begin >= L) return;  // empty split: the merge never reads it
     if (L == 0) {                          // empty sequence: out = 0, lse = -inf
-        for (int i = threadIdx.x; i < G * D; i += W * 32)
-            p.out[((size_t)b * p.Hq + kvh * G + i / D) * D + (i % D)] = __float2bfloat16_rn(0.f);
+        for (int i = threadIdx.x; i < nrows * D; i += W * 32)
+            p.out[grow(i / D) * D + (i % D)] = __float2bfloat16_rn(0.f);
         if (p.lse)
-            for (int i = threadIdx.x; i < G; i += W * 32)
-                p.lse[(size_t)b * p.Hq + kvh * G + i] = -__int_as_float(0x7f800000);
+            for (int i = threadIdx.x; i < nrows; i += W * 32) p.lse[grow(i)] = -__int_as_float(0x7f800000);
         return;
     }
     const int tok_end = min(tok_begin + p.chunk_tokens, L);
@@ -231,12 +265,12 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int head = nt * 8 + g;
-            const uint32_t *qp = reinterpret_cast<const uint32_t *>(
-                p.q + ((size_t)b * p.Hq + kvh * G + (head < G ? head : 0)) * D + 2 * cc);
+            const uint32_t *qp =
+                reinterpret_cast<const uint32_t *>(p.q + grow(head < nrows ? head : 0) * D + 2 * cc);
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
-                qf[ks][nt][0] = head < G ? __ldg(qp + ks * 8) : 0u;
-                qf[ks][nt][1] = head < G ? __ldg(qp + ks * 8 + 4) : 0u;
+                qf[ks][nt][0] = head < nrows ? __ldg(qp + ks * 8) : 0u;
+                qf[ks][nt][1] = head < nrows ? __ldg(qp + ks * 8 + 4) : 0u;
             }
         }
     } else {
@@ -246,11 +280,10 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int head = nt * 8 + g;
-            const uint2 *qp = reinterpret_cast<const uint2 *>(
-                p.q + ((size_t)b * p.Hq + kvh * G + (head < G ? head : 0)) * D + 4 * cc);
+            const uint2 *qp = reinterpret_cast<const uint2 *>(p.q + grow(head < nrows ? head : 0) * D + 4 * cc);
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
-                raw[ks][nt] = head < G ? __ldg(qp + ks * 4) : make_uint2(0u, 0u);
+                raw[ks][nt] = head < nrows ? __ldg(qp + ks * 4) : make_uint2(0u, 0u);
                 qmax = fmaxf(qmax, fmaxf(fmaxf(fabsf(bf16_lo(raw[ks][nt].x)), fabsf(bf16_hi(raw[ks][nt].x))),
                                          fmaxf(fabsf(bf16_lo(raw[ks][nt].y)), fabsf(bf16_hi(raw[ks][nt].y)))));
             }
@@ -376,6 +409,18 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
         lt_run[nt][0] = lt_run[nt][1] = 0.f;
     }
 
+    // MQ: the key limit of each of this lane's score columns (rows nt*8 + 2cc + j), and the
+    // first key some row of the block must not see (stages from there on take the masked body)
+    int klim[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int r = nt * 8 + 2 * cc + j;
+            klim[nt][j] = r < nrows ? key_limit(r) : L - 1;
+        }
+    const int causal_from = key_limit(0) + 1;
+
     auto key_valid = [&](int t) -> bool {
         return t < tok_end && sm_tab[(t >> p.log2P) - page_begin] >= 0;
     };
@@ -492,7 +537,7 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
                     float v = (kTwoChains ? sc[mt][nt][e] + sc2[mt][nt][e] : sc[mt][nt][e]) * kmul[mt][e >> 1];
                     if (MASKED) {
                         const int t = t0 + mt * 16 + g + ((e >> 1) << 3);
-                        if (!key_valid(t)) v = -__int_as_float(0x7f800000);
+                        if (!key_valid(t) || (MQ && t > klim[nt][e & 1])) v = -__int_as_float(0x7f800000);
                     }
                     sc[mt][nt][e] = v;
                 }
@@ -626,7 +671,7 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
         }
         const int t0 = tok_begin + s * T;
         const uint32_t kbase = ring_addr + (uint32_t)((warp * R + slot) * STAGE);
-        if ((t0 + T > tok_end) || any_bad)
+        if ((t0 + T > tok_end) || any_bad || (MQ && t0 + T > causal_from))
             run_stage(std::true_type{}, t0, kbase, slot);
         else
             run_stage(std::false_type{}, t0, kbase, slot);
@@ -720,7 +765,7 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
 
     const bool direct = (n_chunks == 1);
     if (direct) {  // the only split of this sequence: final bf16 output and lse
-        for (int i = threadIdx.x; i < G * D / 2; i += W * 32) {
+        for (int i = threadIdx.x; i < nrows * D / 2; i += W * 32) {
             const int h = (2 * i) / D, d = 2 * i - h * D;
             float o0 = 0.f, o1 = 0.f;
 #pragma unroll
@@ -729,17 +774,16 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
                 o0 += red[(w * H8 + h) * RS + d] * f;
                 o1 += red[(w * H8 + h) * RS + d + 1] * f;
             }
-            const size_t row = (size_t)b * p.Hq + kvh * G + h;
+            const size_t row = grow(h);
             *reinterpret_cast<uint32_t *>(p.out + row * D + d) = pack_bf16x2(o0, o1);
         }
-        if (threadIdx.x < G && p.lse) p.lse[(size_t)b * p.Hq + kvh * G + threadIdx.x] = sm_lse[threadIdx.x];
+        if (threadIdx.x < nrows && p.lse) p.lse[grow(threadIdx.x)] = sm_lse[threadIdx.x];
         return;
     }
 
     // ---- one of several splits: write this split's normalised output and lse ----
-    const size_t rows = (size_t)p.B * p.Hq;
-    const size_t row0 = (size_t)b * p.Hq + kvh * G;
-    for (int i = threadIdx.x; i < G * D / 4; i += W * 32) {
+    const size_t rows = p.total_rows;
+    for (int i = threadIdx.x; i < nrows * D / 4; i += W * 32) {
         const int h = (4 * i) / D, d = 4 * i - h * D;
         float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -751,9 +795,9 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
             o.z += r[2] * f;
             o.w += r[3] * f;
         }
-        *reinterpret_cast<float4 *>(p.part_out + ((size_t)c * rows + row0 + h) * D + d) = o;
+        *reinterpret_cast<float4 *>(p.part_out + ((size_t)c * rows + grow(h)) * D + d) = o;
     }
-    if (threadIdx.x < G) p.part_lse[(size_t)c * rows + row0 + threadIdx.x] = sm_lse[threadIdx.x];
+    if (threadIdx.x < nrows) p.part_lse[(size_t)c * rows + grow(threadIdx.x)] = sm_lse[threadIdx.x];
 
     // ---- the last split of this (b, kv head) to finish merges all of them ----------
     // Log-sum-exp merge (FlashQuant wiki "CUDA Kernels", split_k_reduce.cu
@@ -764,7 +808,8 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
     __syncthreads();
     int *flag = reinterpret_cast<int *>(base + lay.flag);
     if (threadIdx.x == 0)
-        *flag = atomicInc(reinterpret_cast<unsigned *>(p.counters + b * p.Hkv + kvh), (unsigned)(n_chunks - 1)) ==
+        *flag = atomicInc(reinterpret_cast<unsigned *>(p.counters + ((size_t)b * p.q_tiles + qt) * p.Hkv + kvh),
+                          (unsigned)(n_chunks - 1)) ==
                 (unsigned)(n_chunks - 1);
     __syncthreads();
     if (!*flag) return;
@@ -778,7 +823,7 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
     const float ninf = -__int_as_float(0x7f800000);
     constexpr int V4 = D / 4;
     constexpr int NE = 2;
-    const int nvec = G * V4;
+    const int nvec = nrows * V4;
     for (int e0 = threadIdx.x; e0 < nvec; e0 += NE * W * 32) {
         float4 a[NE];
         float m[NE], wsum[NE];
@@ -791,8 +836,8 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
             a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
             m[k] = ninf;
             wsum[k] = 0.f;
-            lp[k] = p.part_lse + row0 + h;
-            op[k] = reinterpret_cast<const float4 *>(p.part_out + (row0 + h) * D) + d4;
+            lp[k] = p.part_lse + grow(h);
+            op[k] = reinterpret_cast<const float4 *>(p.part_out + grow(h) * D) + d4;
         }
 #pragma unroll 8
         for (int sidx = 0; sidx < n_chunks; ++sidx) {
@@ -820,8 +865,8 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
             uint2 packed;
             packed.x = pack_bf16x2(a[k].x * inv, a[k].y * inv);
             packed.y = pack_bf16x2(a[k].z * inv, a[k].w * inv);
-            *reinterpret_cast<uint2 *>(p.out + (row0 + h) * D + 4 * d4) = packed;
-            if (d4 == 0 && p.lse) p.lse[row0 + h] = m[k] == ninf ? ninf : m[k] + __logf(wsum[k]);
+            *reinterpret_cast<uint2 *>(p.out + grow(h) * D + 4 * d4) = packed;
+            if (d4 == 0 && p.lse) p.lse[grow(h)] = m[k] == ninf ? ninf : m[k] + __logf(wsum[k]);
         }
     }
 }

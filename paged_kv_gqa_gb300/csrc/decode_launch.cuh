@@ -1,6 +1,7 @@
-// decode_launch.cuh -- launch of one decode-kernel variant (head dim D, head tiles
-// NT, bf16 or fp8 cache).  Instantiated by decode_bf16.cu and decode_fp8.cu, one
-// translation unit per cache type, so the two families compile in parallel.
+// decode_launch.cuh -- launch of one decode-kernel variant (head dim D, row tiles
+// NT, bf16 or fp8 cache, one or several query rows per sequence).  Instantiated by
+// decode_{bf16,fp8}.cu and prefill_{bf16,fp8}.cu, one translation unit per family,
+// so the families compile in parallel.
 #pragma once
 
 #include <cuda.h>
@@ -13,19 +14,23 @@
 
 namespace pkv {
 
-// Dispatch on (D, NT) for one cache type; defined in decode_bf16.cu / decode_fp8.cu.
-pkv_status launch_decode_bf16(int D, int NT, const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
-                              const pkv_plan &plan, int B, int Hkv, int device, cudaStream_t stream);
-pkv_status launch_decode_fp8(int D, int NT, const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
-                             const pkv_plan &plan, int B, int Hkv, int device, cudaStream_t stream);
+// Dispatch on (D, NT) for one family; defined in decode_{bf16,fp8}.cu, prefill_{bf16,fp8}.cu.
+#define PKV_DECLARE_LAUNCH(NAME)                                                                             \
+    pkv_status NAME(int D, int NT, const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,        \
+                    const pkv_plan &plan, int B, int Hkv, int device, cudaStream_t stream);
+PKV_DECLARE_LAUNCH(launch_decode_bf16)
+PKV_DECLARE_LAUNCH(launch_decode_fp8)
+PKV_DECLARE_LAUNCH(launch_prefill_bf16)
+PKV_DECLARE_LAUNCH(launch_prefill_fp8)
+#undef PKV_DECLARE_LAUNCH
 
-template <int D, int NT, bool KV8>
+template <int D, int NT, bool KV8, bool MQ>
 pkv_status launch_decode_variant(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
                                  const pkv_plan &plan, int B, int Hkv, int device, cudaStream_t stream)
 {
     static bool attr_set[64] = {};
     static std::mutex mu;
-    auto kern = decode_split_kernel<D, NT, KV8>;
+    auto kern = decode_split_kernel<D, NT, KV8, MQ>;
     if (device < 0 || device >= 64) return PKV_ERR_UNSUPPORTED;
     {
         std::lock_guard<std::mutex> lock(mu);
@@ -35,24 +40,25 @@ pkv_status launch_decode_variant(const CUtensorMap &mk, const CUtensorMap &mv, c
             attr_set[device] = true;
         }
     }
-    dim3 grid(Hkv, plan.num_splits, B);
+    dim3 grid(Hkv * plan.q_tiles, plan.num_splits, B);
     dim3 block(plan.warps * 32);
     kern<<<grid, block, plan.smem_bytes, stream>>>(mk, mv, p);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-#define PKV_DECODE_DISPATCH(KV8)                                                                       \
-    switch (D * 8 + NT) {                                                                              \
-        case 64 * 8 + 1: return launch_decode_variant<64, 1, KV8>(mk, mv, p, plan, B, Hkv, device, stream);   \
-        case 64 * 8 + 2: return launch_decode_variant<64, 2, KV8>(mk, mv, p, plan, B, Hkv, device, stream);   \
-        case 64 * 8 + 4: return launch_decode_variant<64, 4, KV8>(mk, mv, p, plan, B, Hkv, device, stream);   \
-        case 128 * 8 + 1: return launch_decode_variant<128, 1, KV8>(mk, mv, p, plan, B, Hkv, device, stream); \
-        case 128 * 8 + 2: return launch_decode_variant<128, 2, KV8>(mk, mv, p, plan, B, Hkv, device, stream); \
-        case 128 * 8 + 4: return launch_decode_variant<128, 4, KV8>(mk, mv, p, plan, B, Hkv, device, stream); \
-        case 256 * 8 + 1: return launch_decode_variant<256, 1, KV8>(mk, mv, p, plan, B, Hkv, device, stream); \
-        case 256 * 8 + 2: return launch_decode_variant<256, 2, KV8>(mk, mv, p, plan, B, Hkv, device, stream); \
-        case 256 * 8 + 4: return launch_decode_variant<256, 4, KV8>(mk, mv, p, plan, B, Hkv, device, stream); \
-        default: return PKV_ERR_UNSUPPORTED;                                                           \
+#define PKV_V(DD, NN, KV8, MQ) launch_decode_variant<DD, NN, KV8, MQ>(mk, mv, p, plan, B, Hkv, device, stream)
+#define PKV_DECODE_DISPATCH(KV8, MQ)                         \
+    switch (D * 8 + NT) {                                    \
+        case 64 * 8 + 1: return PKV_V(64, 1, KV8, MQ);       \
+        case 64 * 8 + 2: return PKV_V(64, 2, KV8, MQ);       \
+        case 64 * 8 + 4: return PKV_V(64, 4, KV8, MQ);       \
+        case 128 * 8 + 1: return PKV_V(128, 1, KV8, MQ);     \
+        case 128 * 8 + 2: return PKV_V(128, 2, KV8, MQ);     \
+        case 128 * 8 + 4: return PKV_V(128, 4, KV8, MQ);     \
+        case 256 * 8 + 1: return PKV_V(256, 1, KV8, MQ);     \
+        case 256 * 8 + 2: return PKV_V(256, 2, KV8, MQ);     \
+        case 256 * 8 + 4: return PKV_V(256, 4, KV8, MQ);     \
+        default: return PKV_ERR_UNSUPPORTED;                 \
     }
 
 }  // namespace pkv

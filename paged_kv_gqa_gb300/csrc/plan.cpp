@@ -45,13 +45,13 @@ RuntimeTiling tiling_for(int D)
 
 static size_t pad256(size_t x) { return (x + 255) / 256 * 256; }
 
-WorkspaceLayout workspace_layout(int S, int B, int Hq, int Hkv, int D)
+WorkspaceLayout workspace_layout(int S, size_t n_counters, size_t total_rows, int D)
 {
     WorkspaceLayout w;
     w.counters = kWorkspaceHeader;
-    w.part_lse = w.counters + pad256((size_t)B * Hkv * sizeof(int));
-    w.part_out = w.part_lse + pad256((size_t)S * B * Hq * sizeof(float));
-    w.total = S <= 1 ? kWorkspaceHeader : w.part_out + (size_t)S * B * Hq * D * sizeof(float);
+    w.part_lse = w.counters + pad256(n_counters * sizeof(int));
+    w.part_out = w.part_lse + pad256((size_t)S * total_rows * sizeof(float));
+    w.total = S <= 1 ? kWorkspaceHeader : w.part_out + (size_t)S * total_rows * D * sizeof(float);
     return w;
 }
 
@@ -69,17 +69,25 @@ pkv_status validate_shape(int B, int Hq, int Hkv, int D, int page_size, int max_
 }
 
 pkv_status make_plan(int B, int Hq, int Hkv, int D, int page_size, int max_pages, int num_sms,
-                     int num_splits, pkv_plan *plan, bool kv8)
+                     int num_splits, pkv_plan *plan, bool kv8, long group_rows, long total_rows)
 {
-    if (!plan || num_sms <= 0 || num_splits < 0) return PKV_ERR_INVALID_ARG;
+    if (!plan || num_sms <= 0 || num_splits < 0 || group_rows < 0 || total_rows < 0) return PKV_ERR_INVALID_ARG;
     const pkv_status v = validate_shape(B, Hq, Hkv, D, page_size, max_pages);
     if (v != PKV_OK) return v;
     const int G = Hq / Hkv;
 
+    // A block serves up to 32 (token, query head) rows of one (sequence, kv head) group
+    // (all G heads of a decode step); longer groups take several query tiles.
+    const long rows = group_rows > 0 ? group_rows : G;
+    const int NT = head_tiles((int)std::min<long>(rows, 32));
+    const long q_tiles = (rows + NT * 8 - 1) / (NT * 8);
+    if ((long)B * Hkv * q_tiles >= (1l << 31)) return PKV_ERR_INVALID_ARG;
+    if (B > 65535) return PKV_ERR_UNSUPPORTED;  // sequences are the grid's z dimension
+    const long out_rows = total_rows > 0 ? total_rows : (long)B * Hq;
+
     const RuntimeTiling t = tiling_for(D);
-    const int NT = head_tiles(G);
     const int max_tokens = max_pages * page_size;
-    const int units = std::max(1, B * Hkv);
+    const int units = std::max(1, (int)(B * Hkv * q_tiles));
 
     // Resident blocks per SM: the shared-memory limit (sized with the largest table slice
     // the auto plan uses) or the variant's register budget, whichever is lower.
@@ -132,6 +140,7 @@ pkv_status make_plan(int B, int Hq, int Hkv, int D, int page_size, int max_pages
     const int max_chunk = (kMaxTablePages - 2) * page_size;
     if (chunk > max_chunk) chunk = max_chunk / t.T * t.T;
     S = (max_tokens + chunk - 1) / chunk;
+    if ((long)S * Hkv * q_tiles * B >= (1l << 31)) return PKV_ERR_INVALID_ARG;
 
     const SmemLayout lay = smem_layout(D, t.T, t.W, R, NT, chunk, page_size, kv8);
     if (lay.dynamic > kSmemPerBlockMax) return PKV_ERR_UNSUPPORTED;
@@ -143,10 +152,12 @@ pkv_status make_plan(int B, int Hq, int Hkv, int D, int page_size, int max_pages
     plan->warps = t.W;
     plan->ring_stages = R;
     plan->blocks_per_sm = per_sm;
-    plan->grid_blocks = S * Hkv * B;
+    plan->grid_blocks = (int)(S * Hkv * q_tiles * B);
     plan->smem_bytes = lay.dynamic;
     plan->merge_needed = S > 1 ? 1 : 0;
-    plan->workspace_bytes = workspace_layout(S, B, Hq, Hkv, D).total;
+    plan->workspace_bytes = workspace_layout(S, (size_t)B * Hkv * q_tiles, (size_t)out_rows, D).total;
+    plan->q_tiles = (int)q_tiles;
+    plan->rows_per_block = NT * 8;
     return PKV_OK;
 }
 

@@ -109,14 +109,17 @@ constexpr size_t kWorkspaceHeader = 256;
 struct WorkspaceLayout {
     size_t counters, part_lse, part_out, total;
 };
-WorkspaceLayout workspace_layout(int S, int B, int Hq, int Hkv, int D);
+// n_counters: one per (sequence, kv head, query tile); total_rows: rows of out (B*Hq for decode).
+WorkspaceLayout workspace_layout(int S, size_t n_counters, size_t total_rows, int D);
 
 // Shape checks shared by every entry point (no CUDA call).
 pkv_status validate_shape(int B, int Hq, int Hkv, int D, int page_size, int max_pages);
 
 // Validates the shape (not pointers) and fills `plan` for the bf16-cache kernel or,
-// with kv8, the fp8-cache one.
+// with kv8, the fp8-cache one.  group_rows: (token, query head) rows of one (sequence,
+// kv head) group, at most max_q_len * G (0: decode, G rows); total_rows: rows of the
+// output, total_q * Hq (0: B * Hq).
 pkv_status make_plan(int B, int Hq, int Hkv, int D, int page_size, int max_pages, int num_sms,
-                     int num_splits, pkv_plan *plan, bool kv8 = false);
+                     int num_splits, pkv_plan *plan, bool kv8 = false, long group_rows = 0, long total_rows = 0);
 
 }  // namespace pkv

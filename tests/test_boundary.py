@@ -37,7 +37,7 @@ def test_no_internal_symbols_leak():
     import subprocess
     out = subprocess.run(["nm", "-D", "--defined-only", pkv.LIB_PATH], capture_output=True, text=True).stdout
     exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
-    ours = {n for n in exported if n.startswith(("pkv", "paged_decode", "paged_kv", "split_kv"))}
+    ours = {n for n in exported if n.startswith(("pkv", "paged_decode", "paged_kv", "paged_prefill", "split_kv"))}
     assert ours == set(_declared())
 
 

@@ -1,0 +1,139 @@
+"""Several query rows per sequence (multi-token decode, chunked paged prefill) on the GPU,
+through the C-ABI, against the CPU oracle.
+
+Bars: max |out - oracle| <= 1.5e-2, max |lse - oracle| <= 1e-3; one row per request
+reproduces the decode kernel bit for bit; split counts agree to the split-count bar.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_gqa_gb300 as pkv
+from paged_kv_gqa_gb300 import _build
+from gpu_util import LSE_TOL, OUT_TOL, max_abs_diff, run_gpu, split_invariance_violation
+from workloads import Case, make_prefill_case, used_slot_mask
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    _build.build()
+    return pkv.load()
+
+
+def _spec(B, Hq, Hkv, D, P, seed=0):
+    return dict(B=B, Hq=Hq, Hkv=Hkv, D=D, P=P, lens=("fixed", 1), seed=seed)
+
+
+def run_prefill(case, causal=True, num_splits=0, fp8=None, expect_status=0, max_q_len=None):
+    c = case if case.q.is_cuda else case.to("cuda")
+    q_lens = np.diff(case.qo_indptr.cpu().numpy())
+    mq = int(max_q_len if max_q_len is not None else max(1, q_lens.max() if q_lens.size else 1))
+    total_q = c.q.shape[0]
+    cache = "fp8" if fp8 is not None else "bf16"
+    ws = torch.zeros(pkv.paged_prefill_attn_workspace_size(c.B, c.Hq, c.Hkv, c.D, c.P, c.max_pages, total_q, mq,
+                                                           num_splits=num_splits, cache=cache),
+                     dtype=torch.uint8, device="cuda")
+    out = torch.full((total_q, c.Hq, c.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((total_q, c.Hq), float("nan"), dtype=torch.float32, device="cuda")
+    if fp8 is not None:
+        k8, v8, ks, vs = (torch.from_numpy(np.ascontiguousarray(a)).cuda() for a in fp8)
+        pkv.paged_prefill_attn(c.q, k8, v8, c.qo_indptr, c.block_table, c.seq_lens, mq, c.scale, out, lse, ws,
+                               causal=causal, num_splits=num_splits, fp8_scales=(ks, vs))
+    else:
+        pkv.paged_prefill_attn(c.q, c.k_cache, c.v_cache, c.qo_indptr, c.block_table, c.seq_lens, mq, c.scale, out,
+                               lse, ws, causal=causal, num_splits=num_splits)
+    status = pkv.pkv_check_status(ws)
+    assert status == expect_status, "device status %s" % pkv.STATUS.get(status, status)
+    return out, lse
+
+
+def compare(case, out, lse, causal=True, fp8=None, select=None):
+    q, k, v, bt, sl = case.host_bits()
+    qo = case.qo_indptr.cpu().numpy()
+    kw = dict(fp8=fp8) if fp8 is not None else dict(k_bits=k, v_bits=v)
+    ro, rl = oracle.paged_prefill(q, qo, bt, sl, case.scale, causal=causal, select=select, **kw)
+    o, l = out.float().cpu().numpy(), lse.cpu().numpy()
+    if select is not None:
+        idx = np.asarray(list(select))
+        o, l = o[idx[:, 0], idx[:, 1]], l[idx[:, 0], idx[:, 1]]
+    return max_abs_diff(o, ro), max_abs_diff(l, rl)
+
+
+SMALL = [
+    # B, Hq, Hkv, D, P, q_lens, kv_lens
+    (2, 8, 2, 64, 16, [3, 5], [40, 300]),
+    (3, 32, 8, 128, 16, [4, 1, 2], [1000, 17, 2]),      # 32 rows per group: one tile of 32
+    (2, 32, 8, 128, 16, [7, 3], [64, 500]),            # 56 rows: two tiles
+    (2, 16, 2, 128, 8, [1, 6], [9, 6]),               # a request as long as its cache
+    (1, 8, 1, 256, 64, [12], [700]),
+    (2, 16, 2, 256, 16, [2, 3], [129, 4000]),
+    (3, 4, 4, 64, 32, [33, 1, 5], [60, 3, 5]),         # G = 1, 33 rows: two tiles
+    (2, 8, 2, 128, 16, [6, 0], [2, 100]),              # 6 rows over 2 keys; an empty request
+]
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("B,Hq,Hkv,D,P,q_lens,kv_lens", SMALL, ids=lambda x: str(x).replace(" ", ""))
+def test_small_cases_full_oracle(B, Hq, Hkv, D, P, q_lens, kv_lens, causal):
+    case = make_prefill_case(_spec(B, Hq, Hkv, D, P, seed=B + D + sum(q_lens)), q_lens, kv_lens, poison=True)
+    out, lse = run_prefill(case, causal=causal)
+    eo, el = compare(case, out, lse, causal=causal)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,D,P,q_lens,kv_lens", SMALL[:6], ids=lambda x: str(x).replace(" ", ""))
+def test_fp8_cache(B, Hq, Hkv, D, P, q_lens, kv_lens):
+    case = make_prefill_case(_spec(B, Hq, Hkv, D, P, seed=7 * B + D), q_lens, kv_lens, poison=True)
+    _, k, v, _, _ = case.host_bits()
+    k8, ks = oracle.quantize_pool(k)
+    v8, vs = oracle.quantize_pool(v)
+    unused = ~used_slot_mask(case)
+    for sc in (ks, vs):
+        sc.transpose(0, 2, 1)[unused] = np.nan
+    out, lse = run_prefill(case, fp8=(k8, v8, ks, vs))
+    eo, el = compare(case, out, lse, fp8=(k8, v8, ks, vs))
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_one_row_per_request_is_the_decode_kernel(causal):
+    case = make_prefill_case(_spec(5, 32, 8, 128, 16, seed=3), [1] * 5, [1, 17, 300, 1024, 4000], poison=True)
+    for splits in (0, 1, 3):
+        o1, l1 = run_prefill(case, causal=causal, num_splits=splits)
+        dcase = Case(**case.__dict__)
+        o2, l2 = run_gpu(dcase, num_splits=splits)
+        assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+        assert torch.equal(l1.view(torch.int32), l2.view(torch.int32))
+
+
+def test_split_counts_agree():
+    case = make_prefill_case(_spec(3, 32, 8, 128, 16, seed=4), [4, 2, 3], [3000, 1200, 64])
+    ref = run_prefill(case, num_splits=1)
+    for splits in (0, 3, 7):
+        out, lse = run_prefill(case, num_splits=splits)
+        excess, frac, _ = split_invariance_violation(out.float().cpu().numpy(), ref[0].float().cpu().numpy())
+        assert excess <= 0 and max_abs_diff(lse.cpu().numpy(), ref[1].cpu().numpy()) <= 2e-3
+
+
+def test_malformed_row_ranges_are_skipped_and_reported():
+    case = make_prefill_case(_spec(3, 8, 2, 64, 16, seed=5), [2, 3, 1], [50, 60, 70])
+    good_o, good_l = run_prefill(case)
+    bad = Case(**case.__dict__)
+    bad.qo_indptr = torch.tensor([0, 2, 9, 6], dtype=torch.int32)  # request 1 claims rows 2..8 (past total_q = 6)
+    out, lse = run_prefill(bad, expect_status=-9, max_q_len=3)
+    # request 0 is untouched by the bad range; request 2's range (9 > 6 rows... negative length) is skipped too
+    assert torch.equal(out[:2].view(torch.int16), good_o[:2].view(torch.int16))
+    assert torch.isnan(out[2:].float()).all()  # never written
+
+
+def test_multi_token_step_at_full_size():
+    # the batch workload's shape with four new tokens per sequence (a speculative / multi-token step)
+    case = make_prefill_case("batch", [4] * 8, None, device="cuda")
+    out, lse = run_prefill(case)
+    rows = [(t, h) for t in range(0, 32, 3) for h in (0, 13, 31)]
+    eo, el = compare(case, out, lse, select=rows)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()

@@ -229,10 +229,11 @@ def algorithmic_bytes(case: Case, cache: str = "bf16") -> dict:
     n_pages = (lens + case.P - 1) // case.P
     row = case.D * 2 if cache == "bf16" else case.D + 4  # bytes per (token, kv head) of K (or V)
     kv = 2 * int(lens.sum()) * case.Hkv * row
-    qo = 2 * case.B * case.Hq * case.D * 2
-    lse = case.B * case.Hq * 4
+    q_rows = case.B if case.qo_indptr is None else int(case.q.shape[0])  # several rows per sequence
+    qo = 2 * q_rows * case.Hq * case.D * 2
+    lse = q_rows * case.Hq * 4
     table = int(n_pages.sum()) * 4
-    total = kv + qo + lse + table + 4 * case.B
+    total = kv + qo + lse + table + 4 * case.B + (0 if case.qo_indptr is None else 4 * (case.B + 1))
     tail = 2 * int((n_pages * case.P - lens).sum()) * case.Hkv * row
     return dict(total=total, kv=kv, q_out=qo, lse=lse, table=table, tail_bytes=tail,
                 flops=4 * int(lens.sum()) * case.Hq * case.D)
