@@ -517,13 +517,92 @@ def run_append(args) -> None:
                       "bytes_per_call": moved, "gpu_launches": args.steps}), flush=True)
 
 
+def run_step(args) -> None:
+    """One serving iteration on the batch workload: write each sequence's newest key and
+    value (the last slot of its length), then decode over its keys.  Timed per step with
+    CUDA events (L2 flushed before each step) four ways: serialised launches, programmatic
+    dependent launch (PDL), the step captured in a CUDA graph, and a graph with PDL."""
+    import torch
+    import paged_kv_gqa_gb300 as pkv
+    from workloads import algorithmic_bytes, make_case
+
+    if args.impl == "reference" or int(os.environ.get("RANK", "0")) != 0:
+        return
+    dev = torch.device("cuda", 0)
+    case = make_case("batch", device=dev)
+    fp8 = args.cache == "fp8"
+    g = torch.Generator(device=dev)
+    g.manual_seed(77)
+    kn = torch.randn(case.B, case.Hkv, case.D, generator=g, device=dev).to(torch.bfloat16)
+    vn = torch.randn(case.B, case.Hkv, case.D, generator=g, device=dev).to(torch.bfloat16)
+    pos = (case.seq_lens - 1).to(torch.int32)
+    pools = pkv.quantize_pool_fp8(case.k_cache, case.v_cache) if fp8 else None
+    ws = torch.zeros(pkv.paged_decode_attn_workspace_size(case.B, case.Hq, case.Hkv, case.D, case.P, case.max_pages,
+                                                          cache=args.cache), dtype=torch.uint8, device=dev)
+    out = torch.empty(case.B, case.Hq, case.D, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(case.B, case.Hq, dtype=torch.float32, device=dev)
+    flush = L2Flush(torch, dev, getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 << 20))
+    stream = torch.cuda.Stream(dev)
+
+    def step():
+        if fp8:
+            pkv.paged_kv_append_fp8(kn, vn, case.block_table, pos, *pools, stream=stream)
+            pkv.paged_decode_attn_fp8(case.q, *pools, case.block_table, case.seq_lens, case.scale, out, lse, ws,
+                                      stream=stream)
+        else:
+            pkv.paged_kv_append(kn, vn, case.block_table, pos, case.k_cache, case.v_cache, stream=stream)
+            pkv.paged_decode_attn(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens, case.scale,
+                                  out, lse, ws, stream=stream)
+
+    def timed(run):
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                flush.fill_(1)
+                run()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)]
+            for s_, e_ in ev:
+                flush.fill_(2)
+                s_.record(stream)
+                run()
+                e_.record(stream)
+        torch.cuda.synchronize()
+        return sum(s_.elapsed_time(e_) for s_, e_ in ev) / len(ev) * 1e3
+
+    res = {}
+    for mode in ("serialised", "pdl", "graph", "graph+pdl"):
+        pkv.set_programmatic_launch("pdl" in mode)
+        if mode.startswith("graph"):
+            with torch.cuda.stream(stream):
+                step()  # first calls outside capture (attribute setup, tensor-map cache)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                step()
+            res[mode] = timed(graph.replay)
+        else:
+            res[mode] = timed(step)
+    pkv.set_programmatic_launch(False)
+    assert pkv.pkv_check_status(ws) == 0
+    ab = algorithmic_bytes(case, cache=args.cache)["total"] + 2 * 2 * case.B * case.Hkv * case.D * 2
+    best = min(res.values())
+    print(json.dumps({"metric": "decode step (KV append + paged decode attention): us/step", "value": round(best, 3),
+                      "unit": "us", "higher_is_better": False, "steps": args.steps, "warmup": args.warmup,
+                      "us_per_step": {k: round(v, 3) for k, v in res.items()},
+                      "gb_per_s_best": round(ab / (best * 1e-6) / 1e9, 1),
+                      "config": {"workload": "step", "base": "batch", "cache": args.cache, "B": case.B, "Hq": case.Hq,
+                                 "Hkv": case.Hkv, "D": case.D, "page_size": case.P,
+                                 "l2": "flushed before every timed step (write 2 x L2, read another 2 x L2)"},
+                      "gpu_launches": 2 * args.steps * 4}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="batch",
-                    choices=["tiny", "batch", "ragged", "long", "bigpage", "bigpage_g16", "append"])
+                    choices=["tiny", "batch", "ragged", "long", "bigpage", "bigpage_g16", "append", "step"])
     ap.add_argument("--cache", default="bf16", choices=["bf16", "fp8"])
     ap.add_argument("--q-len", type=int, default=1,
                     help="new tokens per sequence (causal multi-token step); 1 = decode")
@@ -538,6 +617,8 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.workload == "append":
         run_append(args)
+    elif args.workload == "step":
+        run_step(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

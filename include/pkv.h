@@ -80,6 +80,19 @@ PKV_API const char *pkv_status_string(int status);
 /* Library version as 10000*major + 100*minor + patch. */
 PKV_API int pkv_version(void);
 
+/*
+ * Programmatic dependent launch (PDL).  enable != 0: every later launch by this
+ * library (any stream, any thread of the process) carries the
+ * programmatic-stream-serialization attribute, so a kernel may begin launching
+ * while the previous kernel in its stream still runs; each kernel waits for that
+ * kernel's completion (griddepcontrol.wait) before reading any input, so results
+ * are unchanged.  The KV append lets the following kernel launch at once; the decode
+ * kernel lets it launch once its blocks have streamed their keys.  The overlap
+ * hides the launch gap between the steps of a decode iteration (append, then
+ * attention), also inside CUDA graphs.  Returns the previous setting (0 at load).
+ */
+PKV_API int pkv_set_programmatic_launch(int enable);
+
 /* ------------------------------------------------------------------ planning */
 
 /*

@@ -11,13 +11,20 @@
 #include <cstring>
 #include <mutex>
 
+#include <atomic>
+
 #include "append_kernel.cuh"
 #include "decode_launch.cuh"
+#include "launch_util.h"
 #include "merge_kernel.cuh"
 #include "pkv.h"
 #include "plan.h"
 
 namespace pkv {
+
+std::atomic<int> g_pdl{0};
+bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
+
 namespace {
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s: far above any healthy copy
@@ -173,12 +180,11 @@ pkv_status launch_merge(int D, const MergeParams &mp, cudaStream_t stream)
     const int rows = mp.B * mp.Hq;
     dim3 grid((rows + kMergeWarps - 1) / kMergeWarps), block(kMergeWarps * 32);
     switch (D) {
-        case 64: merge_kernel<64><<<grid, block, 0, stream>>>(mp); break;
-        case 128: merge_kernel<128><<<grid, block, 0, stream>>>(mp); break;
-        case 256: merge_kernel<256><<<grid, block, 0, stream>>>(mp); break;
+        case 64: return launch_kernel(merge_kernel<64>, grid, block, 0, stream, mp) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+        case 128: return launch_kernel(merge_kernel<128>, grid, block, 0, stream, mp) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+        case 256: return launch_kernel(merge_kernel<256>, grid, block, 0, stream, mp) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
         default: return PKV_ERR_UNSUPPORTED;
     }
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 // The fp8 cache's scale tensors (on == false: a bf16 cache).
@@ -336,6 +342,8 @@ const char *pkv_status_string(int status)
 }
 
 int pkv_version(void) { return 100; }
+
+int pkv_set_programmatic_launch(int enable) { return g_pdl.exchange(enable ? 1 : 0); }
 
 pkv_status pkv_plan_query(int B, int Hq, int Hkv, int D, int page_size, int max_pages, int num_sms, int num_splits,
                           pkv_plan *plan)
@@ -533,8 +541,10 @@ pkv_status paged_kv_append(const pkv_bf16 *k_new, const pkv_bf16 *v_new, const i
     ap.num_pages = num_pages;
     ap.max_pages = max_pages;
     const long units = (long)B * Hkv;
-    kv_append_kernel<<<(unsigned)((units + kAppendWarps - 1) / kAppendWarps), kAppendWarps * 32, 0, stream>>>(ap);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    return launch_kernel(kv_append_kernel, dim3((unsigned)((units + kAppendWarps - 1) / kAppendWarps)),
+                         dim3(kAppendWarps * 32), 0, stream, ap) == cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
 }
 
 pkv_status paged_kv_append_fp8(const pkv_bf16 *k_new, const pkv_bf16 *v_new, const int32_t *block_table,
@@ -566,13 +576,14 @@ pkv_status paged_kv_append_fp8(const pkv_bf16 *k_new, const pkv_bf16 *v_new, con
     ap.max_pages = max_pages;
     const long units = (long)B * Hkv;
     const unsigned grid = (unsigned)((units + kAppendWarps - 1) / kAppendWarps);
+    cudaError_t e;
     switch (D) {
-        case 64: kv_append_fp8_kernel<64><<<grid, kAppendWarps * 32, 0, stream>>>(ap); break;
-        case 128: kv_append_fp8_kernel<128><<<grid, kAppendWarps * 32, 0, stream>>>(ap); break;
-        case 256: kv_append_fp8_kernel<256><<<grid, kAppendWarps * 32, 0, stream>>>(ap); break;
+        case 64: e = launch_kernel(kv_append_fp8_kernel<64>, dim3(grid), dim3(kAppendWarps * 32), 0, stream, ap); break;
+        case 128: e = launch_kernel(kv_append_fp8_kernel<128>, dim3(grid), dim3(kAppendWarps * 32), 0, stream, ap); break;
+        case 256: e = launch_kernel(kv_append_fp8_kernel<256>, dim3(grid), dim3(kAppendWarps * 32), 0, stream, ap); break;
         default: return PKV_ERR_UNSUPPORTED;
     }
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 pkv_status pkv_check_status(const void *workspace, cudaStream_t stream, int *device_status)

@@ -40,6 +40,8 @@ constexpr int kAppendWarps = 8;
 
 __global__ void __launch_bounds__(kAppendWarps * 32) kv_append_kernel(const AppendParams p)
 {
+    griddep_launch_dependents();  // the decode step that follows may start launching
+    griddep_wait();               // the new rows may come from the previous kernel
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int unit = blockIdx.x * kAppendWarps + warp;  // (b, kv head)
     if (unit >= p.B * p.Hkv) return;
@@ -144,6 +146,8 @@ __device__ __forceinline__ float quantize_row_e4m3(const uint16_t *src, uint8_t 
 template <int D>
 __global__ void __launch_bounds__(kAppendWarps * 32) kv_append_fp8_kernel(const Fp8AppendParams p)
 {
+    griddep_launch_dependents();
+    griddep_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int unit = blockIdx.x * kAppendWarps + warp;  // (b, kv head)
     if (unit >= p.B * p.Hkv) return;

@@ -171,6 +171,15 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
     const int g = lane >> 2, cc = lane & 3;
     const int G = p.G;
 
+    // Launched with PDL, the block gets here while the previous kernel (say the KV
+    // append) may still run: fetch the tensor maps (kernel parameters), then wait for
+    // its writes before reading any input.
+    if (threadIdx.x == 0) {
+        prefetch_tensor_map(&tmK);
+        prefetch_tensor_map(&tmV);
+    }
+    griddep_wait();
+
     // ---- length, split range ------------------------------------------------
     const int Lmax = p.max_pages * p.P;
     int L = p.seq_lens[b];
@@ -239,10 +248,6 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
     int *sm_tab = reinterpret_cast<int *>(base + lay.table);
     float *red = reinterpret_cast<float *>(base);  // reuses the ring after the main loop
 
-    if (threadIdx.x == 0) {  // the first copies need the tensor maps: fetch them early
-        prefetch_tensor_map(&tmK);
-        prefetch_tensor_map(&tmV);
-    }
     // ---- page ids of this warp's first R stages, one per lane, straight from the block
     // table: the first copies then wait for one table read instead of the whole staging
     constexpr int kMaxBoxes = T / 8;  // boxes per stage at the smallest page size
@@ -683,6 +688,8 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
         }
     }
     (void)failed;
+
+    griddep_launch_dependents();  // streaming done: the next kernel may start launching
 
     if constexpr (KV8) {  // back to value units; the f32 denominator normalises
         const float f = exp2i(ev_run);

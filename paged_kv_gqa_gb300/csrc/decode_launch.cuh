@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "decode_kernel.cuh"
+#include "launch_util.h"
 #include "plan.h"
 
 namespace pkv {
@@ -42,8 +43,8 @@ pkv_status launch_decode_variant(const CUtensorMap &mk, const CUtensorMap &mv, c
     }
     dim3 grid(Hkv * plan.q_tiles, plan.num_splits, B);
     dim3 block(plan.warps * 32);
-    kern<<<grid, block, plan.smem_bytes, stream>>>(mk, mv, p);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    return launch_kernel(kern, grid, block, (size_t)plan.smem_bytes, stream, mk, mv, p) == cudaSuccess ? PKV_OK
+                                                                                              : PKV_ERR_CUDA;
 }
 
 #define PKV_V(DD, NN, KV8, MQ) launch_decode_variant<DD, NN, KV8, MQ>(mk, mv, p, plan, B, Hkv, device, stream)

@@ -37,6 +37,7 @@ constexpr int kMergeWarps = 4;
 template <int D>
 __global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const MergeParams p)
 {
+    griddep_wait();  // the partials may come from the previous kernel (PDL)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row = blockIdx.x * kMergeWarps + warp;
     const int rows = p.B * p.Hq;

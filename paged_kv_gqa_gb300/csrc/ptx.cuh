@@ -77,6 +77,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     return false;
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+
+// Waits until the grids this one depends on (PDL) have completed and their memory is
+// visible; returns at once when the launch has no such dependency.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next grid in the stream (launched with PDL) start launching its blocks.  It
+// still waits in griddep_wait for this grid to complete, so this is a scheduling hint.
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 // ------------------------------------------------------------------ TMA
 
 // 3-D tiled tensor copy global -> shared, completing on an mbarrier, with an

@@ -1,0 +1,118 @@
+"""Programmatic dependent launch (PDL) and graph capture of a decode step on the GPU.
+
+With PDL on, each kernel of the library may start launching while the previous one runs
+and waits (griddepcontrol.wait) before reading its inputs, so the results must equal the
+serialised launches bit for bit: an append followed at once by the decode that reads the
+appended keys, repeated back to back, on both caches, eagerly and inside a CUDA graph.
+"""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_gqa_gb300 as pkv
+from paged_kv_gqa_gb300 import _build
+from workloads import make_case
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    _build.build()
+    lib = pkv.load()
+    yield lib
+    pkv.set_programmatic_launch(False)
+
+
+class Step:
+    """One decode iteration on the batch shape: write each sequence's newest key and value
+    (the last slot of its length), then attend over all its keys."""
+
+    def __init__(self, cache, seed):
+        c = make_case(dict(B=8, Hq=32, Hkv=8, D=128, P=16, lens=("uniform", 200, 3000), seed=seed), device="cuda")
+        self.c = c
+        self.cache = cache
+        g = torch.Generator(device="cuda")
+        g.manual_seed(seed + 1)
+        self.steps = 6
+        self.kn = [torch.randn(c.B, c.Hkv, c.D, generator=g, device="cuda").to(torch.bfloat16) for _ in range(self.steps)]
+        self.vn = [torch.randn(c.B, c.Hkv, c.D, generator=g, device="cuda").to(torch.bfloat16) for _ in range(self.steps)]
+        self.pos = (c.seq_lens - 1).to(torch.int32)
+        if cache == "fp8":
+            self.pools = list(pkv.quantize_pool_fp8(c.k_cache, c.v_cache))
+        self.k0 = c.k_cache.clone()
+        self.v0 = c.v_cache.clone()
+        ws = pkv.paged_decode_attn_workspace_size(c.B, c.Hq, c.Hkv, c.D, c.P, c.max_pages, cache=cache)
+        self.ws = torch.zeros(ws, dtype=torch.uint8, device="cuda")
+        self.out = torch.empty(self.steps, c.B, c.Hq, c.D, dtype=torch.bfloat16, device="cuda")
+        self.lse = torch.empty(self.steps, c.B, c.Hq, dtype=torch.float32, device="cuda")
+
+    def reset(self):
+        # in place: a captured graph keeps the addresses of these tensors
+        self.c.k_cache.copy_(self.k0)
+        self.c.v_cache.copy_(self.v0)
+        if self.cache == "fp8":
+            for dst, src in zip(self.pools, pkv.quantize_pool_fp8(self.c.k_cache, self.c.v_cache)):
+                dst.copy_(src)
+        self.out.fill_(float("nan"))
+        self.lse.fill_(float("nan"))
+
+    def run(self, stream=None):
+        c = self.c
+        for i in range(self.steps):
+            if self.cache == "fp8":
+                pkv.paged_kv_append_fp8(self.kn[i], self.vn[i], c.block_table, self.pos, *self.pools, stream=stream)
+                pkv.paged_decode_attn_fp8(c.q, *self.pools, c.block_table, c.seq_lens, c.scale, self.out[i],
+                                          self.lse[i], self.ws, stream=stream)
+            else:
+                pkv.paged_kv_append(self.kn[i], self.vn[i], c.block_table, self.pos, c.k_cache, c.v_cache,
+                                    stream=stream)
+                pkv.paged_decode_attn(c.q, c.k_cache, c.v_cache, c.block_table, c.seq_lens, c.scale, self.out[i],
+                                      self.lse[i], self.ws, stream=stream)
+
+
+@pytest.mark.parametrize("cache", ["bf16", "fp8"])
+def test_pdl_results_equal_serialised_launches(cache):
+    st = Step(cache, seed=11)
+    pkv.set_programmatic_launch(False)
+    st.reset()
+    st.run()
+    torch.cuda.synchronize()
+    ref_o, ref_l = st.out.clone(), st.lse.clone()
+    assert torch.isfinite(ref_o.float()).all()
+    # each step's output depends on the key appended just before it
+    assert not torch.equal(ref_o[0], ref_o[1])
+    assert pkv.set_programmatic_launch(True) is False
+    for _ in range(3):
+        st.reset()
+        st.run()
+        torch.cuda.synchronize()
+        assert torch.equal(st.out.view(torch.int16), ref_o.view(torch.int16))
+        assert torch.equal(st.lse.view(torch.int32), ref_l.view(torch.int32))
+    assert pkv.pkv_check_status(st.ws) == 0
+    pkv.set_programmatic_launch(False)
+
+
+@pytest.mark.parametrize("cache", ["bf16", "fp8"])
+def test_pdl_inside_a_cuda_graph(cache):
+    st = Step(cache, seed=12)
+    pkv.set_programmatic_launch(False)
+    st.reset()
+    st.run()
+    torch.cuda.synchronize()
+    ref_o, ref_l = st.out.clone(), st.lse.clone()
+    pkv.set_programmatic_launch(True)
+    st.reset()
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        st.run(stream=s)
+    for _ in range(2):
+        st.reset()
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(st.out.view(torch.int16), ref_o.view(torch.int16))
+        assert torch.equal(st.lse.view(torch.int32), ref_l.view(torch.int32))
+    pkv.set_programmatic_launch(False)
