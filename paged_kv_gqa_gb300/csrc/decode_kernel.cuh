@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
     decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const DecodeParams p)
 {
-    constexpr int T = Tiling<D>::T;
+    constexpr int T = stage_keys(D, NT, KV8);
     constexpr int W = Tiling<D>::W;
     constexpr int R = ring_depth(D, NT, KV8);
     constexpr int DC = D / 64;            // 128-byte box columns per key row

@@ -85,7 +85,8 @@ pkv_status make_plan(int B, int Hq, int Hkv, int D, int page_size, int max_pages
     if (B > 65535) return PKV_ERR_UNSUPPORTED;  // sequences are the grid's z dimension
     const long out_rows = total_rows > 0 ? total_rows : (long)B * Hq;
 
-    const RuntimeTiling t = tiling_for(D);
+    RuntimeTiling t = tiling_for(D);
+    t.T = stage_keys(D, NT, kv8);
     const int max_tokens = max_pages * page_size;
     const int units = std::max(1, (int)(B * Hkv * q_tiles));
 

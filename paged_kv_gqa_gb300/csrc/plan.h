@@ -43,12 +43,18 @@ PKV_HD constexpr int target_blocks(int D, int NT, bool kv8)
     return D == 256 ? ((kv8 && NT <= 2) ? 2 : 1) : NT == 1 ? 3 : 2;
 }
 
+// Keys per stage: the fp8 kernel with one head tile at D = 128 takes 32 (two mma
+// tiles), so the per-stage work (wait, copy issue, scale bookkeeping) is spread over
+// twice the keys; everything else takes the tiling's T.
+PKV_HD constexpr int stage_keys(int D, int NT, bool kv8) { return (kv8 && D == 128 && NT == 1) ? 32 : (D == 64 ? 32 : 16); }
+
 // Ring depth per warp (stages in flight), sized so a block's ring fits its share of
 // shared memory: an fp8 stage is half the bytes of a bf16 one.
 PKV_HD constexpr int ring_depth(int D, int NT, bool kv8)
 {
     return D == 256 ? (kv8 ? (target_blocks(D, NT, kv8) == 2 ? 3 : 6) : 3)
-                    : target_blocks(D, NT, kv8) >= 3 ? (kv8 ? 4 : 2) : (kv8 ? 6 : 3);
+                    : target_blocks(D, NT, kv8) >= 3 ? (kv8 ? (stage_keys(D, NT, kv8) == 32 && D == 128 ? 2 : 4) : 2)
+                                                     : (kv8 ? 6 : 3);
 }
 
 // Shared-memory carve-up of one decode block (byte offsets from a 1024-aligned
