@@ -358,6 +358,7 @@ def run_pkv(args) -> None:
     if dist:
         dist.barrier()
     clocks = sampler.stop()
+    floor_us = _event_floor_us(torch, flush, stream)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     mean_ms = sum(step_ms) / len(step_ms)
     mean_ms = max_over_ranks(mean_ms, dist, dev)
@@ -403,10 +404,28 @@ def run_pkv(args) -> None:
         "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_call * args.steps,
         "clocks": clocks, "device_status": status, "wall_s_timed_region": round(t_wall, 3),
+        "event_floor_us": floor_us,
     }
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def _event_floor_us(torch, flush, stream, n=200):
+    """Mean time of a trivial kernel timed exactly like a step (events after the same flush):
+    the launch and event overhead under every step time."""
+    tiny = torch.zeros(16, device=flush.wbuf.device)
+    for _ in range(10):
+        flush.fill_(1)
+        tiny.add_(1)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for s_, e_ in ev:
+        flush.fill_(1)
+        s_.record(stream)
+        tiny.add_(1)
+        e_.record(stream)
+    torch.cuda.synchronize()
+    return round(sum(s_.elapsed_time(e_) for s_, e_ in ev) / n * 1e3, 3)
 
 
 def _quantiles(xs):
