@@ -57,8 +57,23 @@ def measured_peaks() -> dict:
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "source": "fallback"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d.get("bf16_tflops", 1900.0)),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def causal_flops(case) -> int:
+    """Multiply-add flops of a causal several-rows call: row i of a request with n rows and
+    L keys sees L - n + i + 1 keys; each key costs 4 D flops per query head (scores, PV)."""
+    import numpy as np
+    lens = case.seq_lens.cpu().numpy().astype(np.int64)
+    qo = case.qo_indptr.cpu().numpy().astype(np.int64)
+    keys = 0
+    for b in range(case.B):
+        n, L = int(qo[b + 1] - qo[b]), int(lens[b])
+        i = np.arange(n)
+        keys += int(np.clip(L - n + i + 1, 0, L).sum())
+    return 4 * keys * case.Hq * case.D
 
 
 def profiled_traffic(workload: str):
@@ -292,6 +307,7 @@ def run_pkv(args) -> None:
     else:
         case = make_case(args.workload, device=dev)
     fp8 = args.cache == "fp8"
+    pkv.set_prefill_tensor_cores(bool(getattr(args, "tc", 1)))
     pools8 = None
     if fp8:  # quantise the pools on the device, then drop the bf16 copies
         pools8 = pkv.quantize_pool_fp8(case.k_cache, case.v_cache)
@@ -405,6 +421,12 @@ def run_pkv(args) -> None:
         "gpu_launches": launches_per_call * args.steps,
         "clocks": clocks, "device_status": status, "wall_s_timed_region": round(t_wall, 3),
         "event_floor_us": floor_us,
+        "tensor": None if q_len == 1 else {
+            "kernel": "prefill_tc_kernel (tcgen05)" if (getattr(args, "tc", 1) and not fp8 and case.D == 128 and
+                                                         q_len * case.G >= 128) else "decode_split_kernel<multi-row>",
+            "tflops": round(causal_flops(case) / (mean_ms * 1e-3) / 1e12, 2),
+            "peak_tflops": peaks["bf16_tflops"],
+            "frac": round(causal_flops(case) / (mean_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)},
     }
     print(json.dumps(line), flush=True)
     if dist:
@@ -625,6 +647,7 @@ def main():
     ap.add_argument("--cache", default="bf16", choices=["bf16", "fp8"])
     ap.add_argument("--q-len", type=int, default=1,
                     help="new tokens per sequence (causal multi-token step); 1 = decode")
+    ap.add_argument("--tc", type=int, default=1, help="several-rows calls: 1 = tensor-core kernel where it applies")
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)

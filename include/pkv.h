@@ -93,6 +93,16 @@ PKV_API int pkv_version(void);
  */
 PKV_API int pkv_set_programmatic_launch(int enable);
 
+/*
+ * Tensor-core path of paged_prefill_attn (bf16 cache, D = 128, at least 128
+ * (token, query head) rows per (sequence, kv head) group, i.e. max_q_len * Hq/Hkv
+ * >= 128): one CTA per 128 rows runs the score and PV products on tcgen05 (5th-
+ * generation tensor cores, accumulators in tensor memory).  On by default; with
+ * enable = 0 such calls take the mma.sync kernel (for comparisons).  Process-wide;
+ * returns the previous setting.
+ */
+PKV_API int pkv_set_prefill_tensor_cores(int enable);
+
 /* ------------------------------------------------------------------ planning */
 
 /*

@@ -19,7 +19,7 @@ __all__ = [
     "paged_decode_attn", "paged_decode_attn_ex", "split_kv_merge", "pkv_check_status",
     "pkv_reset_status", "pkv_selftest_wait_timeout", "paged_decode_attn_static_scratch", "paged_kv_append",
     "paged_decode_attn_fp8", "paged_kv_append_fp8", "quantize_pool_fp8", "paged_prefill_attn",
-    "paged_prefill_attn_workspace_size", "prefill_plan_query", "set_programmatic_launch",
+    "paged_prefill_attn_workspace_size", "prefill_plan_query", "set_programmatic_launch", "set_prefill_tensor_cores",
     "EXPORTED_SYMBOLS",
     "STATUS",
 ]
@@ -41,6 +41,7 @@ EXPORTED_SYMBOLS = [
     "paged_kv_append", "paged_decode_attn_fp8", "paged_kv_append_fp8", "pkv_plan_query_kv",
     "paged_decode_attn_workspace_size_kv", "paged_prefill_attn", "paged_prefill_attn_fp8",
     "pkv_plan_query_prefill", "paged_prefill_attn_workspace_size", "pkv_set_programmatic_launch",
+    "pkv_set_prefill_tensor_cores",
 ]
 
 KV_DTYPES = {"bf16": 0, "fp8": 1}
@@ -99,6 +100,7 @@ def load(path: str = LIB_PATH):
                                            P]),
             "pkv_plan_query_prefill": (I, [I, I, I, I, I, I, I, I, I, I, I, ctypes.POINTER(PkvPlan)]),
             "pkv_set_programmatic_launch": (I, [I]),
+            "pkv_set_prefill_tensor_cores": (I, [I]),
             "paged_prefill_attn_workspace_size": (I, [I, I, I, I, I, I, I, I, I, I, I, ctypes.POINTER(S)]),
             "paged_kv_append_fp8": (I, [P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P]),
         }
@@ -118,6 +120,12 @@ def _check(status: int, where: str):
 def set_programmatic_launch(enable: bool) -> bool:
     """Turns programmatic dependent launch on or off for every later launch; returns the old setting."""
     return bool(load().pkv_set_programmatic_launch(int(bool(enable))))
+
+
+def set_prefill_tensor_cores(enable: bool) -> bool:
+    """Routes long multi-row calls (bf16, D=128, >= 128 rows per group) to the tcgen05 kernel
+    (default) or the mma.sync kernel; returns the old setting."""
+    return bool(load().pkv_set_prefill_tensor_cores(int(bool(enable))))
 
 
 def status_string(status: int) -> str:

@@ -16,6 +16,7 @@
 #include "append_kernel.cuh"
 #include "decode_launch.cuh"
 #include "launch_util.h"
+#include "prefill_tc_kernel.cuh"
 #include "merge_kernel.cuh"
 #include "pkv.h"
 #include "plan.h"
@@ -24,6 +25,7 @@ namespace pkv {
 
 std::atomic<int> g_pdl{0};
 bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
+std::atomic<int> g_prefill_tc{1};
 
 namespace {
 
@@ -199,6 +201,64 @@ struct MultiRows {
     int total_q = 0, max_q_len = 0, causal = 0;
 };
 
+// Several rows per sequence with at least 128 rows per (sequence, kv head) group, bf16
+// cache, D = 128: the tensor-core kernel (prefill_tc_kernel.cuh), one CTA per 128 rows,
+// no key splits (the rows give the parallelism).  Needs only the workspace's status word.
+pkv_status prefill_tc(const pkv_bf16 *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
+                      const int32_t *seq_lens, int B, int Hq, int Hkv, int page_size, int num_pages, int max_pages,
+                      float scale, pkv_bf16 *out, float *lse, void *workspace, const MultiRows &mr, int device,
+                      cudaStream_t stream)
+{
+    constexpr int D = 128;
+    const int box_t = page_size < kTcKeys ? page_size : kTcKeys;
+    CUtensorMap mk, mv;
+    pkv_status st = get_pool_map(k_cache, num_pages, page_size, Hkv, D, box_t, device, 3, &mk);
+    if (st != PKV_OK) return st;
+    st = get_pool_map(v_cache, num_pages, page_size, Hkv, D, box_t, device, 3, &mv);
+    if (st != PKV_OK) return st;
+    const int G = Hq / Hkv;
+    const long q_tiles = ((long)mr.max_q_len * G + kTcRows - 1) / kTcRows;
+    if ((long)Hkv * q_tiles >= (1l << 31) || B > 65535) return PKV_ERR_UNSUPPORTED;
+    static bool attr_set[64] = {};
+    static std::mutex mu;
+    if (device < 0 || device >= 64) return PKV_ERR_UNSUPPORTED;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!attr_set[device]) {
+            if (cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     TcSmem::dynamic) != cudaSuccess)
+                return PKV_ERR_CUDA;
+            attr_set[device] = true;
+        }
+    }
+    PrefillTcParams p;
+    p.q = reinterpret_cast<const __nv_bfloat16 *>(q);
+    p.qo_indptr = mr.qo_indptr;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    p.lse = lse;
+    p.status = static_cast<int *>(workspace);
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = G;
+    p.P = page_size;
+    p.log2P = log2_exact(page_size);
+    p.num_pages = num_pages;
+    p.max_pages = max_pages;
+    p.total_q = mr.total_q;
+    p.max_q_len = mr.max_q_len;
+    p.causal = mr.causal;
+    p.q_tiles = (int)q_tiles;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+    p.wait_limit_ns = kWaitLimitNs;
+    return launch_kernel(prefill_tc_kernel, dim3((unsigned)(Hkv * q_tiles), (unsigned)B), dim3(128),
+                         (size_t)TcSmem::dynamic, stream, mk, mv, p) == cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
+}
+
 pkv_status decode_impl(const pkv_bf16 *q, const void *k_cache, const void *v_cache, Fp8Scales fp8,
                        const int32_t *block_table, const int32_t *seq_lens, int B, int Hq, int Hkv, int D,
                        int page_size, int num_pages, int max_pages, float scale, pkv_bf16 *out, float *lse,
@@ -225,6 +285,9 @@ pkv_status decode_impl(const pkv_bf16 *q, const void *k_cache, const void *v_cac
     int device = 0, sms = 0;
     pkv_status st = current_device_sms(&device, &sms);
     if (st != PKV_OK) return st;
+    if (mq && !kv8 && D == 128 && group_rows >= kTcRows && g_prefill_tc.load(std::memory_order_relaxed))
+        return prefill_tc(q, k_cache, v_cache, block_table, seq_lens, B, Hq, Hkv, page_size, num_pages, max_pages,
+                          scale, out, lse, workspace, mr, device, stream);
     pkv_plan plan;
     st = make_plan(B, Hq, Hkv, D, page_size, max_pages, sms, num_splits, &plan, kv8, group_rows, total_rows);
     if (st != PKV_OK) return st;
@@ -344,6 +407,8 @@ const char *pkv_status_string(int status)
 int pkv_version(void) { return 100; }
 
 int pkv_set_programmatic_launch(int enable) { return g_pdl.exchange(enable ? 1 : 0); }
+
+int pkv_set_prefill_tensor_cores(int enable) { return g_prefill_tc.exchange(enable ? 1 : 0); }
 
 pkv_status pkv_plan_query(int B, int Hq, int Hkv, int D, int page_size, int max_pages, int num_sms, int num_splits,
                           pkv_plan *plan)

@@ -137,3 +137,51 @@ def test_multi_token_step_at_full_size():
     eo, el = compare(case, out, lse, select=rows)
     assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
     assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+
+
+# ------------------------------------------------------------------ the tensor-core path
+# bf16 cache, D = 128, at least 128 (token, head) rows per (sequence, kv head) group
+
+TC = [
+    # B, Hq, Hkv, D, P, q_lens, kv_lens
+    (3, 32, 8, 128, 16, [40, 33, 64], [40, 500, 2000]),   # G = 4: 160, 132, 256 rows
+    (2, 8, 1, 128, 64, [20, 17], [300, 17]),               # G = 8, a request as long as its cache
+    (1, 16, 2, 128, 8, [130], [130]),                      # 1040 rows: 9 tiles, 8-key pages
+    (2, 32, 8, 128, 256, [64, 3], [600, 5]),               # 256-key pages; a short request in the batch
+    (2, 16, 4, 128, 32, [70, 0], [70, 40]),                # an empty request
+]
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("B,Hq,Hkv,D,P,q_lens,kv_lens", TC, ids=lambda x: str(x).replace(" ", ""))
+def test_tensor_core_path_full_oracle(B, Hq, Hkv, D, P, q_lens, kv_lens, causal):
+    pkv.set_prefill_tensor_cores(True)
+    case = make_prefill_case(_spec(B, Hq, Hkv, D, P, seed=3 * B + P + sum(q_lens)), q_lens, kv_lens, poison=True)
+    out, lse = run_prefill(case, causal=causal)
+    eo, el = compare(case, out, lse, causal=causal)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+
+
+def test_tensor_core_and_mma_sync_paths_agree():
+    case = make_prefill_case(_spec(2, 32, 8, 128, 16, seed=9), [48, 40], [1000, 300])
+    pkv.set_prefill_tensor_cores(False)
+    ref_o, ref_l = run_prefill(case)
+    pkv.set_prefill_tensor_cores(True)
+    out, lse = run_prefill(case)
+    excess, _, _ = split_invariance_violation(out.float().cpu().numpy(), ref_o.float().cpu().numpy(), tol=OUT_TOL)
+    assert excess <= 0
+    assert max_abs_diff(lse.cpu().numpy(), ref_l.cpu().numpy()) <= 1e-4
+
+
+def test_tensor_core_path_bad_page_is_skipped_and_reported():
+    case = make_prefill_case(_spec(2, 32, 8, 128, 16, seed=10), [40, 40], [200, 300])
+    bt = case.block_table.clone()
+    bt[1, 3] = case.num_pages + 7
+    bad = Case(**case.__dict__)
+    bad.block_table = bt
+    pkv.set_prefill_tensor_cores(True)
+    out, lse = run_prefill(bad, expect_status=-6)
+    # request 0 is untouched; request 1 attends to its other keys only
+    o0, l0 = run_prefill(case)
+    assert torch.equal(out[:40].view(torch.int16), o0[:40].view(torch.int16))
+    assert torch.isfinite(out.float()).all()
