@@ -307,7 +307,7 @@ def run_pkv(args) -> None:
     else:
         case = make_case(args.workload, device=dev)
     fp8 = args.cache == "fp8"
-    pkv.set_prefill_tensor_cores(bool(getattr(args, "tc", 1)))
+    pkv.set_prefill_tensor_cores({0: "off", 1: "auto", 2: "always"}[getattr(args, "tc", 1)])
     pools8 = None
     if fp8:  # quantise the pools on the device, then drop the bf16 copies
         pools8 = pkv.quantize_pool_fp8(case.k_cache, case.v_cache)
@@ -422,8 +422,8 @@ def run_pkv(args) -> None:
         "clocks": clocks, "device_status": status, "wall_s_timed_region": round(t_wall, 3),
         "event_floor_us": floor_us,
         "tensor": None if q_len == 1 else {
-            "kernel": "prefill_tc_kernel (tcgen05)" if (getattr(args, "tc", 1) and not fp8 and case.D == 128 and
-                                                         q_len * case.G >= 128) else "decode_split_kernel<multi-row>",
+            "kernel": "prefill_tc_kernel (tcgen05)" if _takes_tensor_cores(args, case, q_len, fp8, props)
+                      else "decode_split_kernel<multi-row>",
             "tflops": round(causal_flops(case) / (mean_ms * 1e-3) / 1e12, 2),
             "peak_tflops": peaks["bf16_tflops"],
             "frac": round(causal_flops(case) / (mean_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)},
@@ -558,6 +558,15 @@ def run_append(args) -> None:
                       "bytes_per_call": moved, "gpu_launches": args.steps}), flush=True)
 
 
+def _takes_tensor_cores(args, case, q_len, fp8, props) -> bool:
+    """The library's routing of a several-rows call (see pkv_set_prefill_tensor_cores)."""
+    mode = getattr(args, "tc", 1)
+    rows = q_len * case.G
+    if mode == 0 or fp8 or case.D != 128 or rows < 128 or case.scale <= 0:
+        return False
+    return mode == 2 or case.B * case.Hkv * -(-rows // 128) >= props.multi_processor_count
+
+
 def run_step(args) -> None:
     """One serving iteration on the batch workload: write each sequence's newest key and
     value (the last slot of its length), then decode over its keys.  Timed per step with
@@ -647,7 +656,9 @@ def main():
     ap.add_argument("--cache", default="bf16", choices=["bf16", "fp8"])
     ap.add_argument("--q-len", type=int, default=1,
                     help="new tokens per sequence (causal multi-token step); 1 = decode")
-    ap.add_argument("--tc", type=int, default=1, help="several-rows calls: 1 = tensor-core kernel where it applies")
+    ap.add_argument("--tc", type=int, default=1, choices=[0, 1, 2],
+                    help="several-rows calls: 0 = mma.sync kernel, 1 = library routing (tensor cores when the grid "
+                         "fills the GPU), 2 = tensor-core kernel wherever it applies")
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)

@@ -122,10 +122,22 @@ def set_programmatic_launch(enable: bool) -> bool:
     return bool(load().pkv_set_programmatic_launch(int(bool(enable))))
 
 
-def set_prefill_tensor_cores(enable: bool) -> bool:
-    """Routes long multi-row calls (bf16, D=128, >= 128 rows per group) to the tcgen05 kernel
-    (default) or the mma.sync kernel; returns the old setting."""
-    return bool(load().pkv_set_prefill_tensor_cores(int(bool(enable))))
+TC_MODES = {"off": 0, "auto": 1, "always": 2}
+
+
+def set_prefill_tensor_cores(mode="auto") -> str:
+    """Routing of long multi-row calls (bf16, D=128, >= 128 rows per group): "off" = the
+    mma.sync kernel, "auto" (default) = the tcgen05 kernel when its grid has at least one
+    CTA per SM, "always" = the tcgen05 kernel.  True/False mean "auto"/"off".  Returns the
+    previous mode."""
+    if isinstance(mode, bool):
+        mode = "auto" if mode else "off"
+    if mode not in TC_MODES:
+        raise ValueError("mode must be one of %s" % sorted(TC_MODES))
+    old = load().pkv_set_prefill_tensor_cores(TC_MODES[mode])
+    if old < 0:
+        raise PkvError(old, "pkv_set_prefill_tensor_cores")
+    return {v: k for k, v in TC_MODES.items()}[old]
 
 
 def status_string(status: int) -> str:

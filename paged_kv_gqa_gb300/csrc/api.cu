@@ -25,7 +25,7 @@ namespace pkv {
 
 std::atomic<int> g_pdl{0};
 bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
-std::atomic<int> g_prefill_tc{1};
+std::atomic<int> g_prefill_tc{PKV_TC_AUTO};
 
 namespace {
 
@@ -202,7 +202,7 @@ struct MultiRows {
 };
 
 // Several rows per sequence with at least 128 rows per (sequence, kv head) group, bf16
-// cache, D = 128: the tensor-core kernel (prefill_tc_kernel.cuh), one CTA per 128 rows,
+// cache, D = 128, scale > 0: the tensor-core kernel (prefill_tc_kernel.cuh), one CTA per 128 rows,
 // no key splits (the rows give the parallelism).  Needs only the workspace's status word.
 pkv_status prefill_tc(const pkv_bf16 *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
                       const int32_t *seq_lens, int B, int Hq, int Hkv, int page_size, int num_pages, int max_pages,
@@ -253,7 +253,7 @@ pkv_status prefill_tc(const pkv_bf16 *q, const void *k_cache, const void *v_cach
     p.q_tiles = (int)q_tiles;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
     p.wait_limit_ns = kWaitLimitNs;
-    return launch_kernel(prefill_tc_kernel, dim3((unsigned)(Hkv * q_tiles), (unsigned)B), dim3(128),
+    return launch_kernel(prefill_tc_kernel, dim3((unsigned)(Hkv * q_tiles), (unsigned)B), dim3(kTcThreads),
                          (size_t)TcSmem::dynamic, stream, mk, mv, p) == cudaSuccess
                ? PKV_OK
                : PKV_ERR_CUDA;
@@ -285,7 +285,10 @@ pkv_status decode_impl(const pkv_bf16 *q, const void *k_cache, const void *v_cac
     int device = 0, sms = 0;
     pkv_status st = current_device_sms(&device, &sms);
     if (st != PKV_OK) return st;
-    if (mq && !kv8 && D == 128 && group_rows >= kTcRows && g_prefill_tc.load(std::memory_order_relaxed))
+    const int tc_mode = g_prefill_tc.load(std::memory_order_relaxed);
+    const long tc_ctas = (long)B * Hkv * ((group_rows + kTcRows - 1) / kTcRows);
+    if (mq && !kv8 && D == 128 && group_rows >= kTcRows && scale > 0.f &&
+        (tc_mode == PKV_TC_ALWAYS || (tc_mode == PKV_TC_AUTO && tc_ctas >= sms)))
         return prefill_tc(q, k_cache, v_cache, block_table, seq_lens, B, Hq, Hkv, page_size, num_pages, max_pages,
                           scale, out, lse, workspace, mr, device, stream);
     pkv_plan plan;
@@ -408,7 +411,11 @@ int pkv_version(void) { return 100; }
 
 int pkv_set_programmatic_launch(int enable) { return g_pdl.exchange(enable ? 1 : 0); }
 
-int pkv_set_prefill_tensor_cores(int enable) { return g_prefill_tc.exchange(enable ? 1 : 0); }
+int pkv_set_prefill_tensor_cores(int mode)
+{
+    if (mode != PKV_TC_OFF && mode != PKV_TC_AUTO && mode != PKV_TC_ALWAYS) return PKV_ERR_INVALID_ARG;
+    return g_prefill_tc.exchange(mode);
+}
 
 pkv_status pkv_plan_query(int B, int Hq, int Hkv, int D, int page_size, int max_pages, int num_sms, int num_splits,
                           pkv_plan *plan)

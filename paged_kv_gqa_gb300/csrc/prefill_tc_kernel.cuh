@@ -1,24 +1,36 @@
 // prefill_tc_kernel.cuh -- several query rows per sequence on the 5th-generation tensor
 // cores (tcgen05), for groups long enough to fill 128-row tiles (chunked prefill).
 //
-// One CTA (4 warps) per 128 (token, query head) rows of one (sequence, kv head) group,
-// the rows packed token-major as in the multi-row decode kernel (AstrAI "CUDA Kernels",
-// "Q Scheduling and KV Addressing": the query heads of one kv-head group share each
-// K/V tile).  The CTA walks the keys its rows may see in tiles of 128:
+// One CTA per 128 (token, query head) rows of one (sequence, kv head) group, the rows
+// packed token-major as in the multi-row decode kernel (AstrAI "CUDA Kernels", "Q
+// Scheduling and KV Addressing": the query heads of one kv-head group share each K/V
+// tile).  The CTA walks the keys its rows may see in tiles of 128:
 //     S  = Q K^T       tcgen05.mma M=128 rows, N=128 keys, K=D; S in tensor memory
-//     softmax          thread r owns row r = TMEM lane r: the row max and sums need no
-//                      shuffles; the base-2 online recurrence of the decode kernel
-//     O += P V         tcgen05.mma M=128 rows, N=D, K=128 keys; O in tensor memory,
-//                      rescaled in place (tcgen05.ld/st) only when a warp's running
-//                      maximum moved
+//     softmax          thread r of the softmax warps owns row r = TMEM lane r: the row
+//                      maximum and sums need no shuffles
+//     O += P V         tcgen05.mma M=128 rows, N=D, K=128 keys; O in tensor memory
+// Warp specialisation: warps 0-3 run the softmax; one lane of warp 4 issues the TMA
+// copies and the MMAs.  S is double-buffered in tensor memory, so the score MMA of tile
+// j+1 runs while the softmax warps work on tile j, and the PV MMA of tile j runs while
+// they load and exponentiate tile j+1.  K has two shared-memory stages and V three, so
+// each copy is issued two tiles ahead of its MMA.  mbarriers hand every buffer over
+// (copies: complete_tx; MMAs: tcgen05.commit; softmax: one arrival per warp).
+// The online softmax keeps a reference maximum per row and moves it only when a tile's
+// maximum exceeds it by more than 2^8 (probabilities stay <= 256, well inside f32 and
+// bf16), so O is rescaled in tensor memory (tcgen05.ld/st) only then; l and O share the
+// reference, so the result is the same softmax.  The sum of the bf16-rounded
+// probabilities that normalises O comes from the tensor cores too: one more MMA per key
+// tile multiplies P by a column of ones into a 16-column accumulator beside O.  The f32
+// sum l, kept by the softmax threads, gives the log-sum-exp.  The scores' scale must be
+// positive (the host routes other scales elsewhere): the row maximum is then taken on
+// the unscaled scores and each exponent is one FMA.
 // Q, K and V tiles sit in shared memory 128B-swizzled, K-major ([D/64][rows][64]) as the
 // TMA boxes land them; P is written by the softmax threads in the same layout; V is
-// read MN-major (N = dims contiguous).  K/V tiles are double-buffered; one thread
-// issues the copies and the MMAs, whose completions arrive on mbarriers
-// (tcgen05.commit).  Keys past the sequence's length, or in a page whose id is out of
-// range, are masked in the scores and zeroed in V's shared-memory rows (0 * NaN would
-// reach the output).  Every wait is bounded; on a timeout the status word is set, the
-// CTA stops issuing work and releases its tensor memory.
+// read MN-major (N = dims contiguous).  Keys past the last one the CTA's rows may see, or
+// in a page whose id is out of range, are masked in the scores and zeroed in V's rows
+// by the issuing lane before the PV MMA (0 * NaN would reach the output).  Every wait is
+// bounded; on a timeout the status word is set, the issuing lane waits (bounded) for its
+// copies and MMAs in flight, and every warp stops.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -42,31 +54,42 @@ struct PrefillTcParams {
     unsigned long long wait_limit_ns;
 };
 
-constexpr int kTcRows = 128;  // rows per CTA (the MMA's M)
-constexpr int kTcKeys = 128;  // keys per tile (the score MMA's N)
+constexpr int kTcRows = 128;     // rows per CTA (the MMA's M)
+constexpr int kTcKeys = 128;     // keys per tile (the score MMA's N)
+constexpr int kTcThreads = 160;  // 4 softmax warps + 1 issuing warp
+constexpr int kTcKStages = 2;
+constexpr int kTcVStages = 3;
+constexpr int kTcPageRing = 4;   // tiles whose page ids are kept
 
 // Shared memory (bytes from a 1024-aligned base) of the D = 128 kernel.
 struct TcSmem {
-    static constexpr int kTile = kTcRows * 128 * 2;  // 128 rows x 128 dims bf16, as 2 column blocks
-    static constexpr int q = 0, p = kTile;
-    static constexpr int kv = 2 * kTile;             // stage s: K at kv + s*2*kTile, V 1 tile after
-    static constexpr int bars = 6 * kTile;           // 2 copy barriers, S done, O done
-    static constexpr int ok = bars + 64;             // [2 stages][16 boxes] page-valid flags
-    static constexpr int tmem_slot = ok + 2 * 16 * 4;
+    static constexpr int kTile = kTcRows * 128 * 2;  // 128 rows x 128 dims (or keys) bf16, 2 column blocks
+    static constexpr int q = 0;
+    static constexpr int p = kTile;
+    static constexpr int k = 2 * kTile;                      // K stage s at k + s * kTile
+    static constexpr int v = k + kTcKStages * kTile;         // V stage s at v + s * kTile
+    static constexpr int ones = v + kTcVStages * kTile;      // 16 x 64 bf16 ones, the B operand of the row-sum MMA
+    static constexpr int bars = ones + 2048;                 // 32 mbarriers
+    static constexpr int pages = bars + 32 * 8;              // [kTcPageRing][16] page id of each box, -1: none
+    static constexpr int tmem_slot = pages + kTcPageRing * 16 * 4;
     static constexpr int total = tmem_slot + 16;
-    static constexpr int dynamic = total + 1024;
+    static constexpr int dynamic = total;                    // the dynamic shared memory starts 1024-aligned
 };
+static_assert(TcSmem::dynamic <= 232448, "prefill_tc_kernel: shared memory above the per-block limit");
 
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const PrefillTcParams p)
 {
     constexpr int D = 128;
     constexpr int kTile = TcSmem::kTile;
     constexpr int kBlk = kTcRows * 128;  // bytes of one 64-column block of a tile
+    const float kNegInf = __int_as_float(0xff800000);
+    constexpr float kRescaleGap = 8.f;   // move the reference maximum only past 2^8
     const int kvh = (int)(blockIdx.x % (unsigned)p.Hkv), qt = (int)(blockIdx.x / (unsigned)p.Hkv);
     const int b = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool issuer_warp = warp == 4;
     const int G = p.G;
 
     if (tid == 0) {
@@ -89,37 +112,62 @@ __global__ void __launch_bounds__(128, 1)
         if (tid == 0 && kvh == 0 && qt == 0) atomicCAS(p.status, 0, PKV_ERR_BAD_SEQ_LEN);
         L = 0;
     }
-    // this thread's row: token, head, global row, last key it may see
-    const int r = tid;
-    const bool row_ok = r < nrows;
+    // a softmax thread's row: token, head, global row, last key it may see
+    const int r = tid & 127;
+    const bool row_ok = !issuer_warp && r < nrows;
     const int tok = (row0 + (row_ok ? r : 0)) / G, head = (row0 + (row_ok ? r : 0)) % G;
     const size_t grow = (size_t)(q_base + tok) * p.Hq + kvh * G + head;
-    const int klim = p.causal ? L - n_q + tok : L - 1;
+    const int klim = !row_ok ? -1 : (p.causal ? L - n_q + tok : L - 1);
     // keys any row of the CTA may see
     const int last_tok = (row0 + nrows - 1) / G;
     const int n_keys = max(0, p.causal ? min(L, L - n_q + last_tok + 1) : L);
     const int n_tiles = (n_keys + kTcKeys - 1) / kTcKeys;
 
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw_addr = smem_addr(smem_raw);
-    const uint32_t base = (raw_addr + 1023u) & ~1023u;
-    uint8_t *sbase = smem_raw + (base - raw_addr);
-    const uint32_t sQ = base + TcSmem::q, sP = base + TcSmem::p;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t base = smem_addr(smem_raw);
+    if (base & 1023u) {  // the swizzled tiles need a 1024-aligned base
+        if (tid == 0) atomicCAS(p.status, 0, PKV_ERR_UNSUPPORTED);
+        return;
+    }
+    uint8_t *sbase = smem_raw;
+    const uint32_t sQ = base + TcSmem::q, sP = base + TcSmem::p, sOnes = base + TcSmem::ones;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sbase + TcSmem::bars);
-    int *sm_ok = reinterpret_cast<int *>(sbase + TcSmem::ok);
+    int *sm_pg = reinterpret_cast<int *>(sbase + TcSmem::pages);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + TcSmem::tmem_slot);
-    const uint32_t bar_full0 = smem_addr(&bars[0]), bar_s = smem_addr(&bars[2]), bar_o = smem_addr(&bars[3]);
-    auto sK = [&](int st) { return base + TcSmem::kv + (uint32_t)(st * 2 * kTile); };
-    auto sV = [&](int st) { return sK(st) + (uint32_t)kTile; };
+    auto bar = [&](int i) { return smem_addr(&bars[i]); };
+    auto k_full = [&](int s) { return bar(0 + s); };    // 2
+    auto k_empty = [&](int s) { return bar(2 + s); };   // 2
+    auto v_full = [&](int s) { return bar(4 + s); };    // 3
+    auto v_empty = [&](int s) { return bar(7 + s); };   // 3
+    auto s_full = [&](int s) { return bar(10 + s); };   // 2
+    auto s_free = [&](int s) { return bar(12 + s); };   // 2
+    const uint32_t p_full = bar(14), o_done = bar(15), drain = bar(16);
+    auto sK = [&](int s) { return base + TcSmem::k + (uint32_t)(s * kTile); };
+    auto sV = [&](int s) { return base + TcSmem::v + (uint32_t)(s * kTile); };
 
     if (tid == 0) {
-        for (int i = 0; i < 4; ++i) mbar_init(smem_addr(&bars[i]), 1);
+        for (int s = 0; s < kTcKStages; ++s) {
+            mbar_init(k_full(s), 1);
+            mbar_init(k_empty(s), 1);
+        }
+        for (int s = 0; s < kTcVStages; ++s) {
+            mbar_init(v_full(s), 1);
+            mbar_init(v_empty(s), 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(s_full(s), 2);  // the MMA's commit + the issuing lane (publishes the tile's page ids)
+            mbar_init(s_free(s), 4);
+        }
+        mbar_init(p_full, 4);
+        mbar_init(o_done, 1);
+        mbar_init(drain, 1);
         fence_barrier_init();
     }
-    if (warp == 0) tc_alloc(smem_addr(tmem_slot), 256);  // S: columns 0..127, O: 128..255
+    // TMEM columns: S0 0..127, S1 128..255, O 256..383, the row sums of bf16 P 384..399
+    if (warp == 0) tc_alloc(smem_addr(tmem_slot), 512);
 
     // Q rows into shared memory, 128B-swizzled [2 column blocks][128 rows][128 B]
-    {
+    if (!issuer_warp) {
         const uint4 *src = reinterpret_cast<const uint4 *>(p.q + grow * D);
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
@@ -127,217 +175,319 @@ __global__ void __launch_bounds__(128, 1)
             const int dc = c >> 3, cc = c & 7;
             st_shared_v4(sQ + (uint32_t)(dc * kBlk + r * 128 + ((cc ^ (r & 7)) << 4)), v.x, v.y, v.z, v.w);
         }
+        constexpr uint32_t kOne2 = 0x3F803F80u;  // two bf16 ones
+        st_shared_v4(sOnes + (uint32_t)(r * 16), kOne2, kOne2, kOne2, kOne2);
     }
     fence_proxy_async_shared();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tS = tmem, tO = tmem + 128u;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-
-    const uint64_t policy = l2_policy_evict_first();
-    const int box_t = p.P < kTcKeys ? p.P : kTcKeys;
+    const uint32_t tO = tmem + 256u, tL = tmem + 384u;
+    auto tS = [&](int sb) { return tmem + (uint32_t)(sb * 128); };
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const int log2box = p.log2P < 7 ? p.log2P : 7;
+    const int box_t = 1 << log2box;
     const int nbox = kTcKeys / box_t;
-    // copies of key tile j into stage st (thread 0)
-    auto issue = [&](int j, int st) {
-        const uint32_t bar = bar_full0 + 8u * (uint32_t)st;
-        uint32_t bytes = 0;
-        int ids[16];
-        for (int x = 0; x < nbox; ++x) {
-            const int key = j * kTcKeys + x * box_t;
-            int pg = -1;
-            if (key < n_keys) {
-                pg = p.block_table[(size_t)b * p.max_pages + (key >> p.log2P)];
-                if ((unsigned)pg >= (unsigned)p.num_pages) {
-                    atomicCAS(p.status, 0, PKV_ERR_BAD_PAGE_INDEX);
-                    pg = -1;
+    bool failed = false;
+
+    if (issuer_warp) {
+        if (n_tiles > 0) {
+            // The whole warp walks the loop (every lane waits on the same barriers); lane
+            // x looks up the page of box x, lane 0 issues the copies and the MMAs.
+            const uint64_t policy = l2_policy_evict_first();
+            const bool leader = lane == 0;
+            // raw block-table entry of box `lane` of tile j (loaded a tile before it is published)
+            auto fetch = [&](int j) {
+                const int key = j * kTcKeys + lane * box_t;
+                return (lane < nbox && j < n_tiles && key < n_keys)
+                           ? p.block_table[(size_t)b * p.max_pages + (key >> p.log2P)]
+                           : -1;
+            };
+            // page ids of tile j into the ring (-1: no key there, or an id out of range)
+            auto publish = [&](int j, int raw) {
+                if (lane < nbox) {
+                    const bool has_key = j * kTcKeys + lane * box_t < n_keys;
+                    int pg = has_key ? raw : -1;
+                    if (has_key && (unsigned)raw >= (unsigned)p.num_pages) {
+                        atomicCAS(p.status, 0, PKV_ERR_BAD_PAGE_INDEX);
+                        pg = -1;
+                    }
+                    sm_pg[(j % kTcPageRing) * 16 + lane] = pg;
+                }
+                __syncwarp();
+            };
+            auto load = [&](const CUtensorMap *map, uint32_t dst, uint32_t full, int j) {
+                if (!leader) return;
+                const int *ids = sm_pg + (j % kTcPageRing) * 16;
+                uint32_t bytes = 0;
+                for (int x = 0; x < nbox; ++x)
+                    if (ids[x] >= 0) bytes += 2u * (uint32_t)box_t * 128u;
+                mbar_arrive_expect_tx(full, bytes);
+                for (int x = 0; x < nbox; ++x) {
+                    if (ids[x] < 0) continue;
+                    const int row = ids[x] * p.P + ((j * kTcKeys + x * box_t) & (p.P - 1));
+#pragma unroll
+                    for (int dc = 0; dc < 2; ++dc)
+                        tma_load_3d(dst + (uint32_t)(dc * kBlk + x * box_t * 128), map, dc * 64, kvh, row, full,
+                                    policy);
+                }
+            };
+            // zeroes the V rows of tile j whose keys are invalid (past n_keys, bad page): a row
+            // is 2 column blocks x 8 chunks of 16 bytes; lanes 0-15 clear the even rows, 16-31
+            // the odd ones, lane & 15 naming the chunk
+            auto zero_invalid_v = [&](int j) {
+                const int *ids = sm_pg + (j % kTcPageRing) * 16;
+                const bool tail = (j + 1) * kTcKeys > n_keys;
+                bool bad = false;
+                for (int x = 0; x < nbox; ++x) bad |= ids[x] < 0;
+                if (!tail && !bad) return;
+                const uint32_t dst = sV(j % kTcVStages) + (uint32_t)(((lane >> 3) & 1) * kBlk + (lane & 7) * 16);
+                for (int k = lane >> 4; k < kTcKeys; k += 2)
+                    if (j * kTcKeys + k >= n_keys || ids[k >> log2box] < 0)
+                        st_shared_v4(dst + (uint32_t)(k * 128), 0u, 0u, 0u, 0u);
+                fence_proxy_async_shared();
+                __syncwarp();
+            };
+            constexpr uint32_t kIdS = tc_idesc_bf16(kTcRows, kTcKeys, false);
+            constexpr uint32_t kIdO = tc_idesc_bf16(kTcRows, D, true);
+            constexpr uint32_t kIdL = tc_idesc_bf16(kTcRows, 16, false);
+            int k_issued = 0, v_issued = 0, k_seen = 0, v_seen = 0;
+            publish(0, fetch(0));
+            publish(1, fetch(1));
+            int next_raw = fetch(2);  // tile 2's entries, published when K(2) is issued
+            load(&tmK, sK(0), k_full(0), 0);
+            load(&tmV, sV(0), v_full(0), 0);
+            k_issued = v_issued = 1;
+            if (n_tiles > 1) {
+                load(&tmK, sK(1), k_full(1), 1);
+                k_issued = 2;
+            }
+            for (int j = 0; j <= n_tiles; ++j) {
+                if (j < n_tiles) {  // S(j) = Q K(j)^T into S buffer j & 1
+                    const int ks = j % kTcKStages, sb = j & 1;
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait_bounded(k_full(ks), (uint32_t)((j / kTcKStages) & 1), p.wait_limit_ns) &&
+                                        (j < 2 || mbar_wait_bounded(s_free(sb), (uint32_t)(((j >> 1) - 1) & 1),
+                                                                    p.wait_limit_ns)))) {
+                        failed = true;
+                        break;
+                    }
+                    k_seen = j + 1;
+                    if (leader) {
+                        tc_fence_after();
+#pragma unroll
+                        for (int dc = 0; dc < 2; ++dc)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                tc_mma_bf16(tS(sb), tc_desc(sQ + (uint32_t)(dc * kBlk + k * 32), 16, 1024),
+                                            tc_desc(sK(ks) + (uint32_t)(dc * kBlk + k * 32), 16, 1024), kIdS,
+                                            (dc | k) != 0);
+                        tc_commit(s_full(sb));
+                        tc_commit(k_empty(ks));
+                        mbar_arrive(s_full(sb));
+                    }
+                    __syncwarp();
+                }
+                if (j >= 1) {  // O += P(j-1) V(j-1)
+                    const int t = j - 1, vs = t % kTcVStages;
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(v_full(vs), (uint32_t)((t / kTcVStages) & 1),
+                                                                   p.wait_limit_ns))) {
+                        failed = true;
+                        break;
+                    }
+                    v_seen = t + 1;
+                    zero_invalid_v(t);
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(p_full, (uint32_t)(t & 1), p.wait_limit_ns))) {
+                        failed = true;
+                        break;
+                    }
+                    if (leader) {
+                        tc_fence_after();
+#pragma unroll
+                        for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const uint64_t pdesc = tc_desc(sP + (uint32_t)(kb * kBlk + k * 32), 16, 1024);
+                                tc_mma_bf16(tO, pdesc,
+                                            tc_desc(sV(vs) + (uint32_t)((kb * 64 + k * 16) * 128), (uint32_t)kBlk,
+                                                    1024),
+                                            kIdO, t > 0 || (kb | k) != 0);
+                                tc_mma_bf16(tL, pdesc, tc_desc(sOnes + (uint32_t)(k * 32), 16, 1024), kIdL,
+                                            t > 0 || (kb | k) != 0);
+                            }
+                        tc_commit(o_done);
+                        tc_commit(v_empty(vs));
+                    }
+                    __syncwarp();
+                }
+                if (j + 2 < n_tiles) {  // K(j+2) into the stage S(j) reads
+                    const int ks = j % kTcKStages;
+                    publish(j + 2, next_raw);
+                    next_raw = fetch(j + 3);
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(k_empty(ks), (uint32_t)((j / kTcKStages) & 1),
+                                                                   p.wait_limit_ns))) {
+                        failed = true;
+                        break;
+                    }
+                    load(&tmK, sK(ks), k_full(ks), j + 2);
+                    k_issued = j + 3;
+                }
+                if (j + 1 < n_tiles) {  // V(j+1) into the stage PV(j-2) read
+                    const int t = j + 1, vs = t % kTcVStages;
+                    if (t >= kTcVStages &&
+                        !__all_sync(0xffffffffu, mbar_wait_bounded(v_empty(vs), (uint32_t)((t / kTcVStages - 1) & 1),
+                                                                   p.wait_limit_ns))) {
+                        failed = true;
+                        break;
+                    }
+                    load(&tmV, sV(vs), v_full(vs), t);
+                    v_issued = t + 1;
                 }
             }
-            ids[x] = pg;
-            sm_ok[st * 16 + x] = pg >= 0;
-            if (pg >= 0) bytes += 2u * 2u * (uint32_t)box_t * 128u;
-        }
-        mbar_arrive_expect_tx(bar, bytes);
-        for (int x = 0; x < nbox; ++x) {
-            if (ids[x] < 0) continue;
-            const int key = j * kTcKeys + x * box_t;
-            const int row = ids[x] * p.P + (key & (p.P - 1));
-#pragma unroll
-            for (int dc = 0; dc < 2; ++dc) {
-                const uint32_t off = (uint32_t)(dc * kBlk + x * box_t * 128);
-                tma_load_3d(sK(st) + off, &tmK, dc * 64, kvh, row, bar, policy);
-                tma_load_3d(sV(st) + off, &tmV, dc * 64, kvh, row, bar, policy);
+            // let the copies (after a timeout) and the MMAs in flight finish before the CTA exits
+            if (leader) {
+                for (int t = k_seen; t < k_issued; ++t)
+                    mbar_wait_bounded(k_full(t % kTcKStages), (uint32_t)((t / kTcKStages) & 1), p.wait_limit_ns);
+                for (int t = v_seen; t < v_issued; ++t)
+                    mbar_wait_bounded(v_full(t % kTcVStages), (uint32_t)((t / kTcVStages) & 1), p.wait_limit_ns);
+                tc_commit(drain);
+                if (!mbar_wait_bounded(drain, 0, p.wait_limit_ns)) failed = true;
             }
         }
-    };
-    if (tid == 0) {
-        if (n_tiles > 0) issue(0, 0);
-        if (n_tiles > 1) issue(1, 1);
-    }
-
-    float m_run = -__int_as_float(0x7f800000), l_run = 0.f, lt_run = 0.f;
-    bool failed = false;
-    constexpr uint32_t kIdS = tc_idesc_bf16(kTcRows, kTcKeys, false);
-    constexpr uint32_t kIdO = tc_idesc_bf16(kTcRows, D, true);
-    for (int j = 0; j < n_tiles; ++j) {
-        const int st = j & 1;
-        const uint32_t ph = (uint32_t)((j >> 1) & 1);
-        const bool got = mbar_wait_bounded(bar_full0 + 8u * (uint32_t)st, ph, p.wait_limit_ns);
-        if (!__syncthreads_and(got)) {
-            failed = true;
-            break;
-        }
-        // keys of this tile that are not valid: zero their V rows (0 * NaN would reach O)
-        const bool tail = (j + 1) * kTcKeys > n_keys;
-        int bad_box = 0;
-        for (int x = 0; x < nbox; ++x) bad_box |= !sm_ok[st * 16 + x];
-        if (tail || bad_box) {
-            const int key = j * kTcKeys + r;
-            if (key >= n_keys || !sm_ok[st * 16 + r / box_t]) {
+    } else if (n_tiles > 0) {
+        // ---- softmax warps: thread r owns row r
+        const float c = p.scale_log2;  // > 0
+        float m_ref = kNegInf, l_run = 0.f;
+        const int row_lim = min(n_keys, klim + 1);  // keys [0, row_lim) are visible to this row
+        for (int j = 0; j < n_tiles; ++j) {
+            const int sb = j & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(s_full(sb), (uint32_t)((j >> 1) & 1), p.wait_limit_ns))) {
+                failed = true;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sr[kTcKeys];
+            tc_ld128(tS(sb) + lane_off, sr);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_free(sb));
+            // masking: none on tiles every row of the warp sees whole, the row's limit on
+            // the diagonal, a key bitmask where a page is missing
+            const int *ids = sm_pg + (j % kTcPageRing) * 16;
+            bool pages_ok = true;
+            for (int x = 0; x < nbox; ++x) pages_ok &= ids[x] >= 0;
+            const int lim = row_lim - j * kTcKeys;
+            if (!pages_ok) {
+                uint32_t okw[4] = {0u, 0u, 0u, 0u};
+                for (int x = 0; x < nbox; ++x) {
+                    if (ids[x] < 0) continue;
+                    const int k0 = x << log2box, k1 = k0 + box_t;
+                    for (int w = k0 >> 5; w < ((k1 + 31) >> 5); ++w) {
+                        const int lo = max(k0, 32 * w) - 32 * w, n = min(k1, 32 * w + 32) - 32 * w - lo;
+                        okw[w] |= (n == 32 ? 0xffffffffu : ((1u << n) - 1u)) << lo;
+                    }
+                }
 #pragma unroll
-                for (int dc = 0; dc < 2; ++dc)
+                for (int i = 0; i < kTcKeys; ++i)
+                    if (!((okw[i >> 5] >> (i & 31)) & 1u) || i >= lim) sr[i] = 0xff800000u;  // -inf
+            } else if (__any_sync(0xffffffffu, lim < kTcKeys)) {
 #pragma unroll
-                    for (int cc = 0; cc < 8; ++cc)
-                        st_shared_v4(sV(st) + (uint32_t)(dc * kBlk + r * 128 + cc * 16), 0u, 0u, 0u, 0u);
+                for (int i = 0; i < kTcKeys; ++i)
+                    if (i >= lim) sr[i] = 0xff800000u;
+            }
+            // tile maximum of the unscaled scores, eight chains
+            float mx8[8];
+#pragma unroll
+            for (int a = 0; a < 8; ++a) mx8[a] = __uint_as_float(sr[a]);
+#pragma unroll
+            for (int i = 8; i < kTcKeys; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sr[i]));
+            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+                             c;
+            // reference maximum: set at the first visible key, moved only past a 2^8 rise
+            float alpha = 1.f;
+            if (mx != kNegInf && (m_ref == kNegInf || mx > m_ref + kRescaleGap)) {
+                alpha = m_ref == kNegInf ? 0.f : ex2(m_ref - mx);
+                m_ref = mx;
+                l_run *= alpha;
+            }
+            const float neg_ref = m_ref == kNegInf ? 0.f : -m_ref;
+            float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            uint32_t pw[kTcKeys / 2];
+#pragma unroll
+            for (int i = 0; i < kTcKeys / 2; ++i) {
+                const float p0 = ex2(fmaf(__uint_as_float(sr[2 * i]), c, neg_ref));
+                const float p1 = ex2(fmaf(__uint_as_float(sr[2 * i + 1]), c, neg_ref));
+                pw[i] = pack_bf16x2(p0, p1);
+                ls[i & 7] += p0 + p1;
+            }
+            l_run += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+            // PV(j-1) must be done before O is rescaled and the P buffer rewritten
+            if (j >= 1) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(o_done, (uint32_t)((j - 1) & 1), p.wait_limit_ns))) {
+                    failed = true;
+                    break;
+                }
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                    for (int cb = 0; cb < 4; ++cb) {
+                        float v[32];
+                        tc_ld32(tO + lane_off + (uint32_t)(cb * 32), v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] *= alpha;
+                        tc_st32(tO + lane_off + (uint32_t)(cb * 32), v);
+                    }
+                    tc_st1(tL + lane_off, tc_ld1(tL + lane_off) * alpha);
+                }
+            }
+            // P (bf16) into shared memory, K-major 128B-swizzled [2 key blocks][128 rows][128 B]
+#pragma unroll
+            for (int cc16 = 0; cc16 < 16; ++cc16) {
+                const int kb = cc16 >> 3, cc = cc16 & 7;
+                st_shared_v4(sP + (uint32_t)(kb * kBlk + r * 128 + ((cc ^ (r & 7)) << 4)), pw[4 * cc16],
+                             pw[4 * cc16 + 1], pw[4 * cc16 + 2], pw[4 * cc16 + 3]);
             }
             fence_proxy_async_shared();
-            __syncthreads();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
         }
-        // S = Q K^T
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int dc = 0; dc < 2; ++dc)
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    tc_mma_bf16(tS, tc_desc(sQ + (uint32_t)(dc * kBlk + k * 32), 16, 1024),
-                                tc_desc(sK(st) + (uint32_t)(dc * kBlk + k * 32), 16, 1024), kIdS, (dc | k) != 0);
-            tc_commit(bar_s);
-        }
-        if (!__syncthreads_and(mbar_wait_bounded(bar_s, (uint32_t)(j & 1), p.wait_limit_ns))) {
+        // epilogue: out = O / lt, lse = (m + log2 l) ln 2
+        if (!failed &&
+            !__all_sync(0xffffffffu, mbar_wait_bounded(o_done, (uint32_t)((n_tiles - 1) & 1), p.wait_limit_ns)))
             failed = true;
-            break;
-        }
-        tc_fence_after();
-        // softmax of this thread's row over the tile's 128 keys
-        float sv[kTcKeys];
-#pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
-            float v[32];
-            tc_ld32(tS + lane_off + (uint32_t)(cb * 32), v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) sv[cb * 32 + i] = v[i];
-        }
-        const int key0 = j * kTcKeys;
-        const int lim = row_ok ? klim : -1;  // the last key this row sees (rows past the group see none)
-        float mx = -__int_as_float(0x7f800000);
-        if (tail || bad_box) {
-#pragma unroll
-            for (int i = 0; i < kTcKeys; ++i) {
-                const int key = key0 + i;
-                float v = sv[i] * p.scale_log2;
-                if (key > lim || key >= n_keys || !sm_ok[st * 16 + i / box_t]) v = -__int_as_float(0x7f800000);
-                sv[i] = v;
-                mx = fmaxf(mx, v);
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < kTcKeys; ++i) {
-                float v = sv[i] * p.scale_log2;
-                if (key0 + i > lim) v = -__int_as_float(0x7f800000);
-                sv[i] = v;
-                mx = fmaxf(mx, v);
-            }
-        }
-        const float m_new = fmaxf(m_run, mx);
-        const float mref = m_new == -__int_as_float(0x7f800000) ? 0.f : m_new;
-        const float alpha = ex2(m_run - mref);
-        m_run = m_new;
-        l_run *= alpha;
-        lt_run *= alpha;
-        // the previous PV must be done before O is rescaled and P overwritten
-        if (j > 0 && !__syncthreads_and(mbar_wait_bounded(bar_o, (uint32_t)((j - 1) & 1), p.wait_limit_ns))) {
-            failed = true;
-            break;
-        }
-        if (j > 0) {
+        if (!failed) {
             tc_fence_after();
-            // tile j-1's stage is free (its S and PV are done): refill it with tile j+1
-            if (tid == 0 && j + 1 < n_tiles) issue(j + 1, (j + 1) & 1);
-        }
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            const bool empty = m_ref == kNegInf;
+            const float lt = tc_ld1(tL + lane_off);  // collective: every lane loads
+            const float inv = empty ? 0.f : 1.f / lt;
+            uint32_t *dst = reinterpret_cast<uint32_t *>(p.out + grow * D);
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb) {
                 float v[32];
                 tc_ld32(tO + lane_off + (uint32_t)(cb * 32), v);
+                if (row_ok)
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] *= alpha;
-                tc_st32(tO + lane_off + (uint32_t)(cb * 32), v);
+                    for (int i = 0; i < 16; ++i) dst[cb * 16 + i] = pack_bf16x2(v[2 * i] * inv, v[2 * i + 1] * inv);
             }
-        }
-        // P (bf16) into shared memory, K-major 128B-swizzled [2 key blocks][128 rows][128 B]
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float p0 = ex2(sv[c * 8 + 2 * e] - mref), p1 = ex2(sv[c * 8 + 2 * e + 1] - mref);
-                w[e] = pack_bf16x2(p0, p1);
-                l_run += p0 + p1;
-                lt_run += bf16_lo(w[e]) + bf16_hi(w[e]);
-            }
-            const int kb = c >> 3, cc = c & 7;
-            st_shared_v4(sP + (uint32_t)(kb * kBlk + r * 128 + ((cc ^ (r & 7)) << 4)), w[0], w[1], w[2], w[3]);
-        }
-        fence_proxy_async_shared();
-        tc_fence_before();
-        __syncthreads();
-        // O += P V
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    tc_mma_bf16(tO, tc_desc(sP + (uint32_t)(kb * kBlk + k * 32), 16, 1024),
-                                tc_desc(sV(st) + (uint32_t)((kb * 64 + k * 16) * 128), (uint32_t)kBlk, 1024), kIdO,
-                                j > 0 || (kb | k) != 0);
-            tc_commit(bar_o);
+            if (row_ok && p.lse) p.lse[grow] = empty ? kNegInf : (m_ref + __log2f(l_run)) * 0.693147180559945309f;
         }
     }
-    // wait for the last PV, then the epilogue: out = O / lt, lse = (m + log2 l) ln 2
-    if (!failed && n_tiles > 0 &&
-        !__syncthreads_and(mbar_wait_bounded(bar_o, (uint32_t)((n_tiles - 1) & 1), p.wait_limit_ns)))
-        failed = true;
-    if (failed) {
-        if (tid == 0) atomicCAS(p.status, 0, PKV_ERR_DEVICE_TIMEOUT);
-    } else {
-        // tcgen05.ld is collective per warp: every lane loads, rows of the group store
-        tc_fence_after();
-        const bool empty = n_tiles == 0 || m_run == -__int_as_float(0x7f800000);
-        const float inv = empty ? 0.f : 1.f / lt_run;
+    if (!issuer_warp && n_tiles == 0 && row_ok) {  // no key visible to the CTA: out = 0, lse = -inf
         uint32_t *dst = reinterpret_cast<uint32_t *>(p.out + grow * D);
-#pragma unroll
-        for (int cb = 0; cb < 4; ++cb) {
-            float v[32];
-            if (n_tiles > 0) {
-                tc_ld32(tO + lane_off + (uint32_t)(cb * 32), v);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = 0.f;
-            }
-            if (row_ok)
-#pragma unroll
-                for (int i = 0; i < 16; ++i) dst[cb * 16 + i] = pack_bf16x2(v[2 * i] * inv, v[2 * i + 1] * inv);
-        }
-        if (row_ok && p.lse)
-            p.lse[grow] = empty ? -__int_as_float(0x7f800000) : (m_run + __log2f(l_run)) * 0.693147180559945309f;
+        for (int i = 0; i < D / 2; ++i) dst[i] = 0u;
+        if (p.lse) p.lse[grow] = kNegInf;
     }
+    if (failed) atomicCAS(p.status, 0, PKV_ERR_DEVICE_TIMEOUT);
     griddep_launch_dependents();
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tc_dealloc(tmem, 256);
+    if (warp == 0) {
+        tc_fence_after();
+        tc_dealloc(tmem, 512);
+    }
 }
 
 }  // namespace pkv

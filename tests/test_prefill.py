@@ -155,7 +155,7 @@ TC = [
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("B,Hq,Hkv,D,P,q_lens,kv_lens", TC, ids=lambda x: str(x).replace(" ", ""))
 def test_tensor_core_path_full_oracle(B, Hq, Hkv, D, P, q_lens, kv_lens, causal):
-    pkv.set_prefill_tensor_cores(True)
+    pkv.set_prefill_tensor_cores("always")
     case = make_prefill_case(_spec(B, Hq, Hkv, D, P, seed=3 * B + P + sum(q_lens)), q_lens, kv_lens, poison=True)
     out, lse = run_prefill(case, causal=causal)
     eo, el = compare(case, out, lse, causal=causal)
@@ -164,9 +164,9 @@ def test_tensor_core_path_full_oracle(B, Hq, Hkv, D, P, q_lens, kv_lens, causal)
 
 def test_tensor_core_and_mma_sync_paths_agree():
     case = make_prefill_case(_spec(2, 32, 8, 128, 16, seed=9), [48, 40], [1000, 300])
-    pkv.set_prefill_tensor_cores(False)
+    pkv.set_prefill_tensor_cores("off")
     ref_o, ref_l = run_prefill(case)
-    pkv.set_prefill_tensor_cores(True)
+    pkv.set_prefill_tensor_cores("always")
     out, lse = run_prefill(case)
     excess, _, _ = split_invariance_violation(out.float().cpu().numpy(), ref_o.float().cpu().numpy(), tol=OUT_TOL)
     assert excess <= 0
@@ -179,7 +179,7 @@ def test_tensor_core_path_bad_page_is_skipped_and_reported():
     bt[1, 3] = case.num_pages + 7
     bad = Case(**case.__dict__)
     bad.block_table = bt
-    pkv.set_prefill_tensor_cores(True)
+    pkv.set_prefill_tensor_cores("always")
     out, lse = run_prefill(bad, expect_status=-6)
     # request 0 is untouched; request 1 attends to its other keys only
     o0, l0 = run_prefill(case)
