@@ -214,7 +214,7 @@ pkv_status prefill_tc(const pkv_bf16 *q, const void *k_cache, const void *v_cach
     CUtensorMap mk, mv;
     pkv_status st = get_pool_map(k_cache, num_pages, page_size, Hkv, D, box_t, device, 3, &mk);
     if (st != PKV_OK) return st;
-    st = get_pool_map(v_cache, num_pages, page_size, Hkv, D, box_t, device, 3, &mv);
+    st = get_pool_map(v_cache, num_pages, page_size, Hkv, D, box_t, device, 4, &mv);  // one copy per page box
     if (st != PKV_OK) return st;
     const int G = Hq / Hkv;
     const long q_tiles = ((long)mr.max_q_len * G + kTcRows - 1) / kTcRows;

@@ -9,12 +9,14 @@
 //     softmax          thread r of the softmax warps owns row r = TMEM lane r: the row
 //                      maximum and sums need no shuffles
 //     O += P V         tcgen05.mma M=128 rows, N=D, K=128 keys; O in tensor memory
-// Warp specialisation: warps 0-3 run the softmax; one lane of warp 4 issues the TMA
-// copies and the MMAs.  S is double-buffered in tensor memory, so the score MMA of tile
-// j+1 runs while the softmax warps work on tile j, and the PV MMA of tile j runs while
-// they load and exponentiate tile j+1.  K has two shared-memory stages and V three, so
-// each copy is issued two tiles ahead of its MMA.  mbarriers hand every buffer over
-// (copies: complete_tx; MMAs: tcgen05.commit; softmax: one arrival per warp).
+// Warp specialisation: warps 0-3 run the softmax, one lane of warp 4 issues the MMAs,
+// warp 5 copies K and warp 6 copies V (TMA; every lane issues one 16-key box half, as
+// one thread's copies issue too slowly to feed the tensor cores from page-sized boxes).
+// S is double-buffered in tensor memory, so the score MMA of tile j+1 runs while the
+// softmax warps work on tile j, and the PV MMA of tile j runs while they load and
+// exponentiate tile j+1.  K and V have three shared-memory stages each.  mbarriers hand
+// every buffer over (copies: complete_tx; MMAs: tcgen05.commit; softmax: one arrival
+// per warp).
 // The online softmax keeps a reference maximum per row and moves it only when a tile's
 // maximum exceeds it by more than 2^8 (probabilities stay <= 256, well inside f32 and
 // bf16), so O is rescaled in tensor memory (tcgen05.ld/st) only then; l and O share the
@@ -24,9 +26,11 @@
 // sum l, kept by the softmax threads, gives the log-sum-exp.  The scores' scale must be
 // positive (the host routes other scales elsewhere): the row maximum is then taken on
 // the unscaled scores and each exponent is one FMA.
-// Q, K and V tiles sit in shared memory 128B-swizzled, K-major ([D/64][rows][64]) as the
-// TMA boxes land them; P is written by the softmax threads in the same layout; V is
-// read MN-major (N = dims contiguous).  Keys past the last one the CTA's rows may see, or
+// Q and K tiles sit in shared memory 128B-swizzled, K-major ([D/64][rows][64]) as the
+// TMA boxes land them (two copies, one per 64 dims, per page box).  V is read MN-major
+// (N = dims contiguous) in the layout one copy per page box lands: [box][D/64][keys][64].
+// P (bf16) goes from the softmax threads' registers to tensor memory (tcgen05.st) and
+// is the A operand of the PV MMA there.  Keys past the last one the CTA's rows may see, or
 // in a page whose id is out of range, are masked in the scores and zeroed in V's rows
 // by the issuing lane before the PV MMA (0 * NaN would reach the output).  Every wait is
 // bounded; on a timeout the status word is set, the issuing lane waits (bounded) for its
@@ -56,17 +60,16 @@ struct PrefillTcParams {
 
 constexpr int kTcRows = 128;     // rows per CTA (the MMA's M)
 constexpr int kTcKeys = 128;     // keys per tile (the score MMA's N)
-constexpr int kTcThreads = 160;  // 4 softmax warps + 1 issuing warp
-constexpr int kTcKStages = 2;
+constexpr int kTcThreads = 224;  // 4 softmax warps, the MMA warp, the K and V copy warps
+constexpr int kTcKStages = 3;
 constexpr int kTcVStages = 3;
-constexpr int kTcPageRing = 4;   // tiles whose page ids are kept
+constexpr int kTcPageRing = 8;   // tiles whose page ids are kept
 
 // Shared memory (bytes from a 1024-aligned base) of the D = 128 kernel.
 struct TcSmem {
     static constexpr int kTile = kTcRows * 128 * 2;  // 128 rows x 128 dims (or keys) bf16, 2 column blocks
     static constexpr int q = 0;
-    static constexpr int p = kTile;
-    static constexpr int k = 2 * kTile;                      // K stage s at k + s * kTile
+    static constexpr int k = kTile;                          // K stage s at k + s * kTile
     static constexpr int v = k + kTcKStages * kTile;         // V stage s at v + s * kTile
     static constexpr int ones = v + kTcVStages * kTile;      // 16 x 64 bf16 ones, the B operand of the row-sum MMA
     static constexpr int bars = ones + 2048;                 // 32 mbarriers
@@ -89,7 +92,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int kvh = (int)(blockIdx.x % (unsigned)p.Hkv), qt = (int)(blockIdx.x / (unsigned)p.Hkv);
     const int b = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const bool issuer_warp = warp == 4;
+    const bool issuer_warp = warp >= 4;  // the MMA warp and the copy warps
     const int G = p.G;
 
     if (tid == 0) {
@@ -130,18 +133,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return;
     }
     uint8_t *sbase = smem_raw;
-    const uint32_t sQ = base + TcSmem::q, sP = base + TcSmem::p, sOnes = base + TcSmem::ones;
+    const uint32_t sQ = base + TcSmem::q, sOnes = base + TcSmem::ones;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sbase + TcSmem::bars);
     int *sm_pg = reinterpret_cast<int *>(sbase + TcSmem::pages);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + TcSmem::tmem_slot);
     auto bar = [&](int i) { return smem_addr(&bars[i]); };
-    auto k_full = [&](int s) { return bar(0 + s); };    // 2
-    auto k_empty = [&](int s) { return bar(2 + s); };   // 2
-    auto v_full = [&](int s) { return bar(4 + s); };    // 3
-    auto v_empty = [&](int s) { return bar(7 + s); };   // 3
-    auto s_full = [&](int s) { return bar(10 + s); };   // 2
-    auto s_free = [&](int s) { return bar(12 + s); };   // 2
-    const uint32_t p_full = bar(14), o_done = bar(15), drain = bar(16);
+    constexpr int kKFull = 0, kKEmpty = kKFull + kTcKStages, kVFull = kKEmpty + kTcKStages,
+                  kVEmpty = kVFull + kTcVStages, kSFull = kVEmpty + kTcVStages, kSFree = kSFull + 2,
+                  kPFull = kSFree + 2, kODone = kPFull + 1, kDrain = kODone + 1;
+    static_assert(kDrain < 32, "prefill_tc_kernel: more mbarriers than the shared-memory slots");
+    auto k_full = [&](int s) { return bar(kKFull + s); };
+    auto k_empty = [&](int s) { return bar(kKEmpty + s); };
+    auto v_full = [&](int s) { return bar(kVFull + s); };
+    auto v_empty = [&](int s) { return bar(kVEmpty + s); };
+    auto s_full = [&](int s) { return bar(kSFull + s); };
+    auto s_free = [&](int s) { return bar(kSFree + s); };
+    const uint32_t p_full = bar(kPFull), o_done = bar(kODone), drain = bar(kDrain);
     auto sK = [&](int s) { return base + TcSmem::k + (uint32_t)(s * kTile); };
     auto sV = [&](int s) { return base + TcSmem::v + (uint32_t)(s * kTile); };
 
@@ -163,7 +170,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_init(drain, 1);
         fence_barrier_init();
     }
-    // TMEM columns: S0 0..127, S1 128..255, O 256..383, the row sums of bf16 P 384..399
+    // TMEM columns: S0 0..127, S1 128..255, O 256..383, the row sums of bf16 P 384..399,
+    // P (bf16 pairs) 448..511
     if (warp == 0) tc_alloc(smem_addr(tmem_slot), 512);
 
     // Q rows into shared memory, 128B-swizzled [2 column blocks][128 rows][128 B]
@@ -183,7 +191,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tO = tmem + 256u, tL = tmem + 384u;
+    const uint32_t tO = tmem + 256u, tL = tmem + 384u, tP = tmem + 448u;
     auto tS = [&](int sb) { return tmem + (uint32_t)(sb * 128); };
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const int log2box = p.log2P < 7 ? p.log2P : 7;
@@ -191,169 +199,148 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int nbox = kTcKeys / box_t;
     bool failed = false;
 
-    if (issuer_warp) {
-        if (n_tiles > 0) {
-            // The whole warp walks the loop (every lane waits on the same barriers); lane
-            // x looks up the page of box x, lane 0 issues the copies and the MMAs.
-            const uint64_t policy = l2_policy_evict_first();
-            const bool leader = lane == 0;
-            // raw block-table entry of box `lane` of tile j (loaded a tile before it is published)
-            auto fetch = [&](int j) {
-                const int key = j * kTcKeys + lane * box_t;
-                return (lane < nbox && j < n_tiles && key < n_keys)
-                           ? p.block_table[(size_t)b * p.max_pages + (key >> p.log2P)]
-                           : -1;
-            };
-            // page ids of tile j into the ring (-1: no key there, or an id out of range)
-            auto publish = [&](int j, int raw) {
-                if (lane < nbox) {
-                    const bool has_key = j * kTcKeys + lane * box_t < n_keys;
-                    int pg = has_key ? raw : -1;
-                    if (has_key && (unsigned)raw >= (unsigned)p.num_pages) {
-                        atomicCAS(p.status, 0, PKV_ERR_BAD_PAGE_INDEX);
-                        pg = -1;
-                    }
-                    sm_pg[(j % kTcPageRing) * 16 + lane] = pg;
+    if (warp >= 5 && n_tiles > 0) {
+        // ---- copy warps: warp 5 streams K into its 2 stages, warp 6 V into its 3; lane
+        // 2x + h copies half h (64 dims) of box x (box_t keys of one page)
+        const bool is_k = warp == 5;
+        const int stages = is_k ? kTcKStages : kTcVStages;
+        const uint64_t policy = l2_policy_evict_first();
+        // K: lane 2x + h copies half h (64 dims) of box x; V: lane x copies box x whole
+        const int x = is_k ? lane >> 1 : lane, dc = is_k ? lane & 1 : 0;
+        // block-table entry of box x of tile j (lanes x < nbox), read a tile before its use
+        auto fetch = [&](int j) {
+            const int key = j * kTcKeys + x * box_t;
+            return (dc == 0 && x < nbox && j < n_tiles && key < n_keys)
+                       ? p.block_table[(size_t)b * p.max_pages + (key >> p.log2P)]
+                       : -1;
+        };
+        int raw = fetch(0);
+        int issued = 0;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int st = j % stages;
+            const int next_raw = fetch(j + 1);
+            const bool has_key = x < nbox && j * kTcKeys + x * box_t < n_keys;
+            const int pg_raw = is_k ? __shfl_sync(0xffffffffu, raw, lane & ~1) : raw;
+            const int pg = has_key && (unsigned)pg_raw < (unsigned)p.num_pages ? pg_raw : -1;
+            if (is_k && dc == 0 && has_key && pg < 0) atomicCAS(p.status, 0, PKV_ERR_BAD_PAGE_INDEX);
+            const uint32_t ok = __ballot_sync(0xffffffffu, pg >= 0);  // one bit per copy
+            if (j >= stages) {
+                const uint32_t empty = is_k ? k_empty(st) : v_empty(st);
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait_bounded(empty, (uint32_t)((j / stages - 1) & 1), p.wait_limit_ns))) {
+                    failed = true;
+                    break;
                 }
+            }
+            if (is_k) {  // publish the tile's page ids (read by the softmax and the MMA warp)
+                if (dc == 0 && x < nbox) sm_pg[(j % kTcPageRing) * 16 + x] = pg;
                 __syncwarp();
-            };
-            auto load = [&](const CUtensorMap *map, uint32_t dst, uint32_t full, int j) {
-                if (!leader) return;
-                const int *ids = sm_pg + (j % kTcPageRing) * 16;
-                uint32_t bytes = 0;
-                for (int x = 0; x < nbox; ++x)
-                    if (ids[x] >= 0) bytes += 2u * (uint32_t)box_t * 128u;
-                mbar_arrive_expect_tx(full, bytes);
-                for (int x = 0; x < nbox; ++x) {
-                    if (ids[x] < 0) continue;
-                    const int row = ids[x] * p.P + ((j * kTcKeys + x * box_t) & (p.P - 1));
+            }
+            const uint32_t full = is_k ? k_full(st) : v_full(st);
+            const uint32_t copy_bytes = (uint32_t)box_t * (is_k ? 128u : 256u);
+            if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)__popc(ok) * copy_bytes);
+            __syncwarp();
+            if (pg >= 0) {
+                const int row = pg * p.P + ((j * kTcKeys + x * box_t) & (p.P - 1));
+                if (is_k)
+                    tma_load_3d(sK(st) + (uint32_t)(dc * kBlk + x * box_t * 128), &tmK, dc * 64, kvh, row, full,
+                                policy);
+                else
+                    tma_load_4d(sV(st) + (uint32_t)(x * box_t * 256), &tmV, 0, row, 0, kvh, full, policy);
+            }
+            issued = j + 1;
+            raw = next_raw;
+        }
+        // the last copies have landed before the CTA exits (consumed, or waited for here)
+        for (int t = max(0, issued - stages); t < issued; ++t)
+            mbar_wait_bounded(is_k ? k_full(t % stages) : v_full(t % stages), (uint32_t)((t / stages) & 1),
+                              p.wait_limit_ns);
+    } else if (warp == 4 && n_tiles > 0) {
+        // ---- MMA warp: every lane waits, lane 0 issues
+        const bool leader = lane == 0;
+        // zeroes the V rows of tile j whose keys are invalid (past n_keys, bad page): key k
+        // is row k % box_t of box k / box_t, 2 halves x 8 chunks of 16 bytes; lanes 0-15
+        // clear the even keys, 16-31 the odd ones, lane & 15 naming the chunk
+        auto zero_invalid_v = [&](int j) {
+            const int *ids = sm_pg + (j % kTcPageRing) * 16;
+            const bool tail = (j + 1) * kTcKeys > n_keys;
+            bool bad = false;
+            for (int bx = 0; bx < nbox; ++bx) bad |= ids[bx] < 0;
+            if (!tail && !bad) return;
+            const uint32_t dst = sV(j % kTcVStages) + (uint32_t)(((lane >> 3) & 1) * box_t * 128 + (lane & 7) * 16);
+            for (int k = lane >> 4; k < kTcKeys; k += 2)
+                if (j * kTcKeys + k >= n_keys || ids[k >> log2box] < 0)
+                    st_shared_v4(dst + (uint32_t)((k >> log2box) * box_t * 256 + (k & (box_t - 1)) * 128), 0u, 0u,
+                                 0u, 0u);
+            fence_proxy_async_shared();
+            __syncwarp();
+        };
+        // V operand of the 16-key MMA step kk: 8-key groups 1024 bytes apart within a box
+        // (the 64-dim halves box_t * 128 apart), or, with 8-key boxes, one box per group
+        auto v_desc = [&](uint32_t stage, int kk) {
+            const int k0 = kk * 16;
+            return box_t == 8 ? tc_desc(stage + (uint32_t)(kk * 4096), 1024, 2048)
+                              : tc_desc(stage + (uint32_t)((k0 >> log2box) * box_t * 256 + (k0 & (box_t - 1)) * 128),
+                                        (uint32_t)(box_t * 128), 1024);
+        };
+        constexpr uint32_t kIdS = tc_idesc_bf16(kTcRows, kTcKeys, false);
+        constexpr uint32_t kIdO = tc_idesc_bf16(kTcRows, D, true);
+        constexpr uint32_t kIdL = tc_idesc_bf16(kTcRows, 16, false);
+        for (int j = 0; j <= n_tiles; ++j) {
+            if (j < n_tiles) {  // S(j) = Q K(j)^T into S buffer j & 1
+                const int ks = j % kTcKStages, sb = j & 1;
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait_bounded(k_full(ks), (uint32_t)((j / kTcKStages) & 1), p.wait_limit_ns) &&
+                                    (j < 2 || mbar_wait_bounded(s_free(sb), (uint32_t)(((j >> 1) - 1) & 1),
+                                                                p.wait_limit_ns)))) {
+                    failed = true;
+                    break;
+                }
+                if (leader) {
+                    tc_fence_after();
 #pragma unroll
                     for (int dc = 0; dc < 2; ++dc)
-                        tma_load_3d(dst + (uint32_t)(dc * kBlk + x * box_t * 128), map, dc * 64, kvh, row, full,
-                                    policy);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            tc_mma_bf16(tS(sb), tc_desc(sQ + (uint32_t)(dc * kBlk + k * 32), 16, 1024),
+                                        tc_desc(sK(ks) + (uint32_t)(dc * kBlk + k * 32), 16, 1024), kIdS,
+                                        (dc | k) != 0);
+                    tc_commit(s_full(sb));
+                    tc_commit(k_empty(ks));
+                    mbar_arrive(s_full(sb));
                 }
-            };
-            // zeroes the V rows of tile j whose keys are invalid (past n_keys, bad page): a row
-            // is 2 column blocks x 8 chunks of 16 bytes; lanes 0-15 clear the even rows, 16-31
-            // the odd ones, lane & 15 naming the chunk
-            auto zero_invalid_v = [&](int j) {
-                const int *ids = sm_pg + (j % kTcPageRing) * 16;
-                const bool tail = (j + 1) * kTcKeys > n_keys;
-                bool bad = false;
-                for (int x = 0; x < nbox; ++x) bad |= ids[x] < 0;
-                if (!tail && !bad) return;
-                const uint32_t dst = sV(j % kTcVStages) + (uint32_t)(((lane >> 3) & 1) * kBlk + (lane & 7) * 16);
-                for (int k = lane >> 4; k < kTcKeys; k += 2)
-                    if (j * kTcKeys + k >= n_keys || ids[k >> log2box] < 0)
-                        st_shared_v4(dst + (uint32_t)(k * 128), 0u, 0u, 0u, 0u);
-                fence_proxy_async_shared();
                 __syncwarp();
-            };
-            constexpr uint32_t kIdS = tc_idesc_bf16(kTcRows, kTcKeys, false);
-            constexpr uint32_t kIdO = tc_idesc_bf16(kTcRows, D, true);
-            constexpr uint32_t kIdL = tc_idesc_bf16(kTcRows, 16, false);
-            int k_issued = 0, v_issued = 0, k_seen = 0, v_seen = 0;
-            publish(0, fetch(0));
-            publish(1, fetch(1));
-            int next_raw = fetch(2);  // tile 2's entries, published when K(2) is issued
-            load(&tmK, sK(0), k_full(0), 0);
-            load(&tmV, sV(0), v_full(0), 0);
-            k_issued = v_issued = 1;
-            if (n_tiles > 1) {
-                load(&tmK, sK(1), k_full(1), 1);
-                k_issued = 2;
             }
-            for (int j = 0; j <= n_tiles; ++j) {
-                if (j < n_tiles) {  // S(j) = Q K(j)^T into S buffer j & 1
-                    const int ks = j % kTcKStages, sb = j & 1;
-                    if (!__all_sync(0xffffffffu,
-                                    mbar_wait_bounded(k_full(ks), (uint32_t)((j / kTcKStages) & 1), p.wait_limit_ns) &&
-                                        (j < 2 || mbar_wait_bounded(s_free(sb), (uint32_t)(((j >> 1) - 1) & 1),
-                                                                    p.wait_limit_ns)))) {
-                        failed = true;
-                        break;
-                    }
-                    k_seen = j + 1;
-                    if (leader) {
-                        tc_fence_after();
-#pragma unroll
-                        for (int dc = 0; dc < 2; ++dc)
-#pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                tc_mma_bf16(tS(sb), tc_desc(sQ + (uint32_t)(dc * kBlk + k * 32), 16, 1024),
-                                            tc_desc(sK(ks) + (uint32_t)(dc * kBlk + k * 32), 16, 1024), kIdS,
-                                            (dc | k) != 0);
-                        tc_commit(s_full(sb));
-                        tc_commit(k_empty(ks));
-                        mbar_arrive(s_full(sb));
-                    }
-                    __syncwarp();
+            if (j >= 1) {  // O += P(j-1) V(j-1)
+                const int t = j - 1, vs = t % kTcVStages;
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(v_full(vs), (uint32_t)((t / kTcVStages) & 1),
+                                                               p.wait_limit_ns))) {
+                    failed = true;
+                    break;
                 }
-                if (j >= 1) {  // O += P(j-1) V(j-1)
-                    const int t = j - 1, vs = t % kTcVStages;
-                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(v_full(vs), (uint32_t)((t / kTcVStages) & 1),
-                                                                   p.wait_limit_ns))) {
-                        failed = true;
-                        break;
-                    }
-                    v_seen = t + 1;
-                    zero_invalid_v(t);
-                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(p_full, (uint32_t)(t & 1), p.wait_limit_ns))) {
-                        failed = true;
-                        break;
-                    }
-                    if (leader) {
-                        tc_fence_after();
+                zero_invalid_v(t);
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(p_full, (uint32_t)(t & 1), p.wait_limit_ns))) {
+                    failed = true;
+                    break;
+                }
+                if (leader) {
+                    tc_fence_after();
 #pragma unroll
-                        for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                const uint64_t pdesc = tc_desc(sP + (uint32_t)(kb * kBlk + k * 32), 16, 1024);
-                                tc_mma_bf16(tO, pdesc,
-                                            tc_desc(sV(vs) + (uint32_t)((kb * 64 + k * 16) * 128), (uint32_t)kBlk,
-                                                    1024),
-                                            kIdO, t > 0 || (kb | k) != 0);
-                                tc_mma_bf16(tL, pdesc, tc_desc(sOnes + (uint32_t)(k * 32), 16, 1024), kIdL,
-                                            t > 0 || (kb | k) != 0);
-                            }
-                        tc_commit(o_done);
-                        tc_commit(v_empty(vs));
+                    for (int kk = 0; kk < 8; ++kk) {
+                        tc_mma_bf16_ts(tO, tP + (uint32_t)(kk * 8), v_desc(sV(vs), kk), kIdO, t > 0 || kk > 0);
+                        tc_mma_bf16_ts(tL, tP + (uint32_t)(kk * 8), tc_desc(sOnes + (uint32_t)((kk & 3) * 32), 16, 1024),
+                                       kIdL, t > 0 || kk > 0);
                     }
-                    __syncwarp();
+                    tc_commit(o_done);
+                    tc_commit(v_empty(vs));
                 }
-                if (j + 2 < n_tiles) {  // K(j+2) into the stage S(j) reads
-                    const int ks = j % kTcKStages;
-                    publish(j + 2, next_raw);
-                    next_raw = fetch(j + 3);
-                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(k_empty(ks), (uint32_t)((j / kTcKStages) & 1),
-                                                                   p.wait_limit_ns))) {
-                        failed = true;
-                        break;
-                    }
-                    load(&tmK, sK(ks), k_full(ks), j + 2);
-                    k_issued = j + 3;
-                }
-                if (j + 1 < n_tiles) {  // V(j+1) into the stage PV(j-2) read
-                    const int t = j + 1, vs = t % kTcVStages;
-                    if (t >= kTcVStages &&
-                        !__all_sync(0xffffffffu, mbar_wait_bounded(v_empty(vs), (uint32_t)((t / kTcVStages - 1) & 1),
-                                                                   p.wait_limit_ns))) {
-                        failed = true;
-                        break;
-                    }
-                    load(&tmV, sV(vs), v_full(vs), t);
-                    v_issued = t + 1;
-                }
+                __syncwarp();
             }
-            // let the copies (after a timeout) and the MMAs in flight finish before the CTA exits
-            if (leader) {
-                for (int t = k_seen; t < k_issued; ++t)
-                    mbar_wait_bounded(k_full(t % kTcKStages), (uint32_t)((t / kTcKStages) & 1), p.wait_limit_ns);
-                for (int t = v_seen; t < v_issued; ++t)
-                    mbar_wait_bounded(v_full(t % kTcVStages), (uint32_t)((t / kTcVStages) & 1), p.wait_limit_ns);
-                tc_commit(drain);
-                if (!mbar_wait_bounded(drain, 0, p.wait_limit_ns)) failed = true;
-            }
+        }
+        // the MMAs in flight finish before the CTA exits
+        if (leader) {
+            tc_commit(drain);
+            if (!mbar_wait_bounded(drain, 0, p.wait_limit_ns)) failed = true;
         }
     } else if (n_tiles > 0) {
         // ---- softmax warps: thread r owns row r
@@ -442,14 +429,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tc_st1(tL + lane_off, tc_ld1(tL + lane_off) * alpha);
                 }
             }
-            // P (bf16) into shared memory, K-major 128B-swizzled [2 key blocks][128 rows][128 B]
-#pragma unroll
-            for (int cc16 = 0; cc16 < 16; ++cc16) {
-                const int kb = cc16 >> 3, cc = cc16 & 7;
-                st_shared_v4(sP + (uint32_t)(kb * kBlk + r * 128 + ((cc ^ (r & 7)) << 4)), pw[4 * cc16],
-                             pw[4 * cc16 + 1], pw[4 * cc16 + 2], pw[4 * cc16 + 3]);
-            }
-            fence_proxy_async_shared();
+            // P (bf16 pairs) into this row's lane of tensor memory
+            tc_st64(tP + lane_off, pw);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
