@@ -307,7 +307,7 @@ def run_pkv(args) -> None:
     else:
         case = make_case(args.workload, device=dev)
     fp8 = args.cache == "fp8"
-    pkv.set_prefill_tensor_cores({0: "off", 1: "auto", 2: "always"}[getattr(args, "tc", 1)])
+    pkv.set_prefill_tensor_cores({0: "off", 1: "auto", 2: "always", 3: "rows128"}[getattr(args, "tc", 1)])
     pools8 = None
     if fp8:  # quantise the pools on the device, then drop the bf16 copies
         pools8 = pkv.quantize_pool_fp8(case.k_cache, case.v_cache)
@@ -422,8 +422,9 @@ def run_pkv(args) -> None:
         "clocks": clocks, "device_status": status, "wall_s_timed_region": round(t_wall, 3),
         "event_floor_us": floor_us,
         "tensor": None if q_len == 1 else {
-            "kernel": "prefill_tc_kernel (tcgen05)" if _takes_tensor_cores(args, case, q_len, fp8, props)
-                      else "decode_split_kernel<multi-row>",
+            "kernel": {0: "decode_split_kernel<multi-row>", 128: "prefill_tc_kernel (tcgen05, 128 rows/CTA)",
+                       256: "prefill_tc2_kernel (tcgen05, 256 rows/CTA)"}[
+                           _tensor_core_rows(args, case, q_len, fp8, props)],
             "tflops": round(causal_flops(case) / (mean_ms * 1e-3) / 1e12, 2),
             "peak_tflops": peaks["bf16_tflops"],
             "frac": round(causal_flops(case) / (mean_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)},
@@ -558,13 +559,23 @@ def run_append(args) -> None:
                       "bytes_per_call": moved, "gpu_launches": args.steps}), flush=True)
 
 
-def _takes_tensor_cores(args, case, q_len, fp8, props) -> bool:
-    """The library's routing of a several-rows call (see pkv_set_prefill_tensor_cores)."""
+def _tensor_core_rows(args, case, q_len, fp8, props) -> int:
+    """Rows per CTA of the tensor-core kernel the library routes a several-rows call to
+    (0: the mma.sync kernel; see pkv_set_prefill_tensor_cores)."""
     mode = getattr(args, "tc", 1)
     rows = q_len * case.G
     if mode == 0 or fp8 or case.D != 128 or rows < 128 or case.scale <= 0:
-        return False
-    return mode == 2 or case.B * case.Hkv * -(-rows // 128) >= props.multi_processor_count
+        return 0
+    if mode == 2:
+        return 256 if rows >= 256 else 128
+    if mode == 3:
+        return 128
+    if rows < 256:
+        return 128
+    max_tiles = max(1, -(-case.max_pages * case.P // 128))   # key splits as the library plans them
+    chunk = -(-max_tiles // min(max(-(-max_tiles // 32), 1), 65535))
+    splits = -(-max_tiles // chunk)
+    return 256 if 2 * case.B * case.Hkv * -(-rows // 256) * splits >= props.multi_processor_count else 128
 
 
 def run_step(args) -> None:
@@ -656,9 +667,10 @@ def main():
     ap.add_argument("--cache", default="bf16", choices=["bf16", "fp8"])
     ap.add_argument("--q-len", type=int, default=1,
                     help="new tokens per sequence (causal multi-token step); 1 = decode")
-    ap.add_argument("--tc", type=int, default=1, choices=[0, 1, 2],
+    ap.add_argument("--tc", type=int, default=1, choices=[0, 1, 2, 3],
                     help="several-rows calls: 0 = mma.sync kernel, 1 = library routing (tensor cores when the grid "
-                         "fills the GPU), 2 = tensor-core kernel wherever it applies")
+                         "fills the GPU), 2 = tensor-core kernel wherever it applies (256 rows per CTA where the "
+                         "group has them), 3 = tensor-core kernel with 128 rows per CTA")
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)

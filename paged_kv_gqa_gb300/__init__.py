@@ -122,14 +122,16 @@ def set_programmatic_launch(enable: bool) -> bool:
     return bool(load().pkv_set_programmatic_launch(int(bool(enable))))
 
 
-TC_MODES = {"off": 0, "auto": 1, "always": 2}
+TC_MODES = {"off": 0, "auto": 1, "always": 2, "rows128": 3}
 
 
 def set_prefill_tensor_cores(mode="auto") -> str:
     """Routing of long multi-row calls (bf16, D=128, >= 128 rows per group): "off" = the
-    mma.sync kernel, "auto" (default) = the tcgen05 kernel when its grid has at least one
-    CTA per SM, "always" = the tcgen05 kernel.  True/False mean "auto"/"off".  Returns the
-    previous mode."""
+    mma.sync kernel; "auto" (default) = the tcgen05 kernel with 256 rows per CTA when the
+    group has them and that grid (key splits included) has a CTA per two SMs, else with 128
+    rows; "always" = the tcgen05 kernel (256 rows per CTA where the group has them);
+    "rows128" = the tcgen05 kernel with 128 rows per CTA.  True/False mean "auto"/"off".
+    Returns the previous mode."""
     if isinstance(mode, bool):
         mode = "auto" if mode else "off"
     if mode not in TC_MODES:

@@ -11,11 +11,13 @@
 #include <cstring>
 #include <mutex>
 
+#include <algorithm>
 #include <atomic>
 
 #include "append_kernel.cuh"
 #include "decode_launch.cuh"
 #include "launch_util.h"
+#include "prefill_tc2_kernel.cuh"
 #include "prefill_tc_kernel.cuh"
 #include "merge_kernel.cuh"
 #include "pkv.h"
@@ -202,13 +204,17 @@ struct MultiRows {
 };
 
 // Several rows per sequence with at least 128 rows per (sequence, kv head) group, bf16
-// cache, D = 128, scale > 0: the tensor-core kernel (prefill_tc_kernel.cuh), one CTA per 128 rows,
-// no key splits (the rows give the parallelism).  Needs only the workspace's status word.
+// cache, D = 128, scale > 0: a tensor-core kernel, one CTA per cta_rows (128:
+// prefill_tc_kernel.cuh, 256: prefill_tc2_kernel.cuh) rows, no key splits (the rows give
+// the parallelism).  Needs only the workspace's status word.
 pkv_status prefill_tc(const pkv_bf16 *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
                       const int32_t *seq_lens, int B, int Hq, int Hkv, int page_size, int num_pages, int max_pages,
-                      float scale, pkv_bf16 *out, float *lse, void *workspace, const MultiRows &mr, int device,
-                      cudaStream_t stream)
+                      float scale, pkv_bf16 *out, float *lse, void *workspace, size_t workspace_bytes,
+                      int num_splits, const MultiRows &mr, int device, cudaStream_t stream, int cta_rows)
 {
+    const bool two = cta_rows == kTc2Rows;
+    const TcSplit sp = tc_split_plan(B, Hq, Hkv, page_size, max_pages, mr.total_q, mr.max_q_len, num_splits, cta_rows);
+    if (workspace_bytes < sp.ws.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
     constexpr int D = 128;
     const int box_t = page_size < kTcKeys ? page_size : kTcKeys;
     CUtensorMap mk, mv;
@@ -217,18 +223,21 @@ pkv_status prefill_tc(const pkv_bf16 *q, const void *k_cache, const void *v_cach
     st = get_pool_map(v_cache, num_pages, page_size, Hkv, D, box_t, device, 4, &mv);  // one copy per page box
     if (st != PKV_OK) return st;
     const int G = Hq / Hkv;
-    const long q_tiles = ((long)mr.max_q_len * G + kTcRows - 1) / kTcRows;
+    const long q_tiles = sp.q_tiles;
     if ((long)Hkv * q_tiles >= (1l << 31) || B > 65535) return PKV_ERR_UNSUPPORTED;
-    static bool attr_set[64] = {};
+    static bool attr_set[2][64] = {};
     static std::mutex mu;
     if (device < 0 || device >= 64) return PKV_ERR_UNSUPPORTED;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (!attr_set[device]) {
-            if (cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     TcSmem::dynamic) != cudaSuccess)
-                return PKV_ERR_CUDA;
-            attr_set[device] = true;
+        if (!attr_set[two][device]) {
+            const cudaError_t e =
+                two ? cudaFuncSetAttribute(prefill_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           Tc2Smem::dynamic)
+                    : cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           TcSmem::dynamic);
+            if (e != cudaSuccess) return PKV_ERR_CUDA;
+            attr_set[two][device] = true;
         }
     }
     PrefillTcParams p;
@@ -239,6 +248,12 @@ pkv_status prefill_tc(const pkv_bf16 *q, const void *k_cache, const void *v_cach
     p.out = reinterpret_cast<__nv_bfloat16 *>(out);
     p.lse = lse;
     p.status = static_cast<int *>(workspace);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    p.counters = reinterpret_cast<int *>(ws + sp.ws.counters);
+    p.part_lse = reinterpret_cast<float *>(ws + sp.ws.part_lse);
+    p.part_out = reinterpret_cast<float *>(ws + sp.ws.part_out);
+    p.total_rows = (size_t)mr.total_q * Hq;
+    p.chunk_tiles = sp.chunk_tiles;
     p.B = B;
     p.Hq = Hq;
     p.Hkv = Hkv;
@@ -253,10 +268,31 @@ pkv_status prefill_tc(const pkv_bf16 *q, const void *k_cache, const void *v_cach
     p.q_tiles = (int)q_tiles;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
     p.wait_limit_ns = kWaitLimitNs;
-    return launch_kernel(prefill_tc_kernel, dim3((unsigned)(Hkv * q_tiles), (unsigned)B), dim3(kTcThreads),
-                         (size_t)TcSmem::dynamic, stream, mk, mv, p) == cudaSuccess
-               ? PKV_OK
-               : PKV_ERR_CUDA;
+    const dim3 grid((unsigned)(Hkv * q_tiles), (unsigned)sp.splits, (unsigned)B);
+    const cudaError_t e =
+        two ? launch_kernel(prefill_tc2_kernel, grid, dim3(kTc2Threads), (size_t)Tc2Smem::dynamic, stream, mk, mv, p)
+            : launch_kernel(prefill_tc_kernel, grid, dim3(kTcThreads), (size_t)TcSmem::dynamic, stream, mk, mv, p);
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// Rows per CTA of the tensor-core kernel a several-rows call takes (0: the mma.sync kernel),
+// for a call the tensor-core kernels apply to (group_rows >= 128).  Auto: 256 rows when the
+// group has them and that grid (with its key splits) has at least half a CTA per SM, else
+// 128 rows; both kernels split long groups' keys, so the mma.sync kernel is not taken.
+int tensor_core_rows(int mode, int B, int Hq, int Hkv, int page_size, int max_pages, const MultiRows &mr,
+                     int num_splits, long group_rows, int sms)
+{
+    switch (mode) {
+    case PKV_TC_ALWAYS: return group_rows >= kTc2Rows ? kTc2Rows : kTcRows;
+    case PKV_TC_ROWS128: return kTcRows;
+    case PKV_TC_AUTO: {
+        if (group_rows < kTc2Rows) return kTcRows;
+        const TcSplit sp =
+            tc_split_plan(B, Hq, Hkv, page_size, max_pages, mr.total_q, mr.max_q_len, num_splits, kTc2Rows);
+        return 2l * B * Hkv * sp.q_tiles * sp.splits >= sms ? kTc2Rows : kTcRows;
+    }
+    default: return 0;
+    }
 }
 
 pkv_status decode_impl(const pkv_bf16 *q, const void *k_cache, const void *v_cache, Fp8Scales fp8,
@@ -285,12 +321,14 @@ pkv_status decode_impl(const pkv_bf16 *q, const void *k_cache, const void *v_cac
     int device = 0, sms = 0;
     pkv_status st = current_device_sms(&device, &sms);
     if (st != PKV_OK) return st;
-    const int tc_mode = g_prefill_tc.load(std::memory_order_relaxed);
-    const long tc_ctas = (long)B * Hkv * ((group_rows + kTcRows - 1) / kTcRows);
-    if (mq && !kv8 && D == 128 && group_rows >= kTcRows && scale > 0.f &&
-        (tc_mode == PKV_TC_ALWAYS || (tc_mode == PKV_TC_AUTO && tc_ctas >= sms)))
-        return prefill_tc(q, k_cache, v_cache, block_table, seq_lens, B, Hq, Hkv, page_size, num_pages, max_pages,
-                          scale, out, lse, workspace, mr, device, stream);
+    if (mq && !kv8 && D == 128 && group_rows >= kTcRows && scale > 0.f) {
+        const int tc_rows = tensor_core_rows(g_prefill_tc.load(std::memory_order_relaxed), B, Hq, Hkv, page_size,
+                                             max_pages, mr, num_splits, group_rows, sms);
+        if (tc_rows)
+            return prefill_tc(q, k_cache, v_cache, block_table, seq_lens, B, Hq, Hkv, page_size, num_pages,
+                              max_pages, scale, out, lse, workspace, workspace_bytes_, num_splits, mr, device, stream,
+                              tc_rows);
+    }
     pkv_plan plan;
     st = make_plan(B, Hq, Hkv, D, page_size, max_pages, sms, num_splits, &plan, kv8, group_rows, total_rows);
     if (st != PKV_OK) return st;
@@ -413,7 +451,8 @@ int pkv_set_programmatic_launch(int enable) { return g_pdl.exchange(enable ? 1 :
 
 int pkv_set_prefill_tensor_cores(int mode)
 {
-    if (mode != PKV_TC_OFF && mode != PKV_TC_AUTO && mode != PKV_TC_ALWAYS) return PKV_ERR_INVALID_ARG;
+    if (mode != PKV_TC_OFF && mode != PKV_TC_AUTO && mode != PKV_TC_ALWAYS && mode != PKV_TC_ROWS128)
+        return PKV_ERR_INVALID_ARG;
     return g_prefill_tc.exchange(mode);
 }
 
@@ -545,8 +584,16 @@ pkv_status pkv_plan_query_prefill(int B, int Hq, int Hkv, int D, int page_size, 
 {
     if (kv_dtype != PKV_KV_BF16 && kv_dtype != PKV_KV_FP8_E4M3) return PKV_ERR_INVALID_ARG;
     if (total_q < 0 || max_q_len < 1 || Hkv <= 0) return PKV_ERR_INVALID_ARG;
-    return make_plan(B, Hq, Hkv, D, page_size, max_pages, num_sms, num_splits, plan, kv_dtype == PKV_KV_FP8_E4M3,
-                     (long)max_q_len * (Hkv > 0 ? Hq / Hkv : 1), (long)total_q * Hq);
+    const long group_rows = (long)max_q_len * (Hq / Hkv);
+    const pkv_status st = make_plan(B, Hq, Hkv, D, page_size, max_pages, num_sms, num_splits, plan,
+                                    kv_dtype == PKV_KV_FP8_E4M3, group_rows, (long)total_q * Hq);
+    if (st != PKV_OK || kv_dtype != PKV_KV_BF16 || D != 128 || group_rows < kTcRows) return st;
+    // the tensor-core kernels may take the call: room for their split partials too
+    for (int rows : {kTcRows, kTc2Rows}) {
+        const TcSplit sp = tc_split_plan(B, Hq, Hkv, page_size, max_pages, total_q, max_q_len, num_splits, rows);
+        plan->workspace_bytes = std::max(plan->workspace_bytes, sp.ws.total);
+    }
+    return PKV_OK;
 }
 
 pkv_status paged_prefill_attn_workspace_size(int B, int Hq, int Hkv, int D, int page_size, int max_pages,

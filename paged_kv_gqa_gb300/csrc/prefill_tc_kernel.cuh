@@ -53,10 +53,67 @@ struct PrefillTcParams {
     __nv_bfloat16 *out;      // [total_q, Hq, D]
     float *lse;              // [total_q, Hq] or nullptr
     int *status;
+    // key splits: a CTA takes chunk_tiles key tiles of its group; a group with more than
+    // one chunk writes per-split partials and its last split merges them
+    float *part_lse;         // [splits, total_q * Hq] natural-log lse of each split
+    float *part_out;         // [splits, total_q * Hq, D] each split's normalised output
+    int *counters;           // [B, q_tiles, Hkv] splits finished per group (wraps to 0 after the last)
+    size_t total_rows;       // total_q * Hq
+    int chunk_tiles;
     int B, Hq, Hkv, G, P, log2P, num_pages, max_pages, total_q, max_q_len, causal, q_tiles;
     float scale_log2;
     unsigned long long wait_limit_ns;
 };
+
+// The last split of a group to finish merges the splits' partial outputs of one row with the
+// log-sum-exp recurrence (FlashQuant wiki "CUDA Kernels", split_k_reduce.cu "Algorithm":
+// split s weighs exp(lse_s - max lse)), in split order, 32 dims at a time.
+__device__ __forceinline__ void tc_merge_row(const PrefillTcParams &p, int n_chunks, size_t grow)
+{
+    constexpr float kLog2e = 1.4426950408889634074f;
+    const float ninf = __int_as_float(0xff800000);
+    float m = ninf;
+    for (int c = 0; c < n_chunks; ++c) m = fmaxf(m, __ldcg(p.part_lse + c * p.total_rows + grow));
+    const float mr = m == ninf ? 0.f : m;
+    float wsum = 0.f;
+    for (int c = 0; c < n_chunks; ++c) wsum += ex2((__ldcg(p.part_lse + c * p.total_rows + grow) - mr) * kLog2e);
+    const float inv = m == ninf ? 0.f : 1.f / wsum;
+    uint32_t *dst = reinterpret_cast<uint32_t *>(p.out + grow * 128);
+    for (int cb = 0; cb < 4; ++cb) {
+        float4 a[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c = 0; c < n_chunks; ++c) {
+            const float w = ex2((__ldcg(p.part_lse + c * p.total_rows + grow) - mr) * kLog2e) * inv;
+            const float4 *src = reinterpret_cast<const float4 *>(p.part_out + (c * p.total_rows + grow) * 128) + cb * 8;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 v = __ldcg(src + i);
+                a[i].x += v.x * w;
+                a[i].y += v.y * w;
+                a[i].z += v.z * w;
+                a[i].w += v.w * w;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            dst[cb * 16 + 2 * i] = pack_bf16x2(a[i].x, a[i].y);
+            dst[cb * 16 + 2 * i + 1] = pack_bf16x2(a[i].z, a[i].w);
+        }
+    }
+    if (p.lse) p.lse[grow] = m == ninf ? ninf : m + __logf(wsum);
+}
+
+// A split's row result into the partials (O / lt in f32, natural-log lse); o holds 32 of
+// the row's 128 dims, columns 32 cb .. 32 cb + 31.
+__device__ __forceinline__ void tc_store_partial(const PrefillTcParams &p, int c, size_t grow, int cb,
+                                                 const float (&o)[32], float inv)
+{
+    float4 *dst = reinterpret_cast<float4 *>(p.part_out + (c * p.total_rows + grow) * 128) + cb * 8;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
+}
 
 constexpr int kTcRows = 128;     // rows per CTA (the MMA's M)
 constexpr int kTcKeys = 128;     // keys per tile (the score MMA's N)
@@ -90,7 +147,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const float kNegInf = __int_as_float(0xff800000);
     constexpr float kRescaleGap = 8.f;   // move the reference maximum only past 2^8
     const int kvh = (int)(blockIdx.x % (unsigned)p.Hkv), qt = (int)(blockIdx.x / (unsigned)p.Hkv);
-    const int b = blockIdx.y;
+    const int split = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool issuer_warp = warp >= 4;  // the MMA warp and the copy warps
     const int G = p.G;
@@ -124,7 +181,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // keys any row of the CTA may see
     const int last_tok = (row0 + nrows - 1) / G;
     const int n_keys = max(0, p.causal ? min(L, L - n_q + last_tok + 1) : L);
-    const int n_tiles = (n_keys + kTcKeys - 1) / kTcKeys;
+    // key tiles of the group, split into chunks of chunk_tiles; this CTA takes chunk `split`
+    // (tiles t0 .. t0 + n_tiles - 1); a group with no key tile is handled by split 0
+    const int g_tiles = (n_keys + kTcKeys - 1) / kTcKeys;
+    const int n_chunks = (g_tiles + p.chunk_tiles - 1) / p.chunk_tiles;
+    if (split >= max(n_chunks, 1)) return;
+    const int t0 = split * p.chunk_tiles;
+    const int n_tiles = min(p.chunk_tiles, g_tiles - t0);
+    const bool direct = n_chunks <= 1;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t base = smem_addr(smem_raw);
@@ -209,7 +273,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int x = is_k ? lane >> 1 : lane, dc = is_k ? lane & 1 : 0;
         // block-table entry of box x of tile j (lanes x < nbox), read a tile before its use
         auto fetch = [&](int j) {
-            const int key = j * kTcKeys + x * box_t;
+            const int key = (t0 + j) * kTcKeys + x * box_t;
             return (dc == 0 && x < nbox && j < n_tiles && key < n_keys)
                        ? p.block_table[(size_t)b * p.max_pages + (key >> p.log2P)]
                        : -1;
@@ -219,7 +283,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int j = 0; j < n_tiles; ++j) {
             const int st = j % stages;
             const int next_raw = fetch(j + 1);
-            const bool has_key = x < nbox && j * kTcKeys + x * box_t < n_keys;
+            const bool has_key = x < nbox && (t0 + j) * kTcKeys + x * box_t < n_keys;
             const int pg_raw = is_k ? __shfl_sync(0xffffffffu, raw, lane & ~1) : raw;
             const int pg = has_key && (unsigned)pg_raw < (unsigned)p.num_pages ? pg_raw : -1;
             if (is_k && dc == 0 && has_key && pg < 0) atomicCAS(p.status, 0, PKV_ERR_BAD_PAGE_INDEX);
@@ -241,7 +305,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)__popc(ok) * copy_bytes);
             __syncwarp();
             if (pg >= 0) {
-                const int row = pg * p.P + ((j * kTcKeys + x * box_t) & (p.P - 1));
+                const int row = pg * p.P + (((t0 + j) * kTcKeys + x * box_t) & (p.P - 1));
                 if (is_k)
                     tma_load_3d(sK(st) + (uint32_t)(dc * kBlk + x * box_t * 128), &tmK, dc * 64, kvh, row, full,
                                 policy);
@@ -263,13 +327,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // clear the even keys, 16-31 the odd ones, lane & 15 naming the chunk
         auto zero_invalid_v = [&](int j) {
             const int *ids = sm_pg + (j % kTcPageRing) * 16;
-            const bool tail = (j + 1) * kTcKeys > n_keys;
+            const bool tail = (t0 + j + 1) * kTcKeys > n_keys;
             bool bad = false;
             for (int bx = 0; bx < nbox; ++bx) bad |= ids[bx] < 0;
             if (!tail && !bad) return;
             const uint32_t dst = sV(j % kTcVStages) + (uint32_t)(((lane >> 3) & 1) * box_t * 128 + (lane & 7) * 16);
             for (int k = lane >> 4; k < kTcKeys; k += 2)
-                if (j * kTcKeys + k >= n_keys || ids[k >> log2box] < 0)
+                if ((t0 + j) * kTcKeys + k >= n_keys || ids[k >> log2box] < 0)
                     st_shared_v4(dst + (uint32_t)((k >> log2box) * box_t * 256 + (k & (box_t - 1)) * 128), 0u, 0u,
                                  0u, 0u);
             fence_proxy_async_shared();
@@ -364,7 +428,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int *ids = sm_pg + (j % kTcPageRing) * 16;
             bool pages_ok = true;
             for (int x = 0; x < nbox; ++x) pages_ok &= ids[x] >= 0;
-            const int lim = row_lim - j * kTcKeys;
+            const int lim = row_lim - (t0 + j) * kTcKeys;
             if (!pages_ok) {
                 uint32_t okw[4] = {0u, 0u, 0u, 0u};
                 for (int x = 0; x < nbox; ++x) {
@@ -445,15 +509,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const float lt = tc_ld1(tL + lane_off);  // collective: every lane loads
             const float inv = empty ? 0.f : 1.f / lt;
             uint32_t *dst = reinterpret_cast<uint32_t *>(p.out + grow * D);
+            const float row_lse = empty ? kNegInf : (m_ref + __log2f(l_run)) * 0.693147180559945309f;
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb) {
                 float v[32];
                 tc_ld32(tO + lane_off + (uint32_t)(cb * 32), v);
-                if (row_ok)
+                if (row_ok && direct) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) dst[cb * 16 + i] = pack_bf16x2(v[2 * i] * inv, v[2 * i + 1] * inv);
+                } else if (row_ok) {
+                    tc_store_partial(p, split, grow, cb, v, inv);
+                }
             }
-            if (row_ok && p.lse) p.lse[grow] = empty ? kNegInf : (m_ref + __log2f(l_run)) * 0.693147180559945309f;
+            if (row_ok && direct && p.lse) p.lse[grow] = row_lse;
+            if (row_ok && !direct) p.part_lse[split * p.total_rows + grow] = row_lse;
         }
     }
     if (!issuer_warp && n_tiles == 0 && row_ok) {  // no key visible to the CTA: out = 0, lse = -inf
@@ -468,6 +537,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 0) {
         tc_fence_after();
         tc_dealloc(tmem, 512);
+    }
+    if (!direct) {  // the group's last split to finish merges the partials (also after a timeout,
+                    // so the counter returns to 0 for the next call)
+        int *last = reinterpret_cast<int *>(sbase + TcSmem::tmem_slot + 4);
+        __threadfence();
+        __syncthreads();
+        if (tid == 0)
+            *last = atomicInc(reinterpret_cast<unsigned *>(p.counters + ((size_t)b * p.q_tiles + qt) * p.Hkv + kvh),
+                              (unsigned)(n_chunks - 1)) == (unsigned)(n_chunks - 1);
+        __syncthreads();
+        if (*last) {
+            __threadfence();
+            if (row_ok) tc_merge_row(p, n_chunks, grow);
+        }
     }
 }
 

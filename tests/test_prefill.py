@@ -149,39 +149,81 @@ TC = [
     (1, 16, 2, 128, 8, [130], [130]),                      # 1040 rows: 9 tiles, 8-key pages
     (2, 32, 8, 128, 256, [64, 3], [600, 5]),               # 256-key pages; a short request in the batch
     (2, 16, 4, 128, 32, [70, 0], [70, 40]),                # an empty request
+    (2, 16, 2, 128, 64, [40, 9], [3000, 9]),               # 320 rows: a 256-row CTA whose second tile is partial
+    (1, 32, 8, 128, 16, [96], [96]),                       # 384 rows, causal from the first key
 ]
 
 
+@pytest.mark.parametrize("mode", ["always", "rows128"])  # 256 rows per CTA where the group has them; 128
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("B,Hq,Hkv,D,P,q_lens,kv_lens", TC, ids=lambda x: str(x).replace(" ", ""))
-def test_tensor_core_path_full_oracle(B, Hq, Hkv, D, P, q_lens, kv_lens, causal):
-    pkv.set_prefill_tensor_cores("always")
+def test_tensor_core_path_full_oracle(B, Hq, Hkv, D, P, q_lens, kv_lens, causal, mode):
+    pkv.set_prefill_tensor_cores(mode)
     case = make_prefill_case(_spec(B, Hq, Hkv, D, P, seed=3 * B + P + sum(q_lens)), q_lens, kv_lens, poison=True)
     out, lse = run_prefill(case, causal=causal)
     eo, el = compare(case, out, lse, causal=causal)
     assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
 
 
-def test_tensor_core_and_mma_sync_paths_agree():
-    case = make_prefill_case(_spec(2, 32, 8, 128, 16, seed=9), [48, 40], [1000, 300])
+@pytest.mark.parametrize("mode", ["always", "rows128"])
+def test_tensor_core_and_mma_sync_paths_agree(mode):
+    case = make_prefill_case(_spec(2, 32, 8, 128, 16, seed=9), [80, 40], [1000, 300])
     pkv.set_prefill_tensor_cores("off")
     ref_o, ref_l = run_prefill(case)
-    pkv.set_prefill_tensor_cores("always")
+    pkv.set_prefill_tensor_cores(mode)
     out, lse = run_prefill(case)
     excess, _, _ = split_invariance_violation(out.float().cpu().numpy(), ref_o.float().cpu().numpy(), tol=OUT_TOL)
     assert excess <= 0
     assert max_abs_diff(lse.cpu().numpy(), ref_l.cpu().numpy()) <= 1e-4
 
 
-def test_tensor_core_path_bad_page_is_skipped_and_reported():
-    case = make_prefill_case(_spec(2, 32, 8, 128, 16, seed=10), [40, 40], [200, 300])
+@pytest.mark.parametrize("mode", ["always", "rows128"])
+def test_tensor_core_path_bad_page_is_skipped_and_reported(mode):
+    case = make_prefill_case(_spec(2, 32, 8, 128, 16, seed=10), [70, 40], [200, 300])
     bt = case.block_table.clone()
     bt[1, 3] = case.num_pages + 7
     bad = Case(**case.__dict__)
     bad.block_table = bt
-    pkv.set_prefill_tensor_cores("always")
+    pkv.set_prefill_tensor_cores(mode)
     out, lse = run_prefill(bad, expect_status=-6)
     # request 0 is untouched; request 1 attends to its other keys only
     o0, l0 = run_prefill(case)
-    assert torch.equal(out[:40].view(torch.int16), o0[:40].view(torch.int16))
+    assert torch.equal(out[:70].view(torch.int16), o0[:70].view(torch.int16))
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("mode", ["always", "rows128"])
+@pytest.mark.parametrize("splits", [0, 3, 16])
+def test_tensor_core_key_splits(mode, splits):
+    # 9000 keys: several 32-tile chunks per group, merged by the last split; a short request beside it
+    case = make_prefill_case(_spec(2, 16, 2, 128, 16, seed=21), [40, 20], [9000, 300], poison=True)
+    pkv.set_prefill_tensor_cores(mode)
+    out, lse = run_prefill(case, num_splits=splits)
+    rows = [(t, h) for t in range(0, 60, 7) for h in (0, 5, 15)]
+    eo, el = compare(case, out, lse, select=rows)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("mode", ["always", "rows128"])
+def test_tensor_core_splits_reuse_the_workspace(mode):
+    # the merge counters wrap to 0 after each call: repeated calls on one workspace agree bit for bit
+    c = make_prefill_case(_spec(2, 16, 2, 128, 16, seed=22), [40, 33], [6000, 4500]).to("cuda")
+    pkv.set_prefill_tensor_cores(mode)
+    total_q, mq = c.q.shape[0], 40
+    ws = torch.zeros(pkv.paged_prefill_attn_workspace_size(c.B, c.Hq, c.Hkv, c.D, c.P, c.max_pages, total_q, mq,
+                                                           num_splits=4), dtype=torch.uint8, device="cuda")
+    results = []
+    for _ in range(3):
+        out = torch.full((total_q, c.Hq, c.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((total_q, c.Hq), float("nan"), dtype=torch.float32, device="cuda")
+        pkv.paged_prefill_attn(c.q, c.k_cache, c.v_cache, c.qo_indptr, c.block_table, c.seq_lens, mq, c.scale, out,
+                               lse, ws, num_splits=4)
+        assert pkv.pkv_check_status(ws) == 0
+        results.append((out, lse))
+    for out, lse in results[1:]:
+        assert torch.equal(out.view(torch.int16), results[0][0].view(torch.int16))
+        assert torch.equal(lse.view(torch.int32), results[0][1].view(torch.int32))
+    ref = run_prefill(c, num_splits=1)
+    excess, _, _ = split_invariance_violation(results[0][0].float().cpu().numpy(), ref[0].float().cpu().numpy())
+    assert excess <= 0 and max_abs_diff(results[0][1].cpu().numpy(), ref[1].cpu().numpy()) <= 2e-3
