@@ -16,9 +16,10 @@
 // MMA order per key tile j is PV_A(j), S_A(j+1), PV_B(j), S_B(j+1), so the tensor cores
 // compute one tile's products while the other tile's softmax runs.
 // The online softmax keeps a reference maximum per row that moves only when a tile's
-// maximum exceeds it by more than 2^8 (O is rescaled in tensor memory then).  O is
-// normalised by the sum of the bf16-rounded probabilities (kept by the softmax threads)
-// and the log-sum-exp uses the f32 sum.  The scale must be positive.
+// maximum exceeds it by more than 2^8 (O is rescaled in tensor memory then).  O and the
+// log-sum-exp use the f32 sum of the probabilities (O is accumulated from their bf16
+// roundings, so the normalisation differs from theirs by at most 2^-9 relative).  The
+// scale must be positive.
 // Every wait is bounded; on a timeout the status word is set and every warp stops after
 // its copies and MMAs in flight have finished.
 #pragma once
@@ -327,7 +328,7 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
     } else if (softmax_warp && n_tiles > 0) {
         // ---- softmax warps of tile qx: thread r owns row r
         const float c = p.scale_log2;  // > 0
-        float m_ref = kNegInf, l_run = 0.f, lt_run = 0.f;
+        float m_ref = kNegInf, l_run = 0.f;
         const int row_lim = min(n_keys, klim + 1);  // keys [0, row_lim) are visible to this row
         for (int j = 0; j < n_tiles; ++j) {
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(s_full(qx), (uint32_t)(j & 1), p.wait_limit_ns))) {
@@ -361,22 +362,25 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
                 for (int i = 0; i < kTcKeys; ++i)
                     if (i >= lim) sr[i] = 0xff800000u;
             }
-            // tile maximum of the unscaled scores, eight chains
+            // tile maximum of the unscaled scores: eight chains of three-input max
             float mx8[8];
 #pragma unroll
             for (int a = 0; a < 8; ++a) mx8[a] = __uint_as_float(sr[a]);
 #pragma unroll
-            for (int i = 8; i < kTcKeys; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sr[i]));
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
-                             c;
+            for (int i = 8; i < kTcKeys; i += 16)
+#pragma unroll
+                for (int a = 0; a < 8; ++a)
+                    mx8[a] = i + 8 + a < kTcKeys
+                                 ? fmax3(mx8[a], __uint_as_float(sr[i + a]), __uint_as_float(sr[i + 8 + a]))
+                                 : fmaxf(mx8[a], __uint_as_float(sr[i + a]));
+            const float mx =
+                fmaxf(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], fmax3(mx8[5], mx8[6], mx8[7]))) * c;
             // reference maximum: set at the first visible key, moved only past a 2^8 rise
             float alpha = 1.f;
             if (mx != kNegInf && (m_ref == kNegInf || mx > m_ref + kRescaleGap)) {
                 alpha = m_ref == kNegInf ? 0.f : ex2(m_ref - mx);
                 m_ref = mx;
                 l_run *= alpha;
-                lt_run *= alpha;
             }
             // PV(j-1) completed before S(j) was issued: O may be rescaled now
             if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
@@ -390,18 +394,27 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
                 }
             }
             const float neg_ref = m_ref == kNegInf ? 0.f : -m_ref;
-            float ls[4] = {0.f, 0.f, 0.f, 0.f}, lts[4] = {0.f, 0.f, 0.f, 0.f};
+            // p = 2^(s c - m) for two keys at a time (packed f32 pairs for the FMA and the sums)
+            const uint64_t c2 = f32x2(c, c), nr2 = f32x2(neg_ref, neg_ref);
+            uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
             uint32_t pw[kTcKeys / 2];
 #pragma unroll
             for (int i = 0; i < kTcKeys / 2; ++i) {
-                const float p0 = ex2(fmaf(__uint_as_float(sr[2 * i]), c, neg_ref));
-                const float p1 = ex2(fmaf(__uint_as_float(sr[2 * i + 1]), c, neg_ref));
+                float a0, a1;
+                f32x2_split(fma_f32x2(f32x2(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), c2, nr2), a0,
+                            a1);
+                const float p0 = ex2(a0), p1 = ex2(a1);
                 pw[i] = pack_bf16x2(p0, p1);
-                ls[i & 3] += p0 + p1;
-                lts[i & 3] += bf16_lo(pw[i]) + bf16_hi(pw[i]);
+                ls2[i & 3] = add_f32x2(ls2[i & 3], f32x2(p0, p1));
             }
-            l_run += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            lt_run += (lts[0] + lts[1]) + (lts[2] + lts[3]);
+            {
+                float l0, l1, l2, l3, l4, l5, l6, l7;
+                f32x2_split(ls2[0], l0, l1);
+                f32x2_split(ls2[1], l2, l3);
+                f32x2_split(ls2[2], l4, l5);
+                f32x2_split(ls2[3], l6, l7);
+                l_run += ((l0 + l1) + (l2 + l3)) + ((l4 + l5) + (l6 + l7));
+            }
             // P (bf16 pairs) into the first 64 columns of this row's S lane
             tc_st64(tS(qx) + lane_off, pw);
             tc_fence_before();
@@ -415,7 +428,7 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
         if (!failed) {
             tc_fence_after();
             const bool empty = m_ref == kNegInf;
-            const float inv = empty ? 0.f : 1.f / lt_run;
+            const float inv = empty ? 0.f : 1.f / l_run;
             uint32_t *dst = reinterpret_cast<uint32_t *>(p.out + grow * D);
             const float row_lse = empty ? kNegInf : (m_ref + __log2f(l_run)) * 0.693147180559945309f;
 #pragma unroll
