@@ -216,3 +216,37 @@ def test_plan_rejects_unknown_kv_dtype(lib):
     assert lib.pkv_plan_query_kv(8, 32, 8, 128, 16, 64, 152, 0, 2, ctypes.byref(plan)) == -1
     n = ctypes.c_size_t(0)
     assert lib.paged_decode_attn_workspace_size_kv(8, 32, 8, 128, 16, 64, 0, 0, 7, ctypes.byref(n)) == -1
+
+
+def test_tensor_core_routing_modes(lib):
+    # the process-wide switch: each mode round-trips, unknown ones are refused on both sides
+    old = pkv.set_prefill_tensor_cores("auto")
+    try:
+        for mode in ("off", "always", "rows128", "auto"):
+            pkv.set_prefill_tensor_cores(mode)
+        assert pkv.set_prefill_tensor_cores("rows128") == "auto"
+        assert pkv.set_prefill_tensor_cores(True) == "rows128"
+        assert pkv.set_prefill_tensor_cores(False) == "auto"
+        assert pkv.set_prefill_tensor_cores("auto") == "off"
+        with pytest.raises(ValueError):
+            pkv.set_prefill_tensor_cores("fast")
+        assert lib.pkv_set_prefill_tensor_cores(7) == -1
+        assert pkv.set_prefill_tensor_cores("auto") == "auto"  # the refused call changed nothing
+    finally:
+        pkv.set_prefill_tensor_cores(old)
+
+
+@pytest.mark.parametrize("max_pages,num_splits,splits", [(1024, 0, 4), (1024, 3, 3), (256, 0, 1), (1024, 1, 1)])
+def test_prefill_workspace_covers_tensor_core_splits(lib, max_pages, num_splits, splits):
+    # bf16, D = 128, 512 rows per group: the tensor-core kernels may take the call, so the plan's
+    # workspace holds their split partials: splits x rows x (D + 1) floats plus a counter per
+    # (sequence, query tile, kv head); 16-key pages, chunks of 32 tiles of 128 keys (4096 keys)
+    B, Hq, Hkv, D, P, max_q = 4, 32, 8, 128, 16, 128
+    total_q = B * max_q
+    plan = pkv.prefill_plan_query(B, Hq, Hkv, D, P, max_pages, total_q, max_q, 152, num_splits=num_splits)
+    rows = total_q * Hq
+    if splits > 1:
+        assert plan["workspace_bytes"] >= splits * rows * (D + 1) * 4 + B * 4 * Hkv * 4
+    # the fp8 cache never takes the tensor-core kernels: its plan is the mma.sync kernel's alone
+    fp8 = pkv.prefill_plan_query(B, Hq, Hkv, D, P, max_pages, total_q, max_q, 152, num_splits=num_splits, cache="fp8")
+    assert fp8["workspace_bytes"] <= plan["workspace_bytes"] or splits == 1
