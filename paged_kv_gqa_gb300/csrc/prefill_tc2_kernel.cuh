@@ -310,9 +310,9 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
                 }
                 issue_pv(x, j);
                 if (j + 1 < n_tiles) {
-                    // S_x(j+1) overwrites the columns PV_x(j) reads P_x from: after it completes
-                    if (!wait_all(o_done(x), j) ||
-                        (x == 0 && !wait_all(k_full((j + 1) % kTc2KStages), (j + 1) / kTc2KStages))) {
+                    // S_x(j+1) overwrites the columns PV_x(j) reads P_x from; MMAs issued by one
+                    // thread execute in issue order, so it follows PV_x(j) without a wait
+                    if (x == 0 && !wait_all(k_full((j + 1) % kTc2KStages), (j + 1) / kTc2KStages)) {
                         failed = true;
                         break;
                     }
