@@ -16,10 +16,10 @@
 // MMA order per key tile j is PV_A(j), S_A(j+1), PV_B(j), S_B(j+1), so the tensor cores
 // compute one tile's products while the other tile's softmax runs.
 // The online softmax keeps a reference maximum per row that moves only when a tile's
-// maximum exceeds it by more than 2^8 (O is rescaled in tensor memory then).  O and the
-// log-sum-exp use the f32 sum of the probabilities (O is accumulated from their bf16
-// roundings, so the normalisation differs from theirs by at most 2^-9 relative).  The
-// scale must be positive.
+// maximum exceeds it by more than 2^8 (O is rescaled in tensor memory then).  O is
+// normalised by the sum of the bf16-rounded probabilities it was accumulated from, the
+// log-sum-exp uses the f32 sum (both sums kept with packed f32x2 adds).  The scale must
+// be positive.
 // Every wait is bounded; on a timeout the status word is set and every warp stops after
 // its copies and MMAs in flight have finished.
 #pragma once
@@ -62,7 +62,8 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
     constexpr int kBlk = 128 * 128;      // bytes of one 64-column block of a tile
     const float kNegInf = __int_as_float(0xff800000);
     constexpr float kRescaleGap = 8.f;   // move the reference maximum only past 2^8
-    const int kvh = (int)(blockIdx.x % (unsigned)p.Hkv), qp = (int)(blockIdx.x / (unsigned)p.Hkv);
+    // a sequence's last query tiles (the longest under the causal mask) are launched first
+    const int kvh = (int)(blockIdx.x % (unsigned)p.Hkv), qp = p.q_tiles - 1 - (int)(blockIdx.x / (unsigned)p.Hkv);
     const int split = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool softmax_warp = warp < 8;
@@ -119,8 +120,8 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
     auto bar = [&](int i) { return smem_addr(&bars[i]); };
     constexpr int kKFull = 0, kKEmpty = kKFull + kTc2KStages, kVFull = kKEmpty + kTc2KStages,
                   kVEmpty = kVFull + kTc2VStages, kSFull = kVEmpty + kTc2VStages, kPFull = kSFull + 2,
-                  kODone = kPFull + 2, kDrain = kODone + 2;
-    static_assert(kDrain < 32, "prefill_tc2_kernel: more mbarriers than the shared-memory slots");
+                  kODone = kPFull + 2, kDrain = kODone + 2, kQFull = kDrain + 1;
+    static_assert(kQFull < 32, "prefill_tc2_kernel: more mbarriers than the shared-memory slots");
     auto k_full = [&](int s) { return bar(kKFull + s); };
     auto k_empty = [&](int s) { return bar(kKEmpty + s); };
     auto v_full = [&](int s) { return bar(kVFull + s); };
@@ -128,7 +129,7 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
     auto s_full = [&](int x) { return bar(kSFull + x); };   // per query tile
     auto p_full = [&](int x) { return bar(kPFull + x); };
     auto o_done = [&](int x) { return bar(kODone + x); };
-    const uint32_t drain = bar(kDrain);
+    const uint32_t drain = bar(kDrain), q_full = bar(kQFull);
     auto sQ = [&](int x) { return base + Tc2Smem::q + (uint32_t)(x * kTile); };
     auto sK = [&](int s) { return base + Tc2Smem::k + (uint32_t)(s * kTile); };
     auto sV = [&](int s) { return base + Tc2Smem::v + (uint32_t)(s * kTile); };
@@ -148,22 +149,12 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
             mbar_init(o_done(x), 1);
         }
         mbar_init(drain, 1);
+        mbar_init(q_full, 8);  // one arrival per softmax warp once its Q rows are in shared memory
         fence_barrier_init();
     }
     // TMEM columns: S_A 0..127, S_B 128..255, O_A 256..383, O_B 384..511; P_x in S_x 0..63
     if (warp == 0) tc_alloc(smem_addr(tmem_slot), 512);
 
-    // Q rows into shared memory, 128B-swizzled [2 column blocks][128 rows][128 B] per tile
-    if (softmax_warp) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(p.q + grow * D);
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            const uint4 v = row_ok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-            const int dc = c >> 3, cc = c & 7;
-            st_shared_v4(sQ(qx) + (uint32_t)(dc * kBlk + r * 128 + ((cc ^ (r & 7)) << 4)), v.x, v.y, v.z, v.w);
-        }
-    }
-    fence_proxy_async_shared();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -291,7 +282,7 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
             }
             __syncwarp();
         };
-        if (wait_all(k_full(0), 0)) {
+        if (wait_all(q_full, 0) && wait_all(k_full(0), 0)) {
             issue_s(0, 0);
             issue_s(1, 0);
         } else {
@@ -326,9 +317,22 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
             if (!mbar_wait_bounded(drain, 0, p.wait_limit_ns)) failed = true;
         }
     } else if (softmax_warp && n_tiles > 0) {
-        // ---- softmax warps of tile qx: thread r owns row r
+        // ---- softmax warps of tile qx: thread r owns row r.  Q rows into shared memory first
+        // (128B-swizzled [2 column blocks][128 rows][128 B] per tile), while the copies start.
+        {
+            const uint4 *src = reinterpret_cast<const uint4 *>(p.q + grow * D);
+#pragma unroll
+            for (int cq = 0; cq < 16; ++cq) {
+                const uint4 v = row_ok ? __ldg(src + cq) : make_uint4(0u, 0u, 0u, 0u);
+                const int dc = cq >> 3, cc = cq & 7;
+                st_shared_v4(sQ(qx) + (uint32_t)(dc * kBlk + r * 128 + ((cc ^ (r & 7)) << 4)), v.x, v.y, v.z, v.w);
+            }
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_full);
+        }
         const float c = p.scale_log2;  // > 0
-        float m_ref = kNegInf, l_run = 0.f;
+        float m_ref = kNegInf, l_run = 0.f, lt_run = 0.f;
         const int row_lim = min(n_keys, klim + 1);  // keys [0, row_lim) are visible to this row
         for (int j = 0; j < n_tiles; ++j) {
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(s_full(qx), (uint32_t)(j & 1), p.wait_limit_ns))) {
@@ -381,6 +385,7 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
                 alpha = m_ref == kNegInf ? 0.f : ex2(m_ref - mx);
                 m_ref = mx;
                 l_run *= alpha;
+                lt_run *= alpha;
             }
             // PV(j-1) completed before S(j) was issued: O may be rescaled now
             if (j >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
@@ -396,7 +401,7 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
             const float neg_ref = m_ref == kNegInf ? 0.f : -m_ref;
             // p = 2^(s c - m) for two keys at a time (packed f32 pairs for the FMA and the sums)
             const uint64_t c2 = f32x2(c, c), nr2 = f32x2(neg_ref, neg_ref);
-            uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
+            uint64_t ls2[2] = {0ull, 0ull}, lts2[2] = {0ull, 0ull};
             uint32_t pw[kTcKeys / 2];
 #pragma unroll
             for (int i = 0; i < kTcKeys / 2; ++i) {
@@ -405,15 +410,17 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
                             a1);
                 const float p0 = ex2(a0), p1 = ex2(a1);
                 pw[i] = pack_bf16x2(p0, p1);
-                ls2[i & 3] = add_f32x2(ls2[i & 3], f32x2(p0, p1));
+                ls2[i & 1] = add_f32x2(ls2[i & 1], f32x2(p0, p1));
+                lts2[i & 1] = add_f32x2(lts2[i & 1], f32x2(bf16_lo(pw[i]), bf16_hi(pw[i])));
             }
             {
-                float l0, l1, l2, l3, l4, l5, l6, l7;
+                float l0, l1, l2, l3;
                 f32x2_split(ls2[0], l0, l1);
                 f32x2_split(ls2[1], l2, l3);
-                f32x2_split(ls2[2], l4, l5);
-                f32x2_split(ls2[3], l6, l7);
-                l_run += ((l0 + l1) + (l2 + l3)) + ((l4 + l5) + (l6 + l7));
+                l_run += (l0 + l1) + (l2 + l3);
+                f32x2_split(lts2[0], l0, l1);
+                f32x2_split(lts2[1], l2, l3);
+                lt_run += (l0 + l1) + (l2 + l3);
             }
             // P (bf16 pairs) into the first 64 columns of this row's S lane
             tc_st64(tS(qx) + lane_off, pw);
@@ -428,8 +435,8 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
         if (!failed) {
             tc_fence_after();
             const bool empty = m_ref == kNegInf;
-            const float inv = empty ? 0.f : 1.f / l_run;
-            uint32_t *dst = reinterpret_cast<uint32_t *>(p.out + grow * D);
+            const float inv = empty ? 0.f : 1.f / lt_run;
+            uint4 *dst = reinterpret_cast<uint4 *>(p.out + grow * D);
             const float row_lse = empty ? kNegInf : (m_ref + __log2f(l_run)) * 0.693147180559945309f;
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb) {
@@ -437,7 +444,11 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
                 tc_ld32(tO(qx) + lane_off + (uint32_t)(cb * 32), v);  // collective: every lane loads
                 if (row_ok && direct) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) dst[cb * 16 + i] = pack_bf16x2(v[2 * i] * inv, v[2 * i + 1] * inv);
+                    for (int i = 0; i < 4; ++i)
+                        dst[cb * 4 + i] = make_uint4(pack_bf16x2(v[8 * i] * inv, v[8 * i + 1] * inv),
+                                                     pack_bf16x2(v[8 * i + 2] * inv, v[8 * i + 3] * inv),
+                                                     pack_bf16x2(v[8 * i + 4] * inv, v[8 * i + 5] * inv),
+                                                     pack_bf16x2(v[8 * i + 6] * inv, v[8 * i + 7] * inv));
                 } else if (row_ok) {
                     tc_store_partial(p, split, grow, cb, v, inv);
                 }
