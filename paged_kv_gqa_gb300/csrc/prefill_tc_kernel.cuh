@@ -146,7 +146,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr int kBlk = kTcRows * 128;  // bytes of one 64-column block of a tile
     const float kNegInf = __int_as_float(0xff800000);
     constexpr float kRescaleGap = 8.f;   // move the reference maximum only past 2^8
-    const int kvh = (int)(blockIdx.x % (unsigned)p.Hkv), qt = (int)(blockIdx.x / (unsigned)p.Hkv);
+    // a sequence's last query tiles (the longest under the causal mask) are launched first
+    const int kvh = (int)(blockIdx.x % (unsigned)p.Hkv), qt = p.q_tiles - 1 - (int)(blockIdx.x / (unsigned)p.Hkv);
     const int split = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool issuer_warp = warp >= 4;  // the MMA warp and the copy warps
@@ -204,15 +205,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     auto bar = [&](int i) { return smem_addr(&bars[i]); };
     constexpr int kKFull = 0, kKEmpty = kKFull + kTcKStages, kVFull = kKEmpty + kTcKStages,
                   kVEmpty = kVFull + kTcVStages, kSFull = kVEmpty + kTcVStages, kSFree = kSFull + 2,
-                  kPFull = kSFree + 2, kODone = kPFull + 1, kDrain = kODone + 1;
-    static_assert(kDrain < 32, "prefill_tc_kernel: more mbarriers than the shared-memory slots");
+                  kPFull = kSFree + 2, kODone = kPFull + 1, kDrain = kODone + 1, kQFull = kDrain + 1;
+    static_assert(kQFull < 32, "prefill_tc_kernel: more mbarriers than the shared-memory slots");
     auto k_full = [&](int s) { return bar(kKFull + s); };
     auto k_empty = [&](int s) { return bar(kKEmpty + s); };
     auto v_full = [&](int s) { return bar(kVFull + s); };
     auto v_empty = [&](int s) { return bar(kVEmpty + s); };
     auto s_full = [&](int s) { return bar(kSFull + s); };
     auto s_free = [&](int s) { return bar(kSFree + s); };
-    const uint32_t p_full = bar(kPFull), o_done = bar(kODone), drain = bar(kDrain);
+    const uint32_t p_full = bar(kPFull), o_done = bar(kODone), drain = bar(kDrain), q_full = bar(kQFull);
     auto sK = [&](int s) { return base + TcSmem::k + (uint32_t)(s * kTile); };
     auto sV = [&](int s) { return base + TcSmem::v + (uint32_t)(s * kTile); };
 
@@ -232,25 +233,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_init(p_full, 4);
         mbar_init(o_done, 1);
         mbar_init(drain, 1);
+        mbar_init(q_full, 4);  // one arrival per softmax warp once its Q rows are in shared memory
         fence_barrier_init();
     }
     // TMEM columns: S0 0..127, S1 128..255, O 256..383, the row sums of bf16 P 384..399,
     // P (bf16 pairs) 448..511
     if (warp == 0) tc_alloc(smem_addr(tmem_slot), 512);
 
-    // Q rows into shared memory, 128B-swizzled [2 column blocks][128 rows][128 B]
-    if (!issuer_warp) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(p.q + grow * D);
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            const uint4 v = row_ok ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-            const int dc = c >> 3, cc = c & 7;
-            st_shared_v4(sQ + (uint32_t)(dc * kBlk + r * 128 + ((cc ^ (r & 7)) << 4)), v.x, v.y, v.z, v.w);
-        }
-        constexpr uint32_t kOne2 = 0x3F803F80u;  // two bf16 ones
-        st_shared_v4(sOnes + (uint32_t)(r * 16), kOne2, kOne2, kOne2, kOne2);
-    }
-    fence_proxy_async_shared();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -354,7 +343,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (j < n_tiles) {  // S(j) = Q K(j)^T into S buffer j & 1
                 const int ks = j % kTcKStages, sb = j & 1;
                 if (!__all_sync(0xffffffffu,
-                                mbar_wait_bounded(k_full(ks), (uint32_t)((j / kTcKStages) & 1), p.wait_limit_ns) &&
+                                (j > 0 || mbar_wait_bounded(q_full, 0, p.wait_limit_ns)) &&
+                                    mbar_wait_bounded(k_full(ks), (uint32_t)((j / kTcKStages) & 1), p.wait_limit_ns) &&
                                     (j < 2 || mbar_wait_bounded(s_free(sb), (uint32_t)(((j >> 1) - 1) & 1),
                                                                 p.wait_limit_ns)))) {
                     failed = true;
@@ -407,7 +397,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!mbar_wait_bounded(drain, 0, p.wait_limit_ns)) failed = true;
         }
     } else if (n_tiles > 0) {
-        // ---- softmax warps: thread r owns row r
+        // ---- softmax warps: thread r owns row r.  Q rows (128B-swizzled [2 column blocks][128
+        // rows][128 B]) and the ones tile into shared memory first, while the copies start.
+        {
+            const uint4 *src = reinterpret_cast<const uint4 *>(p.q + grow * D);
+#pragma unroll
+            for (int cq = 0; cq < 16; ++cq) {
+                const uint4 v = row_ok ? __ldg(src + cq) : make_uint4(0u, 0u, 0u, 0u);
+                const int dc = cq >> 3, cc = cq & 7;
+                st_shared_v4(sQ + (uint32_t)(dc * kBlk + r * 128 + ((cc ^ (r & 7)) << 4)), v.x, v.y, v.z, v.w);
+            }
+            constexpr uint32_t kOne2 = 0x3F803F80u;  // two bf16 ones
+            st_shared_v4(sOnes + (uint32_t)(r * 16), kOne2, kOne2, kOne2, kOne2);
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_full);
+        }
         const float c = p.scale_log2;  // > 0
         float m_ref = kNegInf, l_run = 0.f;
         const int row_lim = min(n_keys, klim + 1);  // keys [0, row_lim) are visible to this row
@@ -508,7 +513,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const bool empty = m_ref == kNegInf;
             const float lt = tc_ld1(tL + lane_off);  // collective: every lane loads
             const float inv = empty ? 0.f : 1.f / lt;
-            uint32_t *dst = reinterpret_cast<uint32_t *>(p.out + grow * D);
+            uint4 *dst = reinterpret_cast<uint4 *>(p.out + grow * D);
             const float row_lse = empty ? kNegInf : (m_ref + __log2f(l_run)) * 0.693147180559945309f;
 #pragma unroll
             for (int cb = 0; cb < 4; ++cb) {
@@ -516,7 +521,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc_ld32(tO + lane_off + (uint32_t)(cb * 32), v);
                 if (row_ok && direct) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) dst[cb * 16 + i] = pack_bf16x2(v[2 * i] * inv, v[2 * i + 1] * inv);
+                    for (int i = 0; i < 4; ++i)
+                        dst[cb * 4 + i] = make_uint4(pack_bf16x2(v[8 * i] * inv, v[8 * i + 1] * inv),
+                                                     pack_bf16x2(v[8 * i + 2] * inv, v[8 * i + 3] * inv),
+                                                     pack_bf16x2(v[8 * i + 4] * inv, v[8 * i + 5] * inv),
+                                                     pack_bf16x2(v[8 * i + 6] * inv, v[8 * i + 7] * inv));
                 } else if (row_ok) {
                     tc_store_partial(p, split, grow, cb, v, inv);
                 }
