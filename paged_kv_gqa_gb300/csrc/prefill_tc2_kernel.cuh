@@ -479,9 +479,12 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
             *last = atomicInc(reinterpret_cast<unsigned *>(p.counters + ((size_t)b * p.q_tiles + qp) * p.Hkv + kvh),
                               (unsigned)(n_chunks - 1)) == (unsigned)(n_chunks - 1);
         __syncthreads();
-        if (*last) {
+        if (*last) {  // every warp merges rows warp, warp + W, ... of this CTA
             __threadfence();
-            if (row_ok) tc_merge_row(p, n_chunks, grow);
+            for (int cr = warp; cr < nrows; cr += kTc2Threads / 32) {
+                const int rt = (row0 + cr) / G, rh = (row0 + cr) % G;
+                tc_merge_row_warp(p, n_chunks, (size_t)(q_base + rt) * p.Hq + kvh * G + rh, lane);
+            }
         }
     }
 }

@@ -67,41 +67,50 @@ struct PrefillTcParams {
 
 // The last split of a group to finish merges the splits' partial outputs of one row with the
 // log-sum-exp recurrence (FlashQuant wiki "CUDA Kernels", split_k_reduce.cu "Algorithm":
-// split s weighs exp(lse_s - max lse)), in split order, 32 dims at a time.
-__device__ __forceinline__ void tc_merge_row(const PrefillTcParams &p, int n_chunks, size_t grow)
+// split s weighs exp(lse_s - max lse)), in split order.  One warp per row: lane l owns dims
+// 4l .. 4l + 3, so each split's partial row is one coalesced 512-byte load; lane s % 32
+// computes split s's weight, eight splits' loads are in flight at a time.
+__device__ __forceinline__ void tc_merge_row_warp(const PrefillTcParams &p, int n_chunks, size_t grow, int lane)
 {
     constexpr float kLog2e = 1.4426950408889634074f;
     const float ninf = __int_as_float(0xff800000);
     float m = ninf;
-    for (int c = 0; c < n_chunks; ++c) m = fmaxf(m, __ldcg(p.part_lse + c * p.total_rows + grow));
+    for (int c = lane; c < n_chunks; c += 32) m = fmaxf(m, __ldcg(p.part_lse + c * p.total_rows + grow));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     const float mr = m == ninf ? 0.f : m;
     float wsum = 0.f;
-    for (int c = 0; c < n_chunks; ++c) wsum += ex2((__ldcg(p.part_lse + c * p.total_rows + grow) - mr) * kLog2e);
+    for (int c = lane; c < n_chunks; c += 32) wsum += ex2((__ldcg(p.part_lse + c * p.total_rows + grow) - mr) * kLog2e);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
     const float inv = m == ninf ? 0.f : 1.f / wsum;
-    uint32_t *dst = reinterpret_cast<uint32_t *>(p.out + grow * 128);
-    for (int cb = 0; cb < 4; ++cb) {
-        float4 a[8];
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = 0; c0 < n_chunks; c0 += 32) {
+        // weight of split c0 + lane, broadcast below
+        const float wl = c0 + lane < n_chunks
+                             ? ex2((__ldcg(p.part_lse + (c0 + lane) * p.total_rows + grow) - mr) * kLog2e) * inv
+                             : 0.f;
+        const int nc = min(32, n_chunks - c0);
+        for (int k0 = 0; k0 < nc; k0 += 8) {
+            float4 v[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) a[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c = 0; c < n_chunks; ++c) {
-            const float w = ex2((__ldcg(p.part_lse + c * p.total_rows + grow) - mr) * kLog2e) * inv;
-            const float4 *src = reinterpret_cast<const float4 *>(p.part_out + (c * p.total_rows + grow) * 128) + cb * 8;
+            for (int k = 0; k < 8; ++k)
+                v[k] = k0 + k < nc ? __ldcg(reinterpret_cast<const float4 *>(
+                                              p.part_out + ((size_t)(c0 + k0 + k) * p.total_rows + grow) * 128) +
+                                          lane)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 v = __ldcg(src + i);
-                a[i].x += v.x * w;
-                a[i].y += v.y * w;
-                a[i].z += v.z * w;
-                a[i].w += v.w * w;
+            for (int k = 0; k < 8; ++k) {
+                const float w = __shfl_sync(0xffffffffu, wl, (k0 + k) & 31);
+                a.x += v[k].x * w;
+                a.y += v[k].y * w;
+                a.z += v[k].z * w;
+                a.w += v[k].w * w;
             }
         }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            dst[cb * 16 + 2 * i] = pack_bf16x2(a[i].x, a[i].y);
-            dst[cb * 16 + 2 * i + 1] = pack_bf16x2(a[i].z, a[i].w);
-        }
     }
-    if (p.lse) p.lse[grow] = m == ninf ? ninf : m + __logf(wsum);
+    reinterpret_cast<uint2 *>(p.out + grow * 128)[lane] = make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
+    if (lane == 0 && p.lse) p.lse[grow] = m == ninf ? ninf : m + __logf(wsum);
 }
 
 // A split's row result into the partials (O / lt in f32, natural-log lse); o holds 32 of
@@ -556,9 +565,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             *last = atomicInc(reinterpret_cast<unsigned *>(p.counters + ((size_t)b * p.q_tiles + qt) * p.Hkv + kvh),
                               (unsigned)(n_chunks - 1)) == (unsigned)(n_chunks - 1);
         __syncthreads();
-        if (*last) {
+        if (*last) {  // every warp merges rows warp, warp + W, ... of this CTA
             __threadfence();
-            if (row_ok) tc_merge_row(p, n_chunks, grow);
+            for (int cr = warp; cr < nrows; cr += kTcThreads / 32) {
+                const int rt = (row0 + cr) / G, rh = (row0 + cr) % G;
+                tc_merge_row_warp(p, n_chunks, (size_t)(q_base + rt) * p.Hq + kvh * G + rh, lane);
+            }
         }
     }
 }
