@@ -232,15 +232,20 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
         // clear the even keys, 16-31 the odd ones, lane & 15 naming the chunk
         auto zero_invalid_v = [&](int j) {
             const int *ids = sm_pg + (j % kTc2PageRing) * 16;
-            const bool tail = (t0 + j + 1) * kTcKeys > n_keys;
-            bool bad = false;
-            for (int bx = 0; bx < nbox; ++bx) bad |= ids[bx] < 0;
-            if (!tail && !bad) return;
+            const int first_past = min(kTcKeys, max(0, n_keys - (t0 + j) * kTcKeys));  // keys past n_keys: [first_past, 128)
+            bool bad = false;  // a missing page among the keys before that
+            for (int bx = 0; bx < nbox; ++bx) bad |= ids[bx] < 0 && (bx << log2box) < first_past;
+            if (first_past == kTcKeys && !bad) return;
             const uint32_t dst = sV(j % kTc2VStages) + (uint32_t)(((lane >> 3) & 1) * box_t * 128 + (lane & 7) * 16);
-            for (int k = lane >> 4; k < kTcKeys; k += 2)
-                if ((t0 + j) * kTcKeys + k >= n_keys || ids[k >> log2box] < 0)
-                    st_shared_v4(dst + (uint32_t)((k >> log2box) * box_t * 256 + (k & (box_t - 1)) * 128), 0u, 0u,
-                                 0u, 0u);
+            auto zero_key = [&](int k) {
+                st_shared_v4(dst + (uint32_t)((k >> log2box) * box_t * 256 + (k & (box_t - 1)) * 128), 0u, 0u, 0u, 0u);
+            };
+            for (int k = first_past + (lane >> 4); k < kTcKeys; k += 2) zero_key(k);
+            if (bad)
+                for (int bx = 0; bx < nbox; ++bx)
+                    if (ids[bx] < 0 && (bx << log2box) < first_past)
+                        for (int k = (bx << log2box) + (lane >> 4); k < min((bx + 1) << log2box, first_past); k += 2)
+                            zero_key(k);
             fence_proxy_async_shared();
             __syncwarp();
         };
