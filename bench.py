@@ -572,10 +572,13 @@ def _tensor_core_rows(args, case, q_len, fp8, props) -> int:
         return 128
     if rows < 256:
         return 128
+    sms = props.multi_processor_count
     max_tiles = max(1, -(-case.max_pages * case.P // 128))   # key splits as the library plans them
-    chunk = -(-max_tiles // min(max(-(-max_tiles // 32), 1), 65535))
+    groups = case.B * case.Hkv * -(-rows // 256)
+    s = sms // groups if groups < sms else -(-max_tiles // 64)
+    chunk = -(-max_tiles // min(max(s, 1), max_tiles, 65535))
     splits = -(-max_tiles // chunk)
-    return 256 if 2 * case.B * case.Hkv * -(-rows // 256) * splits >= props.multi_processor_count else 128
+    return 256 if 2 * groups * splits >= sms else 128
 
 
 def run_step(args) -> None:

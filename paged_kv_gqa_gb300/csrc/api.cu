@@ -210,10 +210,11 @@ struct MultiRows {
 pkv_status prefill_tc(const pkv_bf16 *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
                       const int32_t *seq_lens, int B, int Hq, int Hkv, int page_size, int num_pages, int max_pages,
                       float scale, pkv_bf16 *out, float *lse, void *workspace, size_t workspace_bytes,
-                      int num_splits, const MultiRows &mr, int device, cudaStream_t stream, int cta_rows)
+                      int num_splits, const MultiRows &mr, int device, int sms, cudaStream_t stream, int cta_rows)
 {
     const bool two = cta_rows == kTc2Rows;
-    const TcSplit sp = tc_split_plan(B, Hq, Hkv, page_size, max_pages, mr.total_q, mr.max_q_len, num_splits, cta_rows);
+    const TcSplit sp =
+        tc_split_plan(B, Hq, Hkv, page_size, max_pages, mr.total_q, mr.max_q_len, num_splits, cta_rows, sms);
     if (workspace_bytes < sp.ws.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
     constexpr int D = 128;
     const int box_t = page_size < kTcKeys ? page_size : kTcKeys;
@@ -288,7 +289,7 @@ int tensor_core_rows(int mode, int B, int Hq, int Hkv, int page_size, int max_pa
     case PKV_TC_AUTO: {
         if (group_rows < kTc2Rows) return kTcRows;
         const TcSplit sp =
-            tc_split_plan(B, Hq, Hkv, page_size, max_pages, mr.total_q, mr.max_q_len, num_splits, kTc2Rows);
+            tc_split_plan(B, Hq, Hkv, page_size, max_pages, mr.total_q, mr.max_q_len, num_splits, kTc2Rows, sms);
         return 2l * B * Hkv * sp.q_tiles * sp.splits >= sms ? kTc2Rows : kTcRows;
     }
     default: return 0;
@@ -326,8 +327,8 @@ pkv_status decode_impl(const pkv_bf16 *q, const void *k_cache, const void *v_cac
                                              max_pages, mr, num_splits, group_rows, sms);
         if (tc_rows)
             return prefill_tc(q, k_cache, v_cache, block_table, seq_lens, B, Hq, Hkv, page_size, num_pages,
-                              max_pages, scale, out, lse, workspace, workspace_bytes_, num_splits, mr, device, stream,
-                              tc_rows);
+                              max_pages, scale, out, lse, workspace, workspace_bytes_, num_splits, mr, device, sms,
+                              stream, tc_rows);
     }
     pkv_plan plan;
     st = make_plan(B, Hq, Hkv, D, page_size, max_pages, sms, num_splits, &plan, kv8, group_rows, total_rows);
@@ -590,7 +591,8 @@ pkv_status pkv_plan_query_prefill(int B, int Hq, int Hkv, int D, int page_size, 
     if (st != PKV_OK || kv_dtype != PKV_KV_BF16 || D != 128 || group_rows < kTcRows) return st;
     // the tensor-core kernels may take the call: room for their split partials too
     for (int rows : {kTcRows, kTc2Rows}) {
-        const TcSplit sp = tc_split_plan(B, Hq, Hkv, page_size, max_pages, total_q, max_q_len, num_splits, rows);
+        const TcSplit sp =
+            tc_split_plan(B, Hq, Hkv, page_size, max_pages, total_q, max_q_len, num_splits, rows, num_sms);
         plan->workspace_bytes = std::max(plan->workspace_bytes, sp.ws.total);
     }
     return PKV_OK;

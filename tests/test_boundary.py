@@ -236,17 +236,38 @@ def test_tensor_core_routing_modes(lib):
         pkv.set_prefill_tensor_cores(old)
 
 
-@pytest.mark.parametrize("max_pages,num_splits,splits", [(1024, 0, 4), (1024, 3, 3), (256, 0, 1), (1024, 1, 1)])
-def test_prefill_workspace_covers_tensor_core_splits(lib, max_pages, num_splits, splits):
-    # bf16, D = 128, 512 rows per group: the tensor-core kernels may take the call, so the plan's
-    # workspace holds their split partials: splits x rows x (D + 1) floats plus a counter per
-    # (sequence, query tile, kv head); 16-key pages, chunks of 32 tiles of 128 keys (4096 keys)
-    B, Hq, Hkv, D, P, max_q = 4, 32, 8, 128, 16, 128
+def _tc_splits(B, Hkv, G, max_pages, P, max_q, num_splits, rows, sms):
+    """The tensor-core split plan restated: fewer groups than SMs -> one wave of CTAs, else
+    chunks of at most 64 key tiles; num_splits > 0 forces the count."""
+    max_tiles = max(1, -(-max_pages * P // 128))
+    groups = B * Hkv * -(-max_q * G // rows)
+    s = num_splits if num_splits > 0 else (sms // groups if groups < sms else -(-max_tiles // 64))
+    chunk = -(-max_tiles // min(max(s, 1), max_tiles, 65535))
+    return -(-max_tiles // chunk)
+
+
+@pytest.mark.parametrize("B,max_q,max_pages,num_splits,sms", [
+    (4, 128, 1024, 0, 152),    # 64 groups of 256 rows: 2 splits; 128 groups of 128 rows: 1
+    (1, 32, 8192, 0, 152),     # 8 groups: 19 splits (one wave)
+    (64, 64, 2048, 0, 152),    # 512 groups: 64-tile chunks of a 256-tile table, 4 splits
+    (4, 128, 1024, 3, 152),    # forced
+    (8, 512, 256, 0, 152),     # 512 groups, 32 tiles: no split
+])
+def test_prefill_workspace_covers_tensor_core_splits(lib, B, max_q, max_pages, num_splits, sms):
+    # bf16, D = 128, G = 4: the tensor-core kernels may take the call, so the plan's workspace
+    # holds their split partials: splits x rows x (D + 1) floats plus a counter per group
+    Hq, Hkv, D, P = 32, 8, 128, 16
     total_q = B * max_q
-    plan = pkv.prefill_plan_query(B, Hq, Hkv, D, P, max_pages, total_q, max_q, 152, num_splits=num_splits)
+    plan = pkv.prefill_plan_query(B, Hq, Hkv, D, P, max_pages, total_q, max_q, sms, num_splits=num_splits)
     rows = total_q * Hq
-    if splits > 1:
-        assert plan["workspace_bytes"] >= splits * rows * (D + 1) * 4 + B * 4 * Hkv * 4
+    need = 0
+    for cta_rows in (128, 256):
+        s = _tc_splits(B, Hkv, Hq // Hkv, max_pages, P, max_q, num_splits, cta_rows, sms)
+        if s > 1:
+            need = max(need, s * rows * (D + 1) * 4)
+    assert plan["workspace_bytes"] >= need
+    if num_splits == 0 and (B, max_q, max_pages) == (1, 32, 8192):
+        assert need == 19 * rows * (D + 1) * 4  # the 256-row grid: 8 groups -> 152 // 8 = 19 splits
     # the fp8 cache never takes the tensor-core kernels: its plan is the mma.sync kernel's alone
-    fp8 = pkv.prefill_plan_query(B, Hq, Hkv, D, P, max_pages, total_q, max_q, 152, num_splits=num_splits, cache="fp8")
-    assert fp8["workspace_bytes"] <= plan["workspace_bytes"] or splits == 1
+    fp8 = pkv.prefill_plan_query(B, Hq, Hkv, D, P, max_pages, total_q, max_q, sms, num_splits=num_splits, cache="fp8")
+    assert fp8["workspace_bytes"] <= plan["workspace_bytes"]
