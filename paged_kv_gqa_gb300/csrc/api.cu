@@ -22,6 +22,7 @@
 #include "merge_kernel.cuh"
 #include "pkv.h"
 #include "plan.h"
+#include "tc_plan.h"
 
 namespace pkv {
 

@@ -118,21 +118,6 @@ struct WorkspaceLayout {
 // n_counters: one per (sequence, kv head, query tile); total_rows: rows of out (B*Hq for decode).
 WorkspaceLayout workspace_layout(int S, size_t n_counters, size_t total_rows, int D);
 
-// Key splits of the tensor-core several-rows kernels (prefill_tc_kernel.cuh with 128 rows
-// per CTA, prefill_tc2_kernel.cuh with 256): a CTA takes chunk_tiles tiles of 128 keys of
-// its group.  num_splits > 0: that many chunks over the table width.  num_splits = 0: with
-// fewer (sequence, kv head, query tile) groups than SMs, num_sms / groups chunks (about one
-// wave of CTAs); otherwise chunks of at most kTcChunkTiles tiles (8192 keys), which only
-// the longest groups of a ragged batch exceed.  The workspace holds the per-split
-// partials and one counter per group when splits > 1.
-constexpr int kTcChunkTiles = 64;
-struct TcSplit {
-    int splits, chunk_tiles, q_tiles;
-    WorkspaceLayout ws;
-};
-TcSplit tc_split_plan(int B, int Hq, int Hkv, int page_size, int max_pages, int total_q, int max_q_len,
-                      int num_splits, int cta_rows, int num_sms);
-
 // Shape checks shared by every entry point (no CUDA call).
 pkv_status validate_shape(int B, int Hq, int Hkv, int D, int page_size, int max_pages);
 
