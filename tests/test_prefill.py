@@ -227,3 +227,24 @@ def test_tensor_core_splits_reuse_the_workspace(mode):
     ref = run_prefill(c, num_splits=1)
     excess, _, _ = split_invariance_violation(results[0][0].float().cpu().numpy(), ref[0].float().cpu().numpy())
     assert excess <= 0 and max_abs_diff(results[0][1].cpu().numpy(), ref[1].cpu().numpy()) <= 2e-3
+
+
+@pytest.mark.parametrize("workload,q_len", [("batch", 512), ("ragged", 64), ("long", 32)])
+def test_tensor_core_path_at_full_size(workload, q_len):
+    # the workloads and the routing bench.py times (auto: 256 rows per CTA, key splits on ragged and
+    # long), sampled rows against the oracle, and a second call equal bit for bit
+    from workloads import CONFIGS, draw_seq_lens
+    spec = CONFIGS[workload]
+    kv = draw_seq_lens(spec["lens"], spec["B"], spec["P"], spec["seed"])
+    case = make_prefill_case(workload, [q_len] * spec["B"], kv, device="cuda")
+    pkv.set_prefill_tensor_cores("auto")
+    out, lse = run_prefill(case)
+    out2, lse2 = run_prefill(case)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))
+    total_q = case.q.shape[0]
+    rows = [(t, h) for t in range(0, total_q, max(1, total_q // 16)) for h in (0, case.Hq // 2 + 1, case.Hq - 1)]
+    rows += [(total_q - 1, 3)]  # the last token of the last request
+    eo, el = compare(case, out, lse, select=rows)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
