@@ -206,8 +206,9 @@ struct MultiRows {
 
 // Several rows per sequence with at least 128 rows per (sequence, kv head) group, bf16
 // cache, D = 128, scale > 0: a tensor-core kernel, one CTA per cta_rows (128:
-// prefill_tc_kernel.cuh, 256: prefill_tc2_kernel.cuh) rows, no key splits (the rows give
-// the parallelism).  Needs only the workspace's status word.
+// prefill_tc_kernel.cuh, 256: prefill_tc2_kernel.cuh) rows and key split (tc_split_plan).
+// With one split the workspace holds only the status word; with several, also the split
+// counters and the per-split partial outputs and lse that the last split merges.
 pkv_status prefill_tc(const pkv_bf16 *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
                       const int32_t *seq_lens, int B, int Hq, int Hkv, int page_size, int num_pages, int max_pages,
                       float scale, pkv_bf16 *out, float *lse, void *workspace, size_t workspace_bytes,
