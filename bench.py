@@ -564,12 +564,14 @@ def _tensor_core_rows(args, case, q_len, fp8, props) -> int:
     (0: the mma.sync kernel; see pkv_set_prefill_tensor_cores)."""
     mode = getattr(args, "tc", 1)
     rows = q_len * case.G
-    if mode == 0 or fp8 or case.D != 128 or rows < 128 or case.scale <= 0:
+    if mode == 0 or fp8 or case.D != 128 or rows <= 32 or case.scale <= 0:
         return 0
     if mode == 2:
         return 256 if rows >= 256 else 128
     if mode == 3:
         return 128
+    if rows < 128:   # short groups: the tensor cores only on tables of 8192 keys or more
+        return 128 if case.max_pages * case.P >= 8192 else 0
     if rows < 256:
         return 128
     sms = props.multi_processor_count
@@ -671,9 +673,9 @@ def main():
     ap.add_argument("--q-len", type=int, default=1,
                     help="new tokens per sequence (causal multi-token step); 1 = decode")
     ap.add_argument("--tc", type=int, default=1, choices=[0, 1, 2, 3],
-                    help="several-rows calls: 0 = mma.sync kernel, 1 = library routing (tensor cores when the grid "
-                         "fills the GPU), 2 = tensor-core kernel wherever it applies (256 rows per CTA where the "
-                         "group has them), 3 = tensor-core kernel with 128 rows per CTA")
+                    help="several-rows calls: 0 = mma.sync kernel, 1 = library routing (pkv_set_prefill_tensor_cores "
+                         "auto), 2 = tensor-core kernel wherever it applies (256 rows per CTA where the group has "
+                         "them), 3 = tensor-core kernel with 128 rows per CTA")
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)

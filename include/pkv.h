@@ -94,18 +94,25 @@ PKV_API int pkv_version(void);
 PKV_API int pkv_set_programmatic_launch(int enable);
 
 /*
- * Tensor-core path of paged_prefill_attn (bf16 cache, D = 128, scale > 0, at least
- * 128 (token, query head) rows per (sequence, kv head) group, i.e. max_q_len *
- * Hq/Hkv >= 128): the score and PV products run on tcgen05 (5th-generation tensor
- * cores, accumulators in tensor memory), one CTA per 128 or 256 rows of a group and
- * per chunk of 4096 keys (num_splits = 0) or per one of num_splits key ranges; a group
- * with several chunks merges them in the kernel through the workspace.  mode:
- * PKV_TC_OFF = such calls take the mma.sync kernel; PKV_TC_AUTO (the setting at load)
- * = 256 rows per CTA when the group has that many and that grid, B * Hkv *
- * ceil(max_q_len * Hq/Hkv / 256) * splits CTAs, has at least one CTA per two SMs,
- * else 128 rows per CTA; PKV_TC_ALWAYS = 256 rows per CTA when the group has that
- * many, else 128; PKV_TC_ROWS128 = 128 rows per CTA.  Process-wide; returns the
- * previous mode, or PKV_ERR_INVALID_ARG for an unknown one.
+ * Tensor-core path of paged_prefill_attn (bf16 cache, D = 128, scale > 0, more than 32
+ * (token, query head) rows per (sequence, kv head) group, i.e. max_q_len * Hq/Hkv > 32):
+ * the score and PV products run on tcgen05 (5th-generation tensor cores, accumulators in
+ * tensor memory), one CTA per 128 or 256 rows of a group and per key range.  Key ranges
+ * (num_splits = 0): when the groups' CTAs are fewer than the SMs, SMs / CTAs ranges per
+ * group (one wave), else ranges of at most 8192 keys; num_splits > 0 sets the count.  A
+ * group with several ranges merges them in the kernel through the workspace.  A group of
+ * at most 32 rows always takes the mma.sync kernel (one block reads each key once).
+ * mode:
+ *   PKV_TC_OFF     such calls take the mma.sync kernel;
+ *   PKV_TC_AUTO    (the setting at load) groups of 33-127 rows: 128 rows per CTA when
+ *                  max_pages * page_size >= 8192 (the mma.sync kernel would read each
+ *                  key once per 32 rows), else the mma.sync kernel; groups of 128 rows
+ *                  or more: 256 rows per CTA when the group has that many and that grid,
+ *                  B * Hkv * ceil(max_q_len * Hq/Hkv / 256) * ranges CTAs, has at least
+ *                  one CTA per two SMs, else 128 rows per CTA;
+ *   PKV_TC_ALWAYS  256 rows per CTA when the group has that many, else 128;
+ *   PKV_TC_ROWS128 128 rows per CTA.
+ * Process-wide; returns the previous mode, or PKV_ERR_INVALID_ARG for an unknown one.
  */
 enum pkv_tc_mode { PKV_TC_OFF = 0, PKV_TC_AUTO = 1, PKV_TC_ALWAYS = 2, PKV_TC_ROWS128 = 3 };
 PKV_API int pkv_set_prefill_tensor_cores(int mode);

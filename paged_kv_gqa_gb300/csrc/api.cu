@@ -33,6 +33,13 @@ std::atomic<int> g_prefill_tc{PKV_TC_AUTO};
 namespace {
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s: far above any healthy copy
+// Several-rows routing: a group of at most kMqBlockRows (token, head) rows fits one block of
+// the mma.sync kernel, which then reads each key once; larger groups may take the tensor
+// cores, groups below 128 rows only when the block table spans kTcShortGroupKeys keys or more
+// (measured on GB300: 64-row groups on 32K- and 128K-key tables 1.5-1.8x faster there, on a
+// 4K-key table 12% slower).
+constexpr int kMqBlockRows = 32;
+constexpr long kTcShortGroupKeys = 8192;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -279,9 +286,12 @@ pkv_status prefill_tc(const pkv_bf16 *q, const void *k_cache, const void *v_cach
 }
 
 // Rows per CTA of the tensor-core kernel a several-rows call takes (0: the mma.sync kernel),
-// for a call the tensor-core kernels apply to (group_rows >= 128).  Auto: 256 rows when the
-// group has them and that grid (with its key splits) has at least half a CTA per SM, else
-// 128 rows; both kernels split long groups' keys, so the mma.sync kernel is not taken.
+// for a call the tensor-core kernels apply to (more than kMqBlockRows rows per group).
+// Auto: groups of fewer than 128 rows take the 128-row kernel when the block table spans at
+// least kTcShortGroupKeys keys (the mma.sync kernel would read every key once per 32-row
+// block), else the mma.sync kernel; larger groups take 256 rows when the group has them and
+// that grid (with its key splits) has at least half a CTA per SM, else 128 rows; both
+// tensor-core kernels split long groups' keys.
 int tensor_core_rows(int mode, int B, int Hq, int Hkv, int page_size, int max_pages, const MultiRows &mr,
                      int num_splits, long group_rows, int sms)
 {
@@ -289,6 +299,7 @@ int tensor_core_rows(int mode, int B, int Hq, int Hkv, int page_size, int max_pa
     case PKV_TC_ALWAYS: return group_rows >= kTc2Rows ? kTc2Rows : kTcRows;
     case PKV_TC_ROWS128: return kTcRows;
     case PKV_TC_AUTO: {
+        if (group_rows < kTcRows) return (long)max_pages * page_size >= kTcShortGroupKeys ? kTcRows : 0;
         if (group_rows < kTc2Rows) return kTcRows;
         const TcSplit sp =
             tc_split_plan(B, Hq, Hkv, page_size, max_pages, mr.total_q, mr.max_q_len, num_splits, kTc2Rows, sms);
@@ -324,7 +335,7 @@ pkv_status decode_impl(const pkv_bf16 *q, const void *k_cache, const void *v_cac
     int device = 0, sms = 0;
     pkv_status st = current_device_sms(&device, &sms);
     if (st != PKV_OK) return st;
-    if (mq && !kv8 && D == 128 && group_rows >= kTcRows && scale > 0.f) {
+    if (mq && !kv8 && D == 128 && group_rows > kMqBlockRows && scale > 0.f) {
         const int tc_rows = tensor_core_rows(g_prefill_tc.load(std::memory_order_relaxed), B, Hq, Hkv, page_size,
                                              max_pages, mr, num_splits, group_rows, sms);
         if (tc_rows)
@@ -590,7 +601,7 @@ pkv_status pkv_plan_query_prefill(int B, int Hq, int Hkv, int D, int page_size, 
     const long group_rows = (long)max_q_len * (Hq / Hkv);
     const pkv_status st = make_plan(B, Hq, Hkv, D, page_size, max_pages, num_sms, num_splits, plan,
                                     kv_dtype == PKV_KV_FP8_E4M3, group_rows, (long)total_q * Hq);
-    if (st != PKV_OK || kv_dtype != PKV_KV_BF16 || D != 128 || group_rows < kTcRows) return st;
+    if (st != PKV_OK || kv_dtype != PKV_KV_BF16 || D != 128 || group_rows <= kMqBlockRows) return st;
     // the tensor-core kernels may take the call: room for their split partials too
     for (int rows : {kTcRows, kTc2Rows}) {
         const TcSplit sp =

@@ -252,6 +252,7 @@ def _tc_splits(B, Hkv, G, max_pages, P, max_q, num_splits, rows, sms):
     (64, 64, 2048, 0, 152),    # 512 groups: 64-tile chunks of a 256-tile table, 4 splits
     (4, 128, 1024, 3, 152),    # forced
     (8, 512, 256, 0, 152),     # 512 groups, 32 tiles: no split
+    (4, 16, 1024, 0, 152),     # 64 rows per group: the 128-row kernel may take it, 32 groups -> 4 splits
 ])
 def test_prefill_workspace_covers_tensor_core_splits(lib, B, max_q, max_pages, num_splits, sms):
     # bf16, D = 128, G = 4: the tensor-core kernels may take the call, so the plan's workspace

@@ -151,6 +151,9 @@ TC = [
     (2, 16, 4, 128, 32, [70, 0], [70, 40]),                # an empty request
     (2, 16, 2, 128, 64, [40, 9], [3000, 9]),               # 320 rows: a 256-row CTA whose second tile is partial
     (1, 32, 8, 128, 16, [96], [96]),                       # 384 rows, causal from the first key
+    (2, 64, 8, 128, 16, [8, 5], [3000, 40]),               # G = 8: 64 and 40 rows, one partial tile each
+    (3, 32, 8, 128, 32, [9, 12, 1], [500, 12, 700]),       # G = 4: 36, 48 and 4 rows
+    (1, 32, 4, 128, 16, [5], [9000]),                      # 40 rows over a 9000-key table (key splits)
 ]
 
 
@@ -162,6 +165,26 @@ def test_tensor_core_path_full_oracle(B, Hq, Hkv, D, P, q_lens, kv_lens, causal,
     case = make_prefill_case(_spec(B, Hq, Hkv, D, P, seed=3 * B + P + sum(q_lens)), q_lens, kv_lens, poison=True)
     out, lse = run_prefill(case, causal=causal)
     eo, el = compare(case, out, lse, causal=causal)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+
+
+@pytest.mark.parametrize("q_lens,kv_lens,table_keys,kernel", [
+    ([8, 5], [3000, 40], 4096, "off"),        # 64 rows, a 4096-key table: the mma.sync kernel
+    ([8, 5], [3000, 40], 8192, "rows128"),    # the same rows, an 8192-key table: the 128-row tensor-core kernel
+    ([4, 2], [9000, 40], 9008, "off"),        # 32 rows fit one mma.sync block whatever the table
+])
+def test_auto_routing_of_short_groups(q_lens, kv_lens, table_keys, kernel):
+    # auto takes the tensor cores for groups of 33-127 rows only on tables of 8192 keys or more: its
+    # result equals, bit for bit, the one of the kernel the rule names, and matches the oracle
+    case = make_prefill_case(dict(_spec(2, 64, 8, 128, 16, seed=41), max_pages=table_keys // 16), q_lens, kv_lens,
+                             poison=True)
+    assert case.max_pages * case.P == table_keys
+    pkv.set_prefill_tensor_cores("auto")
+    out, lse = run_prefill(case)
+    pkv.set_prefill_tensor_cores(kernel)
+    ref_o, ref_l = run_prefill(case)
+    assert torch.equal(out.view(torch.int16), ref_o.view(torch.int16)) and torch.equal(lse, ref_l)
+    eo, el = compare(case, out, lse)
     assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
 
 
