@@ -577,7 +577,11 @@ def _tensor_core_rows(args, case, q_len, fp8, props) -> int:
     sms = props.multi_processor_count
     max_tiles = max(1, -(-case.max_pages * case.P // 128))   # key splits as the library plans them
     groups = case.B * case.Hkv * -(-rows // 256)
-    s = sms // groups if groups < sms else -(-max_tiles // 64)
+    if groups < sms:
+        s = min((-(-groups * n // sms) * (-(-max_tiles // n) + 16), n)
+                for n in range(1, max(1, min(max_tiles, 4 * sms // groups)) + 1))[1]
+    else:
+        s = -(-max_tiles // 64)
     chunk = -(-max_tiles // min(max(s, 1), max_tiles, 65535))
     splits = -(-max_tiles // chunk)
     return 256 if 2 * groups * splits >= sms else 128

@@ -15,12 +15,25 @@ TcSplit tc_split_plan(int B, int Hq, int Hkv, int page_size, int max_pages, int 
     t.q_tiles = (int)(((long)max_q_len * G + cta_rows - 1) / cta_rows);
     const long groups = std::max(1l, (long)B * Hkv * t.q_tiles);
     long S;
-    if (num_splits > 0)
+    if (num_splits > 0) {
         S = num_splits;
-    else if (groups < num_sms)
-        S = num_sms / groups;
-    else
+    } else if (groups < num_sms) {
+        // a sparse grid: the count whose waves x (tiles per CTA + a CTA's fixed cost) is
+        // least, up to four CTAs per SM's worth of splits; ties keep the smaller count
+        const long s_max = std::max(1l, std::min(max_tiles, 4l * num_sms / groups));
+        long best = -1;
+        S = 1;
+        for (long s = 1; s <= s_max; ++s) {
+            const long waves = (groups * s + num_sms - 1) / num_sms;
+            const long cost = waves * ((max_tiles + s - 1) / s + kTcCtaCostTiles);
+            if (best < 0 || cost < best) {
+                best = cost;
+                S = s;
+            }
+        }
+    } else {
         S = (max_tiles + kTcChunkTiles - 1) / kTcChunkTiles;
+    }
     S = std::min(std::max(S, 1l), std::min(max_tiles, 65535l));
     const long chunk = (max_tiles + S - 1) / S;
     t.chunk_tiles = (int)chunk;

@@ -237,11 +237,19 @@ def test_tensor_core_routing_modes(lib):
 
 
 def _tc_splits(B, Hkv, G, max_pages, P, max_q, num_splits, rows, sms):
-    """The tensor-core split plan restated: fewer groups than SMs -> one wave of CTAs, else
-    chunks of at most 64 key tiles; num_splits > 0 forces the count."""
+    """The tensor-core split plan restated: fewer groups than SMs -> the count that minimises
+    waves x (tiles per CTA + 16), else chunks of at most 64 key tiles; num_splits > 0 forces
+    the count."""
     max_tiles = max(1, -(-max_pages * P // 128))
     groups = B * Hkv * -(-max_q * G // rows)
-    s = num_splits if num_splits > 0 else (sms // groups if groups < sms else -(-max_tiles // 64))
+    if num_splits > 0:
+        s = num_splits
+    elif groups < sms:
+        costs = [(-(-groups * n // sms) * (-(-max_tiles // n) + 16), n)
+                 for n in range(1, max(1, min(max_tiles, 4 * sms // groups)) + 1)]
+        s = min(costs)[1]
+    else:
+        s = -(-max_tiles // 64)
     chunk = -(-max_tiles // min(max(s, 1), max_tiles, 65535))
     return -(-max_tiles // chunk)
 
@@ -252,7 +260,8 @@ def _tc_splits(B, Hkv, G, max_pages, P, max_q, num_splits, rows, sms):
     (64, 64, 2048, 0, 152),    # 512 groups: 64-tile chunks of a 256-tile table, 4 splits
     (4, 128, 1024, 3, 152),    # forced
     (8, 512, 256, 0, 152),     # 512 groups, 32 tiles: no split
-    (4, 16, 1024, 0, 152),     # 64 rows per group: the 128-row kernel may take it, 32 groups -> 4 splits
+    (4, 16, 1024, 0, 152),     # 64 rows per group: the 128-row kernel may take it, 32 groups -> 9 splits
+    (4, 64, 8192, 0, 152),     # the long workload's shape at 16 new tokens: 32 groups -> 9 splits
 ])
 def test_prefill_workspace_covers_tensor_core_splits(lib, B, max_q, max_pages, num_splits, sms):
     # bf16, D = 128, G = 4: the tensor-core kernels may take the call, so the plan's workspace
@@ -268,7 +277,11 @@ def test_prefill_workspace_covers_tensor_core_splits(lib, B, max_q, max_pages, n
             need = max(need, s * rows * (D + 1) * 4)
     assert plan["workspace_bytes"] >= need
     if num_splits == 0 and (B, max_q, max_pages) == (1, 32, 8192):
-        assert need == 19 * rows * (D + 1) * 4  # the 256-row grid: 8 groups -> 152 // 8 = 19 splits
+        assert need == 19 * rows * (D + 1) * 4  # 8 groups of 1024 tiles: 19 splits fill one wave
+    if num_splits == 0 and (B, max_q, max_pages) == (4, 64, 8192):
+        # 32 groups of 1024 tiles: 4 splits (one wave of 128 CTAs, 1 x (256 + 16)) lose to 9 (two
+        # waves of 288 CTAs, 2 x (114 + 16)), measured 434 vs 401 us on the long workload
+        assert need == 9 * rows * (D + 1) * 4
     # the fp8 cache never takes the tensor-core kernels: its plan is the mma.sync kernel's alone
     fp8 = pkv.prefill_plan_query(B, Hq, Hkv, D, P, max_pages, total_q, max_q, sms, num_splits=num_splits, cache="fp8")
     assert fp8["workspace_bytes"] <= plan["workspace_bytes"]
