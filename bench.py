@@ -564,15 +564,15 @@ def _tensor_core_rows(args, case, q_len, fp8, props) -> int:
     (0: the mma.sync kernel; see pkv_set_prefill_tensor_cores)."""
     mode = getattr(args, "tc", 1)
     rows = q_len * case.G
-    if mode == 0 or fp8 or case.D != 128 or rows <= 32 or case.scale <= 0:
+    if mode == 0 or case.D != 128 or rows <= 32 or case.scale <= 0:
         return 0
     if mode == 2:
-        return 256 if rows >= 256 else 128
+        return 128 if fp8 or rows < 256 else 256
     if mode == 3:
         return 128
     if rows < 128:   # short groups: the tensor cores only on tables of 8192 keys or more
         return 128 if case.max_pages * case.P >= 8192 else 0
-    if rows < 256:
+    if rows < 256 or fp8:   # the fp8 cache has the 128-row kernel only
         return 128
     sms = props.multi_processor_count
     max_tiles = max(1, -(-case.max_pages * case.P // 128))   # key splits as the library plans them

@@ -216,38 +216,45 @@ struct MultiRows {
 // prefill_tc_kernel.cuh, 256: prefill_tc2_kernel.cuh) rows and key split (tc_split_plan).
 // With one split the workspace holds only the status word; with several, also the split
 // counters and the per-split partial outputs and lse that the last split merges.
-pkv_status prefill_tc(const pkv_bf16 *q, const void *k_cache, const void *v_cache, const int32_t *block_table,
-                      const int32_t *seq_lens, int B, int Hq, int Hkv, int page_size, int num_pages, int max_pages,
-                      float scale, pkv_bf16 *out, float *lse, void *workspace, size_t workspace_bytes,
-                      int num_splits, const MultiRows &mr, int device, int sms, cudaStream_t stream, int cta_rows)
+pkv_status prefill_tc(const pkv_bf16 *q, const void *k_cache, const void *v_cache, const Fp8Scales &fp8,
+                      const int32_t *block_table, const int32_t *seq_lens, int B, int Hq, int Hkv, int page_size,
+                      int num_pages, int max_pages, float scale, pkv_bf16 *out, float *lse, void *workspace,
+                      size_t workspace_bytes, int num_splits, const MultiRows &mr, int device, int sms,
+                      cudaStream_t stream, int cta_rows)
 {
+    if (fp8.on && cta_rows != kTcRows) return PKV_ERR_UNSUPPORTED;  // the fp8 cache has the 128-row kernel only
     const bool two = cta_rows == kTc2Rows;
+    const int variant = fp8.on ? 2 : two ? 1 : 0;
     const TcSplit sp =
         tc_split_plan(B, Hq, Hkv, page_size, max_pages, mr.total_q, mr.max_q_len, num_splits, cta_rows, sms);
     if (workspace_bytes < sp.ws.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
     constexpr int D = 128;
     const int box_t = page_size < kTcKeys ? page_size : kTcKeys;
     CUtensorMap mk, mv;
-    pkv_status st = get_pool_map(k_cache, num_pages, page_size, Hkv, D, box_t, device, 3, &mk);
+    // bf16: K per 64-dim half (rank 3), V one copy per page box (rank 4); fp8: the codes of a
+    // page box in one copy each (the byte view)
+    pkv_status st = get_pool_map(k_cache, num_pages, page_size, Hkv, D, box_t, device, fp8.on ? 8 : 3, &mk);
     if (st != PKV_OK) return st;
-    st = get_pool_map(v_cache, num_pages, page_size, Hkv, D, box_t, device, 4, &mv);  // one copy per page box
+    st = get_pool_map(v_cache, num_pages, page_size, Hkv, D, box_t, device, fp8.on ? 8 : 4, &mv);
     if (st != PKV_OK) return st;
     const int G = Hq / Hkv;
     const long q_tiles = sp.q_tiles;
     if ((long)Hkv * q_tiles >= (1l << 31) || B > 65535) return PKV_ERR_UNSUPPORTED;
-    static bool attr_set[2][64] = {};
+    static bool attr_set[3][64] = {};
     static std::mutex mu;
     if (device < 0 || device >= 64) return PKV_ERR_UNSUPPORTED;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (!attr_set[two][device]) {
+        if (!attr_set[variant][device]) {
             const cudaError_t e =
-                two ? cudaFuncSetAttribute(prefill_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           Tc2Smem::dynamic)
-                    : cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           TcSmem::dynamic);
+                variant == 1 ? cudaFuncSetAttribute(prefill_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                    Tc2Smem::dynamic)
+                : variant == 2 ? cudaFuncSetAttribute(prefill_tc_kernel<true>,
+                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, Tc8Smem::dynamic)
+                               : cudaFuncSetAttribute(prefill_tc_kernel<false>,
+                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem::dynamic);
             if (e != cudaSuccess) return PKV_ERR_CUDA;
-            attr_set[two][device] = true;
+            attr_set[variant][device] = true;
         }
     }
     PrefillTcParams p;
@@ -258,6 +265,8 @@ pkv_status prefill_tc(const pkv_bf16 *q, const void *k_cache, const void *v_cach
     p.out = reinterpret_cast<__nv_bfloat16 *>(out);
     p.lse = lse;
     p.status = static_cast<int *>(workspace);
+    p.k_scale = fp8.k_scale;
+    p.v_scale = fp8.v_scale;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     p.counters = reinterpret_cast<int *>(ws + sp.ws.counters);
     p.part_lse = reinterpret_cast<float *>(ws + sp.ws.part_lse);
@@ -280,8 +289,12 @@ pkv_status prefill_tc(const pkv_bf16 *q, const void *k_cache, const void *v_cach
     p.wait_limit_ns = kWaitLimitNs;
     const dim3 grid((unsigned)(Hkv * q_tiles), (unsigned)sp.splits, (unsigned)B);
     const cudaError_t e =
-        two ? launch_kernel(prefill_tc2_kernel, grid, dim3(kTc2Threads), (size_t)Tc2Smem::dynamic, stream, mk, mv, p)
-            : launch_kernel(prefill_tc_kernel, grid, dim3(kTcThreads), (size_t)TcSmem::dynamic, stream, mk, mv, p);
+        variant == 1
+            ? launch_kernel(prefill_tc2_kernel, grid, dim3(kTc2Threads), (size_t)Tc2Smem::dynamic, stream, mk, mv, p)
+        : variant == 2 ? launch_kernel(prefill_tc_kernel<true>, grid, dim3(kTc8Threads), (size_t)Tc8Smem::dynamic,
+                                       stream, mk, mv, p)
+                       : launch_kernel(prefill_tc_kernel<false>, grid, dim3(kTcThreads), (size_t)TcSmem::dynamic,
+                                       stream, mk, mv, p);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
@@ -335,11 +348,12 @@ pkv_status decode_impl(const pkv_bf16 *q, const void *k_cache, const void *v_cac
     int device = 0, sms = 0;
     pkv_status st = current_device_sms(&device, &sms);
     if (st != PKV_OK) return st;
-    if (mq && !kv8 && D == 128 && group_rows > kMqBlockRows && scale > 0.f) {
-        const int tc_rows = tensor_core_rows(g_prefill_tc.load(std::memory_order_relaxed), B, Hq, Hkv, page_size,
-                                             max_pages, mr, num_splits, group_rows, sms);
+    if (mq && D == 128 && group_rows > kMqBlockRows && scale > 0.f) {
+        int tc_rows = tensor_core_rows(g_prefill_tc.load(std::memory_order_relaxed), B, Hq, Hkv, page_size,
+                                       max_pages, mr, num_splits, group_rows, sms);
+        if (kv8 && tc_rows) tc_rows = kTcRows;  // the fp8 cache: the 128-row kernel's fp8 instantiation
         if (tc_rows)
-            return prefill_tc(q, k_cache, v_cache, block_table, seq_lens, B, Hq, Hkv, page_size, num_pages,
+            return prefill_tc(q, k_cache, v_cache, fp8, block_table, seq_lens, B, Hq, Hkv, page_size, num_pages,
                               max_pages, scale, out, lse, workspace, workspace_bytes_, num_splits, mr, device, sms,
                               stream, tc_rows);
     }
@@ -601,9 +615,11 @@ pkv_status pkv_plan_query_prefill(int B, int Hq, int Hkv, int D, int page_size, 
     const long group_rows = (long)max_q_len * (Hq / Hkv);
     const pkv_status st = make_plan(B, Hq, Hkv, D, page_size, max_pages, num_sms, num_splits, plan,
                                     kv_dtype == PKV_KV_FP8_E4M3, group_rows, (long)total_q * Hq);
-    if (st != PKV_OK || kv_dtype != PKV_KV_BF16 || D != 128 || group_rows <= kMqBlockRows) return st;
-    // the tensor-core kernels may take the call: room for their split partials too
+    if (st != PKV_OK || D != 128 || group_rows <= kMqBlockRows) return st;
+    // the tensor-core kernels may take the call: room for their split partials too (the fp8
+    // cache has the 128-row kernel only)
     for (int rows : {kTcRows, kTc2Rows}) {
+        if (kv_dtype == PKV_KV_FP8_E4M3 && rows != kTcRows) continue;
         const TcSplit sp =
             tc_split_plan(B, Hq, Hkv, page_size, max_pages, total_q, max_q_len, num_splits, rows, num_sms);
         plan->workspace_bytes = std::max(plan->workspace_bytes, sp.ws.total);

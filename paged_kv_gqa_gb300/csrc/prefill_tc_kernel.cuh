@@ -59,6 +59,9 @@ struct PrefillTcParams {
     float *part_out;         // [splits, total_q * Hq, D] each split's normalised output
     int *counters;           // [B, q_tiles, Hkv] splits finished per group (wraps to 0 after the last)
     size_t total_rows;       // total_q * Hq
+    // fp8 (e4m3) cache: per-(page, kv head, slot) power-of-two scales [num_pages, Hkv, P]
+    // (the codes' pools come through the tensor maps); unused with a bf16 cache
+    const float *k_scale, *v_scale;
     int chunk_tiles;
     int B, Hq, Hkv, G, P, log2P, num_pages, max_pages, total_q, max_q_len, causal, q_tiles;
     float scale_log2;
@@ -126,32 +129,92 @@ __device__ __forceinline__ void tc_store_partial(const PrefillTcParams &p, int c
 
 constexpr int kTcRows = 128;     // rows per CTA (the MMA's M)
 constexpr int kTcKeys = 128;     // keys per tile (the score MMA's N)
-constexpr int kTcThreads = 224;  // 4 softmax warps, the MMA warp, the K and V copy warps
-constexpr int kTcKStages = 3;
-constexpr int kTcVStages = 3;
 constexpr int kTcPageRing = 8;   // tiles whose page ids are kept
 
+// Per cache type: threads, bf16 K and V stages, fp8 staging stages.  bf16: 4 softmax warps,
+// the MMA warp, the K and V copy warps; K and V land by TMA straight into three stages each.
+// fp8: the copy warps land the e4m3 codes and scales in two staging stages, and two K and two
+// V converter warps (7-8, 9-10) write them, dequantised to bf16, into the layout the bf16
+// copies land (two K stages, one V stage: the V tile of a key tile is written only once the
+// previous tile's PV product has read its stage).
+template <bool KV8>
+struct TcCfg {
+    static constexpr int threads = KV8 ? 352 : 224;
+    static constexpr int k_stages = KV8 ? 2 : 3;
+    static constexpr int v_stages = KV8 ? 1 : 3;
+    static constexpr int s8_stages = KV8 ? 2 : 0;
+};
+constexpr int kTcThreads = TcCfg<false>::threads;
+constexpr int kTc8Threads = TcCfg<true>::threads;
+
 // Shared memory (bytes from a 1024-aligned base) of the D = 128 kernel.
-struct TcSmem {
+template <bool KV8>
+struct TcSmemT {
     static constexpr int kTile = kTcRows * 128 * 2;  // 128 rows x 128 dims (or keys) bf16, 2 column blocks
+    static constexpr int kCodes = kTcKeys * 128;      // 128 keys x 128 e4m3 codes
+    // fp8 staging stage: [K codes][V codes] (each as the 128B-swizzled page boxes land) [K scales][V scales]
+    static constexpr int kStage8 = 2 * kCodes + 2 * kTcKeys * 4;
     static constexpr int q = 0;
-    static constexpr int k = kTile;                          // K stage s at k + s * kTile
-    static constexpr int v = k + kTcKStages * kTile;         // V stage s at v + s * kTile
-    static constexpr int ones = v + kTcVStages * kTile;      // 16 x 64 bf16 ones, the B operand of the row-sum MMA
-    static constexpr int bars = ones + 2048;                 // 32 mbarriers
-    static constexpr int pages = bars + 32 * 8;              // [kTcPageRing][16] page id of each box, -1: none
+    static constexpr int k = kTile;                                      // K stage s at k + s * kTile
+    static constexpr int v = k + TcCfg<KV8>::k_stages * kTile;           // V stage s at v + s * kTile
+    static constexpr int ones = v + TcCfg<KV8>::v_stages * kTile;        // 16 x 64 bf16 ones, the B operand of the row-sum MMA
+    static constexpr int s8 = (ones + 2048 + 1023) / 1024 * 1024;       // fp8 staging stage s at s8 + s * kStage8
+    static constexpr int bars = s8 + TcCfg<KV8>::s8_stages * kStage8;    // 32 mbarriers
+    static constexpr int pages = bars + 32 * 8;                          // [kTcPageRing][16] page id of each box, -1: none
     static constexpr int tmem_slot = pages + kTcPageRing * 16 * 4;
     static constexpr int total = tmem_slot + 16;
-    static constexpr int dynamic = total;                    // the dynamic shared memory starts 1024-aligned
+    static constexpr int dynamic = total;                                // the dynamic shared memory starts 1024-aligned
 };
-static_assert(TcSmem::dynamic <= 232448, "prefill_tc_kernel: shared memory above the per-block limit");
+using TcSmem = TcSmemT<false>;
+using Tc8Smem = TcSmemT<true>;
+static_assert(TcSmem::dynamic <= 232448 && Tc8Smem::dynamic <= 232448,
+              "prefill_tc_kernel: shared memory above the per-block limit");
+static_assert(Tc8Smem::kStage8 % 1024 == 0, "prefill_tc_kernel: fp8 staging stages must stay 1024-aligned");
 
-__global__ void __launch_bounds__(kTcThreads, 1)
+// 16 bytes of shared memory, kept in order with the mbarrier waits around it.
+__device__ __forceinline__ uint4 tc_ld_shared_v4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+// 16 e4m3 codes (byte 0 first) times a power-of-two scale -> 16 bf16 in 8 pairs (element 2i
+// in the low half of o[i]): e4m3 -> f16 and f16 -> f32 are exact, the product is exact
+// while it stays a normal f32, and its rounding to bf16 is the one a bf16 copy of the
+// dequantised cache holds.
+__device__ __forceinline__ void e4m3x16_scaled_to_bf16(const uint4 c, float s, uint32_t (&o)[8])
+{
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t h01, h23;
+        e4m3x4_to_f16x2x2(w[i], h01, h23);
+        float a0, a1, a2, a3;
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+            : "=f"(a0), "=f"(a1)
+            : "r"(h01));
+        asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+            : "=f"(a2), "=f"(a3)
+            : "r"(h23));
+        o[2 * i] = pack_bf16x2(a0 * s, a1 * s);
+        o[2 * i + 1] = pack_bf16x2(a2 * s, a3 * s);
+    }
+}
+
+template <bool KV8>
+__global__ void __launch_bounds__(TcCfg<KV8>::threads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                       const PrefillTcParams p)
 {
     constexpr int D = 128;
-    constexpr int kTile = TcSmem::kTile;
+    using Smem = TcSmemT<KV8>;
+    constexpr int kThreads = TcCfg<KV8>::threads;
+    constexpr int kTcKStages = TcCfg<KV8>::k_stages;
+    constexpr int kTcVStages = TcCfg<KV8>::v_stages;
+    constexpr int kS8Stages = TcCfg<KV8>::s8_stages;
+    constexpr int kTile = Smem::kTile;
     constexpr int kBlk = kTcRows * 128;  // bytes of one 64-column block of a tile
     const float kNegInf = __int_as_float(0xff800000);
     constexpr float kRescaleGap = 8.f;   // move the reference maximum only past 2^8
@@ -207,15 +270,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         return;
     }
     uint8_t *sbase = smem_raw;
-    const uint32_t sQ = base + TcSmem::q, sOnes = base + TcSmem::ones;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sbase + TcSmem::bars);
-    int *sm_pg = reinterpret_cast<int *>(sbase + TcSmem::pages);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + TcSmem::tmem_slot);
+    const uint32_t sQ = base + Smem::q, sOnes = base + Smem::ones;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sbase + Smem::bars);
+    int *sm_pg = reinterpret_cast<int *>(sbase + Smem::pages);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sbase + Smem::tmem_slot);
     auto bar = [&](int i) { return smem_addr(&bars[i]); };
     constexpr int kKFull = 0, kKEmpty = kKFull + kTcKStages, kVFull = kKEmpty + kTcKStages,
                   kVEmpty = kVFull + kTcVStages, kSFull = kVEmpty + kTcVStages, kSFree = kSFull + 2,
-                  kPFull = kSFree + 2, kODone = kPFull + 1, kDrain = kODone + 1, kQFull = kDrain + 1;
-    static_assert(kQFull < 32, "prefill_tc_kernel: more mbarriers than the shared-memory slots");
+                  kPFull = kSFree + 2, kODone = kPFull + 1, kDrain = kODone + 1, kQFull = kDrain + 1,
+                  kK8Full = kQFull + 1, kK8Empty = kK8Full + kS8Stages, kV8Full = kK8Empty + kS8Stages,
+                  kV8Empty = kV8Full + kS8Stages, kBarEnd = kV8Empty + kS8Stages;
+    static_assert(kBarEnd <= 32, "prefill_tc_kernel: more mbarriers than the shared-memory slots");
     auto k_full = [&](int s) { return bar(kKFull + s); };
     auto k_empty = [&](int s) { return bar(kKEmpty + s); };
     auto v_full = [&](int s) { return bar(kVFull + s); };
@@ -223,17 +288,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     auto s_full = [&](int s) { return bar(kSFull + s); };
     auto s_free = [&](int s) { return bar(kSFree + s); };
     const uint32_t p_full = bar(kPFull), o_done = bar(kODone), drain = bar(kDrain), q_full = bar(kQFull);
-    auto sK = [&](int s) { return base + TcSmem::k + (uint32_t)(s * kTile); };
-    auto sV = [&](int s) { return base + TcSmem::v + (uint32_t)(s * kTile); };
+    auto k8_full = [&](int s) { return bar(kK8Full + s); };     // fp8: codes and scales of a staging stage landed
+    auto k8_empty = [&](int s) { return bar(kK8Empty + s); };   // fp8: the converters have read the stage
+    auto v8_full = [&](int s) { return bar(kV8Full + s); };
+    auto v8_empty = [&](int s) { return bar(kV8Empty + s); };
+    auto sK = [&](int s) { return base + Smem::k + (uint32_t)(s * kTile); };
+    auto sV = [&](int s) { return base + Smem::v + (uint32_t)(s * kTile); };
+    auto s8 = [&](int s) { return base + Smem::s8 + (uint32_t)(s * Smem::kStage8); };
 
     if (tid == 0) {
+        // bf16: a full K/V stage is the copy lane's expect_tx; fp8: one arrival per converter warp
         for (int s = 0; s < kTcKStages; ++s) {
-            mbar_init(k_full(s), 1);
+            mbar_init(k_full(s), KV8 ? 2 : 1);
             mbar_init(k_empty(s), 1);
         }
         for (int s = 0; s < kTcVStages; ++s) {
-            mbar_init(v_full(s), 1);
+            mbar_init(v_full(s), KV8 ? 2 : 1);
             mbar_init(v_empty(s), 1);
+        }
+        for (int s = 0; s < kS8Stages; ++s) {
+            mbar_init(k8_full(s), 1);
+            mbar_init(k8_empty(s), 2);
+            mbar_init(v8_full(s), 1);
+            mbar_init(v8_empty(s), 2);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(s_full(s), 2);  // the MMA's commit + the issuing lane (publishes the tile's page ids)
@@ -261,8 +338,102 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int nbox = kTcKeys / box_t;
     bool failed = false;
 
-    if (warp >= 5 && n_tiles > 0) {
-        // ---- copy warps: warp 5 streams K into its 2 stages, warp 6 V into its 3; lane
+    if (KV8 && warp >= 7 && n_tiles > 0) {
+        // ---- fp8 converter warps: 7-8 write K tiles, 9-10 V tiles.  A task is 16 codes (one
+        // 16-byte chunk of a key row): read unswizzled from the staging box, scaled to bf16, and
+        // stored as the two 16-byte chunks the bf16 copies would land (128B swizzle on the
+        // row's address bits 7-9)
+        const bool is_k = warp < 9;
+        const int ct = (warp - (is_k ? 7 : 9)) * 32 + lane;  // 0..63
+        for (int j = 0; j < n_tiles; ++j) {
+            const int st8 = j % kS8Stages;
+            const bool ok = mbar_wait_bounded(is_k ? k8_full(st8) : v8_full(st8), (uint32_t)((j / kS8Stages) & 1),
+                                              p.wait_limit_ns) &&
+                            (is_k ? (j < kTcKStages || mbar_wait_bounded(k_empty(j % kTcKStages),
+                                                                          (uint32_t)((j / kTcKStages - 1) & 1),
+                                                                          p.wait_limit_ns))
+                                  : (j < kTcVStages || mbar_wait_bounded(v_empty(j % kTcVStages),
+                                                                          (uint32_t)((j / kTcVStages - 1) & 1),
+                                                                          p.wait_limit_ns)));
+            if (!__all_sync(0xffffffffu, ok)) {
+                failed = true;
+                break;
+            }
+            const uint32_t src = s8(st8) + (is_k ? 0u : (uint32_t)Smem::kCodes);
+            const uint32_t scl = s8(st8) + (uint32_t)(2 * Smem::kCodes) + (is_k ? 0u : (uint32_t)(kTcKeys * 4));
+            const uint32_t dst = is_k ? sK(j % kTcKStages) : sV(j % kTcVStages);
+#pragma unroll 4
+            for (int t = ct; t < kTcKeys * 8; t += 64) {
+                const int key = t >> 3, ch = t & 7, sw = key & 7;
+                const uint4 c = tc_ld_shared_v4(src + (uint32_t)(key * 128 + ((ch ^ sw) << 4)));
+                uint32_t o[8];
+                e4m3x16_scaled_to_bf16(c, ld_shared_f32(scl + (uint32_t)(key * 4)), o);
+                // K: [64-dim block][key][128 B]; V: [box][64-dim block][key in box][128 B]
+                const int half = ch >> 2, c16 = (ch & 3) * 2;
+                const uint32_t row = is_k ? dst + (uint32_t)(half * kBlk + key * 128)
+                                          : dst + (uint32_t)((key >> log2box) * box_t * 256 + half * box_t * 128 +
+                                                             (key & (box_t - 1)) * 128);
+                st_shared_v4(row + (uint32_t)((c16 ^ sw) << 4), o[0], o[1], o[2], o[3]);
+                st_shared_v4(row + (uint32_t)(((c16 + 1) ^ sw) << 4), o[4], o[5], o[6], o[7]);
+            }
+            fence_proxy_async_shared();  // the MMAs read the tile through the async proxy
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(is_k ? k_full(j % kTcKStages) : v_full(j % kTcVStages));
+                mbar_arrive(is_k ? k8_empty(st8) : v8_empty(st8));
+            }
+        }
+    } else if (KV8 && (warp == 5 || warp == 6) && n_tiles > 0) {
+        // ---- fp8 copy warps: warp 5 lands K codes and scales, warp 6 V's, in the staging
+        // stages; lane x copies box x (box_t keys of one page: one code box, one scale run)
+        const bool is_k = warp == 5;
+        const uint64_t policy = l2_policy_evict_first();
+        const int x = lane;
+        auto fetch = [&](int j) {
+            const int key = (t0 + j) * kTcKeys + x * box_t;
+            return (x < nbox && j < n_tiles && key < n_keys) ? p.block_table[(size_t)b * p.max_pages + (key >> p.log2P)]
+                                                            : -1;
+        };
+        int raw = fetch(0);
+        int issued = 0;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int st = j % kS8Stages;
+            const int next_raw = fetch(j + 1);
+            const bool has_key = x < nbox && (t0 + j) * kTcKeys + x * box_t < n_keys;
+            const int pg = has_key && (unsigned)raw < (unsigned)p.num_pages ? raw : -1;
+            if (is_k && has_key && pg < 0) atomicCAS(p.status, 0, PKV_ERR_BAD_PAGE_INDEX);
+            const uint32_t ok = __ballot_sync(0xffffffffu, pg >= 0);
+            if (j >= kS8Stages &&
+                !__all_sync(0xffffffffu, mbar_wait_bounded(is_k ? k8_empty(st) : v8_empty(st),
+                                                           (uint32_t)((j / kS8Stages - 1) & 1), p.wait_limit_ns))) {
+                failed = true;
+                break;
+            }
+            if (is_k) {  // publish the tile's page ids (read by the softmax and the MMA warp)
+                if (x < nbox) sm_pg[(j % kTcPageRing) * 16 + x] = pg;
+                __syncwarp();
+            }
+            const uint32_t full = is_k ? k8_full(st) : v8_full(st);
+            if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)__popc(ok) * (uint32_t)box_t * (128u + 4u));
+            __syncwarp();
+            if (pg >= 0) {
+                const int slot = ((t0 + j) * kTcKeys + x * box_t) & (p.P - 1);
+                const uint32_t codes = s8(st) + (is_k ? 0u : (uint32_t)Smem::kCodes) + (uint32_t)(x * box_t * 128);
+                tma_load_4d(codes, is_k ? &tmK : &tmV, 0, pg * p.P + slot, 0, kvh, full, policy);
+                const uint32_t sdst = s8(st) + (uint32_t)(2 * Smem::kCodes) + (is_k ? 0u : (uint32_t)(kTcKeys * 4)) +
+                                      (uint32_t)(x * box_t * 4);
+                bulk_copy_g2s(sdst, (is_k ? p.k_scale : p.v_scale) + ((size_t)pg * p.Hkv + kvh) * p.P + slot,
+                              (uint32_t)box_t * 4u, full);
+            }
+            issued = j + 1;
+            raw = next_raw;
+        }
+        // the last copies have landed before the CTA exits (consumed, or waited for here)
+        for (int t = max(0, issued - kS8Stages); t < issued; ++t)
+            mbar_wait_bounded(is_k ? k8_full(t % kS8Stages) : v8_full(t % kS8Stages), (uint32_t)((t / kS8Stages) & 1),
+                              p.wait_limit_ns);
+    } else if (!KV8 && warp >= 5 && n_tiles > 0) {
+        // ---- copy warps: warp 5 streams K into its 3 stages, warp 6 V into its 3; lane
         // 2x + h copies half h (64 dims) of box x (box_t keys of one page)
         const bool is_k = warp == 5;
         const int stages = is_k ? kTcKStages : kTcVStages;
@@ -563,7 +734,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     if (!direct) {  // the group's last split to finish merges the partials (also after a timeout,
                     // so the counter returns to 0 for the next call)
-        int *last = reinterpret_cast<int *>(sbase + TcSmem::tmem_slot + 4);
+        int *last = reinterpret_cast<int *>(sbase + Smem::tmem_slot + 4);
         __threadfence();
         __syncthreads();
         if (tid == 0)
@@ -572,7 +743,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncthreads();
         if (*last) {  // every warp merges rows warp, warp + W, ... of this CTA
             __threadfence();
-            for (int cr = warp; cr < nrows; cr += kTcThreads / 32) {
+            for (int cr = warp; cr < nrows; cr += kThreads / 32) {
                 const int rt = (row0 + cr) / G, rh = (row0 + cr) % G;
                 tc_merge_row_warp(p, n_chunks, (size_t)(q_base + rt) * p.Hq + kvh * G + rh, lane);
             }

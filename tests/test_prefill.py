@@ -188,6 +188,65 @@ def test_auto_routing_of_short_groups(q_lens, kv_lens, table_keys, kernel):
     assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
 
 
+def _fp8_pools(case):
+    """Oracle-quantised pools of a case (NaN scales in every unused slot) and the bf16 case
+    holding their dequantised values (exact: power-of-two scales)."""
+    _, k, v, _, _ = case.host_bits()
+    k8, ks = oracle.quantize_pool(k)
+    v8, vs = oracle.quantize_pool(v)
+    unused = ~used_slot_mask(case)
+    for sc in (ks, vs):
+        sc.transpose(0, 2, 1)[unused] = np.nan
+    deq = Case(**case.__dict__)
+    for name, codes, sc in (("k_cache", k8, ks), ("v_cache", v8, vs)):
+        vals = torch.from_numpy(oracle.dequantize_pool(codes, sc).astype(np.float32))
+        setattr(deq, name, vals.to(torch.bfloat16).to(case.k_cache.device))
+    return (k8, v8, ks, vs), deq
+
+
+TC8 = TC  # page sizes 8-256, groups of 36-1040 rows, an empty request, key splits
+
+
+@pytest.mark.parametrize("mode", ["rows128", "always", "auto"])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("B,Hq,Hkv,D,P,q_lens,kv_lens", TC8, ids=lambda x: str(x).replace(" ", ""))
+def test_fp8_tensor_core_path(B, Hq, Hkv, D, P, q_lens, kv_lens, causal, mode):
+    # the fp8 cache on the 128-row tensor-core kernel: bit for bit the bf16 128-row kernel on the
+    # dequantised cache (the converters write exactly the tiles its copies land), and the fp8 oracle
+    case = make_prefill_case(_spec(B, Hq, Hkv, D, P, seed=5 * B + P + sum(q_lens)), q_lens, kv_lens, poison=True)
+    pools, deq = _fp8_pools(case)
+    pkv.set_prefill_tensor_cores(mode)
+    out, lse = run_prefill(case, causal=causal, fp8=pools)
+    eo, el = compare(case, out, lse, causal=causal, fp8=pools)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+    rows = max(q_lens) * (Hq // Hkv)
+    if mode != "auto" or rows >= 128 or case.max_pages * P >= 8192:  # the call took the tensor cores
+        pkv.set_prefill_tensor_cores("rows128")
+        ref_o, ref_l = run_prefill(deq, causal=causal)
+        assert torch.equal(out.view(torch.int16), ref_o.view(torch.int16)) and torch.equal(lse, ref_l)
+
+
+def test_fp8_tensor_core_bad_page_and_key_splits():
+    case = make_prefill_case(_spec(2, 16, 2, 128, 16, seed=23), [40, 20], [9000, 300], poison=True)
+    pools, deq = _fp8_pools(case)
+    pkv.set_prefill_tensor_cores("rows128")
+    for splits in (0, 3, 16):
+        out, lse = run_prefill(case, num_splits=splits, fp8=pools)
+        rows = [(t, h) for t in range(0, 60, 7) for h in (0, 5, 15)]
+        eo, el = compare(case, out, lse, fp8=pools, select=rows)
+        assert eo <= OUT_TOL and el <= LSE_TOL, (splits, eo, el)
+        ref_o, ref_l = run_prefill(deq, num_splits=splits)
+        assert torch.equal(out.view(torch.int16), ref_o.view(torch.int16)) and torch.equal(lse, ref_l)
+    bad = Case(**case.__dict__)
+    bt = case.block_table.clone()
+    bt[1, 3] = case.num_pages + 7
+    bad.block_table = bt
+    out, lse = run_prefill(bad, fp8=pools, expect_status=-6)
+    o0, _ = run_prefill(case, fp8=pools)
+    assert torch.equal(out[:40].view(torch.int16), o0[:40].view(torch.int16))  # request 0 untouched
+    assert torch.isfinite(out.float()).all()
+
+
 @pytest.mark.parametrize("mode", ["always", "rows128"])
 def test_tensor_core_and_mma_sync_paths_agree(mode):
     case = make_prefill_case(_spec(2, 32, 8, 128, 16, seed=9), [80, 40], [1000, 300])
