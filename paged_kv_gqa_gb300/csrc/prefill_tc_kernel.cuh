@@ -135,13 +135,15 @@ constexpr int kTcPageRing = 8;   // tiles whose page ids are kept
 // the MMA warp, the K and V copy warps; K and V land by TMA straight into three stages each.
 // fp8: the copy warps land the e4m3 codes and scales in two staging stages, and two K and two
 // V converter warps (7-8, 9-10) write them, dequantised to bf16, into the layout the bf16
-// copies land (two K stages, one V stage: the V tile of a key tile is written only once the
-// previous tile's PV product has read its stage).
+// copies land: one K stage (a key tile's K is written once the previous tile's score MMA has
+// read the stage, which it does about a tile ahead of the softmax) and two V stages (V waits on
+// the PV products, issued only after the softmax); measured on GB300 9-12% faster than two K
+// stages and one V stage.
 template <bool KV8>
 struct TcCfg {
     static constexpr int threads = KV8 ? 352 : 224;
-    static constexpr int k_stages = KV8 ? 2 : 3;
-    static constexpr int v_stages = KV8 ? 1 : 3;
+    static constexpr int k_stages = KV8 ? 1 : 3;
+    static constexpr int v_stages = KV8 ? 2 : 3;
     static constexpr int s8_stages = KV8 ? 2 : 0;
 };
 constexpr int kTcThreads = TcCfg<false>::threads;
@@ -214,6 +216,7 @@ __global__ void __launch_bounds__(TcCfg<KV8>::threads, 1)
     constexpr int kTcKStages = TcCfg<KV8>::k_stages;
     constexpr int kTcVStages = TcCfg<KV8>::v_stages;
     constexpr int kS8Stages = TcCfg<KV8>::s8_stages;
+    constexpr int kS8Div = kS8Stages > 0 ? kS8Stages : 1;  // the bf16 instantiation compiles the fp8 roles too
     constexpr int kTile = Smem::kTile;
     constexpr int kBlk = kTcRows * 128;  // bytes of one 64-column block of a tile
     const float kNegInf = __int_as_float(0xff800000);
@@ -346,8 +349,8 @@ __global__ void __launch_bounds__(TcCfg<KV8>::threads, 1)
         const bool is_k = warp < 9;
         const int ct = (warp - (is_k ? 7 : 9)) * 32 + lane;  // 0..63
         for (int j = 0; j < n_tiles; ++j) {
-            const int st8 = j % kS8Stages;
-            const bool ok = mbar_wait_bounded(is_k ? k8_full(st8) : v8_full(st8), (uint32_t)((j / kS8Stages) & 1),
+            const int st8 = j % kS8Div;
+            const bool ok = mbar_wait_bounded(is_k ? k8_full(st8) : v8_full(st8), (uint32_t)((j / kS8Div) & 1),
                                               p.wait_limit_ns) &&
                             (is_k ? (j < kTcKStages || mbar_wait_bounded(k_empty(j % kTcKStages),
                                                                           (uint32_t)((j / kTcKStages - 1) & 1),
@@ -397,7 +400,7 @@ __global__ void __launch_bounds__(TcCfg<KV8>::threads, 1)
         int raw = fetch(0);
         int issued = 0;
         for (int j = 0; j < n_tiles; ++j) {
-            const int st = j % kS8Stages;
+            const int st = j % kS8Div;
             const int next_raw = fetch(j + 1);
             const bool has_key = x < nbox && (t0 + j) * kTcKeys + x * box_t < n_keys;
             const int pg = has_key && (unsigned)raw < (unsigned)p.num_pages ? raw : -1;
@@ -405,7 +408,7 @@ __global__ void __launch_bounds__(TcCfg<KV8>::threads, 1)
             const uint32_t ok = __ballot_sync(0xffffffffu, pg >= 0);
             if (j >= kS8Stages &&
                 !__all_sync(0xffffffffu, mbar_wait_bounded(is_k ? k8_empty(st) : v8_empty(st),
-                                                           (uint32_t)((j / kS8Stages - 1) & 1), p.wait_limit_ns))) {
+                                                           (uint32_t)((j / kS8Div - 1) & 1), p.wait_limit_ns))) {
                 failed = true;
                 break;
             }
@@ -430,7 +433,7 @@ __global__ void __launch_bounds__(TcCfg<KV8>::threads, 1)
         }
         // the last copies have landed before the CTA exits (consumed, or waited for here)
         for (int t = max(0, issued - kS8Stages); t < issued; ++t)
-            mbar_wait_bounded(is_k ? k8_full(t % kS8Stages) : v8_full(t % kS8Stages), (uint32_t)((t / kS8Stages) & 1),
+            mbar_wait_bounded(is_k ? k8_full(t % kS8Div) : v8_full(t % kS8Div), (uint32_t)((t / kS8Div) & 1),
                               p.wait_limit_ns);
     } else if (!KV8 && warp >= 5 && n_tiles > 0) {
         // ---- copy warps: warp 5 streams K into its 3 stages, warp 6 V into its 3; lane
