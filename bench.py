@@ -76,6 +76,33 @@ def causal_flops(case) -> int:
     return 4 * keys * case.Hq * case.D
 
 
+def _kernel_name(tc_rows: int, fp8: bool, q_len: int) -> str:
+    if tc_rows == 256:
+        return "prefill_tc2_kernel (tcgen05, 256 rows/CTA)"
+    if tc_rows == 128:
+        return "prefill_tc_kernel<%s> (tcgen05, 128 rows/CTA)" % ("fp8" if fp8 else "bf16")
+    return "decode_split_kernel<%s%s> (one launch per call; split merge fused)" % (
+        "fp8 cache" if fp8 else "bf16 cache", ", multi-row" if q_len > 1 else "")
+
+
+def _roofline(args, case, q_len, fp8, props, peaks, gbs, mean_ms) -> dict:
+    """The roofline of the call's one kernel: the tensor cores for the tcgen05 kernels (causal
+    FLOPs over the measured bf16 peak), HBM bandwidth for the decode kernel (algorithmic bytes
+    over the measured copy bandwidth).  DRAM traffic comes from the committed ncu summary of
+    the same kernel and workload, taken on the current source, else null."""
+    tc_rows = _tensor_core_rows(args, case, q_len, fp8, props) if q_len > 1 else 0
+    name = _kernel_name(tc_rows, fp8, q_len)
+    if tc_rows:
+        tflops = causal_flops(case) / (mean_ms * 1e-3) / 1e12
+        return {"bound": "tensor", "achieved": round(tflops, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(tflops / peaks["bf16_tflops"], 4), "traffic": None, "kernel": name,
+                "peak_source": peaks["source"]}
+    traffic = profiled_traffic(profile_name(args.workload, args.cache)) if q_len == 1 else None
+    return {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": traffic, "kernel": name,
+            "peak_source": peaks["source"]}
+
+
 def profiled_traffic(workload: str):
     """DRAM bytes per launch of the decode kernel from the committed ncu summary,
     only if that summary was taken on the current kernel source."""
@@ -399,7 +426,7 @@ def run_pkv(args) -> None:
         return
     peaks = measured_peaks()
     gbs = weak_scaling_gbs(ab["total"], 1, mean_ms)
-    traffic = profiled_traffic(profile_name(args.workload, args.cache))
+    roofline = _roofline(args, case, q_len, fp8, props, peaks, gbs, mean_ms)
     line = {
         "metric": METRIC, "value": round(gbs * world, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(mean_ms, 5), "higher_is_better": True, "scaling": "weak",
@@ -412,19 +439,13 @@ def run_pkv(args) -> None:
         "pct_of_measured_hbm": round(100 * gbs / peaks["hbm_gbs"], 2),
         "pct_of_nominal_8tbs": round(100 * gbs / NOMINAL_HBM_GBS, 2),
         "algorithmic_bytes": ab["total"], "tail_bytes_touched": ab["tail_bytes"],
-        "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": traffic,
-                     "kernel": "decode_split_kernel%s (one launch per call; split merge fused)" % (
-                         "<fp8 cache>" if fp8 else ""),
-                     "peak_source": peaks["source"]},
+        "roofline": roofline,
         "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_call * args.steps,
         "clocks": clocks, "device_status": status, "wall_s_timed_region": round(t_wall, 3),
         "event_floor_us": floor_us,
         "tensor": None if q_len == 1 else {
-            "kernel": {0: "decode_split_kernel<multi-row>", 128: "prefill_tc_kernel (tcgen05, 128 rows/CTA)",
-                       256: "prefill_tc2_kernel (tcgen05, 256 rows/CTA)"}[
-                           _tensor_core_rows(args, case, q_len, fp8, props)],
+            "kernel": _kernel_name(_tensor_core_rows(args, case, q_len, fp8, props), fp8, q_len),
             "tflops": round(causal_flops(case) / (mean_ms * 1e-3) / 1e12, 2),
             "peak_tflops": peaks["bf16_tflops"],
             "frac": round(causal_flops(case) / (mean_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)},
