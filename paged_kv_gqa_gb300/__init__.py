@@ -126,12 +126,15 @@ TC_MODES = {"off": 0, "auto": 1, "always": 2, "rows128": 3}
 
 
 def set_prefill_tensor_cores(mode="auto") -> str:
-    """Routing of long multi-row calls (bf16, D=128, >= 128 rows per group): "off" = the
-    mma.sync kernel; "auto" (default) = the tcgen05 kernel with 256 rows per CTA when the
-    group has them and that grid (key splits included) has a CTA per two SMs, else with 128
-    rows; "always" = the tcgen05 kernel (256 rows per CTA where the group has them);
-    "rows128" = the tcgen05 kernel with 128 rows per CTA.  True/False mean "auto"/"off".
-    Returns the previous mode."""
+    """Routing of multi-row calls with more than 32 rows per group (D=128, scale > 0; a
+    group of at most 32 rows always takes the mma.sync kernel): "off" = the mma.sync kernel;
+    "auto" (default) = groups of 33-127 rows on the tcgen05 kernel with 128 rows per CTA when
+    the block table spans >= 8192 keys, else the mma.sync kernel; larger groups on the tcgen05
+    kernel with 256 rows per CTA when the group has them and that grid (key splits included)
+    has a CTA per two SMs, else with 128 rows; "always" = the tcgen05 kernel (256 rows per CTA
+    where the group has them); "rows128" = the tcgen05 kernel with 128 rows per CTA.  The fp8
+    cache takes the 128-row kernel wherever a mode names the tcgen05 kernel.  True/False mean
+    "auto"/"off".  Returns the previous mode."""
     if isinstance(mode, bool):
         mode = "auto" if mode else "off"
     if mode not in TC_MODES:
