@@ -330,3 +330,33 @@ def test_tensor_core_path_at_full_size(workload, q_len):
     eo, el = compare(case, out, lse, select=rows)
     assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
     assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("workload,q_len", [("batch", 512), ("ragged", 16), ("long", 8)])
+def test_fp8_tensor_core_path_at_full_size(workload, q_len):
+    # the fp8 cache on the tensor cores at the sizes and in the routing bench.py times (auto: the
+    # 128-row kernel's fp8 instantiation; key splits on long), pools quantised by the oracle:
+    # sampled rows against the fp8 oracle, and a second call equal bit for bit
+    from workloads import CONFIGS, draw_seq_lens
+    spec = CONFIGS[workload]
+    kv = draw_seq_lens(spec["lens"], spec["B"], spec["P"], spec["seed"])
+    case = make_prefill_case(workload, [q_len] * spec["B"], kv)
+    _, k, v, _, _ = case.host_bits()
+    k8, ks = oracle.quantize_pool(k)
+    v8, vs = oracle.quantize_pool(v)
+    del k, v
+    pools = (k8, v8, ks, vs)
+    dcase = case.to("cuda")
+    pkv.set_prefill_tensor_cores("auto")
+    out, lse = run_prefill(dcase, fp8=pools)
+    out2, lse2 = run_prefill(dcase, fp8=pools)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))
+    total_q = case.q.shape[0]
+    rows = [(t, h) for t in range(0, total_q, max(1, total_q // 12)) for h in (0, case.Hq // 2 + 1, case.Hq - 1)]
+    rows += [(total_q - 1, 3)]
+    eo, el = compare(case, out, lse, fp8=pools, select=rows)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    del case, dcase, pools, out, lse, out2, lse2
+    torch.cuda.empty_cache()
