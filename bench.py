@@ -85,12 +85,11 @@ def _kernel_name(tc_rows: int, fp8: bool, q_len: int) -> str:
         "fp8 cache" if fp8 else "bf16 cache", ", multi-row" if q_len > 1 else "")
 
 
-def _roofline(args, case, q_len, fp8, props, peaks, gbs, mean_ms) -> dict:
+def _roofline(args, case, q_len, fp8, tc_rows, peaks, gbs, mean_ms) -> dict:
     """The roofline of the call's one kernel: the tensor cores for the tcgen05 kernels (causal
     FLOPs over the measured bf16 peak), HBM bandwidth for the decode kernel (algorithmic bytes
     over the measured copy bandwidth).  DRAM traffic comes from the committed ncu summary of
     the same kernel and workload, taken on the current source, else null."""
-    tc_rows = _tensor_core_rows(args, case, q_len, fp8, props) if q_len > 1 else 0
     name = _kernel_name(tc_rows, fp8, q_len)
     if tc_rows:
         tflops = causal_flops(case) / (mean_ms * 1e-3) / 1e12
@@ -426,7 +425,9 @@ def run_pkv(args) -> None:
         return
     peaks = measured_peaks()
     gbs = weak_scaling_gbs(ab["total"], 1, mean_ms)
-    roofline = _roofline(args, case, q_len, fp8, props, peaks, gbs, mean_ms)
+    # the kernel the call takes: the library's own plan (rows_per_block 128 or 256 = tensor cores)
+    tc_rows = plan["rows_per_block"] if q_len > 1 and plan["rows_per_block"] >= 128 else 0
+    roofline = _roofline(args, case, q_len, fp8, tc_rows, peaks, gbs, mean_ms)
     line = {
         "metric": METRIC, "value": round(gbs * world, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(mean_ms, 5), "higher_is_better": True, "scaling": "weak",
@@ -445,7 +446,7 @@ def run_pkv(args) -> None:
         "clocks": clocks, "device_status": status, "wall_s_timed_region": round(t_wall, 3),
         "event_floor_us": floor_us,
         "tensor": None if q_len == 1 else {
-            "kernel": _kernel_name(_tensor_core_rows(args, case, q_len, fp8, props), fp8, q_len),
+            "kernel": _kernel_name(tc_rows, fp8, q_len),
             "tflops": round(causal_flops(case) / (mean_ms * 1e-3) / 1e12, 2),
             "peak_tflops": peaks["bf16_tflops"],
             "frac": round(causal_flops(case) / (mean_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)},
@@ -578,34 +579,6 @@ def run_append(args) -> None:
                       "unit": "GB/s", "us_per_call": round(ms * 1e3, 3), "steps": args.steps, "warmup": args.warmup,
                       "config": {"workload": "append", "B": case.B, "Hkv": case.Hkv, "D": case.D, "page_size": case.P},
                       "bytes_per_call": moved, "gpu_launches": args.steps}), flush=True)
-
-
-def _tensor_core_rows(args, case, q_len, fp8, props) -> int:
-    """Rows per CTA of the tensor-core kernel the library routes a several-rows call to
-    (0: the mma.sync kernel; see pkv_set_prefill_tensor_cores)."""
-    mode = getattr(args, "tc", 1)
-    rows = q_len * case.G
-    if mode == 0 or case.D != 128 or rows <= 32 or case.scale <= 0:
-        return 0
-    if mode == 2:
-        return 128 if fp8 or rows < 256 else 256
-    if mode == 3:
-        return 128
-    if rows < 128:   # short groups: the tensor cores only on tables of 8192 keys or more
-        return 128 if case.max_pages * case.P >= 8192 else 0
-    if rows < 256 or fp8:   # the fp8 cache has the 128-row kernel only
-        return 128
-    sms = props.multi_processor_count
-    max_tiles = max(1, -(-case.max_pages * case.P // 128))   # key splits as the library plans them
-    groups = case.B * case.Hkv * -(-rows // 256)
-    if groups < sms:
-        s = min((-(-groups * n // sms) * (-(-max_tiles // n) + 16), n)
-                for n in range(1, max(1, min(max_tiles, 4 * sms // groups)) + 1))[1]
-    else:
-        s = -(-max_tiles // 64)
-    chunk = -(-max_tiles // min(max(s, 1), max_tiles, 65535))
-    splits = -(-max_tiles // chunk)
-    return 256 if 2 * groups * splits >= sms else 128
 
 
 def run_step(args) -> None:

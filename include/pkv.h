@@ -131,9 +131,10 @@ PKV_API int pkv_set_prefill_tensor_cores(int mode);
 typedef struct {
     int num_splits;       /* S: key-range splits per (b, kv head) at full table width */
     int chunk_tokens;     /* keys per split (a multiple of stage_tokens) */
-    int stage_tokens;     /* keys per pipeline stage (one TMA box row set) */
-    int warps;            /* consumer warps per thread block */
-    int ring_stages;      /* stages in flight per warp */
+    int stage_tokens;     /* keys per pipeline stage (one TMA box row set); tensor-core kernels:
+                             keys per tile (128) */
+    int warps;            /* warps per thread block (tensor-core kernels: every role) */
+    int ring_stages;      /* stages in flight per warp; tensor-core kernels: K stages */
     int blocks_per_sm;    /* resident thread blocks per SM the plan assumes */
     int grid_blocks;      /* thread blocks of the split kernel (S * Hkv * B) */
     int smem_bytes;       /* dynamic shared memory per block */
@@ -141,7 +142,8 @@ typedef struct {
                              partials inside the same kernel launch */
     size_t workspace_bytes;
     int q_tiles;          /* blocks per (b, kv head) along its query rows (1 for decode) */
-    int rows_per_block;   /* (token, query head) rows one block serves: 8, 16 or 32 */
+    int rows_per_block;   /* (token, query head) rows one block serves: 8, 16 or 32; 128 or 256
+                             when a several-rows call takes the tensor-core kernels */
 } pkv_plan;
 
 /*
@@ -377,9 +379,10 @@ PKV_API pkv_status paged_kv_append_fp8(const pkv_bf16 *k_new, const pkv_bf16 *v_
  * Workspace: paged_prefill_attn_workspace_size.  A request whose row range breaks
  * the contract is skipped (nothing read or written for it) and
  * PKV_ERR_BAD_QO_INDPTR is recorded.  Decode is the case qo_indptr[b] = b,
- * max_q_len = 1.  The K/V stream is read once per query tile, so the path suits
- * short row counts (decode-like steps, short chunks); long prefills are correct
- * but re-read K/V once per 32 rows.
+ * max_q_len = 1.  Groups of at most 32 rows run on the mma.sync kernel, which reads
+ * the K/V stream once per query tile of up to 32 rows; larger groups may run on the
+ * tensor-core kernels (pkv_set_prefill_tensor_cores), which read it once per 128 or
+ * 256 rows.
  */
 PKV_API pkv_status paged_prefill_attn(const pkv_bf16 *q, const pkv_bf16 *k_cache, const pkv_bf16 *v_cache,
                                       const int32_t *qo_indptr, const int32_t *block_table,
@@ -396,7 +399,11 @@ PKV_API pkv_status paged_prefill_attn_fp8(const pkv_bf16 *q, const uint8_t *k_ca
                                           float *lse, void *workspace, size_t workspace_bytes, int num_splits,
                                           cudaStream_t stream);
 
-/* The plan of a several-rows call (kv_dtype as pkv_plan_query_kv). */
+/* The plan of a several-rows call (kv_dtype as pkv_plan_query_kv), under the tensor-core
+ * routing set when it is queried and for a positive scale (a call with scale <= 0 takes the
+ * mma.sync kernel): when the routing takes the tensor cores, the launch fields are the
+ * tensor-core kernel's (rows_per_block 128 or 256).  workspace_bytes covers the mma.sync
+ * kernel and every tensor-core kernel the call could take under any routing. */
 PKV_API pkv_status pkv_plan_query_prefill(int B, int Hq, int Hkv, int D, int page_size, int max_pages, int total_q,
                                           int max_q_len, int num_sms, int num_splits, int kv_dtype,
                                           pkv_plan *plan);

@@ -211,9 +211,10 @@ struct MultiRows {
     int total_q = 0, max_q_len = 0, causal = 0;
 };
 
-// Several rows per sequence with at least 128 rows per (sequence, kv head) group, bf16
-// cache, D = 128, scale > 0: a tensor-core kernel, one CTA per cta_rows (128:
-// prefill_tc_kernel.cuh, 256: prefill_tc2_kernel.cuh) rows and key split (tc_split_plan).
+// Several rows per sequence with more than 32 rows per (sequence, kv head) group (the routing
+// of tensor_core_rows), D = 128, scale > 0: a tensor-core kernel, one CTA per cta_rows (128:
+// prefill_tc_kernel.cuh, bf16 or fp8 cache; 256: prefill_tc2_kernel.cuh, bf16) rows and key
+// split (tc_split_plan).
 // With one split the workspace holds only the status word; with several, also the split
 // counters and the per-split partial outputs and lse that the last split merges.
 pkv_status prefill_tc(const pkv_bf16 *q, const void *k_cache, const void *v_cache, const Fp8Scales &fp8,
@@ -617,12 +618,36 @@ pkv_status pkv_plan_query_prefill(int B, int Hq, int Hkv, int D, int page_size, 
                                     kv_dtype == PKV_KV_FP8_E4M3, group_rows, (long)total_q * Hq);
     if (st != PKV_OK || D != 128 || group_rows <= kMqBlockRows) return st;
     // the tensor-core kernels may take the call: room for their split partials too (the fp8
-    // cache has the 128-row kernel only)
+    // cache has the 128-row kernel only), whatever the routing when the call is made
+    const bool kv8 = kv_dtype == PKV_KV_FP8_E4M3;
     for (int rows : {kTcRows, kTc2Rows}) {
-        if (kv_dtype == PKV_KV_FP8_E4M3 && rows != kTcRows) continue;
+        if (kv8 && rows != kTcRows) continue;
         const TcSplit sp =
             tc_split_plan(B, Hq, Hkv, page_size, max_pages, total_q, max_q_len, num_splits, rows, num_sms);
         plan->workspace_bytes = std::max(plan->workspace_bytes, sp.ws.total);
+    }
+    // the launch under the current routing (for a positive scale): a tensor-core kernel's
+    // replaces the mma.sync kernel's
+    MultiRows mr;
+    mr.total_q = total_q;
+    mr.max_q_len = max_q_len;
+    int tc_rows = tensor_core_rows(g_prefill_tc.load(std::memory_order_relaxed), B, Hq, Hkv, page_size, max_pages,
+                                   mr, num_splits, group_rows, num_sms);
+    if (kv8 && tc_rows) tc_rows = kTcRows;
+    if (tc_rows) {
+        const TcSplit sp =
+            tc_split_plan(B, Hq, Hkv, page_size, max_pages, total_q, max_q_len, num_splits, tc_rows, num_sms);
+        plan->num_splits = sp.splits;
+        plan->chunk_tokens = sp.chunk_tiles * kTcKeys;
+        plan->stage_tokens = kTcKeys;
+        plan->warps = (tc_rows == kTc2Rows ? kTc2Threads : kv8 ? kTc8Threads : kTcThreads) / 32;
+        plan->ring_stages = tc_rows == kTc2Rows ? kTc2KStages : kv8 ? TcCfg<true>::k_stages : TcCfg<false>::k_stages;
+        plan->blocks_per_sm = 1;
+        plan->grid_blocks = (int)((long)Hkv * sp.q_tiles * sp.splits * B);
+        plan->smem_bytes = tc_rows == kTc2Rows ? Tc2Smem::dynamic : kv8 ? Tc8Smem::dynamic : TcSmem::dynamic;
+        plan->merge_needed = sp.splits > 1 ? 1 : 0;
+        plan->q_tiles = sp.q_tiles;
+        plan->rows_per_block = tc_rows;
     }
     return PKV_OK;
 }

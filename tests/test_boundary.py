@@ -285,3 +285,40 @@ def test_prefill_workspace_covers_tensor_core_splits(lib, B, max_q, max_pages, n
     # the fp8 cache never takes the tensor-core kernels: its plan is the mma.sync kernel's alone
     fp8 = pkv.prefill_plan_query(B, Hq, Hkv, D, P, max_pages, total_q, max_q, sms, num_splits=num_splits, cache="fp8")
     assert fp8["workspace_bytes"] <= plan["workspace_bytes"]
+
+
+@pytest.mark.parametrize("shape,cache,expect", [
+    # (B, Hq, Hkv, D, P, max_pages, max_q): rows per group = max_q * Hq / Hkv
+    ((8, 32, 8, 128, 16, 247, 512), "bf16", {"off": 0, "auto": 256, "always": 256, "rows128": 128}),
+    ((8, 32, 8, 128, 16, 247, 512), "fp8", {"off": 0, "auto": 128, "always": 128, "rows128": 128}),
+    ((4, 64, 8, 128, 16, 8192, 8), "bf16", {"off": 0, "auto": 128, "always": 128, "rows128": 128}),  # 64 rows, 128K keys
+    ((4, 64, 8, 128, 16, 8192, 8), "fp8", {"off": 0, "auto": 128, "always": 128, "rows128": 128}),
+    ((4, 64, 8, 128, 16, 256, 8), "bf16", {"off": 0, "auto": 0, "always": 128, "rows128": 128}),     # 64 rows, 4K keys
+    ((4, 64, 8, 128, 16, 8192, 4), "bf16", {"off": 0, "auto": 0, "always": 0, "rows128": 0}),         # 32 rows: one block
+    ((1, 8, 1, 128, 16, 2, 32), "bf16", {"off": 0, "auto": 128, "always": 256, "rows128": 128}),      # 256 rows, 1 CTA
+    ((2, 16, 2, 64, 16, 8192, 64), "bf16", {"off": 0, "auto": 0, "always": 0, "rows128": 0}),         # D = 64
+])
+def test_prefill_plan_names_the_kernel_the_routing_takes(lib, shape, cache, expect):
+    # the plan of a several-rows call under each routing: rows_per_block 128 / 256 = the tensor-core
+    # kernels (with their key splits and grid), else the mma.sync kernel's plan (<= 32 rows per block)
+    B, Hq, Hkv, D, P, max_pages, max_q = shape
+    total_q = B * max_q
+    old = pkv.set_prefill_tensor_cores("auto")
+    try:
+        ws = set()
+        for mode, rows in expect.items():
+            pkv.set_prefill_tensor_cores(mode)
+            plan = pkv.prefill_plan_query(B, Hq, Hkv, D, P, max_pages, total_q, max_q, 152, cache=cache)
+            ws.add(plan["workspace_bytes"])
+            if rows == 0:
+                assert plan["rows_per_block"] <= 32, (mode, plan)
+                continue
+            assert plan["rows_per_block"] == rows, (mode, plan)
+            s = _tc_splits(B, Hkv, Hq // Hkv, max_pages, P, max_q, 0, rows, 152)
+            q_tiles = -(-max_q * (Hq // Hkv) // rows)
+            assert plan["num_splits"] == s and plan["q_tiles"] == q_tiles
+            assert plan["grid_blocks"] == B * Hkv * q_tiles * s and plan["merge_needed"] == (s > 1)
+            assert plan["blocks_per_sm"] == 1 and plan["stage_tokens"] == 128
+        assert len(ws) == 1  # the workspace covers every routing, so it does not depend on the mode
+    finally:
+        pkv.set_prefill_tensor_cores(old)
