@@ -4,13 +4,55 @@ ragged by qo_indptr, with or without the causal mask aligned to the end of the k
 Each pin ties the new entry point to something independent of it: the single-row
 decode oracle (one row per request, a truncated length for the causal rows, each row
 as its own request), torch's float64 attention with an explicit mask, and the
-definition's special cases (rows that see no key, the fp8 cache)."""
+definition's special cases (rows that see no key, the fp8 cache), and hand-derived cases
+(tests/golden/hand_cases.json, "prefill")."""
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from workloads import bits_to_bf16, make_case, make_prefill_case
+from workloads import bf16_bits, bits_to_bf16, make_case, make_prefill_case
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_cases.json")
+
+
+def _golden_prefill():
+    with open(GOLDEN) as f:
+        return json.load(f)["prefill"]
+
+
+def _bits(a):
+    return bf16_bits(torch.as_tensor(np.asarray(a, dtype=np.float32)).to(torch.bfloat16))
+
+
+def _num(x):
+    return float("-inf") if x == "-inf" else float(x)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("case", _golden_prefill(), ids=lambda c: c["name"])
+def test_golden_prefill(case, causal):
+    P, Hkv, D, npg = case["P"], case["Hkv"], case["D"], case["num_pages"]
+    k = np.zeros((npg, P, Hkv, D), np.float32)
+    v = np.zeros((npg, P, Hkv, D), np.float32)
+    for pg, rows in case["pages"].items():
+        for slot, (kr, vr) in enumerate(zip(rows["k"], rows["v"])):
+            k[int(pg), slot] = kr
+            v[int(pg), slot] = vr
+    scale = float(np.float32(case["scale"]))  # the C interface passes the scale as a float32
+    out, lse = oracle.paged_prefill(_bits(case["q"]), np.asarray(case["qo_indptr"], np.int32),
+                                    np.asarray(case["block_table"], np.int32), np.asarray(case["seq_lens"], np.int32),
+                                    scale, causal=causal, k_bits=_bits(k), v_bits=_bits(v))
+    want = case["causal" if causal else "noncausal"]
+    want_out = np.asarray(want["out"], np.float64)
+    want_lse = np.vectorize(_num)(np.asarray(want["lse"], dtype=object)).astype(np.float64)
+    assert np.abs(out - want_out).max() <= case["tol"] + 1e-12
+    inf = np.isinf(want_lse)
+    assert np.array_equal(np.isneginf(lse), inf)
+    assert np.abs(lse[~inf] - want_lse[~inf]).max() <= case["tol"] + 1e-12
 
 
 def _spec(B, Hq, Hkv, D, P, seed=0):
