@@ -1,5 +1,6 @@
 // prefill_tc_kernel.cuh -- several query rows per sequence on the 5th-generation tensor
-// cores (tcgen05), for groups long enough to fill 128-row tiles (chunked prefill).
+// cores (tcgen05), for groups of more than 32 rows (chunked prefill, multi-token steps over
+// long tables); a bf16 cache, or an fp8 (e4m3) one (the KV8 instantiation: see TcCfg).
 //
 // One CTA per 128 (token, query head) rows of one (sequence, kv head) group, the rows
 // packed token-major as in the multi-row decode kernel (AstrAI "CUDA Kernels", "Q
@@ -14,7 +15,8 @@
 // one thread's copies issue too slowly to feed the tensor cores from page-sized boxes).
 // S is double-buffered in tensor memory, so the score MMA of tile j+1 runs while the
 // softmax warps work on tile j, and the PV MMA of tile j runs while they load and
-// exponentiate tile j+1.  K and V have three shared-memory stages each.  mbarriers hand
+// exponentiate tile j+1.  K and V have three shared-memory stages each (bf16 cache; the
+// fp8 instantiation's stages are in TcCfg).  mbarriers hand
 // every buffer over (copies: complete_tx; MMAs: tcgen05.commit; softmax: one arrival
 // per warp).
 // The online softmax keeps a reference maximum per row and moves it only when a tile's
