@@ -322,3 +322,40 @@ def test_prefill_plan_names_the_kernel_the_routing_takes(lib, shape, cache, expe
         assert len(ws) == 1  # the workspace covers every routing, so it does not depend on the mode
     finally:
         pkv.set_prefill_tensor_cores(old)
+
+
+def _call_prefill(lib, fp8=False, q=0x1000, k=0x2000, v=0x3000, qo=0x9000, bt=0x4000, sl=0x5000, B=2, Hq=8, Hkv=2,
+                  D=128, P=16, num_pages=64, max_pages=8, total_q=6, max_q_len=4, causal=1, scale=0.125, out=0x6000,
+                  lse=0x7000, ws=0x8000, ws_bytes=1 << 20, splits=0, ks=0xa000, vs=0xb000):
+    """Fake (never dereferenced) pointers: every case below must be rejected on the host."""
+    V = ctypes.c_void_p
+    if fp8:
+        return lib.paged_prefill_attn_fp8(V(q), V(k), V(v), V(ks), V(vs), V(qo), V(bt), V(sl), B, Hq, Hkv, D, P,
+                                          num_pages, max_pages, total_q, max_q_len, causal, ctypes.c_float(scale),
+                                          V(out), V(lse), V(ws), ws_bytes, splits, None)
+    return lib.paged_prefill_attn(V(q), V(k), V(v), V(qo), V(bt), V(sl), B, Hq, Hkv, D, P, num_pages, max_pages,
+                                  total_q, max_q_len, causal, ctypes.c_float(scale), V(out), V(lse), V(ws), ws_bytes,
+                                  splits, None)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+@pytest.mark.parametrize("kw,status", [
+    (dict(qo=0), -1), (dict(total_q=-1), -1), (dict(max_q_len=0), -1), (dict(causal=2), -1),
+    (dict(q=0), -1), (dict(bt=0), -1), (dict(Hq=6, Hkv=4), -1), (dict(scale=float("inf")), -1),
+    (dict(D=96), -2), (dict(P=12), -2),
+    (dict(qo=0x9004), -3), (dict(q=0x1008), -3), (dict(out=0x6008), -3),
+])
+def test_prefill_host_rejects_bad_arguments(lib, fp8, kw, status):
+    # the several-rows entry points check their row ranges and pointers on the host, before any launch
+    assert _call_prefill(lib, fp8=fp8, **kw) == status
+
+
+def test_prefill_fp8_scales_are_checked(lib):
+    assert _call_prefill(lib, fp8=True, ks=0) == -1
+    assert _call_prefill(lib, fp8=True, vs=0) == -1
+    assert _call_prefill(lib, fp8=True, ks=0xa004) == -3
+
+
+def test_prefill_without_rows_is_a_noop(lib):
+    assert _call_prefill(lib, total_q=0, q=0, k=0, v=0) == 0
+    assert _call_prefill(lib, fp8=True, total_q=0, q=0, k=0, v=0) == 0
