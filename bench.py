@@ -11,6 +11,11 @@ inside it).
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--cache bf16|fp8]
                     [--impl pkv|reference]
 
+The default workload is the long-context one (B=4, Hq=64, Hkv=8, D=128, 16-key pages,
+131072 keys per sequence, ~2.1 GB of K/V): the largest single-GPU configuration, the one
+whose split count and merge matter most.  After the headline, every decode workload is
+timed once more on both caches in the same process (`per_config`).
+
 Prints one JSON line (rank 0).  `value` is achieved GB/s of algorithmic bytes
 (K and V of the valid keys, q, out, lse, used block-table entries, lengths)
 summed over all ranks, divided by the max over ranks of the time per step.
@@ -138,54 +143,130 @@ class L2Flush:
 
 
 class ClockSampler:
-    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+    """SM clock and clock-event (throttle) reasons of the timed GPU while the timed region runs.
+
+    Two read-only sources: NVML, called through ctypes from a thread that polls every
+    `interval_s` and stamps each sample with the host clock (so that only samples taken
+    between the first and the last timed event are kept), and one `nvidia-smi --query-gpu`
+    snapshot just before the first timed event and one just after the last.  Nothing is
+    set: only query functions are called."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # clock-event reason bits of the NVML API (nvmlClocksEventReason*)
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    REJECT = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "hw_power_brake_slowdown")
 
-    def __init__(self, device_index: int):
+    def __init__(self, device_index: int, pci_bus_id: str = None, interval_s: float = 0.001):
         self.device_index = device_index
-        self.samples = []
-        self.proc = None
+        self.pci_bus_id = pci_bus_id
+        self.interval_s = interval_s
+        self.samples = []  # (host time, sm MHz, reason bits, power W)
+        self.snapshots = {}
+        self.nvml = None
+        self.handle = None
+        self.max_mhz = None
+        self.stop_flag = threading.Event()
         self.thread = None
+        self.window = None
+
+    def _nvml_open(self):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return False
+        if lib.nvmlInit_v2() != 0:
+            return False
+        h = ctypes.c_void_p()
+        ok = False
+        if self.pci_bus_id:
+            ok = lib.nvmlDeviceGetHandleByPciBusId_v2(self.pci_bus_id.encode(), ctypes.byref(h)) == 0
+        if not ok:
+            ok = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.device_index), ctypes.byref(h)) == 0
+        if not ok:
+            return False
+        self.nvml, self.handle = lib, h
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, ctypes.c_int(1), ctypes.byref(mx)) == 0:  # 1 = NVML_CLOCK_SM
+            self.max_mhz = float(mx.value)
+        return True
+
+    def _nvml_sample(self):
+        import ctypes
+        lib, h = self.nvml, self.handle
+        mhz, bits, mw = ctypes.c_uint(), ctypes.c_ulonglong(), ctypes.c_uint()
+        t = time.perf_counter()
+        if lib.nvmlDeviceGetClockInfo(h, ctypes.c_int(1), ctypes.byref(mhz)) != 0:
+            return
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        if get_reasons(h, ctypes.byref(bits)) != 0:
+            bits.value = 0
+        power = mw.value / 1000.0 if lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw)) == 0 else None
+        self.samples.append((t, float(mhz.value), int(bits.value), power))
+
+    def _poll(self):
+        while not self.stop_flag.is_set():
+            self._nvml_sample()
+            time.sleep(self.interval_s)
+
+    def snapshot(self, tag: str):
+        """One nvidia-smi reading (read-only query), kept under `tag`."""
+        try:
+            r = subprocess.run(["nvidia-smi", "-i", str(self.device_index), "--query-gpu=" + self.QUERY,
+                                "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=20)
+            parts = [p.strip() for p in r.stdout.strip().splitlines()[0].split(",")]
+        except (OSError, subprocess.SubprocessError, IndexError):
+            return
+        if len(parts) >= 9:
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            self.snapshots[tag] = {"sm_mhz": _num(parts[1]), "sm_max_mhz": _num(parts[2]), "power_w": _num(parts[3]),
+                                   "reasons": [names[i] for i in range(4) if parts[5 + i].lower() == "active"]}
 
     def start(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.device_index), "--query-gpu=" + self.QUERY,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except (OSError, FileNotFoundError):
-            self.proc = None
-            return
-        self.thread = threading.Thread(target=self._read, daemon=True)
-        self.thread.start()
+        if self._nvml_open():
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
 
-    def _read(self):
-        for line in self.proc.stdout:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 9:
-                self.samples.append(parts)
+    def mark(self, t0: float, t1: float):
+        """The host-clock window of the timed region (first event recorded .. last event done)."""
+        self.window = (t0, t1)
 
     def stop(self) -> dict:
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
+        self.stop_flag.set()
         if self.thread:
             self.thread.join(timeout=5)
-        sm = [float(s[1]) for s in self.samples if s[1].replace(".", "", 1).isdigit()]
-        mx = [float(s[2]) for s in self.samples if s[2].replace(".", "", 1).isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for s in self.samples for i in range(4) if s[5 + i].lower() == "active"})
-        power = [float(s[3]) for s in self.samples if s[3].replace(".", "", 1).isdigit()]
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(self.samples),
-                "power_w_max": max(power) if power else None}
+        if self.nvml is not None:
+            self.nvml.nvmlShutdown()
+        lo, hi = self.window if self.window else (-1e30, 1e30)
+        inside = [s for s in self.samples if lo <= s[0] <= hi]
+        sm = [s[1] for s in inside]
+        reasons = sorted({name for s in inside for bit, name in self.REASON_BITS.items() if s[2] & bit})
+        for snap in self.snapshots.values():
+            reasons = sorted(set(reasons) | set(snap["reasons"]))
+        power = [s[3] for s in inside if s[3] is not None]
+        mx = self.max_mhz or max([s.get("sm_max_mhz") or 0 for s in self.snapshots.values()] or [0]) or None
+        med = statistics.median(sm) if sm else None
+        if med is None:  # no sample inside the region: the bracketing snapshots
+            vals = [s["sm_mhz"] for s in self.snapshots.values() if s.get("sm_mhz")]
+            med = statistics.median(vals) if vals else None
+        return {"sm_mhz": med, "sm_max_mhz": mx, "reasons": reasons,
+                "samples_in_timed_region": len(inside), "sampler": "NVML every %.0f ms" % (self.interval_s * 1e3)
+                if self.nvml is not None else "nvidia-smi snapshots only",
+                "sm_mhz_min_max": [min(sm), max(sm)] if sm else None,
+                "power_w_max": max(power) if power else None,
+                "snapshots": self.snapshots,
+                "rejected": any(r in self.REJECT for r in reasons)}
+
+
+def _num(s):
+    try:
+        return float(s)
+    except ValueError:
+        return None
 
 
 def dist_setup(n_gpus: int):
@@ -383,12 +464,12 @@ def run_pkv(args) -> None:
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(local, _pci_bus_id(props))
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
+    sampler.snapshot("before_first_event")
     sampler.start()
-    time.sleep(0.3)
     t_wall0 = time.perf_counter()
     for i in range(args.steps):
         flush.fill_(i & 0xff)
@@ -396,7 +477,10 @@ def run_pkv(args) -> None:
         call()
         ends[i].record(stream)
     torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall0
+    t_wall1 = time.perf_counter()
+    t_wall = t_wall1 - t_wall0
+    sampler.mark(t_wall0, t_wall1)
+    sampler.snapshot("after_last_event")
     if dist:
         dist.barrier()
     clocks = sampler.stop()
@@ -418,6 +502,10 @@ def run_pkv(args) -> None:
             cpu = _cpu_baseline(hc, args.cpu_seconds, fp8=tuple(t.cpu().numpy() for t in pools8))
         else:
             cpu = _cpu_baseline(case.to("cpu"), args.cpu_seconds)
+
+    per_config = None
+    if not args.no_per_config and q_len == 1 and world == 1:
+        per_config = _per_config(args, pkv, torch, dev, stream, flush, props.multi_processor_count)
 
     if rank != 0:
         if dist:
@@ -444,6 +532,7 @@ def run_pkv(args) -> None:
         "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_call * args.steps,
         "clocks": clocks, "device_status": status, "wall_s_timed_region": round(t_wall, 3),
+        "per_config": per_config,
         "event_floor_us": floor_us,
         "tensor": None if q_len == 1 else {
             "kernel": _kernel_name(tc_rows, fp8, q_len),
@@ -454,6 +543,66 @@ def run_pkv(args) -> None:
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def _per_config(args, pkv, torch, dev, stream, flush, sms):
+    """Every decode workload on both caches, measured in this process after the headline:
+    mean event time per call (L2 flushed before each), achieved GB/s of algorithmic bytes and
+    the fraction of the measured copy bandwidth.  Each workload's inputs are built, timed and
+    freed in turn."""
+    from workloads import CONFIG_ORDER, algorithmic_bytes, make_case
+    peak = measured_peaks()["hbm_gbs"]
+    steps = max(20, min(args.steps, 200))
+    res = {"steps": steps, "warmup": 3, "peak_gbs": peak, "bf16": {}, "fp8": {}}
+    for name in CONFIG_ORDER:
+        case = make_case(name, device=dev)
+        pools8 = None
+        for cache in ("bf16", "fp8"):
+            if cache == "fp8":
+                pools8 = pkv.quantize_pool_fp8(case.k_cache, case.v_cache)
+                case.k_cache = case.v_cache = None
+            ws = torch.zeros(pkv.paged_decode_attn_workspace_size(case.B, case.Hq, case.Hkv, case.D, case.P,
+                                                                  case.max_pages, cache=cache),
+                             dtype=torch.uint8, device=dev)
+            out = torch.empty((case.B, case.Hq, case.D), dtype=torch.bfloat16, device=dev)
+            lse = torch.empty((case.B, case.Hq), dtype=torch.float32, device=dev)
+            if cache == "fp8":
+                call = lambda: pkv.paged_decode_attn_fp8(case.q, *pools8, case.block_table, case.seq_lens,
+                                                         case.scale, out, lse, ws, stream=stream)
+            else:
+                call = lambda: pkv.paged_decode_attn(case.q, case.k_cache, case.v_cache, case.block_table,
+                                                     case.seq_lens, case.scale, out, lse, ws, stream=stream)
+            for _ in range(3):
+                flush.fill_(1)
+                call()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+            for s_, e_ in ev:
+                flush.fill_(2)
+                s_.record(stream)
+                call()
+                e_.record(stream)
+            torch.cuda.synchronize()
+            if pkv.pkv_check_status(ws) != 0:
+                raise RuntimeError("device status %d on %s/%s" % (pkv.pkv_check_status(ws), name, cache))
+            ms = sum(s_.elapsed_time(e_) for s_, e_ in ev) / steps
+            ab = algorithmic_bytes(case, cache=cache)["total"]
+            gbs = ab / (ms * 1e-3) / 1e9
+            plan = pkv.plan_query(case.B, case.Hq, case.Hkv, case.D, case.P, case.max_pages, sms, cache=cache)
+            res[cache][name] = {"us_per_call": round(ms * 1e3, 3), "gbs": round(gbs, 1),
+                                "frac": round(gbs / peak, 4), "algorithmic_bytes": ab,
+                                "num_splits": plan["num_splits"], "gpu_launches": steps}
+            del ws, out, lse
+        del case, pools8
+        torch.cuda.empty_cache()
+    return res
+
+
+def _pci_bus_id(props):
+    """The device's PCI address in NVML's form, from torch's device properties (None if absent)."""
+    try:
+        return "%08x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+    except (AttributeError, TypeError):
+        return None
 
 
 def _event_floor_us(torch, flush, stream, n=200):
@@ -663,9 +812,9 @@ def run_step(args) -> None:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="batch",
+    ap.add_argument("--workload", default="long",
                     choices=["tiny", "batch", "ragged", "long", "bigpage", "bigpage_g16", "append", "step"])
     ap.add_argument("--cache", default="bf16", choices=["bf16", "fp8"])
     ap.add_argument("--q-len", type=int, default=1,
@@ -678,6 +827,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the table of every decode workload on both caches after the headline")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--ref-seconds", type=float, default=1.0)
     args = ap.parse_args()

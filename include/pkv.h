@@ -68,7 +68,13 @@ typedef enum {
     PKV_ERR_WORKSPACE_TOO_SMALL = -4, /* workspace_bytes below the size query's answer */
     PKV_ERR_CUDA = -5,                /* a CUDA runtime/driver call failed */
     PKV_ERR_BAD_PAGE_INDEX = -6,      /* device: a used block_table entry outside [0, num_pages) */
-    PKV_ERR_DEVICE_TIMEOUT = -7,      /* device: a bounded wait for a copy ran out */
+    PKV_ERR_DEVICE_TIMEOUT = -7,      /* device: a bounded wait for a copy ran out (2 s).  The
+                                         block that saw it waits, bounded again, for its other
+                                         copies in flight and exits; a copy that outlasts that
+                                         wait too may still land in shared memory the block no
+                                         longer owns.  After this status, treat the call's
+                                         outputs and every later result on the same CUDA
+                                         context as untrustworthy until the process restarts. */
     PKV_ERR_BAD_SEQ_LEN = -8,         /* device: seq_lens[b] < 0 or > max_pages * page_size */
     PKV_ERR_BAD_QO_INDPTR = -9        /* device: a request's query rows outside [0, total_q) or more
                                          than max_q_len of them */
@@ -256,13 +262,17 @@ PKV_API pkv_status paged_decode_attn_ex(const pkv_bf16 *q, const pkv_bf16 *k_cac
  *                  kernels are done, in stream order.
  *
  * The first call on a device looks up the array's device address for that
- * device (make that call before any stream capture).  A shape whose plan
+ * device (make that call before any stream capture) and keeps it for the life
+ * of the process: it is not looked up again after cudaDeviceReset or anything
+ * else that tears down the device's primary context, so do not call this
+ * entry point after such a reset.  A shape whose plan
  * needs more than 32 MiB of partials returns PKV_ERR_WORKSPACE_TOO_SMALL
  * before anything runs; use paged_decode_attn with a workspace for those.
  * Every call first clears the status word and the split-completion
  * counters.  All calls on a device share the array: calls that may overlap
  * on the GPU (other streams, other host threads) race on it and must be
- * ordered by the caller.
+ * ordered by the caller.  A call rejected on the host (a bad argument, a
+ * misaligned pointer, too large a plan) touches neither the GPU nor the array.
  */
 PKV_API pkv_status paged_decode_attn_static_scratch(const pkv_bf16 *q, const pkv_bf16 *k_cache,
                                                     const pkv_bf16 *v_cache, const int32_t *block_table,

@@ -323,6 +323,35 @@ int tensor_core_rows(int mode, int B, int Hq, int Hkv, int page_size, int max_pa
     }
 }
 
+// The host checks of a decode call that need neither the device nor a plan, in the order the
+// entry points report them: sizes and scale, the shape, then (B > 0) null pointers, 16-byte
+// alignment and the pool's key count.  own_scratch: the call's workspace is the library's own
+// array, so `workspace` is not checked.  Returns PKV_OK with *nothing_to_do set for B == 0.
+pkv_status check_decode_args(const pkv_bf16 *q, const void *k_cache, const void *v_cache, const Fp8Scales &fp8,
+                             const int32_t *block_table, const int32_t *seq_lens, int B, int Hq, int Hkv, int D,
+                             int page_size, int num_pages, int max_pages, float scale, const pkv_bf16 *out,
+                             const float *lse, const void *workspace, bool own_scratch, int num_splits,
+                             bool *nothing_to_do)
+{
+    *nothing_to_do = false;
+    if (num_pages <= 0 || num_splits < 0 || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+    const pkv_status shape_ok = validate_shape(B, Hq, Hkv, D, page_size, max_pages);
+    if (shape_ok != PKV_OK) return shape_ok;
+    if (B == 0) {
+        *nothing_to_do = true;
+        return PKV_OK;
+    }
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out || (!own_scratch && !workspace))
+        return PKV_ERR_INVALID_ARG;
+    if (fp8.on && (!fp8.k_scale || !fp8.v_scale)) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(block_table) ||
+        !aligned16(seq_lens) || !aligned16(out) || (lse && !aligned16(lse)) || (!own_scratch && !aligned16(workspace)))
+        return PKV_ERR_MISALIGNED;
+    if (fp8.on && (!aligned16(fp8.k_scale) || !aligned16(fp8.v_scale))) return PKV_ERR_MISALIGNED;
+    if ((long)num_pages * page_size >= (1l << 31)) return PKV_ERR_INVALID_ARG;
+    return PKV_OK;
+}
+
 pkv_status decode_impl(const pkv_bf16 *q, const void *k_cache, const void *v_cache, Fp8Scales fp8,
                        const int32_t *block_table, const int32_t *seq_lens, int B, int Hq, int Hkv, int D,
                        int page_size, int num_pages, int max_pages, float scale, pkv_bf16 *out, float *lse,
@@ -331,17 +360,11 @@ pkv_status decode_impl(const pkv_bf16 *q, const void *k_cache, const void *v_cac
 {
     const bool kv8 = fp8.on;
     const bool mq = mr.qo_indptr != nullptr;
-    if (num_pages <= 0 || num_splits < 0 || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
-    const pkv_status shape_ok = validate_shape(B, Hq, Hkv, D, page_size, max_pages);
-    if (shape_ok != PKV_OK) return shape_ok;
-    if (B == 0) return PKV_OK;
-    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out || !workspace) return PKV_ERR_INVALID_ARG;
-    if (kv8 && (!fp8.k_scale || !fp8.v_scale)) return PKV_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(block_table) ||
-        !aligned16(seq_lens) || !aligned16(out) || (lse && !aligned16(lse)) || !aligned16(workspace))
-        return PKV_ERR_MISALIGNED;
-    if (kv8 && (!aligned16(fp8.k_scale) || !aligned16(fp8.v_scale))) return PKV_ERR_MISALIGNED;
-    if ((long)num_pages * page_size >= (1l << 31)) return PKV_ERR_INVALID_ARG;
+    bool nothing_to_do = false;
+    const pkv_status args_ok = check_decode_args(q, k_cache, v_cache, fp8, block_table, seq_lens, B, Hq, Hkv, D,
+                                                 page_size, num_pages, max_pages, scale, out, lse, workspace,
+                                                 false, num_splits, &nothing_to_do);
+    if (args_ok != PKV_OK || nothing_to_do) return args_ok;
     if (mq && !aligned16(mr.qo_indptr)) return PKV_ERR_MISALIGNED;
     const long group_rows = mq ? (long)mr.max_q_len * (Hq / Hkv) : 0;
     const long total_rows = mq ? (long)mr.total_q * Hq : (long)B * Hq;
@@ -804,8 +827,10 @@ pkv_status pkv_selftest_wait_timeout(void *workspace, unsigned timeout_us, cudaS
 //
 // The array's name is only a host-side stand-in for the device variable, so
 // its device address is looked up with cudaGetSymbolAddress, once per device,
-// with that device current, on the first call on that device.  Make that
-// first call before any stream capture.  All calls share the array and it
+// with that device current, on the first call on that device, and kept for the
+// life of the process (not refreshed after cudaDeviceReset, which would leave it
+// stale).  Make that first call before any stream capture.  All calls share the
+// array and it
 // keeps the previous call's contents: each call clears the status word before
 // its kernels run, and calls that overlap on the GPU (different streams, or
 // different host threads, without ordering) race on it.
@@ -844,12 +869,14 @@ extern "C" pkv_status paged_decode_attn_static_scratch(const pkv_bf16 *q, const 
                                                        pkv_bf16 *out, float *lse, int *device_status,
                                                        cudaStream_t stream)
 {
-    // Host-side checks first, so a rejected call touches neither the GPU nor the scratch.
-    if (num_pages <= 0 || !std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
-    const pkv_status shape_ok = validate_shape(B, Hq, Hkv, D, page_size, max_pages);
-    if (shape_ok != PKV_OK) return shape_ok;
-    if (B == 0) return PKV_OK;
-    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out) return PKV_ERR_INVALID_ARG;
+    // Every host-side check of the workspace entry point first (its workspace is the library's
+    // own array), so a rejected call touches neither the GPU nor the scratch.
+    bool nothing_to_do = false;
+    const pkv_status args_ok =
+        pkv::check_decode_args(q, k_cache, v_cache, pkv::Fp8Scales{}, block_table, seq_lens, B, Hq, Hkv, D,
+                               page_size, num_pages, max_pages, scale, out, lse, nullptr, true, 0,
+                               &nothing_to_do);
+    if (args_ok != PKV_OK || nothing_to_do) return args_ok;
     if (device_status && (reinterpret_cast<uintptr_t>(device_status) & 3u)) return PKV_ERR_MISALIGNED;
 
     int device = 0, sms = 0;
@@ -866,7 +893,8 @@ extern "C" pkv_status paged_decode_attn_static_scratch(const pkv_bf16 *q, const 
     // The status word and the split-completion counters must start at zero (a previous
     // call that gave up part-way could have left a counter raised); the partials are
     // fully written before they are read.
-    const size_t zero_bytes = workspace_layout(plan.num_splits, (size_t)B * Hkv, (size_t)B * Hq, D).part_lse;
+    const size_t zero_bytes =
+        workspace_layout(plan.num_splits, (size_t)B * Hkv * plan.q_tiles, (size_t)B * Hq, D).part_lse;
     if (cudaMemsetAsync(scratch, 0, zero_bytes, stream) != cudaSuccess) return PKV_ERR_CUDA;
     st = paged_decode_attn(q, k_cache, v_cache, block_table, seq_lens, B, Hq, Hkv, D, page_size, num_pages,
                            max_pages, scale, out, lse, scratch, kStaticScratchBytes, stream);

@@ -662,7 +662,7 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
         }
     };
 
-    bool failed = false;
+    int failed_it = -1;
     for (int it = 0;; ++it) {
         const int s = warp + it * W;
         if (s >= n_stages) break;
@@ -671,7 +671,7 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
         const bool ok = mbar_wait_bounded(smem_addr(&bars[warp * R + slot]), parity, p.wait_limit_ns);
         if (!__all_sync(0xffffffffu, ok)) {
             if (lane == 0) record_status(p.status, PKV_ERR_DEVICE_TIMEOUT);
-            failed = true;
+            failed_it = it;
             break;
         }
         const int t0 = tok_begin + s * T;
@@ -687,7 +687,13 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
             if (ns < n_stages) issue(ns, slot);
         }
     }
-    (void)failed;
+    if (failed_it >= 0) {
+        // A copy outlasted its limit.  The warp's later stages (up to R - 1 of them) were issued
+        // too: wait for each, bounded, so that none lands in shared memory after the block has
+        // exited unless it also outlasts the limit.
+        for (int it = failed_it + 1; it < failed_it + R && warp + it * W < n_stages; ++it)
+            mbar_wait_bounded(smem_addr(&bars[warp * R + it % R]), (uint32_t)((it / R) & 1), p.wait_limit_ns);
+    }
 
     griddep_launch_dependents();  // streaming done: the next kernel may start launching
 

@@ -81,3 +81,54 @@ def split_invariance_violation(a, b, tol=SPLIT_TOL):
     d = np.abs(a - b)
     allowed = np.maximum(tol, bf16_ulp(np.maximum(np.abs(a), np.abs(b))))
     return float(np.max(d - allowed)), float(np.mean(d > 0)), float(np.max(d))
+
+
+def bf16_adjacent(a, b):
+    """True where a and b (float arrays holding bf16 values) are neighbouring bf16 numbers:
+    the same sign and bit patterns one apart."""
+    ia = torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
+    ib = torch.from_numpy(np.ascontiguousarray(b, np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
+    same_sign = (ia < 0) == (ib < 0)
+    return same_sign & (np.abs(ia.astype(np.int32) - ib.astype(np.int32)) == 1)
+
+
+def split_straddle_check(a, b, oracle_rows, tol=SPLIT_TOL, out_tol=OUT_TOL):
+    """The split-count bar on bf16 outputs, with every element past it proved a rounding straddle.
+
+    a, b: outputs of the same call at two split counts, float arrays [rows..., D] of bf16
+    values.  Split counts only reorder f32 sums, so where |a - b| > tol the two f32 results
+    must have straddled a bf16 rounding boundary.  Each such element must therefore be
+      (i)   one bf16 step: a and b neighbouring bf16 numbers;
+      (ii)  a genuine straddle: the fp64 oracle value lies within tol of the midpoint of a and b
+            (the rounding boundary both f32 sums sat beside);
+      (iii) within out_tol of the oracle on both sides.
+    oracle_rows(idx) returns the fp64 oracle outputs [n, D] for the row indices idx ([n, ndim-1]).
+    Returns (number of elements past tol, max |a - b|, max |oracle - midpoint| over them); raises
+    AssertionError naming the first element that breaks (i)-(iii)."""
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    d = np.abs(a - b)
+    big = d > tol
+    n_big = int(big.sum())
+    if n_big == 0:
+        return 0, float(d.max()) if d.size else 0.0, 0.0
+    lead = np.argwhere(big)[:, :-1]
+    rows = np.unique(lead, axis=0)
+    ref = np.asarray(oracle_rows(rows), np.float64).reshape(len(rows), a.shape[-1])
+    pos = {tuple(r): i for i, r in enumerate(rows.tolist())}
+    worst_mid = 0.0
+    for e in np.argwhere(big):
+        r, col = tuple(e[:-1].tolist()), int(e[-1])
+        x, y, o = a[tuple(e)], b[tuple(e)], ref[pos[r], col]
+        assert bf16_adjacent(np.array([x]), np.array([y]))[0], ("not one bf16 step", r, col, x, y)
+        mid = 0.5 * (x + y)
+        worst_mid = max(worst_mid, abs(o - mid))
+        assert abs(o - mid) <= tol, ("not a rounding straddle", r, col, x, y, o)
+        assert abs(x - o) <= out_tol and abs(y - o) <= out_tol, ("past the oracle bar", r, col, x, y, o)
+    return n_big, float(d.max()), worst_mid
+
+
+def decode_oracle_rows(case):
+    """oracle_rows for split_straddle_check on a decode case: (b, h) rows -> fp64 outputs."""
+    q, k, v, bt, sl = case.host_bits()
+    return lambda rows: oracle.paged_decode(q, k, v, bt, sl, case.scale, select=[tuple(r) for r in rows])[0]

@@ -359,3 +359,24 @@ def test_prefill_fp8_scales_are_checked(lib):
 def test_prefill_without_rows_is_a_noop(lib):
     assert _call_prefill(lib, total_q=0, q=0, k=0, v=0) == 0
     assert _call_prefill(lib, fp8=True, total_q=0, q=0, k=0, v=0) == 0
+
+
+def test_static_scratch_rejects_bad_arguments_before_touching_cuda(lib):
+    # Without a GPU any CUDA call would fail (PKV_ERR_CUDA), so a misaligned or malformed call
+    # that returns its own status was rejected before the scratch array was touched.
+    V = ctypes.c_void_p
+
+    def call(q=0x1000, bt=0x4000, out=0x6000, lse=0x7000, status=0x9000, B=2, D=128, num_pages=64, scale=0.125):
+        return lib.paged_decode_attn_static_scratch(V(q), V(0x2000), V(0x3000), V(bt), V(0x5000), B, 8, 2, D, 16,
+                                                    num_pages, 8, ctypes.c_float(scale), V(out), V(lse), V(status),
+                                                    None)
+    assert call(q=0x1008) == -3
+    assert call(bt=0x4004) == -3
+    assert call(lse=0x7002) == -3
+    assert call(status=0x9002) == -3
+    assert call(out=0) == -1
+    assert call(num_pages=0) == -1
+    assert call(num_pages=1 << 27) == -1  # num_pages * page_size past int32
+    assert call(scale=float("inf")) == -1
+    assert call(D=96) == -2
+    assert call(B=0, q=0) == 0

@@ -4,14 +4,18 @@ With PDL on, each kernel of the library may start launching while the previous o
 and waits (griddepcontrol.wait) before reading its inputs, so the results must equal the
 serialised launches bit for bit: an append followed at once by the decode that reads the
 appended keys, repeated back to back, on both caches, eagerly and inside a CUDA graph.
+Every step's output is also held to the oracle, which replays the same appends on a host
+copy of the pool (a race that broke the serialised launches too would show there).
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_kv_gqa_gb300 as pkv
 from paged_kv_gqa_gb300 import _build
-from workloads import make_case
+from gpu_util import LSE_TOL, OUT_TOL, max_abs_diff
+from workloads import bf16_bits, make_case
 
 pytestmark = pytest.mark.gpu
 
@@ -71,6 +75,29 @@ class Step:
                                       self.lse[i], self.ws, stream=stream)
 
 
+def assert_steps_match_oracle(st):
+    """Replays the step's appends on the oracle's host copy of the pool (the fp8 pool made by
+    the oracle's own quantiser) and holds each step's out and lse to the oracle bars."""
+    c = st.c
+    q, bt, sl = bf16_bits(c.q), c.block_table.cpu().numpy(), c.seq_lens.cpu().numpy()
+    pos = st.pos.cpu().numpy()
+    k, v = bf16_bits(st.k0), bf16_bits(st.v0)
+    if st.cache == "fp8":
+        (k8, ks), (v8, vs) = oracle.quantize_pool(k), oracle.quantize_pool(v)
+    for i in range(st.steps):
+        kn, vn = bf16_bits(st.kn[i]), bf16_bits(st.vn[i])
+        if st.cache == "fp8":
+            k8, v8, ks, vs, rej = oracle.kv_append_fp8(kn, vn, bt, pos, k8, v8, ks, vs)
+            ro, rl = oracle.paged_decode_fp8(q, k8, v8, ks, vs, bt, sl, c.scale)
+        else:
+            k, v, rej = oracle.kv_append(kn, vn, bt, pos, k, v)
+            ro, rl = oracle.paged_decode(q, k, v, bt, sl, c.scale)
+        assert rej == 0
+        eo = max_abs_diff(st.out[i].float().cpu().numpy(), ro)
+        el = max_abs_diff(st.lse[i].cpu().numpy(), rl)
+        assert eo <= OUT_TOL and el <= LSE_TOL, (i, eo, el)
+
+
 @pytest.mark.parametrize("cache", ["bf16", "fp8"])
 def test_pdl_results_equal_serialised_launches(cache):
     st = Step(cache, seed=11)
@@ -91,6 +118,7 @@ def test_pdl_results_equal_serialised_launches(cache):
         assert torch.equal(st.lse.view(torch.int32), ref_l.view(torch.int32))
     assert pkv.pkv_check_status(st.ws) == 0
     pkv.set_programmatic_launch(False)
+    assert_steps_match_oracle(st)
 
 
 @pytest.mark.parametrize("cache", ["bf16", "fp8"])
@@ -116,3 +144,5 @@ def test_pdl_inside_a_cuda_graph(cache):
         assert torch.equal(st.out.view(torch.int16), ref_o.view(torch.int16))
         assert torch.equal(st.lse.view(torch.int32), ref_l.view(torch.int32))
     pkv.set_programmatic_launch(False)
+    assert pkv.pkv_check_status(st.ws) == 0
+    assert_steps_match_oracle(st)

@@ -11,7 +11,7 @@ import torch
 import oracle
 import paged_kv_gqa_gb300 as pkv
 from paged_kv_gqa_gb300 import _build
-from gpu_util import LSE_TOL, OUT_TOL, max_abs_diff, run_gpu, split_invariance_violation
+from gpu_util import LSE_TOL, OUT_TOL, max_abs_diff, run_gpu, split_invariance_violation, split_straddle_check
 from workloads import Case, make_prefill_case, used_slot_mask
 
 pytestmark = pytest.mark.gpu
@@ -48,6 +48,14 @@ def run_prefill(case, causal=True, num_splits=0, fp8=None, expect_status=0, max_
     status = pkv.pkv_check_status(ws)
     assert status == expect_status, "device status %s" % pkv.STATUS.get(status, status)
     return out, lse
+
+
+def prefill_oracle_rows(case, causal=True):
+    """oracle_rows for split_straddle_check on a several-rows case: (t, h) rows -> fp64 outputs."""
+    q, k, v, bt, sl = case.host_bits()
+    qo = case.qo_indptr.cpu().numpy()
+    return lambda rows: oracle.paged_prefill(q, qo, bt, sl, case.scale, causal=causal, k_bits=k, v_bits=v,
+                                             select=[tuple(r) for r in rows])[0]
 
 
 def compare(case, out, lse, causal=True, fp8=None, select=None):
@@ -112,10 +120,11 @@ def test_one_row_per_request_is_the_decode_kernel(causal):
 def test_split_counts_agree():
     case = make_prefill_case(_spec(3, 32, 8, 128, 16, seed=4), [4, 2, 3], [3000, 1200, 64])
     ref = run_prefill(case, num_splits=1)
+    rows = prefill_oracle_rows(case)
     for splits in (0, 3, 7):
         out, lse = run_prefill(case, num_splits=splits)
-        excess, frac, _ = split_invariance_violation(out.float().cpu().numpy(), ref[0].float().cpu().numpy())
-        assert excess <= 0 and max_abs_diff(lse.cpu().numpy(), ref[1].cpu().numpy()) <= 2e-3
+        split_straddle_check(out.float().cpu().numpy(), ref[0].float().cpu().numpy(), rows)
+        assert max_abs_diff(lse.cpu().numpy(), ref[1].cpu().numpy()) <= 2e-3
 
 
 def test_malformed_row_ranges_are_skipped_and_reported():
@@ -307,8 +316,8 @@ def test_tensor_core_splits_reuse_the_workspace(mode):
         assert torch.equal(out.view(torch.int16), results[0][0].view(torch.int16))
         assert torch.equal(lse.view(torch.int32), results[0][1].view(torch.int32))
     ref = run_prefill(c, num_splits=1)
-    excess, _, _ = split_invariance_violation(results[0][0].float().cpu().numpy(), ref[0].float().cpu().numpy())
-    assert excess <= 0 and max_abs_diff(results[0][1].cpu().numpy(), ref[1].cpu().numpy()) <= 2e-3
+    split_straddle_check(results[0][0].float().cpu().numpy(), ref[0].float().cpu().numpy(), prefill_oracle_rows(c))
+    assert max_abs_diff(results[0][1].cpu().numpy(), ref[1].cpu().numpy()) <= 2e-3
 
 
 @pytest.mark.parametrize("workload,q_len", [("batch", 512), ("ragged", 64), ("long", 32)])
