@@ -100,6 +100,23 @@ PKV_API int pkv_version(void);
 PKV_API int pkv_set_programmatic_launch(int enable);
 
 /*
+ * Split merge through a thread-block cluster (off at load).  enable != 0: a
+ * decode call whose plan has 2-8 splits and whose grid fits one wave of resident
+ * blocks launches the splits of each (b, kv head) as one cluster; each split sends
+ * its normalised partial output and lse into split 0's shared memory (distributed
+ * shared memory, st.async), and split 0 merges them with the same log-sum-exp
+ * recurrence, in the same split order, as the workspace merge (FlashQuant wiki
+ * "CUDA Kernels", split_k_reduce.cu "Algorithm"), so the results are identical
+ * bit for bit.  enable == 0: every merge goes through the workspace (the last
+ * split to finish merges).  Measured on GB300 the cluster merge shortens the
+ * merge itself, but clusters are placed whole, several blocks to an SM, and leave
+ * SMs idle, so it is off by default.  Process-wide, like
+ * pkv_set_programmatic_launch; the plan queries report the choice in
+ * pkv_plan.merge_needed.  Returns the previous setting.
+ */
+PKV_API int pkv_set_cluster_merge(int enable);
+
+/*
  * Tensor-core path of paged_prefill_attn and paged_prefill_attn_fp8 (D = 128, scale > 0,
  * more than 32 (token, query head) rows per (sequence, kv head) group, i.e. max_q_len *
  * Hq/Hkv > 32): the score and PV products run on tcgen05 (5th-generation tensor cores,
@@ -144,8 +161,11 @@ typedef struct {
     int blocks_per_sm;    /* resident thread blocks per SM the plan assumes */
     int grid_blocks;      /* thread blocks of the split kernel (S * Hkv * B) */
     int smem_bytes;       /* dynamic shared memory per block */
-    int merge_needed;     /* 1 when S > 1: the last split block of each (b, kv head) merges the
-                             partials inside the same kernel launch */
+    int merge_needed;     /* 0: S == 1, nothing to merge; 1: the last split block of each (b, kv
+                             head) to finish merges the partials through the workspace, inside
+                             the same kernel launch; 2 (decode, 2 <= S <= 8): the S split blocks
+                             of each (b, kv head) form a thread-block cluster and split 0 merges
+                             the others' partials in its shared memory */
     size_t workspace_bytes;
     int q_tiles;          /* blocks per (b, kv head) along its query rows (1 for decode) */
     int rows_per_block;   /* (token, query head) rows one block serves: 8, 16 or 32; 128 or 256

@@ -29,6 +29,8 @@ namespace pkv {
 std::atomic<int> g_pdl{0};
 bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
 std::atomic<int> g_prefill_tc{PKV_TC_AUTO};
+std::atomic<int> g_cluster_merge{0};
+bool cluster_merge_enabled() { return g_cluster_merge.load(std::memory_order_relaxed) != 0; }
 
 namespace {
 
@@ -40,6 +42,8 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s: far above an
 // 4K-key table 12% slower).
 constexpr int kMqBlockRows = 32;
 constexpr long kTcShortGroupKeys = 8192;
+// Largest batch whose decode blocks rank the sequence lengths themselves (longest first).
+constexpr int kLongestFirstMaxB = 128;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -382,7 +386,8 @@ pkv_status decode_impl(const pkv_bf16 *q, const void *k_cache, const void *v_cac
                               stream, tc_rows);
     }
     pkv_plan plan;
-    st = make_plan(B, Hq, Hkv, D, page_size, max_pages, sms, num_splits, &plan, kv8, group_rows, total_rows);
+    st = make_plan(B, Hq, Hkv, D, page_size, max_pages, sms, num_splits, &plan, kv8, group_rows, total_rows,
+                   cluster_merge_enabled());
     if (st != PKV_OK) return st;
     if (workspace_bytes_ < plan.workspace_bytes) return PKV_ERR_WORKSPACE_TOO_SMALL;
 
@@ -441,6 +446,12 @@ pkv_status decode_impl(const pkv_bf16 *q, const void *k_cache, const void *v_cac
     p.chunk_tokens = plan.chunk_tokens;
     p.num_splits = plan.num_splits;
     p.box4 = box4;
+    p.cluster = plan.merge_needed == 2 ? 1 : 0;
+    // Grids of several waves: longest sequences first (each block ranks the B lengths itself,
+    // B^2 / threads comparisons, so only for batches of at most kLongestFirstMaxB).
+    p.longest_first = ((long)plan.grid_blocks > (long)sms * plan.blocks_per_sm && B > 1 &&
+                       B <= kLongestFirstMaxB) ? 1 : 0;
+
     p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
     p.wait_limit_ns = kWaitLimitNs;
 
@@ -501,6 +512,8 @@ int pkv_version(void) { return 100; }
 
 int pkv_set_programmatic_launch(int enable) { return g_pdl.exchange(enable ? 1 : 0); }
 
+int pkv_set_cluster_merge(int enable) { return g_cluster_merge.exchange(enable ? 1 : 0); }
+
 int pkv_set_prefill_tensor_cores(int mode)
 {
     if (mode != PKV_TC_OFF && mode != PKV_TC_AUTO && mode != PKV_TC_ALWAYS && mode != PKV_TC_ROWS128)
@@ -511,7 +524,8 @@ int pkv_set_prefill_tensor_cores(int mode)
 pkv_status pkv_plan_query(int B, int Hq, int Hkv, int D, int page_size, int max_pages, int num_sms, int num_splits,
                           pkv_plan *plan)
 {
-    return make_plan(B, Hq, Hkv, D, page_size, max_pages, num_sms, num_splits, plan);
+    return make_plan(B, Hq, Hkv, D, page_size, max_pages, num_sms, num_splits, plan, false, 0, 0,
+                     cluster_merge_enabled());
 }
 
 pkv_status paged_decode_attn_workspace_size_ex(int B, int Hq, int Hkv, int D, int page_size, int max_pages,
@@ -531,7 +545,8 @@ pkv_status pkv_plan_query_kv(int B, int Hq, int Hkv, int D, int page_size, int m
                              int num_splits, int kv_dtype, pkv_plan *plan)
 {
     if (kv_dtype != PKV_KV_BF16 && kv_dtype != PKV_KV_FP8_E4M3) return PKV_ERR_INVALID_ARG;
-    return make_plan(B, Hq, Hkv, D, page_size, max_pages, num_sms, num_splits, plan, kv_dtype == PKV_KV_FP8_E4M3);
+    return make_plan(B, Hq, Hkv, D, page_size, max_pages, num_sms, num_splits, plan, kv_dtype == PKV_KV_FP8_E4M3,
+                     0, 0, cluster_merge_enabled());
 }
 
 pkv_status paged_decode_attn_workspace_size_kv(int B, int Hq, int Hkv, int D, int page_size, int max_pages,
@@ -883,7 +898,7 @@ extern "C" pkv_status paged_decode_attn_static_scratch(const pkv_bf16 *q, const 
     pkv_status st = current_device_sms(&device, &sms);
     if (st != PKV_OK) return st;
     pkv_plan plan;
-    st = make_plan(B, Hq, Hkv, D, page_size, max_pages, sms, 0, &plan);
+    st = make_plan(B, Hq, Hkv, D, page_size, max_pages, sms, 0, &plan, false, 0, 0, cluster_merge_enabled());
     if (st != PKV_OK) return st;
     if (plan.workspace_bytes > kStaticScratchBytes) return PKV_ERR_WORKSPACE_TOO_SMALL;
 

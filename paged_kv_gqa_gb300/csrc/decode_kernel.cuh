@@ -110,6 +110,11 @@ struct DecodeParams {
     int B, Hq, Hkv, G, P, log2P, num_pages, max_pages;
     int chunk_tokens, num_splits;
     int box4;                // 1: the tensor maps are 4-D and one box spans all D columns
+    int cluster;             // 1 (decode): the S splits of each (b, kv head) are one thread-block
+                             // cluster and split 0 merges the partials in its shared memory
+    int longest_first;       // 1 (grids of several waves, B <= kLongestFirstMaxB): grid row z
+                             // serves the z-th longest sequence
+
     float scale_log2;        // scale * log2(e)
     unsigned long long wait_limit_ns;
 };
@@ -144,6 +149,55 @@ __device__ __forceinline__ uint32_t code_offset(int r, int c, int log2_box_t)
     return lin ^ (((lin >> 7) & kMask) << 4);
 }
 
+// One split's normalised partial output, dims d .. d+3 of block row h: the warps' accumulators
+// weighted by their combine factors, summed in warp order.
+template <int W, int H8, int RS>
+__device__ __forceinline__ float4 block_partial(const float *red, const float *sm_f, int h, int d)
+{
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+        const float f = sm_f[w * H8 + h];
+        const float *r = red + (w * H8 + h) * RS + d;
+        o.x = __fmaf_rn(r[0], f, o.x);
+        o.y = __fmaf_rn(r[1], f, o.y);
+        o.z = __fmaf_rn(r[2], f, o.z);
+        o.w = __fmaf_rn(r[3], f, o.w);
+    }
+    return o;
+}
+
+// One step of the split merge (FlashQuant wiki "CUDA Kernels", split_k_reduce.cu "Algorithm"),
+// as an online log-sum-exp recurrence over the splits in index order: running maximum m,
+// weight sum wsum and accumulator a (natural-log lse; -inf marks an empty split).  Shared by
+// the workspace merge and the cluster merge, so both give the same bits.
+__device__ __forceinline__ void merge_step(float4 &a, float &m, float &wsum, const float4 v, const float l)
+{
+    const float ninf = -__int_as_float(0x7f800000);
+    const float m_new = fmaxf(m, l);
+    const float mr = m_new == ninf ? 0.f : m_new;  // every split so far empty
+    const float f_old = ex2(__fmul_rn(m - mr, kLog2e)), f_new = ex2(__fmul_rn(l - mr, kLog2e));
+    a.x = __fmaf_rn(a.x, f_old, __fmul_rn(v.x, f_new));
+    a.y = __fmaf_rn(a.y, f_old, __fmul_rn(v.y, f_new));
+    a.z = __fmaf_rn(a.z, f_old, __fmul_rn(v.z, f_new));
+    a.w = __fmaf_rn(a.w, f_old, __fmul_rn(v.w, f_new));
+    wsum = __fmaf_rn(wsum, f_old, f_new);
+    m = m_new;
+}
+
+// The merged result of one output row's dims d .. d+3: bf16 out, and (d == 0) the natural-log lse.
+__device__ __forceinline__ void merge_write(__nv_bfloat16 *out_row, float *lse_row, int d, const float4 a,
+                                           const float m, const float wsum)
+{
+    const float ninf = -__int_as_float(0x7f800000);
+    const float inv = m == ninf ? 0.f : 1.f / wsum;
+    uint2 packed;
+    packed.x = pack_bf16x2(a.x * inv, a.y * inv);
+    packed.y = pack_bf16x2(a.z * inv, a.w * inv);
+    *reinterpret_cast<uint2 *>(out_row + d) = packed;
+    if (d == 0 && lse_row) *lse_row = m == ninf ? ninf : m + __logf(wsum);
+}
+
 template <int D, int NT, bool KV8, bool MQ>
 __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
     decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -166,10 +220,29 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
     // tile qt of the (token, head) rows of the group.
     const int kvh = MQ ? (int)(blockIdx.x % (unsigned)p.Hkv) : (int)blockIdx.x;
     const int qt = MQ ? (int)(blockIdx.x / (unsigned)p.Hkv) : 0;
-    const int c = blockIdx.y, b = blockIdx.z;
+    const int c = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, cc = lane & 3;
     const int G = p.G;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_addr(smem_raw);
+    const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
+    uint8_t *base = smem_raw + (base_addr - raw_addr);
+    const SmemLayout lay = smem_layout(D, T, W, R, NT, p.chunk_tokens, p.P, KV8);
+
+    // Cluster merge: each block initialises its two cluster barriers, then every thread
+    // arrives on the cluster barrier before any block of the cluster may exit; a block that
+    // waits on that barrier later knows every block's barriers are initialised.
+    const uint32_t xbar_ready = base_addr + (uint32_t)lay.xbar, xbar_full = xbar_ready + 8u;
+    if (!MQ && p.cluster) {
+        if (threadIdx.x == 0) {
+            mbar_init(xbar_ready, 1);
+            mbar_init(xbar_full, 1);
+            fence_barrier_init();
+        }
+        cluster_arrive();
+    }
 
     // Launched with PDL, the block gets here while the previous kernel (say the KV
     // append) may still run: fetch the tensor maps (kernel parameters), then wait for
@@ -180,8 +253,36 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
     }
     griddep_wait();
 
-    // ---- length, split range ------------------------------------------------
+    // ---- which sequence: longest first on grids of several waves ---------------
+    // Blocks are dispatched in index order as slots free up, so grid row z takes the z-th
+    // longest sequence (ties by index): the blocks of whole chunks start first and the short
+    // ones fill the last wave, instead of a long sequence's blocks starting last and running
+    // alone at the end.  The ranks are computed in the ring, before any copy lands there.
     const int Lmax = p.max_pages * p.P;
+    int b = (int)blockIdx.z;
+    if (p.longest_first) {
+        int *lens = reinterpret_cast<int *>(base);
+        int *pick = lens + p.B;
+        for (int i = threadIdx.x; i < p.B; i += W * 32) {
+            const int li = p.seq_lens[i];
+            lens[i] = (li < 0 || li > Lmax) ? 0 : li;  // an invalid length counts as empty
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < p.B; i += W * 32) {
+            const int li = lens[i];
+            int rank = 0;
+            for (int j = 0; j < p.B; ++j) {
+                const int lj = lens[j];
+                rank += (lj > li || (lj == li && j < i)) ? 1 : 0;
+            }
+            if (rank == (int)blockIdx.z) *pick = i;
+        }
+        __syncthreads();
+        b = *pick;
+        __syncthreads();  // the ring is free again before the first copies
+    }
+
+    // ---- length, split range ------------------------------------------------
     int L = p.seq_lens[b];
     if (L < 0 || L > Lmax) {  // invalid length: the sequence is treated as empty
         if (threadIdx.x == 0 && c == 0 && kvh == 0) record_status(p.status, PKV_ERR_BAD_SEQ_LEN);
@@ -214,7 +315,8 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
     // MQ with the causal mask: the last key block row r sees (keys past it get -inf)
     auto key_limit = [&](int r) -> int { return (MQ && p.causal) ? L - n_q + (row_begin + r) / G : L - 1; };
 
-    const int tok_begin = c * p.chunk_tokens;
+    const int chunk = p.chunk_tokens;
+    const int tok_begin = c * chunk;
     if (c > 0 && tok_begin >= L) return;  // empty split: the merge never reads it
     if (L == 0) {                          // empty sequence: out = 0, lse = -inf
         for (int i = threadIdx.x; i < nrows * D; i += W * 32)
@@ -223,8 +325,8 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
             for (int i = threadIdx.x; i < nrows; i += W * 32) p.lse[grow(i)] = -__int_as_float(0x7f800000);
         return;
     }
-    const int tok_end = min(tok_begin + p.chunk_tokens, L);
-    const int n_chunks = (L + p.chunk_tokens - 1) / p.chunk_tokens;
+    const int tok_end = min(tok_begin + chunk, L);
+    const int n_chunks = (L + chunk - 1) / chunk;
     const int n_stages = (tok_end - tok_begin + T - 1) / T;
     const int page_begin = tok_begin >> p.log2P;
     const int page_end = ((tok_end - 1) >> p.log2P) + 1;
@@ -232,11 +334,6 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
     const int nbox = T / box_t;
 
     // ---- shared memory ------------------------------------------------------
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw_addr = smem_addr(smem_raw);
-    const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
-    uint8_t *base = smem_raw + (base_addr - raw_addr);
-    const SmemLayout lay = smem_layout(D, T, W, R, NT, p.chunk_tokens, p.P, KV8);
     const uint32_t ring_addr = base_addr + (uint32_t)lay.ring;
     const uint32_t scale_addr = base_addr + (uint32_t)lay.scales;  // KV8: [W*R][K scales T | V scales T]
     uint64_t *bars = reinterpret_cast<uint64_t *>(base + lay.bars);
@@ -725,6 +822,16 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
             lt_run[nt][h2] = lt;
         }
     __syncthreads();  // every warp is done with the ring: reuse it as the combine buffer
+    const bool cl = !MQ && p.cluster && n_chunks > 1;
+    if (cl) {
+        cluster_wait();  // every block of the cluster has initialised its barriers
+        if (c == 0 && threadIdx.x == 0) {
+            // split 0's ring past the combine buffer is free: it takes the partials of splits
+            // 1 .. n_chunks-1, nrows x (D + 1) f32 each (outputs, then lse)
+            mbar_arrive_expect_tx(xbar_full, (uint32_t)((n_chunks - 1) * nrows * (D + 1) * 4));
+            for (int r = 1; r < n_chunks; ++r) mbar_arrive_remote(map_to_rank(xbar_ready, (uint32_t)r));
+        }
+    }
     if (g == 0) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -794,21 +901,51 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
         return;
     }
 
+    // ---- several splits, merged inside the cluster: split 0 holds the partials ----
+    if (cl) {
+        const uint32_t recv = base_addr + (uint32_t)lay.recv;
+        if (c > 0) {
+            // wait (bounded: longer than split 0 can take to stream and signal) until split 0's
+            // ring is free, then store this split's partial there; the stores complete on split
+            // 0's "full" barrier
+            if (!mbar_wait_bounded_cluster(xbar_ready, 0, p.wait_limit_ns * (R + 2))) {
+                if (threadIdx.x == 0) record_status(p.status, PKV_ERR_DEVICE_TIMEOUT);
+                return;
+            }
+            const uint32_t dst = map_to_rank(recv + (uint32_t)((c - 1) * lay.recv_slot), 0u);
+            const uint32_t bar = map_to_rank(xbar_full, 0u);
+            for (int i = threadIdx.x; i < nrows * D / 4; i += W * 32) {
+                const int h = (4 * i) / D, d = 4 * i - h * D;
+                st_async_v4(dst + (uint32_t)((h * D + d) * 4), block_partial<W, H8, RS>(red, sm_f, h, d), bar);
+            }
+            if (threadIdx.x < nrows)
+                st_async_f32(dst + (uint32_t)((H8 * D + threadIdx.x) * 4), sm_lse[threadIdx.x], bar);
+            return;
+        }
+        // split 0: its own partial and the others', merged in split order
+        if (!mbar_wait_bounded_cluster(xbar_full, 0, p.wait_limit_ns * (R + 3)) && threadIdx.x == 0)
+            record_status(p.status, PKV_ERR_DEVICE_TIMEOUT);
+        const float ninf = -__int_as_float(0x7f800000);
+        for (int i = threadIdx.x; i < nrows * D / 4; i += W * 32) {
+            const int h = (4 * i) / D, d = 4 * i - h * D;
+            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+            float m = ninf, wsum = 0.f;
+            merge_step(a, m, wsum, block_partial<W, H8, RS>(red, sm_f, h, d), sm_lse[h]);
+            for (int sidx = 1; sidx < n_chunks; ++sidx) {
+                const float *slot = reinterpret_cast<const float *>(base + lay.recv + (sidx - 1) * lay.recv_slot);
+                merge_step(a, m, wsum, *reinterpret_cast<const float4 *>(slot + h * D + d), slot[H8 * D + h]);
+            }
+            merge_write(p.out + grow(h) * D, p.lse ? p.lse + grow(h) : nullptr, d, a, m, wsum);
+        }
+        return;
+    }
+
     // ---- one of several splits: write this split's normalised output and lse ----
     const size_t rows = p.total_rows;
     for (int i = threadIdx.x; i < nrows * D / 4; i += W * 32) {
         const int h = (4 * i) / D, d = 4 * i - h * D;
-        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int w = 0; w < W; ++w) {
-            const float f = sm_f[w * H8 + h];
-            const float *r = red + (w * H8 + h) * RS + d;
-            o.x += r[0] * f;
-            o.y += r[1] * f;
-            o.z += r[2] * f;
-            o.w += r[3] * f;
-        }
-        *reinterpret_cast<float4 *>(p.part_out + ((size_t)c * rows + grow(h)) * D + d) = o;
+        *reinterpret_cast<float4 *>(p.part_out + ((size_t)c * rows + grow(h)) * D + d) =
+            block_partial<W, H8, RS>(red, sm_f, h, d);
     }
     if (threadIdx.x < nrows) p.part_lse[(size_t)c * rows + grow(threadIdx.x)] = sm_lse[threadIdx.x];
 
@@ -855,31 +992,15 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
 #pragma unroll 8
         for (int sidx = 0; sidx < n_chunks; ++sidx) {
 #pragma unroll
-            for (int k = 0; k < NE; ++k) {
-                const float l = __ldcg(lp[k] + sidx * rows);
-                const float4 v = __ldcg(op[k] + sidx * rows * V4);
-                const float m_new = fmaxf(m[k], l);
-                const float mr = m_new == ninf ? 0.f : m_new;  // every split so far empty
-                const float f_old = ex2((m[k] - mr) * kLog2e), f_new = ex2((l - mr) * kLog2e);
-                a[k].x = a[k].x * f_old + v.x * f_new;
-                a[k].y = a[k].y * f_old + v.y * f_new;
-                a[k].z = a[k].z * f_old + v.z * f_new;
-                a[k].w = a[k].w * f_old + v.w * f_new;
-                wsum[k] = wsum[k] * f_old + f_new;
-                m[k] = m_new;
-            }
+            for (int k = 0; k < NE; ++k)
+                merge_step(a[k], m[k], wsum[k], __ldcg(op[k] + sidx * rows * V4), __ldcg(lp[k] + sidx * rows));
         }
 #pragma unroll
         for (int k = 0; k < NE; ++k) {
             const int e = e0 + k * W * 32;
             if (e >= nvec) continue;
             const int h = e / V4, d4 = e - h * V4;
-            const float inv = m[k] == ninf ? 0.f : 1.f / wsum[k];
-            uint2 packed;
-            packed.x = pack_bf16x2(a[k].x * inv, a[k].y * inv);
-            packed.y = pack_bf16x2(a[k].z * inv, a[k].w * inv);
-            *reinterpret_cast<uint2 *>(p.out + grow(h) * D + 4 * d4) = packed;
-            if (d4 == 0 && p.lse) p.lse[grow(h)] = m[k] == ninf ? ninf : m[k] + __logf(wsum[k]);
+            merge_write(p.out + grow(h) * D, p.lse ? p.lse + grow(h) : nullptr, 4 * d4, a[k], m[k], wsum[k]);
         }
     }
 }

@@ -30,9 +30,14 @@ pkv_status launch_decode_variant(const CUtensorMap &mk, const CUtensorMap &mv, c
                                  const pkv_plan &plan, int B, int Hkv, int device, cudaStream_t stream)
 {
     static bool attr_set[64] = {};
+    static int8_t cluster_ok[64][kMaxClusterSplits + 1] = {};  // 0 unknown, 1 resident, -1 not
     static std::mutex mu;
     auto kern = decode_split_kernel<D, NT, KV8, MQ>;
     if (device < 0 || device >= 64) return PKV_ERR_UNSUPPORTED;
+    dim3 grid(Hkv * plan.q_tiles, plan.num_splits, B);
+    dim3 block(plan.warps * 32);
+    const unsigned S = (unsigned)plan.num_splits;
+    bool cluster = !MQ && p.cluster && S >= 2 && S <= (unsigned)kMaxClusterSplits;
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!attr_set[device]) {
@@ -40,11 +45,23 @@ pkv_status launch_decode_variant(const CUtensorMap &mk, const CUtensorMap &mv, c
                 return PKV_ERR_CUDA;
             attr_set[device] = true;
         }
+        // A cluster that cannot be resident falls back to the workspace merge (first call per
+        // device and cluster size only: an occupancy query, no launch).
+        if (cluster && cluster_ok[device][S] == 0)
+            cluster_ok[device][S] = cluster_fits(kern, block, (size_t)plan.smem_bytes, S) ? 1 : -1;
+        if (cluster && cluster_ok[device][S] < 0) cluster = false;
     }
-    dim3 grid(Hkv * plan.q_tiles, plan.num_splits, B);
-    dim3 block(plan.warps * 32);
-    return launch_kernel(kern, grid, block, (size_t)plan.smem_bytes, stream, mk, mv, p) == cudaSuccess ? PKV_OK
-                                                                                              : PKV_ERR_CUDA;
+    cudaError_t e;
+    if (cluster) {
+        e = launch_kernel_cluster(kern, grid, block, (size_t)plan.smem_bytes, stream, S, mk, mv, p);
+    } else if (p.cluster) {
+        DecodeParams q = p;
+        q.cluster = 0;
+        e = launch_kernel(kern, grid, block, (size_t)plan.smem_bytes, stream, mk, mv, q);
+    } else {
+        e = launch_kernel(kern, grid, block, (size_t)plan.smem_bytes, stream, mk, mv, p);
+    }
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 #define PKV_V(DD, NN, KV8, MQ) launch_decode_variant<DD, NN, KV8, MQ>(mk, mv, p, plan, B, Hkv, device, stream)

@@ -35,6 +35,9 @@ RuntimeTiling tiling_for(int D);
 // Number of 8-wide head tiles (mma N tiles) for group size G.
 inline int head_tiles(int G) { return G <= 8 ? 1 : (G <= 16 ? 2 : 4); }
 
+// Most splits whose partials merge inside a thread-block cluster (the portable cluster size).
+constexpr int kMaxClusterSplits = 8;
+
 // Resident blocks per SM a variant is compiled for (its launch bound, so its register
 // budget).  Variants with one head tile are light enough for three, which hides more
 // latency; D = 256 bf16 tiles fill shared memory with one block, fp8 ones with two.
@@ -70,6 +73,11 @@ struct SmemLayout {
     int f;         // [W][H8] f32 per-warp combine factor
     int lse;       // [H8] f32 block result per head
     int flag;      // one int: "this block merges its group"
+    int xbar;      // cluster merge: two mbarriers (8 B each): "ready" (split 0's ring is free for
+                   // the partials), "full" (every partial has landed in split 0's ring)
+    int recv;      // cluster merge, split 0 only: the partials of splits 1 .. S-1, `recv_slot`
+    int recv_slot; // bytes apart, in the ring after the combine buffer: [H8][D] f32 outputs then
+                   // [H8] f32 lse each
     int table;     // block_table slice (int32), `table_entries` of them
     int table_entries;
     int total;     // bytes from the aligned base
@@ -98,11 +106,21 @@ PKV_HD SmemLayout smem_layout(int D, int T, int W, int R, int NT, int chunk_toke
     s.f = s.lt + W * H8 * 4;
     s.lse = s.f + W * H8 * 4;
     s.flag = s.lse + H8 * 4;
-    s.table = round_up_int(s.flag + 4, 16);
+    s.xbar = round_up_int(s.flag + 4, 8);
+    s.recv = round_up_int(red, 128);
+    s.recv_slot = round_up_int(H8 * (D + 1) * 4, 128);
+    s.table = round_up_int(s.xbar + 16, 16);
     s.table_entries = chunk_tokens / page_size + 2;
     s.total = round_up_int(s.table + s.table_entries * 4, 16);
     s.dynamic = s.total + 1024;
     return s;
+}
+
+// Whether a decode launch of S splits can merge them inside a cluster: 2 <= S <= 8 and split
+// 0's ring holds the combine buffer and the other splits' partials.
+PKV_HD bool cluster_merge_fits(const SmemLayout &lay, int S, int ring_bytes)
+{
+    return S >= 2 && S <= kMaxClusterSplits && lay.recv + (S - 1) * lay.recv_slot <= ring_bytes;
 }
 
 // Workspace layout (byte offsets), used only when S > 1:
@@ -125,7 +143,10 @@ pkv_status validate_shape(int B, int Hq, int Hkv, int D, int page_size, int max_
 // with kv8, the fp8-cache one.  group_rows: (token, query head) rows of one (sequence,
 // kv head) group, at most max_q_len * G (0: decode, G rows); total_rows: rows of the
 // output, total_q * Hq (0: B * Hq).
+// allow_cluster: a decode plan with 2-8 splits may merge them inside a thread-block cluster
+// (plan->merge_needed = 2) when split 0's ring holds the partials.
 pkv_status make_plan(int B, int Hq, int Hkv, int D, int page_size, int max_pages, int num_sms,
-                     int num_splits, pkv_plan *plan, bool kv8 = false, long group_rows = 0, long total_rows = 0);
+                     int num_splits, pkv_plan *plan, bool kv8 = false, long group_rows = 0, long total_rows = 0,
+                     bool allow_cluster = false);
 
 }  // namespace pkv

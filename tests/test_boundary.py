@@ -114,7 +114,7 @@ def test_plan_invariants(lib, name, sms, cache):
     assert (plan["num_splits"] - 1) * plan["chunk_tokens"] < max_tokens
     assert plan["smem_bytes"] <= 232448
     assert plan["grid_blocks"] == plan["num_splits"] * Hkv * B
-    assert plan["merge_needed"] == (1 if plan["num_splits"] > 1 else 0)
+    assert plan["merge_needed"] == (1 if plan["num_splits"] > 1 else 0)  # the cluster merge is off by default
     # K+V bytes of one split stay bounded (<= 2 MiB) so no split becomes a straggler
     assert plan["chunk_tokens"] * 4 * D <= (2 << 20) or plan["num_splits"] == 1
     if plan["num_splits"] > 1:
@@ -380,3 +380,28 @@ def test_static_scratch_rejects_bad_arguments_before_touching_cuda(lib):
     assert call(scale=float("inf")) == -1
     assert call(D=96) == -2
     assert call(B=0, q=0) == 0
+
+
+def test_plan_reports_cluster_merge(lib):
+    # decode with 2-8 splits merges inside a cluster; more splits, one split, several rows per
+    # sequence, or the switch off: the workspace merge (or none)
+    prev = pkv.set_cluster_merge(True)
+    assert prev is False  # off at load
+    try:
+        for S in range(2, 9):
+            assert pkv.plan_query(4, 32, 8, 128, 16, 256, 152, num_splits=S)["merge_needed"] == 2
+            assert pkv.plan_query(4, 32, 8, 128, 16, 256, 152, num_splits=S, cache="fp8")["merge_needed"] == 2
+        # more blocks than one wave (8 x 8 x 8 on 152 SMs x 3): the workspace merge
+        assert pkv.plan_query(8, 32, 8, 128, 16, 256, 152, num_splits=8)["merge_needed"] == 1
+        assert pkv.plan_query(8, 32, 8, 128, 16, 256, 152, num_splits=9)["merge_needed"] == 1
+        # G = 32 at D = 128: split 0's ring cannot hold 5 partials of 32 rows beside its combine buffer
+        assert pkv.plan_query(2, 64, 2, 128, 16, 256, 152, num_splits=6)["merge_needed"] == 1
+        assert pkv.plan_query(2, 32, 2, 128, 16, 256, 152, num_splits=6)["merge_needed"] == 2
+        assert pkv.plan_query(4, 64, 8, 128, 16, 8192, 152)["merge_needed"] == 1      # long: 76 splits
+        assert pkv.plan_query(256, 32, 8, 128, 64, 32, 152)["merge_needed"] == 0      # big pages: one split
+        assert pkv.plan_query(8, 32, 8, 128, 16, 256, 152)["merge_needed"] == 2       # batch: 5 splits
+        assert pkv.prefill_plan_query(8, 32, 8, 128, 16, 256, 32, 4, 152, num_splits=4)["merge_needed"] == 1
+        assert pkv.set_cluster_merge(False) is True
+        assert pkv.plan_query(8, 32, 8, 128, 16, 256, 152, num_splits=4)["merge_needed"] == 1
+    finally:
+        pkv.set_cluster_merge(prev)

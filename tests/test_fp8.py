@@ -300,3 +300,25 @@ def test_fp8_append_then_decode():
     out, lse = run_fp8(stepped, after)
     eo, el = compare_fp8_with_oracle(stepped, after, out, lse)
     assert eo <= OUT_TOL and el <= LSE_TOL
+
+
+@pytest.mark.parametrize("lens,splits", [([1, 1000, 5000], 4), ([1, 1000, 5000], 3), ([4000, 17, 2500], 7)])
+def test_fp8_cluster_merge_equals_workspace_merge(lens, splits):
+    """The fp8 cache's splits merged inside a thread-block cluster give the workspace merge's bits."""
+    case = make_case(_spec(3, 32, 8, 128, 16, seed=41), seq_lens=lens, poison=True)
+    pools = Fp8Pools(case)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    prev = pkv.set_cluster_merge(True)
+    try:
+        plan = pkv.plan_query(case.B, case.Hq, case.Hkv, case.D, case.P, case.max_pages, sms, num_splits=splits,
+                              cache="fp8")
+        assert plan["merge_needed"] == 2, plan
+        a = run_fp8(case, pools, num_splits=splits)
+        pkv.set_cluster_merge(False)
+        b = run_fp8(case, pools, num_splits=splits)
+    finally:
+        pkv.set_cluster_merge(prev)
+    assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
+    assert torch.equal(a[1].view(torch.int32), b[1].view(torch.int32))
+    eo, el = compare_fp8_with_oracle(case, pools, *a)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)

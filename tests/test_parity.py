@@ -209,3 +209,35 @@ def test_split_kv_merge_matches_oracle():
         assert max_abs_diff(out.float().cpu().numpy().reshape(B * Hq, D), ro) <= 1e-2
         assert max_abs_diff(lse.cpu().numpy().reshape(-1), rl) <= 1e-5
         assert np.isneginf(lse[2, 3].item()) and out[2, 3].abs().max().item() == 0
+
+
+@pytest.mark.parametrize("case_args,splits", [
+    (("batch", None), 0),
+    ((_spec(3, 32, 8, 128, 16, seed=3), [1, 1000, 5000]), 2),
+    ((_spec(3, 32, 8, 128, 16, seed=3), [1, 1000, 5000]), 3),
+    ((_spec(3, 32, 8, 128, 16, seed=3), [1, 1000, 5000]), 8),
+    ((_spec(2, 32, 2, 256, 64, seed=4), [3000, 65]), 4),
+    ((_spec(3, 8, 2, 64, 16, seed=6), [700, 0, 33]), 5),
+    ((_spec(2, 32, 2, 128, 16, seed=7), [2000, 900]), 6),
+])
+def test_cluster_merge_equals_workspace_merge(case_args, splits):
+    """Splits merged inside a thread-block cluster (split 0's shared memory) give the same bits
+    as the workspace merge: the same partials, combined by the same recurrence in split order."""
+    spec, lens = case_args
+    case = make_case(spec, seq_lens=lens, device="cuda") if lens else make_case(spec, device="cuda")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    prev = pkv.set_cluster_merge(True)
+    try:
+        plan = pkv.plan_query(case.B, case.Hq, case.Hkv, case.D, case.P, case.max_pages, sms, num_splits=splits)
+        assert plan["merge_needed"] == 2, plan
+        a_out, a_lse = run_gpu(case, num_splits=splits)
+        pkv.set_cluster_merge(False)
+        plan = pkv.plan_query(case.B, case.Hq, case.Hkv, case.D, case.P, case.max_pages, sms, num_splits=splits)
+        assert plan["merge_needed"] == 1, plan
+        b_out, b_lse = run_gpu(case, num_splits=splits)
+    finally:
+        pkv.set_cluster_merge(prev)
+    assert torch.equal(a_out.view(torch.int16), b_out.view(torch.int16))
+    assert torch.equal(a_lse.view(torch.int32), b_lse.view(torch.int32))
+    eo, el = compare_with_oracle(case, a_out, a_lse, select=sample_rows(case, 12))
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
