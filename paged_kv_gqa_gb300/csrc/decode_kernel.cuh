@@ -602,7 +602,9 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
         float vfac = 1.f;  // KV8: rescale of the accumulators when the V-scale exponent rises
         if constexpr (KV8) {
             const uint32_t sb = scale_addr + (uint32_t)((warp * R + slot) * (2 * T * 4));
-            int ev = -126;
+            // the stage's largest V-scale exponent: the exponent of the largest |scale| bit
+            // pattern (non-negative floats order as their bits), over the valid keys
+            uint32_t vbits = 0u;
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -611,11 +613,9 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
                     kmul[mt][h] = ld_shared_f32(sb + (uint32_t)r * 4u) * score_mul;
                     vmul[mt][h] = ld_shared_f32(sb + (uint32_t)(T + r) * 4u);
                     if (MASKED && !key_valid(t0 + r)) vmul[mt][h] = 0.f;
-                    else ev = max(ev, min(126, ilog2f(vmul[mt][h])));
+                    vbits = max(vbits, __float_as_uint(vmul[mt][h]) & 0x7fffffffu);
                 }
-            ev = max(ev, __shfl_xor_sync(0xffffffffu, ev, 4));
-            ev = max(ev, __shfl_xor_sync(0xffffffffu, ev, 8));
-            ev = max(ev, __shfl_xor_sync(0xffffffffu, ev, 16));
+            const int ev = min(126, ilog2f(__uint_as_float(__reduce_max_sync(0xffffffffu, vbits))));
             if (ev > ev_run) {
                 vfac = exp2i(ev_run - ev);
                 ev_run = ev;
