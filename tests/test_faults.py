@@ -79,3 +79,28 @@ def test_workspace_too_small_is_rejected_before_launch():
         pkv.paged_decode_attn(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens, case.scale,
                               out, None, ws)
     assert e.value.status == -4
+
+
+def test_longest_first_order_with_ties_and_bad_lengths():
+    # A grid of several waves (40 sequences x 8 kv heads x 12 splits on one GPU) runs its
+    # sequences longest first, ranked on the device from seq_lens; equal lengths, empty
+    # sequences and invalid lengths (ranked as empty, reported) keep every row where it belongs.
+    lens = [700, 33, 700, 0, 1, 2500, 700, 64, 1000, 33] * 4
+    case = make_case(dict(B=40, Hq=16, Hkv=8, D=64, P=16, lens=("fixed", 1), seed=21), seq_lens=lens, poison=True)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = pkv.plan_query(case.B, case.Hq, case.Hkv, case.D, case.P, case.max_pages, sms, num_splits=12)
+    assert plan["grid_blocks"] > sms * plan["blocks_per_sm"]  # several waves: the longest-first order applies
+    out, lse = run_gpu(case, num_splits=12)
+    eo, el = compare_with_oracle(case, out, lse)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+    bad = Case(**case.__dict__)
+    bad.seq_lens = case.seq_lens.clone()
+    bad.seq_lens[7] = -5
+    bad.seq_lens[12] = case.max_pages * case.P + 1
+    out, lse = run_gpu(bad, num_splits=12, expect_status=-8)
+    ref = Case(**case.__dict__)
+    ref.seq_lens = case.seq_lens.clone()
+    ref.seq_lens[7] = 0
+    ref.seq_lens[12] = 0
+    eo, el = compare_with_oracle(ref, out, lse)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
