@@ -406,7 +406,8 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
             const float neg_ref = m_ref == kNegInf ? 0.f : -m_ref;
             // p = 2^(s c - m) for two keys at a time (packed f32 pairs for the FMA and the sums)
             const uint64_t c2 = f32x2(c, c), nr2 = f32x2(neg_ref, neg_ref);
-            uint64_t ls2[2] = {0ull, 0ull}, lts2[2] = {0ull, 0ull};
+            uint64_t ls2[2] = {0ull, 0ull};
+            float lta[2] = {0.f, 0.f}, ltb[2] = {0.f, 0.f};  // the bf16 sums: low and high halves
             uint32_t pw[kTcKeys / 2];
 #pragma unroll
             for (int i = 0; i < kTcKeys / 2; ++i) {
@@ -416,16 +417,14 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
                 const float p0 = ex2(a0), p1 = ex2(a1);
                 pw[i] = pack_bf16x2(p0, p1);
                 ls2[i & 1] = add_f32x2(ls2[i & 1], f32x2(p0, p1));
-                lts2[i & 1] = add_f32x2(lts2[i & 1], f32x2(bf16_lo(pw[i]), bf16_hi(pw[i])));
+                add_bf16x2_to_f32(pw[i], lta[i & 1], ltb[i & 1]);
             }
             {
                 float l0, l1, l2, l3;
                 f32x2_split(ls2[0], l0, l1);
                 f32x2_split(ls2[1], l2, l3);
                 l_run += (l0 + l1) + (l2 + l3);
-                f32x2_split(lts2[0], l0, l1);
-                f32x2_split(lts2[1], l2, l3);
-                lt_run += (l0 + l1) + (l2 + l3);
+                lt_run += (lta[0] + ltb[0]) + (lta[1] + ltb[1]);
             }
             // P (bf16 pairs) into the first 64 columns of this row's S lane
             tc_st64(tS(qx) + lane_off, pw);

@@ -460,6 +460,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// acc_lo += the low bf16 of v, acc_hi += the high one (mixed-precision adds: the bf16 widened
+// exactly, one rounding in f32).
+__device__ __forceinline__ void add_bf16x2_to_f32(uint32_t v, float &acc_lo, float &acc_hi)
+{
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tadd.f32.bf16 %0, l, %0;\n\tadd.f32.bf16 %1, h, %1;\n\t}"
+        : "+f"(acc_lo), "+f"(acc_hi)
+        : "r"(v));
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
