@@ -81,9 +81,11 @@ def causal_flops(case) -> int:
     return 4 * keys * case.Hq * case.D
 
 
-def _kernel_name(tc_rows: int, fp8: bool, q_len: int) -> str:
+def _kernel_name(tc_rows: int, fp8: bool, q_len: int, D: int = 128) -> str:
     if tc_rows == 256:
         return "prefill_tc2_kernel (tcgen05, 256 rows/CTA)"
+    if tc_rows == 128 and D == 256:
+        return "prefill_tc256_kernel (tcgen05, 128 rows/CTA, 64-key tiles)"
     if tc_rows == 128:
         return "prefill_tc_kernel<%s> (tcgen05, 128 rows/CTA)" % ("fp8" if fp8 else "bf16")
     return "decode_split_kernel<%s%s> (one launch per call; split merge fused)" % (
@@ -95,7 +97,7 @@ def _roofline(args, case, q_len, fp8, tc_rows, peaks, gbs, mean_ms) -> dict:
     FLOPs over the measured bf16 peak), HBM bandwidth for the decode kernel (algorithmic bytes
     over the measured copy bandwidth).  DRAM traffic comes from the committed ncu summary of
     the same kernel and workload, taken on the current source, else null."""
-    name = _kernel_name(tc_rows, fp8, q_len)
+    name = _kernel_name(tc_rows, fp8, q_len, case.D)
     if tc_rows:
         tflops = causal_flops(case) / (mean_ms * 1e-3) / 1e12
         return {"bound": "tensor", "achieved": round(tflops, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
@@ -535,7 +537,7 @@ def run_pkv(args) -> None:
         "per_config": per_config,
         "event_floor_us": floor_us,
         "tensor": None if q_len == 1 else {
-            "kernel": _kernel_name(tc_rows, fp8, q_len),
+            "kernel": _kernel_name(tc_rows, fp8, q_len, case.D),
             "tflops": round(causal_flops(case) / (mean_ms * 1e-3) / 1e12, 2),
             "peak_tflops": peaks["bf16_tflops"],
             "frac": round(causal_flops(case) / (mean_ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4)},

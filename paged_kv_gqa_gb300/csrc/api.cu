@@ -18,6 +18,7 @@
 #include "decode_launch.cuh"
 #include "launch_util.h"
 #include "prefill_tc2_kernel.cuh"
+#include "prefill_tc256_kernel.cuh"
 #include "prefill_tc_kernel.cuh"
 #include "merge_kernel.cuh"
 #include "pkv.h"
@@ -216,25 +217,26 @@ struct MultiRows {
 };
 
 // Several rows per sequence with more than 32 rows per (sequence, kv head) group (the routing
-// of tensor_core_rows), D = 128, scale > 0: a tensor-core kernel, one CTA per cta_rows (128:
-// prefill_tc_kernel.cuh, bf16 or fp8 cache; 256: prefill_tc2_kernel.cuh, bf16) rows and key
-// split (tc_split_plan).
+// of tensor_core_rows), D = 128 (or 256 on a bf16 cache), scale > 0: a tensor-core kernel, one
+// CTA per cta_rows (128: prefill_tc_kernel.cuh, bf16 or fp8 cache, or prefill_tc256_kernel.cuh
+// at D = 256; 256: prefill_tc2_kernel.cuh, bf16) rows and key split (tc_split_plan).
 // With one split the workspace holds only the status word; with several, also the split
 // counters and the per-split partial outputs and lse that the last split merges.
 pkv_status prefill_tc(const pkv_bf16 *q, const void *k_cache, const void *v_cache, const Fp8Scales &fp8,
                       const int32_t *block_table, const int32_t *seq_lens, int B, int Hq, int Hkv, int page_size,
                       int num_pages, int max_pages, float scale, pkv_bf16 *out, float *lse, void *workspace,
                       size_t workspace_bytes, int num_splits, const MultiRows &mr, int device, int sms,
-                      cudaStream_t stream, int cta_rows)
+                      cudaStream_t stream, int cta_rows, int D)
 {
     if (fp8.on && cta_rows != kTcRows) return PKV_ERR_UNSUPPORTED;  // the fp8 cache has the 128-row kernel only
+    if (D != 128 && (D != 256 || fp8.on || cta_rows != kTcRows)) return PKV_ERR_UNSUPPORTED;
     const bool two = cta_rows == kTc2Rows;
-    const int variant = fp8.on ? 2 : two ? 1 : 0;
+    const int variant = D == 256 ? 3 : fp8.on ? 2 : two ? 1 : 0;
     const TcSplit sp =
-        tc_split_plan(B, Hq, Hkv, page_size, max_pages, mr.total_q, mr.max_q_len, num_splits, cta_rows, sms);
+        tc_split_plan(B, Hq, Hkv, page_size, max_pages, mr.total_q, mr.max_q_len, num_splits, cta_rows, sms, D);
     if (workspace_bytes < sp.ws.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
-    constexpr int D = 128;
-    const int box_t = page_size < kTcKeys ? page_size : kTcKeys;
+    const int tile_keys = tc_tile_keys(D);
+    const int box_t = page_size < tile_keys ? page_size : tile_keys;
     CUtensorMap mk, mv;
     // bf16: K per 64-dim half (rank 3), V one copy per page box (rank 4); fp8: the codes of a
     // page box in one copy each (the byte view)
@@ -245,15 +247,17 @@ pkv_status prefill_tc(const pkv_bf16 *q, const void *k_cache, const void *v_cach
     const int G = Hq / Hkv;
     const long q_tiles = sp.q_tiles;
     if ((long)Hkv * q_tiles >= (1l << 31) || B > 65535) return PKV_ERR_UNSUPPORTED;
-    static bool attr_set[3][64] = {};
+    static bool attr_set[4][64] = {};
     static std::mutex mu;
     if (device < 0 || device >= 64) return PKV_ERR_UNSUPPORTED;
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!attr_set[variant][device]) {
             const cudaError_t e =
-                variant == 1 ? cudaFuncSetAttribute(prefill_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                    Tc2Smem::dynamic)
+                variant == 3 ? cudaFuncSetAttribute(prefill_tc256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                    T256Smem::dynamic)
+                : variant == 1 ? cudaFuncSetAttribute(prefill_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                      Tc2Smem::dynamic)
                 : variant == 2 ? cudaFuncSetAttribute(prefill_tc_kernel<true>,
                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Tc8Smem::dynamic)
                                : cudaFuncSetAttribute(prefill_tc_kernel<false>,
@@ -294,7 +298,10 @@ pkv_status prefill_tc(const pkv_bf16 *q, const void *k_cache, const void *v_cach
     p.wait_limit_ns = kWaitLimitNs;
     const dim3 grid((unsigned)(Hkv * q_tiles), (unsigned)sp.splits, (unsigned)B);
     const cudaError_t e =
-        variant == 1
+        variant == 3
+            ? launch_kernel(prefill_tc256_kernel, grid, dim3(kT256Threads), (size_t)T256Smem::dynamic, stream, mk, mv,
+                            p)
+        : variant == 1
             ? launch_kernel(prefill_tc2_kernel, grid, dim3(kTc2Threads), (size_t)Tc2Smem::dynamic, stream, mk, mv, p)
         : variant == 2 ? launch_kernel(prefill_tc_kernel<true>, grid, dim3(kTc8Threads), (size_t)Tc8Smem::dynamic,
                                        stream, mk, mv, p)
@@ -376,14 +383,15 @@ pkv_status decode_impl(const pkv_bf16 *q, const void *k_cache, const void *v_cac
     int device = 0, sms = 0;
     pkv_status st = current_device_sms(&device, &sms);
     if (st != PKV_OK) return st;
-    if (mq && D == 128 && group_rows > kMqBlockRows && scale > 0.f) {
+    if (mq && (D == 128 || (D == 256 && !kv8)) && group_rows > kMqBlockRows && scale > 0.f) {
         int tc_rows = tensor_core_rows(g_prefill_tc.load(std::memory_order_relaxed), B, Hq, Hkv, page_size,
                                        max_pages, mr, num_splits, group_rows, sms);
-        if (kv8 && tc_rows) tc_rows = kTcRows;  // the fp8 cache: the 128-row kernel's fp8 instantiation
+        // the fp8 cache: the 128-row kernel's fp8 instantiation; D = 256: the 128-row kernel of 64-key tiles
+        if ((kv8 || D == 256) && tc_rows) tc_rows = kTcRows;
         if (tc_rows)
             return prefill_tc(q, k_cache, v_cache, fp8, block_table, seq_lens, B, Hq, Hkv, page_size, num_pages,
                               max_pages, scale, out, lse, workspace, workspace_bytes_, num_splits, mr, device, sms,
-                              stream, tc_rows);
+                              stream, tc_rows, D);
     }
     pkv_plan plan;
     st = make_plan(B, Hq, Hkv, D, page_size, max_pages, sms, num_splits, &plan, kv8, group_rows, total_rows,
@@ -654,14 +662,14 @@ pkv_status pkv_plan_query_prefill(int B, int Hq, int Hkv, int D, int page_size, 
     const long group_rows = (long)max_q_len * (Hq / Hkv);
     const pkv_status st = make_plan(B, Hq, Hkv, D, page_size, max_pages, num_sms, num_splits, plan,
                                     kv_dtype == PKV_KV_FP8_E4M3, group_rows, (long)total_q * Hq);
-    if (st != PKV_OK || D != 128 || group_rows <= kMqBlockRows) return st;
-    // the tensor-core kernels may take the call: room for their split partials too (the fp8
-    // cache has the 128-row kernel only), whatever the routing when the call is made
     const bool kv8 = kv_dtype == PKV_KV_FP8_E4M3;
+    if (st != PKV_OK || !(D == 128 || (D == 256 && !kv8)) || group_rows <= kMqBlockRows) return st;
+    // the tensor-core kernels may take the call: room for their split partials too (the fp8
+    // cache and D = 256 have the 128-row kernel only), whatever the routing when the call is made
     for (int rows : {kTcRows, kTc2Rows}) {
-        if (kv8 && rows != kTcRows) continue;
+        if ((kv8 || D == 256) && rows != kTcRows) continue;
         const TcSplit sp =
-            tc_split_plan(B, Hq, Hkv, page_size, max_pages, total_q, max_q_len, num_splits, rows, num_sms);
+            tc_split_plan(B, Hq, Hkv, page_size, max_pages, total_q, max_q_len, num_splits, rows, num_sms, D);
         plan->workspace_bytes = std::max(plan->workspace_bytes, sp.ws.total);
     }
     // the launch under the current routing (for a positive scale): a tensor-core kernel's
@@ -671,18 +679,25 @@ pkv_status pkv_plan_query_prefill(int B, int Hq, int Hkv, int D, int page_size, 
     mr.max_q_len = max_q_len;
     int tc_rows = tensor_core_rows(g_prefill_tc.load(std::memory_order_relaxed), B, Hq, Hkv, page_size, max_pages,
                                    mr, num_splits, group_rows, num_sms);
-    if (kv8 && tc_rows) tc_rows = kTcRows;
+    if ((kv8 || D == 256) && tc_rows) tc_rows = kTcRows;
     if (tc_rows) {
         const TcSplit sp =
-            tc_split_plan(B, Hq, Hkv, page_size, max_pages, total_q, max_q_len, num_splits, tc_rows, num_sms);
+            tc_split_plan(B, Hq, Hkv, page_size, max_pages, total_q, max_q_len, num_splits, tc_rows, num_sms, D);
+        const bool d256 = D == 256;
         plan->num_splits = sp.splits;
-        plan->chunk_tokens = sp.chunk_tiles * kTcKeys;
-        plan->stage_tokens = kTcKeys;
-        plan->warps = (tc_rows == kTc2Rows ? kTc2Threads : kv8 ? kTc8Threads : kTcThreads) / 32;
-        plan->ring_stages = tc_rows == kTc2Rows ? kTc2KStages : kv8 ? TcCfg<true>::k_stages : TcCfg<false>::k_stages;
+        plan->chunk_tokens = sp.chunk_tiles * tc_tile_keys(D);
+        plan->stage_tokens = tc_tile_keys(D);
+        plan->warps = (d256 ? kT256Threads : tc_rows == kTc2Rows ? kTc2Threads : kv8 ? kTc8Threads : kTcThreads) / 32;
+        plan->ring_stages = d256                 ? kT256KStages
+                            : tc_rows == kTc2Rows ? kTc2KStages
+                            : kv8                 ? TcCfg<true>::k_stages
+                                                  : TcCfg<false>::k_stages;
         plan->blocks_per_sm = 1;
         plan->grid_blocks = (int)((long)Hkv * sp.q_tiles * sp.splits * B);
-        plan->smem_bytes = tc_rows == kTc2Rows ? Tc2Smem::dynamic : kv8 ? Tc8Smem::dynamic : TcSmem::dynamic;
+        plan->smem_bytes = d256                 ? T256Smem::dynamic
+                           : tc_rows == kTc2Rows ? Tc2Smem::dynamic
+                           : kv8                 ? Tc8Smem::dynamic
+                                                 : TcSmem::dynamic;
         plan->merge_needed = sp.splits > 1 ? 1 : 0;
         plan->q_tiles = sp.q_tiles;
         plan->rows_per_block = tc_rows;

@@ -405,3 +405,24 @@ def test_plan_reports_cluster_merge(lib):
         assert pkv.plan_query(8, 32, 8, 128, 16, 256, 152, num_splits=4)["merge_needed"] == 1
     finally:
         pkv.set_cluster_merge(prev)
+
+
+def test_prefill_plan_at_head_dim_256(lib):
+    # D = 256 on a bf16 cache: groups of more than 32 rows may take the 128-row tensor-core kernel of
+    # 64-key tiles; the fp8 cache at D = 256 stays on the mma.sync kernel
+    try:
+        pkv.set_prefill_tensor_cores("auto")
+        p = pkv.prefill_plan_query(256, 32, 2, 256, 64, 32, 256 * 8, 8, 152)  # 128 rows per group
+        assert p["rows_per_block"] == 128 and p["stage_tokens"] == 64 and p["warps"] == 7
+        # workspace: the status word, counters and partials of every split the kernel can take
+        for splits in (0, 4):
+            q = pkv.prefill_plan_query(2, 16, 2, 256, 16, 600, 18, 9, 152, num_splits=splits)
+            assert q["rows_per_block"] == 128
+            if q["num_splits"] > 1:
+                assert q["workspace_bytes"] >= q["num_splits"] * 18 * 16 * 256 * 4
+        p8 = pkv.prefill_plan_query(256, 32, 2, 256, 64, 32, 256 * 8, 8, 152, cache="fp8")
+        assert p8["rows_per_block"] <= 32
+        pkv.set_prefill_tensor_cores("off")
+        assert pkv.prefill_plan_query(256, 32, 2, 256, 64, 32, 256 * 8, 8, 152)["rows_per_block"] <= 32
+    finally:
+        pkv.set_prefill_tensor_cores("auto")

@@ -369,3 +369,95 @@ def test_fp8_tensor_core_path_at_full_size(workload, q_len):
     assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
     del case, dcase, pools, out, lse, out2, lse2
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------------ the tensor-core path at D = 256
+# bf16 cache: 128 rows per CTA, 64-key tiles (prefill_tc256_kernel)
+
+TC256 = [
+    # B, Hq, Hkv, D, P, q_lens, kv_lens
+    (2, 32, 2, 256, 64, [8, 5], [2048, 300]),    # G = 16: 128 and 80 rows, 64-key pages (the big-page shape)
+    (2, 16, 4, 256, 16, [40, 33], [500, 33]),    # G = 4: 160 and 132 rows, a request as long as its cache
+    (1, 8, 1, 256, 8, [130], [130]),             # 1040 rows: 9 tiles, 8-key pages (two boxes per 16-key step)
+    (2, 16, 2, 256, 128, [20, 0], [700, 9]),     # 128-key pages (64-key boxes), an empty request
+    (2, 32, 4, 256, 32, [17, 16], [40, 16]),     # 136 and 128 rows over fewer than 64 keys: one partial tile
+    (1, 16, 2, 256, 16, [9], [9000]),            # 72 rows over a 9000-key table: key splits
+]
+
+
+@pytest.mark.parametrize("mode", ["always", "auto"])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("B,Hq,Hkv,D,P,q_lens,kv_lens", TC256, ids=lambda x: str(x).replace(" ", ""))
+def test_tensor_core_path_d256_full_oracle(B, Hq, Hkv, D, P, q_lens, kv_lens, causal, mode):
+    case = make_prefill_case(_spec(B, Hq, Hkv, D, P, seed=7 * B + P + sum(q_lens)), q_lens, kv_lens, poison=True)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    try:
+        pkv.set_prefill_tensor_cores(mode)
+        rows = max(q_lens) * (Hq // Hkv)
+        plan = pkv.prefill_plan_query(B, Hq, Hkv, D, P, case.max_pages, case.q.shape[0], max(q_lens), sms)
+        takes_tc = rows > 32 and (mode == "always" or rows >= 128 or case.max_pages * P >= 8192)
+        assert (plan["rows_per_block"] == 128 and plan["stage_tokens"] == 64) == takes_tc, plan
+        out, lse = run_prefill(case, causal=causal)
+    finally:
+        pkv.set_prefill_tensor_cores("auto")
+    eo, el = compare(case, out, lse, causal=causal)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+
+
+def test_d256_tensor_core_and_mma_sync_paths_agree():
+    case = make_prefill_case(_spec(2, 32, 2, 256, 64, seed=51), [8, 6], [1500, 400])
+    try:
+        pkv.set_prefill_tensor_cores("off")
+        ref_o, ref_l = run_prefill(case)
+        pkv.set_prefill_tensor_cores("always")
+        out, lse = run_prefill(case)
+    finally:
+        pkv.set_prefill_tensor_cores("auto")
+    excess, _, _ = split_invariance_violation(out.float().cpu().numpy(), ref_o.float().cpu().numpy(), tol=OUT_TOL)
+    assert excess <= 0
+    assert max_abs_diff(lse.cpu().numpy(), ref_l.cpu().numpy()) <= 1e-4
+
+
+@pytest.mark.parametrize("splits", [0, 3, 16])
+def test_d256_tensor_core_key_splits_and_bad_page(splits):
+    case = make_prefill_case(_spec(2, 32, 2, 256, 16, seed=52), [8, 4], [9000, 300], poison=True)
+    try:
+        pkv.set_prefill_tensor_cores("always")
+        out, lse = run_prefill(case, num_splits=splits)
+        rows = [(t, h) for t in range(12) for h in (0, 7, 31)]
+        eo, el = compare(case, out, lse, select=rows)
+        assert eo <= OUT_TOL and el <= LSE_TOL, (splits, eo, el)
+        out2, lse2 = run_prefill(case, num_splits=splits)  # the merge counters return to 0
+        assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+        bad = Case(**case.__dict__)
+        bt = case.block_table.clone()
+        bt[1, 2] = case.num_pages + 3
+        bad.block_table = bt
+        o_bad, _ = run_prefill(bad, num_splits=splits, expect_status=-6)
+        assert torch.equal(o_bad[:8].view(torch.int16), out[:8].view(torch.int16))  # request 0 untouched
+        assert torch.isfinite(o_bad.float()).all()
+    finally:
+        pkv.set_prefill_tensor_cores("auto")
+
+
+def test_d256_tensor_core_path_at_full_size():
+    # the big-page G = 16 workload with 8 new tokens per sequence (128 rows per group): auto takes the
+    # D = 256 tensor-core kernel; sampled rows against the oracle, a second call equal bit for bit
+    from workloads import CONFIGS, draw_seq_lens
+    spec = CONFIGS["bigpage_g16"]
+    kv = draw_seq_lens(spec["lens"], spec["B"], spec["P"], spec["seed"])
+    case = make_prefill_case("bigpage_g16", [8] * spec["B"], kv, device="cuda")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    pkv.set_prefill_tensor_cores("auto")
+    plan = pkv.prefill_plan_query(case.B, case.Hq, case.Hkv, case.D, case.P, case.max_pages, case.q.shape[0], 8, sms)
+    assert plan["rows_per_block"] == 128 and plan["stage_tokens"] == 64, plan
+    out, lse = run_prefill(case)
+    out2, lse2 = run_prefill(case)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))
+    total_q = case.q.shape[0]
+    rows = [(t, h) for t in range(0, total_q, max(1, total_q // 16)) for h in (0, 17, case.Hq - 1)]
+    rows += [(total_q - 1, 5)]
+    eo, el = compare(case, out, lse, select=rows)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
