@@ -167,22 +167,63 @@ __device__ __forceinline__ float4 block_partial(const float *red, const float *s
     return o;
 }
 
-// One step of the split merge (FlashQuant wiki "CUDA Kernels", split_k_reduce.cu "Algorithm"),
-// as an online log-sum-exp recurrence over the splits in index order: running maximum m,
-// weight sum wsum and accumulator a (natural-log lse; -inf marks an empty split).  Shared by
-// the workspace merge and the cluster merge, so both give the same bits.
-__device__ __forceinline__ void merge_step(float4 &a, float &m, float &wsum, const float4 v, const float l)
+// The split merge (FlashQuant wiki "CUDA Kernels", split_k_reduce.cu "Algorithm"): per output
+// row, split s weighted by exp(lse_s - M), M the largest lse (natural log; -inf marks an empty
+// split), the weighted outputs summed in split order and divided by the weight sum.  Taken
+// PB splits at a time: the loads of a batch are all issued before any is used (this merge runs
+// at the tail of the kernel, where each round trip to memory is long), the batch's largest lse
+// joins the running maximum m, and what was summed before is rescaled by exp(m_old - m).  With
+// at most PB splits this is the two-pass form exactly.  load(k, s, v, l) gives element k's
+// split-s output (4 dims) and lse.  Shared by the workspace merge and the cluster merge, so
+// both give the same bits.
+template <int NE, int PB, class Load>
+__device__ __forceinline__ void merge_splits(int S, Load load, float4 (&a)[NE], float (&m)[NE], float (&wsum)[NE])
 {
     const float ninf = -__int_as_float(0x7f800000);
-    const float m_new = fmaxf(m, l);
-    const float mr = m_new == ninf ? 0.f : m_new;  // every split so far empty
-    const float f_old = ex2(__fmul_rn(m - mr, kLog2e)), f_new = ex2(__fmul_rn(l - mr, kLog2e));
-    a.x = __fmaf_rn(a.x, f_old, __fmul_rn(v.x, f_new));
-    a.y = __fmaf_rn(a.y, f_old, __fmul_rn(v.y, f_new));
-    a.z = __fmaf_rn(a.z, f_old, __fmul_rn(v.z, f_new));
-    a.w = __fmaf_rn(a.w, f_old, __fmul_rn(v.w, f_new));
-    wsum = __fmaf_rn(wsum, f_old, f_new);
-    m = m_new;
+#pragma unroll
+    for (int k = 0; k < NE; ++k) {
+        a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        m[k] = ninf;
+        wsum[k] = 0.f;
+    }
+    for (int s0 = 0; s0 < S; s0 += PB) {
+        float4 v[NE][PB];
+        float l[NE][PB];
+#pragma unroll
+        for (int j = 0; j < PB; ++j)
+#pragma unroll
+            for (int k = 0; k < NE; ++k) {
+                if (s0 + j < S) {
+                    load(k, s0 + j, v[k][j], l[k][j]);
+                } else {
+                    v[k][j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    l[k][j] = ninf;
+                }
+            }
+#pragma unroll
+        for (int k = 0; k < NE; ++k) {
+            float mb = m[k];
+#pragma unroll
+            for (int j = 0; j < PB; ++j) mb = fmaxf(mb, l[k][j]);
+            const float mr = mb == ninf ? 0.f : mb;  // every split so far empty
+            const float f_old = ex2(__fmul_rn(m[k] - mr, kLog2e));
+            a[k].x = __fmul_rn(a[k].x, f_old);
+            a[k].y = __fmul_rn(a[k].y, f_old);
+            a[k].z = __fmul_rn(a[k].z, f_old);
+            a[k].w = __fmul_rn(a[k].w, f_old);
+            wsum[k] = __fmul_rn(wsum[k], f_old);
+#pragma unroll
+            for (int j = 0; j < PB; ++j) {
+                const float w = ex2(__fmul_rn(l[k][j] - mr, kLog2e));
+                a[k].x = __fmaf_rn(v[k][j].x, w, a[k].x);
+                a[k].y = __fmaf_rn(v[k][j].y, w, a[k].y);
+                a[k].z = __fmaf_rn(v[k][j].z, w, a[k].z);
+                a[k].w = __fmaf_rn(v[k][j].w, w, a[k].w);
+                wsum[k] = __fadd_rn(wsum[k], w);
+            }
+            m[k] = mb;
+        }
+    }
 }
 
 // The merged result of one output row's dims d .. d+3: bf16 out, and (d == 0) the natural-log lse.
@@ -925,17 +966,25 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
         // split 0: its own partial and the others', merged in split order
         if (!mbar_wait_bounded_cluster(xbar_full, 0, p.wait_limit_ns * (R + 3)) && threadIdx.x == 0)
             record_status(p.status, PKV_ERR_DEVICE_TIMEOUT);
-        const float ninf = -__int_as_float(0x7f800000);
         for (int i = threadIdx.x; i < nrows * D / 4; i += W * 32) {
             const int h = (4 * i) / D, d = 4 * i - h * D;
-            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-            float m = ninf, wsum = 0.f;
-            merge_step(a, m, wsum, block_partial<W, H8, RS>(red, sm_f, h, d), sm_lse[h]);
-            for (int sidx = 1; sidx < n_chunks; ++sidx) {
-                const float *slot = reinterpret_cast<const float *>(base + lay.recv + (sidx - 1) * lay.recv_slot);
-                merge_step(a, m, wsum, *reinterpret_cast<const float4 *>(slot + h * D + d), slot[H8 * D + h]);
-            }
-            merge_write(p.out + grow(h) * D, p.lse ? p.lse + grow(h) : nullptr, d, a, m, wsum);
+            float4 a[1];
+            float m[1], wsum[1];
+            merge_splits<1, kMaxClusterSplits>(
+                n_chunks,
+                [&](int, int sidx, float4 &v, float &l) {
+                    if (sidx == 0) {
+                        v = block_partial<W, H8, RS>(red, sm_f, h, d);
+                        l = sm_lse[h];
+                    } else {
+                        const float *slot =
+                            reinterpret_cast<const float *>(base + lay.recv + (sidx - 1) * lay.recv_slot);
+                        v = *reinterpret_cast<const float4 *>(slot + h * D + d);
+                        l = slot[H8 * D + h];
+                    }
+                },
+                a, m, wsum);
+            merge_write(p.out + grow(h) * D, p.lse ? p.lse + grow(h) : nullptr, d, a[0], m[0], wsum[0]);
         }
         return;
     }
@@ -950,10 +999,9 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
     if (threadIdx.x < nrows) p.part_lse[(size_t)c * rows + grow(threadIdx.x)] = sm_lse[threadIdx.x];
 
     // ---- the last split of this (b, kv head) to finish merges all of them ----------
-    // Log-sum-exp merge (FlashQuant wiki "CUDA Kernels", split_k_reduce.cu
-    // "Algorithm"): split s is weighted by exp(lse_s - max_s lse_s), reached below by
-    // an online recurrence.  atomicInc wraps the per-group counter back to 0 on the
-    // last arrival, ready for the next call.
+    // atomicInc wraps the per-group counter back to 0 on the last arrival, ready for the
+    // next call.  The splits are combined in index order whichever block arrives last, so
+    // the result does not depend on scheduling.
     __threadfence();
     __syncthreads();
     int *flag = reinterpret_cast<int *>(base + lay.flag);
@@ -965,36 +1013,28 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
     if (!*flag) return;
     __threadfence();
 
-    // One pass over the splits per output element with the online log-sum-exp recurrence
-    // (running maximum m, weight sum w, accumulator a, all rescaled when m rises), so every
-    // split's lse and output loads are in flight together: this merge runs at the tail of
-    // the kernel and is latency-bound.  The splits are combined in index order whichever
-    // block arrives last, so the result does not depend on scheduling.
-    const float ninf = -__int_as_float(0x7f800000);
     constexpr int V4 = D / 4;
     constexpr int NE = 2;
     const int nvec = nrows * V4;
     for (int e0 = threadIdx.x; e0 < nvec; e0 += NE * W * 32) {
-        float4 a[NE];
-        float m[NE], wsum[NE];
         const float *lp[NE];
         const float4 *op[NE];
 #pragma unroll
         for (int k = 0; k < NE; ++k) {
             const int e = e0 + k * W * 32;
             const int h = (e < nvec ? e : 0) / V4, d4 = (e < nvec ? e : 0) - h * V4;
-            a[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-            m[k] = ninf;
-            wsum[k] = 0.f;
             lp[k] = p.part_lse + grow(h);
             op[k] = reinterpret_cast<const float4 *>(p.part_out + grow(h) * D) + d4;
         }
-#pragma unroll 8
-        for (int sidx = 0; sidx < n_chunks; ++sidx) {
-#pragma unroll
-            for (int k = 0; k < NE; ++k)
-                merge_step(a[k], m[k], wsum[k], __ldcg(op[k] + sidx * rows * V4), __ldcg(lp[k] + sidx * rows));
-        }
+        float4 a[NE];
+        float m[NE], wsum[NE];
+        merge_splits<NE, 8>(
+            n_chunks,
+            [&](int k, int sidx, float4 &v, float &l) {
+                v = __ldcg(op[k] + (size_t)sidx * rows * V4);
+                l = __ldcg(lp[k] + (size_t)sidx * rows);
+            },
+            a, m, wsum);
 #pragma unroll
         for (int k = 0; k < NE; ++k) {
             const int e = e0 + k * W * 32;

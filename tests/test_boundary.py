@@ -115,8 +115,10 @@ def test_plan_invariants(lib, name, sms, cache):
     assert plan["smem_bytes"] <= 232448
     assert plan["grid_blocks"] == plan["num_splits"] * Hkv * B
     assert plan["merge_needed"] == (1 if plan["num_splits"] > 1 else 0)  # the cluster merge is off by default
-    # K+V bytes of one split stay bounded (<= 2 MiB) so no split becomes a straggler
-    assert plan["chunk_tokens"] * 4 * D <= (2 << 20) or plan["num_splits"] == 1
+    # cache bytes of one split (K and V; fp8: codes and scales) stay bounded (<= 2 MiB) so no
+    # split becomes a straggler
+    token_bytes = 4 * D if cache == "bf16" else 2 * D + 8
+    assert plan["chunk_tokens"] * token_bytes <= (2 << 20) or plan["num_splits"] == 1
     if plan["num_splits"] > 1:
         pad = lambda x: (x + 255) // 256 * 256
         ws = 256 + pad(B * Hkv * 4) + pad(plan["num_splits"] * B * Hq * 4) + plan["num_splits"] * B * Hq * D * 4
@@ -397,7 +399,7 @@ def test_plan_reports_cluster_merge(lib):
         # G = 32 at D = 128: split 0's ring cannot hold 5 partials of 32 rows beside its combine buffer
         assert pkv.plan_query(2, 64, 2, 128, 16, 256, 152, num_splits=6)["merge_needed"] == 1
         assert pkv.plan_query(2, 32, 2, 128, 16, 256, 152, num_splits=6)["merge_needed"] == 2
-        assert pkv.plan_query(4, 64, 8, 128, 16, 8192, 152)["merge_needed"] == 1      # long: 76 splits
+        assert pkv.plan_query(4, 64, 8, 128, 16, 8192, 152)["merge_needed"] == 1      # long: 42 splits
         assert pkv.plan_query(256, 32, 8, 128, 64, 32, 152)["merge_needed"] == 0      # big pages: one split
         assert pkv.plan_query(8, 32, 8, 128, 16, 256, 152)["merge_needed"] == 2       # batch: 5 splits
         assert pkv.prefill_plan_query(8, 32, 8, 128, 16, 256, 32, 4, 152, num_splits=4)["merge_needed"] == 1
