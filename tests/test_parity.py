@@ -117,8 +117,9 @@ def test_split_count_invariance(case_args):
 
 @pytest.mark.parametrize("name,counts", [("long", [0, 1, 2, 8]), ("ragged", [0, 1, 2])])
 def test_split_count_invariance_full_size(name, counts):
-    """The full long-context and ragged workloads at the plan's own split count (76 and 7 on a
-    152-SM GB300) against one, two (and eight) splits: where the split count matters most."""
+    """The full long-context and ragged workloads at the plan's own split count (42 and 8 on a
+    152-SM GB300; the long one merged in six batches) against one, two (and eight) splits:
+    where the split count matters most."""
     case = make_case(name, device="cuda")
     plan = pkv.plan_query(case.B, case.Hq, case.Hkv, case.D, case.P, case.max_pages,
                           torch.cuda.get_device_properties(0).multi_processor_count)
