@@ -314,14 +314,17 @@ def run_reference(args) -> None:
     if cache == "fp8":  # the oracle's own quantiser makes its fp8 cache
         k8, ks = oracle.quantize_pool(k)
         v8, vs = oracle.quantize_pool(v)
-        one = lambda: oracle.paged_decode_fp8(q, k8, v8, ks, vs, bt, sl, case.scale, select=rows)
+        run_rows = lambda sel: oracle.paged_decode_fp8(q, k8, v8, ks, vs, bt, sl, case.scale, select=sel)
     else:
-        one = lambda: oracle.paged_decode(q, k, v, bt, sl, case.scale, select=rows)
-    rows, sample = _reference_sample(case, args.ref_seconds)
+        run_rows = lambda sel: oracle.paged_decode(q, k, v, bt, sl, case.scale, select=sel)
+    # each step's sample is sized so that the whole run (warm-up and timed steps) stays within
+    # a few minutes whatever the step count
+    per_step = min(args.ref_seconds, _REFERENCE_RUN_SECONDS / (args.steps + args.warmup))
+    rows, sample, cores = _reference_sample(case, per_step, _oracle_thread_rate(case, run_rows))
+    one = lambda: run_rows(rows)
     ab = algorithmic_bytes(case, cache=cache)
     frac = len(rows) / (case.B * case.Hq)
     step_bytes = ab["total"] * frac
-    cores = os.cpu_count() or 1
     for _ in range(args.warmup):
         one()
     t = []
@@ -344,19 +347,51 @@ def run_reference(args) -> None:
     print(json.dumps(line), flush=True)
 
 
-def _reference_sample(case, seconds_hint):
-    """Rows (b, h) for a bounded CPU sample: every sequence, a stride of heads, so that
-    one oracle pass over them is roughly a second or less on a many-core host."""
+# wall-clock budget of a whole `--impl reference` run (warm-up and timed steps together)
+_REFERENCE_RUN_SECONDS = 150.0
+
+
+def _oracle_thread_rate(case, run_rows) -> float:
+    """fp64 flops a second of one oracle thread on this host: one row of the longest sequence,
+    repeated for at least 20 ms (a warm-up as well)."""
     import numpy as np
-    lens = case.seq_lens.numpy().astype(np.int64)
-    work = float((lens * case.Hq).sum()) * case.D * 4  # fp64 flops of a full pass
-    budget = 2.0e9 * max(0.25, seconds_hint)            # ~2 GFLOP/s/core-ish, times the hint
-    stride = 1
-    while work / stride > budget * (os.cpu_count() or 1) and stride < case.Hq:
-        stride *= 2
-    rows = [(b, h) for b in range(case.B) for h in range(0, case.Hq, stride)]
-    return rows, "all %d sequences, every %d-th query head (%d of %d rows) per step" % (
-        case.B, stride, len(rows), case.B * case.Hq)
+    lens = case.seq_lens.cpu().numpy().astype(np.int64)
+    b = int(np.argmax(lens))
+    flops = max(1, int(lens[b])) * case.D * 4.0
+    n, t = 0, 0.0
+    while t < 0.02 or n == 0:
+        t0 = time.perf_counter()
+        run_rows([(b, 0)])
+        t += time.perf_counter() - t0
+        n += 1
+    return flops * n / t
+
+
+def _reference_sample(case, seconds, rate):
+    """Rows (b, h) for a bounded CPU sample: the first n of a head-major order (head 0 of every
+    sequence, then head 1, ...), n as large as keeps one oracle pass within `seconds` on this
+    host's cores at `rate` fp64 flops a second per thread (the oracle's threads take the rows by
+    a fixed stride), and at least one row.  Returns (rows, description, threads used)."""
+    import numpy as np
+    lens = case.seq_lens.cpu().numpy().astype(np.int64)
+    order = [(b, h) for h in range(case.Hq) for b in range(case.B)]
+    cost = np.array([lens[b] * case.D * 4.0 / rate for b, _ in order])
+    cores = os.cpu_count() or 1
+
+    def pass_seconds(n):
+        t = min(cores, n)
+        return max(cost[i:n:t].sum() for i in range(t))
+
+    lo, hi = 1, len(order)
+    while lo < hi:  # the largest n whose pass fits (pass time grows with n)
+        mid = (lo + hi + 1) // 2
+        if pass_seconds(mid) <= seconds:
+            lo = mid
+        else:
+            hi = mid - 1
+    rows = order[:lo]
+    return rows, "%d of %d rows (head-major: head 0 of every sequence, then head 1, ...) per step" % (
+        len(rows), case.B * case.Hq), min(cores, len(rows))
 
 
 def _config_block(case, args, plan):
@@ -380,20 +415,21 @@ def _cpu_baseline(case, seconds: float, fp8=None) -> dict:
     import oracle
     from workloads import algorithmic_bytes
     q, k, v, bt, sl = case.host_bits()
-    rows, sample = _reference_sample(case, 1.0)
+    if fp8:
+        run_rows = lambda sel: oracle.paged_decode_fp8(q, *fp8, bt, sl, case.scale, select=sel)
+    else:
+        run_rows = lambda sel: oracle.paged_decode(q, k, v, bt, sl, case.scale, select=sel)
+    rows, sample, cores = _reference_sample(case, 1.0, _oracle_thread_rate(case, run_rows))
     frac = len(rows) / (case.B * case.Hq)
     step_bytes = algorithmic_bytes(case, cache="fp8" if fp8 else "bf16")["total"] * frac
     n, t_total = 0, 0.0
     t_end = time.perf_counter() + seconds
     while time.perf_counter() < t_end or n == 0:
         t0 = time.perf_counter()
-        if fp8:
-            oracle.paged_decode_fp8(q, *fp8, bt, sl, case.scale, select=rows)
-        else:
-            oracle.paged_decode(q, k, v, bt, sl, case.scale, select=rows)
+        run_rows(rows)
         t_total += time.perf_counter() - t0
         n += 1
-    return {"value": round(step_bytes * n / t_total / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count() or 1,
+    return {"value": round(step_bytes * n / t_total / 1e9, 4), "unit": "GB/s", "cores": cores,
             "kind": "oracle", "sample": "%s; %d passes in %.1f s" % (sample, n, t_total)}
 
 
