@@ -121,7 +121,7 @@ def test_split_counts_agree():
     case = make_prefill_case(_spec(3, 32, 8, 128, 16, seed=4), [4, 2, 3], [3000, 1200, 64])
     ref = run_prefill(case, num_splits=1)
     rows = prefill_oracle_rows(case)
-    for splits in (0, 3, 7):
+    for splits in (0, 3, 7, 20):  # 20: the in-kernel merge takes the splits in three batches
         out, lse = run_prefill(case, num_splits=splits)
         split_straddle_check(out.float().cpu().numpy(), ref[0].float().cpu().numpy(), rows)
         assert max_abs_diff(lse.cpu().numpy(), ref[1].cpu().numpy()) <= 2e-3
