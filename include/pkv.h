@@ -105,7 +105,7 @@ PKV_API int pkv_set_programmatic_launch(int enable);
  * blocks launches the splits of each (b, kv head) as one cluster; each split sends
  * its normalised partial output and lse into split 0's shared memory (distributed
  * shared memory, st.async), and split 0 merges them with the same log-sum-exp
- * recurrence, in the same split order, as the workspace merge (FlashQuant wiki
+ * combine, in the same split order, as the workspace merge (FlashQuant wiki
  * "CUDA Kernels", split_k_reduce.cu "Algorithm"), so the results are identical
  * bit for bit.  enable == 0: every merge goes through the workspace (the last
  * split to finish merges).  Measured on GB300 the cluster merge shortens the

@@ -223,7 +223,7 @@ def test_split_kv_merge_matches_oracle():
 ])
 def test_cluster_merge_equals_workspace_merge(case_args, splits):
     """Splits merged inside a thread-block cluster (split 0's shared memory) give the same bits
-    as the workspace merge: the same partials, combined by the same recurrence in split order."""
+    as the workspace merge: the same partials, combined by the same batched combine in split order."""
     spec, lens = case_args
     case = make_case(spec, seq_lens=lens, device="cuda") if lens else make_case(spec, device="cuda")
     sms = torch.cuda.get_device_properties(0).multi_processor_count
