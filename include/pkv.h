@@ -128,7 +128,8 @@ PKV_API int pkv_set_cluster_merge(int enable);
  * (num_splits = 0): when the groups' CTAs are fewer than the SMs, SMs / CTAs ranges per
  * group (one wave), else ranges of at most 8192 keys; num_splits > 0 sets the count.  A
  * group with several ranges merges them in the kernel through the workspace.  A group of
- * at most 32 rows always takes the mma.sync kernel (one block reads each key once).
+ * at most 32 rows always takes the mma.sync kernel (one block reads each key once; at
+ * D = 256 a block serves at most 16 rows, so 17-32 rows take two).
  * mode:
  *   PKV_TC_OFF     such calls take the mma.sync kernel;
  *   PKV_TC_AUTO    (the setting at load) groups of 33-127 rows: 128 rows per CTA when
@@ -410,7 +411,7 @@ PKV_API pkv_status paged_kv_append_fp8(const pkv_bf16 *k_new, const pkv_bf16 *v_
  * the contract is skipped (nothing read or written for it) and
  * PKV_ERR_BAD_QO_INDPTR is recorded.  Decode is the case qo_indptr[b] = b,
  * max_q_len = 1.  Groups of at most 32 rows run on the mma.sync kernel, which reads
- * the K/V stream once per query tile of up to 32 rows; larger groups may run on the
+ * the K/V stream once per query tile of up to 32 rows (16 at D = 256); larger groups may run on the
  * tensor-core kernels (pkv_set_prefill_tensor_cores), which read it once per 128 or
  * 256 rows.
  */

@@ -464,7 +464,14 @@ pkv_status decode_impl(const pkv_bf16 *q, const void *k_cache, const void *v_cac
     p.wait_limit_ns = kWaitLimitNs;
 
     const int NT = plan.rows_per_block / 8;
-    if (mq)
+    if (!mq && plan.q_tiles > 1) {
+        // a decode group wider than one block (D = 256, G = 32): the several-rows variant,
+        // one row per sequence (no qo_indptr), serves it as two query tiles
+        p.total_q = B;
+        p.max_q_len = 1;
+        p.causal = 0;
+    }
+    if (mq || plan.q_tiles > 1)
         return kv8 ? launch_prefill_fp8(D, NT, mk, mv, p, plan, B, Hkv, device, stream)
                    : launch_prefill_bf16(D, NT, mk, mv, p, plan, B, Hkv, device, stream);
     return kv8 ? launch_decode_fp8(D, NT, mk, mv, p, plan, B, Hkv, device, stream)

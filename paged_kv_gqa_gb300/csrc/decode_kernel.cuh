@@ -102,7 +102,8 @@ struct DecodeParams {
     int *status;             // workspace status word
     const float *k_scale;    // fp8 cache: [num_pages, Hkv, P] f32 per (token, kv head)
     const float *v_scale;
-    const int *qo_indptr;    // multi-token rows: [B+1] query rows per request (q, out: [total_q, Hq, D])
+    const int *qo_indptr;    // multi-token rows: [B+1] query rows per request (q, out: [total_q, Hq, D]);
+                             // null: one row per sequence (a decode group wider than one block)
     size_t total_rows;       // rows of out / lse / the partials: B*Hq, or total_q*Hq
     int q_tiles;             // multi-token rows: blocks per (request, kv head) along its rows
     int total_q, max_q_len;  // multi-token rows: rows of q, and the most rows one request may have
@@ -333,13 +334,15 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
     // sequence); MQ, rows rr = qt*H8 + r of the group's (token i, head h) rows, rr = i*G + h.
     int n_q = 1, q_base = b, row_begin = 0, nrows = G;
     if constexpr (MQ) {
-        q_base = p.qo_indptr[b];
-        n_q = p.qo_indptr[b + 1] - q_base;
-        if (q_base < 0 || n_q < 0 || n_q > p.max_q_len || q_base + n_q > p.total_q) {
-            // a malformed row range: nothing of this request is read or written
-            if (threadIdx.x == 0 && c == 0 && kvh == 0 && qt == 0) record_status(p.status, PKV_ERR_BAD_QO_INDPTR);
-            return;
-        }
+        if (p.qo_indptr) {
+            q_base = p.qo_indptr[b];
+            n_q = p.qo_indptr[b + 1] - q_base;
+            if (q_base < 0 || n_q < 0 || n_q > p.max_q_len || q_base + n_q > p.total_q) {
+                // a malformed row range: nothing of this request is read or written
+                if (threadIdx.x == 0 && c == 0 && kvh == 0 && qt == 0) record_status(p.status, PKV_ERR_BAD_QO_INDPTR);
+                return;
+            }
+        }  // no qo_indptr: one query row per sequence (a decode group wider than one block)
         row_begin = qt * H8;
         nrows = min(H8, n_q * G - row_begin);
         if (nrows <= 0) return;  // this tile of the group is past the request's rows

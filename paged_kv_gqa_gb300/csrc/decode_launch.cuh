@@ -64,6 +64,7 @@ pkv_status launch_decode_variant(const CUtensorMap &mk, const CUtensorMap &mv, c
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+// (a D = 256 block serves at most 16 rows: no 32-row variant there)
 #define PKV_V(DD, NN, KV8, MQ) launch_decode_variant<DD, NN, KV8, MQ>(mk, mv, p, plan, B, Hkv, device, stream)
 #define PKV_DECODE_DISPATCH(KV8, MQ)                         \
     switch (D * 8 + NT) {                                    \
@@ -75,7 +76,6 @@ pkv_status launch_decode_variant(const CUtensorMap &mk, const CUtensorMap &mv, c
         case 128 * 8 + 4: return PKV_V(128, 4, KV8, MQ);     \
         case 256 * 8 + 1: return PKV_V(256, 1, KV8, MQ);     \
         case 256 * 8 + 2: return PKV_V(256, 2, KV8, MQ);     \
-        case 256 * 8 + 4: return PKV_V(256, 4, KV8, MQ);     \
         default: return PKV_ERR_UNSUPPORTED;                 \
     }
 

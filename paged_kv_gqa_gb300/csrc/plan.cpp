@@ -78,9 +78,10 @@ pkv_status make_plan(int B, int Hq, int Hkv, int D, int page_size, int max_pages
     const int G = Hq / Hkv;
 
     // A block serves up to 32 (token, query head) rows of one (sequence, kv head) group
-    // (all G heads of a decode step); longer groups take several query tiles.
+    // (all G heads of a decode step), 16 at D = 256 (32 rows there need more registers
+    // than a thread has and spill); longer groups take several query tiles.
     const long rows = group_rows > 0 ? group_rows : G;
-    const int NT = head_tiles((int)std::min<long>(rows, 32));
+    const int NT = head_tiles((int)std::min<long>(rows, max_block_rows(D)));
     const long q_tiles = (rows + NT * 8 - 1) / (NT * 8);
     if ((long)B * Hkv * q_tiles >= (1l << 31)) return PKV_ERR_INVALID_ARG;
     if (B > 65535) return PKV_ERR_UNSUPPORTED;  // sequences are the grid's z dimension
@@ -161,14 +162,14 @@ pkv_status make_plan(int B, int Hq, int Hkv, int D, int page_size, int max_pages
     plan->blocks_per_sm = per_sm;
     plan->grid_blocks = (int)(S * Hkv * q_tiles * B);
     plan->smem_bytes = lay.dynamic;
-    // Decode (one row per sequence) with 2-8 splits merges them inside a thread-block cluster
+    // Decode (one row per sequence, one query tile) with 2-8 splits merges them inside a thread-block cluster
     // through split 0's shared memory; otherwise the last split to finish merges through
     // the workspace.
     // Only grids of one wave (every block resident at once): clusters of S blocks placed whole
     // leave slots idle when blocks of many waves come and go (measured on GB300: the ragged
     // workload's 3584 blocks ran 3-40% slower in clusters of 7-8).
     const bool one_wave = (long)S * Hkv * q_tiles * B <= (long)num_sms * per_sm;
-    const bool cluster = allow_cluster && group_rows == 0 && one_wave &&
+    const bool cluster = allow_cluster && group_rows == 0 && q_tiles == 1 && one_wave &&
                          cluster_merge_fits(lay, S, t.W * R * stage_bytes(D, t.T, kv8));
     plan->merge_needed = S > 1 ? (cluster ? 2 : 1) : 0;
     plan->workspace_bytes = workspace_layout(S, (size_t)B * Hkv * q_tiles, (size_t)out_rows, D).total;

@@ -35,6 +35,11 @@ RuntimeTiling tiling_for(int D);
 // Number of 8-wide head tiles (mma N tiles) for group size G.
 inline int head_tiles(int G) { return G <= 8 ? 1 : (G <= 16 ? 2 : 4); }
 
+// Most (token, head) rows one decode block serves: 32, or 16 at D = 256, where the 32-row
+// variant's accumulators and query fragments exceed the register file and spill (measured:
+// ~2.6 KB of spills a thread, 9x slower than two 16-row blocks).
+PKV_HD constexpr int max_block_rows(int D) { return D == 256 ? 16 : 32; }
+
 // Most splits whose partials merge inside a thread-block cluster (the portable cluster size).
 constexpr int kMaxClusterSplits = 8;
 

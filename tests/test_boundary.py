@@ -428,3 +428,20 @@ def test_prefill_plan_at_head_dim_256(lib):
         assert pkv.prefill_plan_query(256, 32, 2, 256, 64, 32, 256 * 8, 8, 152)["rows_per_block"] <= 32
     finally:
         pkv.set_prefill_tensor_cores("auto")
+
+
+def test_head_dim_256_blocks_take_at_most_16_rows(lib):
+    # At D = 256 a decode block serves at most 16 (token, head) rows: a group of 32 query heads, or a
+    # 2-token step of a 16-head group, takes two query tiles (the 32-row variant would spill)
+    for cache in ("bf16", "fp8"):
+        p = pkv.plan_query(2, 64, 2, 256, 16, 100, 152, cache=cache)  # G = 32
+        assert p["rows_per_block"] == 16 and p["q_tiles"] == 2, p
+        assert p["grid_blocks"] == 2 * 2 * 2 * p["num_splits"]
+        if p["num_splits"] > 1:  # the split counters cover both query tiles of every group
+            pad = lambda x: (x + 255) // 256 * 256
+            S = p["num_splits"]
+            assert p["workspace_bytes"] == 256 + pad(2 * 2 * 2 * 4) + pad(S * 2 * 64 * 4) + S * 2 * 64 * 256 * 4
+        q = pkv.prefill_plan_query(256, 32, 2, 256, 64, 32, 256 * 2, 2, 152, cache=cache)  # 32 rows per group
+        assert q["rows_per_block"] == 16 and q["q_tiles"] == 2, q
+    # D = 128 keeps 32-row blocks
+    assert pkv.plan_query(2, 64, 2, 128, 16, 100, 152)["rows_per_block"] == 32

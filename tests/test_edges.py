@@ -69,9 +69,12 @@ def test_zero_and_negative_scale(scale):
 
 
 def test_group_32_at_head_dim_256():
-    """G = 32 (four 8-row head tiles) at D = 256, the largest block the decode kernel takes."""
+    """G = 32 at D = 256: a block there serves at most 16 heads, so each group is two query tiles
+    (the several-rows variant with one row per sequence), each merging its own splits."""
     case = make_case(_spec(2, 64, 2, 256, 16, seed=23), seq_lens=[1500, 33], poison=True)
-    for splits in (1, 0):
+    plan = pkv.plan_query(2, 64, 2, 256, 16, case.max_pages, torch.cuda.get_device_properties(0).multi_processor_count)
+    assert plan["q_tiles"] == 2 and plan["rows_per_block"] == 16, plan
+    for splits in (1, 0, 3, 20):
         out, lse = run_gpu(case, num_splits=splits)
         eo, el = compare_with_oracle(case, out, lse)
         assert eo <= OUT_TOL and el <= LSE_TOL, (splits, eo, el)

@@ -322,3 +322,13 @@ def test_fp8_cluster_merge_equals_workspace_merge(lens, splits):
     assert torch.equal(a[1].view(torch.int32), b[1].view(torch.int32))
     eo, el = compare_fp8_with_oracle(case, pools, *a)
     assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+
+
+def test_fp8_group_32_at_head_dim_256():
+    """G = 32 at D = 256 on the fp8 cache: two 16-head query tiles per group, against the fp8 oracle."""
+    case = make_case(_spec(2, 64, 2, 256, 16, seed=29), seq_lens=[1200, 40], poison=True)
+    pools = Fp8Pools(case)
+    for splits in (1, 0, 5):
+        out, lse = run_fp8(case, pools, num_splits=splits)
+        eo, el = compare_fp8_with_oracle(case, pools, out, lse)
+        assert eo <= OUT_TOL and el <= LSE_TOL, (splits, eo, el)
