@@ -85,7 +85,7 @@ def _kernel_name(tc_rows: int, fp8: bool, q_len: int, D: int = 128) -> str:
     if tc_rows == 256:
         return "prefill_tc2_kernel (tcgen05, 256 rows/CTA)"
     if tc_rows == 128 and D == 256:
-        return "prefill_tc256_kernel (tcgen05, 128 rows/CTA, 64-key tiles)"
+        return "prefill_tc256_kernel<%s> (tcgen05, 128 rows/CTA, 64-key tiles)" % ("fp8" if fp8 else "bf16")
     if tc_rows == 128:
         return "prefill_tc_kernel<%s> (tcgen05, 128 rows/CTA)" % ("fp8" if fp8 else "bf16")
     return "decode_split_kernel<%s%s> (one launch per call; split merge fused)" % (

@@ -117,14 +117,15 @@ PKV_API int pkv_set_programmatic_launch(int enable);
 PKV_API int pkv_set_cluster_merge(int enable);
 
 /*
- * Tensor-core path of paged_prefill_attn and paged_prefill_attn_fp8 (D = 128, scale > 0,
- * more than 32 (token, query head) rows per (sequence, kv head) group, i.e. max_q_len *
- * Hq/Hkv > 32): the score and PV products run on tcgen05 (5th-generation tensor cores,
- * accumulators in tensor memory), one CTA per 128 or 256 rows of a group and per key range.
- * The fp8 cache takes the 128-row kernel, whose converter warps dequantise each key tile
- * (code x scale, exact) into the bf16 tile the bf16 kernel reads: its results equal, bit for
- * bit, those of the bf16 cache holding the dequantised values; where a mode below names 256
- * rows, the fp8 cache takes 128.  Key ranges
+ * Tensor-core path of paged_prefill_attn and paged_prefill_attn_fp8 (D = 128 or 256,
+ * scale > 0, more than 32 (token, query head) rows per (sequence, kv head) group, i.e.
+ * max_q_len * Hq/Hkv > 32): the score and PV products run on tcgen05 (5th-generation tensor
+ * cores, accumulators in tensor memory), one CTA per 128 or 256 rows of a group and per key
+ * range (D = 256: 128 rows per CTA, 64-key tiles).  The fp8 cache takes the 128-row kernels,
+ * whose converter warps dequantise each key tile (code x scale, exact) into the bf16 tile the
+ * bf16 kernel reads: their results equal, bit for bit, those of the bf16 cache holding the
+ * dequantised values; where a mode below names 256 rows, the fp8 cache and D = 256 take 128.
+ * Key ranges
  * (num_splits = 0): when the groups' CTAs are fewer than the SMs, SMs / CTAs ranges per
  * group (one wave), else ranges of at most 8192 keys; num_splits > 0 sets the count.  A
  * group with several ranges merges them in the kernel through the workspace.  A group of

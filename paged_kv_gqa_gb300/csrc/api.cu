@@ -217,7 +217,7 @@ struct MultiRows {
 };
 
 // Several rows per sequence with more than 32 rows per (sequence, kv head) group (the routing
-// of tensor_core_rows), D = 128 (or 256 on a bf16 cache), scale > 0: a tensor-core kernel, one
+// of tensor_core_rows), D = 128 or 256, scale > 0: a tensor-core kernel, one
 // CTA per cta_rows (128: prefill_tc_kernel.cuh, bf16 or fp8 cache, or prefill_tc256_kernel.cuh
 // at D = 256; 256: prefill_tc2_kernel.cuh, bf16) rows and key split (tc_split_plan).
 // With one split the workspace holds only the status word; with several, also the split
@@ -228,10 +228,10 @@ pkv_status prefill_tc(const pkv_bf16 *q, const void *k_cache, const void *v_cach
                       size_t workspace_bytes, int num_splits, const MultiRows &mr, int device, int sms,
                       cudaStream_t stream, int cta_rows, int D)
 {
-    if (fp8.on && cta_rows != kTcRows) return PKV_ERR_UNSUPPORTED;  // the fp8 cache has the 128-row kernel only
-    if (D != 128 && (D != 256 || fp8.on || cta_rows != kTcRows)) return PKV_ERR_UNSUPPORTED;
+    if (fp8.on && cta_rows != kTcRows) return PKV_ERR_UNSUPPORTED;  // the fp8 cache has 128-row kernels only
+    if (D != 128 && (D != 256 || cta_rows != kTcRows)) return PKV_ERR_UNSUPPORTED;
     const bool two = cta_rows == kTc2Rows;
-    const int variant = D == 256 ? 3 : fp8.on ? 2 : two ? 1 : 0;
+    const int variant = D == 256 ? (fp8.on ? 4 : 3) : fp8.on ? 2 : two ? 1 : 0;
     const TcSplit sp =
         tc_split_plan(B, Hq, Hkv, page_size, max_pages, mr.total_q, mr.max_q_len, num_splits, cta_rows, sms, D);
     if (workspace_bytes < sp.ws.total) return PKV_ERR_WORKSPACE_TOO_SMALL;
@@ -247,15 +247,17 @@ pkv_status prefill_tc(const pkv_bf16 *q, const void *k_cache, const void *v_cach
     const int G = Hq / Hkv;
     const long q_tiles = sp.q_tiles;
     if ((long)Hkv * q_tiles >= (1l << 31) || B > 65535) return PKV_ERR_UNSUPPORTED;
-    static bool attr_set[4][64] = {};
+    static bool attr_set[5][64] = {};
     static std::mutex mu;
     if (device < 0 || device >= 64) return PKV_ERR_UNSUPPORTED;
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!attr_set[variant][device]) {
             const cudaError_t e =
-                variant == 3 ? cudaFuncSetAttribute(prefill_tc256_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                    T256Smem::dynamic)
+                variant == 4 ? cudaFuncSetAttribute(prefill_tc256_kernel<true>,
+                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, T2568Smem::dynamic)
+                : variant == 3 ? cudaFuncSetAttribute(prefill_tc256_kernel<false>,
+                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, T256Smem::dynamic)
                 : variant == 1 ? cudaFuncSetAttribute(prefill_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                       Tc2Smem::dynamic)
                 : variant == 2 ? cudaFuncSetAttribute(prefill_tc_kernel<true>,
@@ -298,9 +300,10 @@ pkv_status prefill_tc(const pkv_bf16 *q, const void *k_cache, const void *v_cach
     p.wait_limit_ns = kWaitLimitNs;
     const dim3 grid((unsigned)(Hkv * q_tiles), (unsigned)sp.splits, (unsigned)B);
     const cudaError_t e =
-        variant == 3
-            ? launch_kernel(prefill_tc256_kernel, grid, dim3(kT256Threads), (size_t)T256Smem::dynamic, stream, mk, mv,
-                            p)
+        variant == 4 ? launch_kernel(prefill_tc256_kernel<true>, grid, dim3(kT2568Threads), (size_t)T2568Smem::dynamic,
+                                     stream, mk, mv, p)
+        : variant == 3 ? launch_kernel(prefill_tc256_kernel<false>, grid, dim3(kT256Threads),
+                                       (size_t)T256Smem::dynamic, stream, mk, mv, p)
         : variant == 1
             ? launch_kernel(prefill_tc2_kernel, grid, dim3(kTc2Threads), (size_t)Tc2Smem::dynamic, stream, mk, mv, p)
         : variant == 2 ? launch_kernel(prefill_tc_kernel<true>, grid, dim3(kTc8Threads), (size_t)Tc8Smem::dynamic,
@@ -383,10 +386,10 @@ pkv_status decode_impl(const pkv_bf16 *q, const void *k_cache, const void *v_cac
     int device = 0, sms = 0;
     pkv_status st = current_device_sms(&device, &sms);
     if (st != PKV_OK) return st;
-    if (mq && (D == 128 || (D == 256 && !kv8)) && group_rows > kMqBlockRows && scale > 0.f) {
+    if (mq && (D == 128 || D == 256) && group_rows > kMqBlockRows && scale > 0.f) {
         int tc_rows = tensor_core_rows(g_prefill_tc.load(std::memory_order_relaxed), B, Hq, Hkv, page_size,
                                        max_pages, mr, num_splits, group_rows, sms);
-        // the fp8 cache: the 128-row kernel's fp8 instantiation; D = 256: the 128-row kernel of 64-key tiles
+        // the fp8 cache: the 128-row kernels' fp8 instantiations; D = 256: the 128-row kernel of 64-key tiles
         if ((kv8 || D == 256) && tc_rows) tc_rows = kTcRows;
         if (tc_rows)
             return prefill_tc(q, k_cache, v_cache, fp8, block_table, seq_lens, B, Hq, Hkv, page_size, num_pages,
@@ -670,9 +673,9 @@ pkv_status pkv_plan_query_prefill(int B, int Hq, int Hkv, int D, int page_size, 
     const pkv_status st = make_plan(B, Hq, Hkv, D, page_size, max_pages, num_sms, num_splits, plan,
                                     kv_dtype == PKV_KV_FP8_E4M3, group_rows, (long)total_q * Hq);
     const bool kv8 = kv_dtype == PKV_KV_FP8_E4M3;
-    if (st != PKV_OK || !(D == 128 || (D == 256 && !kv8)) || group_rows <= kMqBlockRows) return st;
+    if (st != PKV_OK || !(D == 128 || D == 256) || group_rows <= kMqBlockRows) return st;
     // the tensor-core kernels may take the call: room for their split partials too (the fp8
-    // cache and D = 256 have the 128-row kernel only), whatever the routing when the call is made
+    // cache and D = 256 have 128-row kernels only), whatever the routing when the call is made
     for (int rows : {kTcRows, kTc2Rows}) {
         if ((kv8 || D == 256) && rows != kTcRows) continue;
         const TcSplit sp =
@@ -694,14 +697,18 @@ pkv_status pkv_plan_query_prefill(int B, int Hq, int Hkv, int D, int page_size, 
         plan->num_splits = sp.splits;
         plan->chunk_tokens = sp.chunk_tiles * tc_tile_keys(D);
         plan->stage_tokens = tc_tile_keys(D);
-        plan->warps = (d256 ? kT256Threads : tc_rows == kTc2Rows ? kTc2Threads : kv8 ? kTc8Threads : kTcThreads) / 32;
-        plan->ring_stages = d256                 ? kT256KStages
+        plan->warps = (d256 ? (kv8 ? kT2568Threads : kT256Threads)
+                       : tc_rows == kTc2Rows ? kTc2Threads
+                       : kv8                 ? kTc8Threads
+                                             : kTcThreads) /
+                      32;
+        plan->ring_stages = d256                 ? (kv8 ? T256Cfg<true>::k_stages : T256Cfg<false>::k_stages)
                             : tc_rows == kTc2Rows ? kTc2KStages
                             : kv8                 ? TcCfg<true>::k_stages
                                                   : TcCfg<false>::k_stages;
         plan->blocks_per_sm = 1;
         plan->grid_blocks = (int)((long)Hkv * sp.q_tiles * sp.splits * B);
-        plan->smem_bytes = d256                 ? T256Smem::dynamic
+        plan->smem_bytes = d256                 ? (kv8 ? T2568Smem::dynamic : T256Smem::dynamic)
                            : tc_rows == kTc2Rows ? Tc2Smem::dynamic
                            : kv8                 ? Tc8Smem::dynamic
                                                  : TcSmem::dynamic;

@@ -2,13 +2,15 @@
 //
 // The 128-row design of prefill_tc_kernel.cuh (a kv-head group's (token, head) rows packed
 // token-major against the group's paged keys; AstrAI "CUDA Kernels", "Q Scheduling and KV
-// Addressing") for D = 256 on a bf16 cache.  The tiles are 64 keys instead of 128, so that Q
+// Addressing") for D = 256, on a bf16 cache or (KV8) an fp8 one.  The tiles are 64 keys instead of 128, so that Q
 // (128 rows x 256 dims), two K stages and two V stages of 64 keys x 256 dims fit in shared
 // memory, and S, O (256 columns) and the row sums fit in tensor memory:
 //   warps 0-3  softmax (thread r = row r = TMEM lane r)
 //   warp 4     MMAs (one lane issues)
 //   warp 5     K copies (TMA, lane 4x + h: 64-dim block h of page box x)
 //   warp 6     V copies (TMA, lane x: page box x, all four 64-dim blocks)
+//   warps 7-10 (fp8 only) converters: the codes and scales warps 5-6 stage, dequantised to bf16
+//              tiles in the layout the bf16 copies land
 // S = Q K^T: M = 128 rows, N = 64 keys, K = 256 (sixteen 16-deep MMAs, Q and K K-major,
 // 128B-swizzled); O += P V: N = 256 dims, K = 64 keys (P from tensor memory, V read MN-major
 // in the layout one copy per page box lands: [box][4 dim blocks][keys][64]); the row sums of
@@ -32,27 +34,51 @@
 namespace pkv {
 
 constexpr int kT256Keys = 64;        // keys per tile
-constexpr int kT256Threads = 224;    // 4 softmax warps, the MMA warp, the K and V copy warps
-constexpr int kT256KStages = 2;
-constexpr int kT256VStages = 2;
+
+// Per cache type: threads, bf16 K and V stages, fp8 staging stages.  bf16: 4 softmax warps,
+// the MMA warp, the K and V copy warps; K and V land by TMA straight into two stages each.
+// fp8: the copy warps land the e4m3 codes and scales in two staging stages, and two K and two
+// V converter warps (7-8, 9-10) write them, dequantised to bf16, into one K and one V stage in
+// the layout the bf16 copies land (two bf16 stages each do not fit beside the staging).
+template <bool KV8>
+struct T256Cfg {
+    static constexpr int threads = KV8 ? 352 : 224;
+    static constexpr int k_stages = KV8 ? 1 : 2;
+    static constexpr int v_stages = KV8 ? 1 : 2;
+    static constexpr int s8_stages = KV8 ? 2 : 0;
+};
+constexpr int kT256Threads = T256Cfg<false>::threads;
+constexpr int kT2568Threads = T256Cfg<true>::threads;
+constexpr int kT256KStages = T256Cfg<false>::k_stages;
 
 // Shared memory (bytes from a 1024-aligned base).
-struct T256Smem {
+template <bool KV8>
+struct T256SmemT {
     static constexpr int kQBlk = kTcRows * 128;                  // one 64-dim block of Q: 128 rows x 128 B
     static constexpr int kKBlk = kT256Keys * 128;                // one 64-dim block of a K tile: 64 keys x 128 B
     static constexpr int kStage = kT256Keys * 256 * 2;           // a K or V tile: 64 keys x 256 dims bf16
+    static constexpr int kCodes = kT256Keys * 256;               // 64 keys x 256 e4m3 codes
     static constexpr int q = 0;                                  // [4 blocks][128 rows][128 B]
     static constexpr int k = 4 * kQBlk;                          // K stage s at k + s * kStage: [4][64][128 B]
-    static constexpr int v = k + kT256KStages * kStage;          // V stage s: [box][4][box keys][128 B]
-    static constexpr int ones = v + kT256VStages * kStage;       // 16 x 64 bf16 ones, the B operand of the row-sum MMA
-    static constexpr int bars = ones + 2048;                     // 32 mbarriers
+    static constexpr int v = k + T256Cfg<KV8>::k_stages * kStage;  // V stage s: [box][4][box keys][128 B]
+    static constexpr int ones = v + T256Cfg<KV8>::v_stages * kStage;  // 16 x 64 bf16 ones, the row-sum MMA's B
+    // fp8 staging stage s at s8 + s * 2 kCodes: [K codes][V codes], each as the page boxes land
+    // ([box][2 blocks of 128 codes][box keys][128 B], 128B-swizzled); its scales at sc8 + s * 512:
+    // [K 64][V 64] f32
+    static constexpr int s8 = (ones + 2048 + 1023) / 1024 * 1024;
+    static constexpr int sc8 = s8 + T256Cfg<KV8>::s8_stages * 2 * kCodes;
+    static constexpr int bars = sc8 + T256Cfg<KV8>::s8_stages * 2 * kT256Keys * 4;  // 32 mbarriers
     static constexpr int pages = bars + 32 * 8;                  // [kTcPageRing][16] page id of each box, -1: none
     static constexpr int tmem_slot = pages + kTcPageRing * 16 * 4;
     static constexpr int total = tmem_slot + 16;
     static constexpr int dynamic = total;                        // the dynamic shared memory starts 1024-aligned
 };
-static_assert(T256Smem::dynamic <= 232448, "prefill_tc256_kernel: shared memory above the per-block limit");
-static_assert(T256Smem::bars % 1024 == 0, "prefill_tc256_kernel: tiles must stay 1024-aligned");
+using T256Smem = T256SmemT<false>;
+using T2568Smem = T256SmemT<true>;
+static_assert(T256Smem::dynamic <= 232448 && T2568Smem::dynamic <= 232448,
+              "prefill_tc256_kernel: shared memory above the per-block limit");
+static_assert(T256Smem::ones % 1024 == 0 && T2568Smem::ones % 1024 == 0,
+              "prefill_tc256_kernel: tiles must stay 1024-aligned");
 
 // A split's row result into the partials (O / lt in f32); o holds dims 32 cb .. 32 cb + 31 of
 // a 256-dim row.
@@ -118,13 +144,19 @@ __device__ __forceinline__ void t256_merge_row_warp(const PrefillTcParams &p, in
     if (lane == 0 && p.lse) p.lse[grow] = m == ninf ? ninf : m + __logf(wsum);
 }
 
-__global__ void __launch_bounds__(kT256Threads, 1)
+template <bool KV8>
+__global__ void __launch_bounds__(T256Cfg<KV8>::threads, 1)
     prefill_tc256_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                          const PrefillTcParams p)
 {
+    using Smem = T256SmemT<KV8>;
     constexpr int D = 256;
     constexpr int KT = kT256Keys;
-    constexpr int kQBlk = T256Smem::kQBlk, kKBlk = T256Smem::kKBlk, kStage = T256Smem::kStage;
+    constexpr int kThreads = T256Cfg<KV8>::threads;
+    constexpr int kKStages = T256Cfg<KV8>::k_stages, kVStages = T256Cfg<KV8>::v_stages;
+    constexpr int kS8Stages = T256Cfg<KV8>::s8_stages;
+    constexpr int kS8Div = kS8Stages > 0 ? kS8Stages : 1;  // the bf16 instantiation compiles the fp8 roles too
+    constexpr int kQBlk = Smem::kQBlk, kKBlk = Smem::kKBlk, kStage = Smem::kStage, kCodes = Smem::kCodes;
     const float kNegInf = __int_as_float(0xff800000);
     constexpr float kRescaleGap = 8.f;   // move the reference maximum only past 2^8
     // a sequence's last query tiles (the longest under the causal mask) are launched first
@@ -178,34 +210,48 @@ __global__ void __launch_bounds__(kT256Threads, 1)
         if (tid == 0) atomicCAS(p.status, 0, PKV_ERR_UNSUPPORTED);
         return;
     }
-    const uint32_t sQ = base + T256Smem::q, sOnes = base + T256Smem::ones;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + T256Smem::bars);
-    int *sm_pg = reinterpret_cast<int *>(smem_raw + T256Smem::pages);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem_raw + T256Smem::tmem_slot);
+    const uint32_t sQ = base + Smem::q, sOnes = base + Smem::ones;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw + Smem::bars);
+    int *sm_pg = reinterpret_cast<int *>(smem_raw + Smem::pages);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem_raw + Smem::tmem_slot);
     auto bar = [&](int i) { return smem_addr(&bars[i]); };
-    constexpr int kKFull = 0, kKEmpty = kKFull + kT256KStages, kVFull = kKEmpty + kT256KStages,
-                  kVEmpty = kVFull + kT256VStages, kSFull = kVEmpty + kT256VStages, kSFree = kSFull + 2,
+    constexpr int kKFull = 0, kKEmpty = kKFull + kKStages, kVFull = kKEmpty + kKStages,
+                  kVEmpty = kVFull + kVStages, kSFull = kVEmpty + kVStages, kSFree = kSFull + 2,
                   kPFull = kSFree + 2, kODone = kPFull + 1, kDrain = kODone + 1, kQFull = kDrain + 1,
-                  kBarEnd = kQFull + 1;
+                  kK8Full = kQFull + 1, kK8Empty = kK8Full + kS8Stages, kV8Full = kK8Empty + kS8Stages,
+                  kV8Empty = kV8Full + kS8Stages, kBarEnd = kV8Empty + kS8Stages;
     static_assert(kBarEnd <= 32, "prefill_tc256_kernel: more mbarriers than the shared-memory slots");
     auto k_full = [&](int s) { return bar(kKFull + s); };
     auto k_empty = [&](int s) { return bar(kKEmpty + s); };
     auto v_full = [&](int s) { return bar(kVFull + s); };
     auto v_empty = [&](int s) { return bar(kVEmpty + s); };
+    auto k8_full = [&](int s) { return bar(kK8Full + s); };    // fp8: codes and scales of a staging stage landed
+    auto k8_empty = [&](int s) { return bar(kK8Empty + s); };  // fp8: the converters have read the stage
+    auto v8_full = [&](int s) { return bar(kV8Full + s); };
+    auto v8_empty = [&](int s) { return bar(kV8Empty + s); };
     auto s_full = [&](int s) { return bar(kSFull + s); };
     auto s_free = [&](int s) { return bar(kSFree + s); };
     const uint32_t p_full = bar(kPFull), o_done = bar(kODone), drain = bar(kDrain), q_full = bar(kQFull);
-    auto sK = [&](int s) { return base + T256Smem::k + (uint32_t)(s * kStage); };
-    auto sV = [&](int s) { return base + T256Smem::v + (uint32_t)(s * kStage); };
+    auto sK = [&](int s) { return base + Smem::k + (uint32_t)(s * kStage); };
+    auto sV = [&](int s) { return base + Smem::v + (uint32_t)(s * kStage); };
+    auto s8 = [&](int s) { return base + Smem::s8 + (uint32_t)(s * 2 * kCodes); };       // fp8 staging codes
+    auto sc8 = [&](int s) { return base + Smem::sc8 + (uint32_t)(s * 2 * KT * 4); };     // fp8 staging scales
 
     if (tid == 0) {
-        for (int s = 0; s < kT256KStages; ++s) {
-            mbar_init(k_full(s), 1);
+        // bf16: a full K/V stage is the copy lane's expect_tx; fp8: one arrival per converter warp
+        for (int s = 0; s < kKStages; ++s) {
+            mbar_init(k_full(s), KV8 ? 2 : 1);
             mbar_init(k_empty(s), 1);
         }
-        for (int s = 0; s < kT256VStages; ++s) {
-            mbar_init(v_full(s), 1);
+        for (int s = 0; s < kVStages; ++s) {
+            mbar_init(v_full(s), KV8 ? 2 : 1);
             mbar_init(v_empty(s), 1);
+        }
+        for (int s = 0; s < kS8Stages; ++s) {
+            mbar_init(k8_full(s), 1);
+            mbar_init(k8_empty(s), 2);
+            mbar_init(v8_full(s), 1);
+            mbar_init(v8_empty(s), 2);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(s_full(s), 2);  // the MMA's commit + the issuing lane (publishes the tile's page ids)
@@ -233,12 +279,107 @@ __global__ void __launch_bounds__(kT256Threads, 1)
     const int nbox = KT / box_t;       // 1 .. 8
     bool failed = false;
 
-    if (warp >= 5 && n_tiles > 0) {
+    if (KV8 && warp >= 7 && n_tiles > 0) {
+        // ---- fp8 converter warps: 7-8 write K tiles, 9-10 V tiles.  A task is 16 codes (one
+        // 16-byte chunk of a key row): read from the staging box (128B-swizzled), scaled to bf16,
+        // and stored as the two 16-byte chunks the bf16 copies would land
+        const bool is_k = warp < 9;
+        const int ct = (warp - (is_k ? 7 : 9)) * 32 + lane;  // 0..63
+        for (int j = 0; j < n_tiles; ++j) {
+            const int st8 = j % kS8Div;
+            const bool ok = mbar_wait_bounded(is_k ? k8_full(st8) : v8_full(st8), (uint32_t)((j / kS8Div) & 1),
+                                              p.wait_limit_ns) &&
+                            (is_k ? (j < kKStages || mbar_wait_bounded(k_empty(j % kKStages),
+                                                                        (uint32_t)((j / kKStages - 1) & 1),
+                                                                        p.wait_limit_ns))
+                                  : (j < kVStages || mbar_wait_bounded(v_empty(j % kVStages),
+                                                                        (uint32_t)((j / kVStages - 1) & 1),
+                                                                        p.wait_limit_ns)));
+            if (!__all_sync(0xffffffffu, ok)) {
+                failed = true;
+                break;
+            }
+            const uint32_t src = s8(st8) + (is_k ? 0u : (uint32_t)kCodes);
+            const uint32_t scl = sc8(st8) + (is_k ? 0u : (uint32_t)(KT * 4));
+            const uint32_t dst = is_k ? sK(j % kKStages) : sV(j % kVStages);
+#pragma unroll 4
+            for (int t = ct; t < KT * 16; t += 64) {
+                const int key = t >> 4, ch = t & 15;
+                const int bx = key >> log2box, r = key & (box_t - 1);
+                // codes: [box][2 blocks of 128][box keys][128 B], swizzled on the key within the box
+                const uint4 c = tc_ld_shared_v4(src + (uint32_t)(bx * box_t * 256 + (ch >> 3) * box_t * 128 + r * 128 +
+                                                                  (((ch & 7) ^ (r & 7)) << 4)));
+                uint32_t o[8];
+                e4m3x16_scaled_to_bf16(c, ld_shared_f32(scl + (uint32_t)(key * 4)), o);
+                // dims 16 ch .. 16 ch + 15: 64-dim block ch / 4, chunks 2 (ch % 4) and the next.
+                // K: [block][key][128 B]; V: [box][block][box key][128 B]
+                const int dc = ch >> 2, c16 = (ch & 3) * 2, sw = is_k ? (key & 7) : (r & 7);
+                const uint32_t row = is_k ? dst + (uint32_t)(dc * kKBlk + key * 128)
+                                          : dst + (uint32_t)(bx * box_t * 512 + dc * box_t * 128 + r * 128);
+                st_shared_v4(row + (uint32_t)((c16 ^ sw) << 4), o[0], o[1], o[2], o[3]);
+                st_shared_v4(row + (uint32_t)(((c16 + 1) ^ sw) << 4), o[4], o[5], o[6], o[7]);
+            }
+            fence_proxy_async_shared();  // the MMAs read the tile through the async proxy
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(is_k ? k_full(j % kKStages) : v_full(j % kVStages));
+                mbar_arrive(is_k ? k8_empty(st8) : v8_empty(st8));
+            }
+        }
+    } else if (KV8 && (warp == 5 || warp == 6) && n_tiles > 0) {
+        // ---- fp8 copy warps: warp 5 lands K codes and scales, warp 6 V's, in the staging
+        // stages; lane x copies box x (box_t keys of one page: one code box, one scale run)
+        const bool is_k = warp == 5;
+        const uint64_t policy = l2_policy_evict_first();
+        const int x = lane;
+        auto fetch = [&](int j) {
+            const int key = (t0 + j) * KT + x * box_t;
+            return (x < nbox && j < n_tiles && key < n_keys) ? p.block_table[(size_t)b * p.max_pages + (key >> p.log2P)]
+                                                            : -1;
+        };
+        int raw = fetch(0);
+        int issued = 0;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int st = j % kS8Div;
+            const int next_raw = fetch(j + 1);
+            const bool has_key = x < nbox && (t0 + j) * KT + x * box_t < n_keys;
+            const int pg = has_key && (unsigned)raw < (unsigned)p.num_pages ? raw : -1;
+            if (is_k && has_key && pg < 0) atomicCAS(p.status, 0, PKV_ERR_BAD_PAGE_INDEX);
+            const uint32_t ok = __ballot_sync(0xffffffffu, pg >= 0);
+            if (j >= kS8Stages &&
+                !__all_sync(0xffffffffu, mbar_wait_bounded(is_k ? k8_empty(st) : v8_empty(st),
+                                                           (uint32_t)((j / kS8Div - 1) & 1), p.wait_limit_ns))) {
+                failed = true;
+                break;
+            }
+            if (is_k) {  // publish the tile's page ids (read by the softmax and the MMA warp)
+                if (x < nbox) sm_pg[(j % kTcPageRing) * 16 + x] = pg;
+                __syncwarp();
+            }
+            const uint32_t full = is_k ? k8_full(st) : v8_full(st);
+            if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)__popc(ok) * (uint32_t)box_t * (256u + 4u));
+            __syncwarp();
+            if (pg >= 0) {
+                const int slot = ((t0 + j) * KT + x * box_t) & (p.P - 1);
+                tma_load_4d(s8(st) + (is_k ? 0u : (uint32_t)kCodes) + (uint32_t)(x * box_t * 256), is_k ? &tmK : &tmV,
+                            0, pg * p.P + slot, 0, kvh, full, policy);
+                bulk_copy_g2s(sc8(st) + (is_k ? 0u : (uint32_t)(KT * 4)) + (uint32_t)(x * box_t * 4),
+                              (is_k ? p.k_scale : p.v_scale) + ((size_t)pg * p.Hkv + kvh) * p.P + slot,
+                              (uint32_t)box_t * 4u, full);
+            }
+            issued = j + 1;
+            raw = next_raw;
+        }
+        // the last copies have landed before the CTA exits (consumed, or waited for here)
+        for (int t = max(0, issued - kS8Stages); t < issued; ++t)
+            mbar_wait_bounded(is_k ? k8_full(t % kS8Div) : v8_full(t % kS8Div), (uint32_t)((t / kS8Div) & 1),
+                              p.wait_limit_ns);
+    } else if (!KV8 && warp >= 5 && n_tiles > 0) {
         // ---- copy warps: warp 5 streams K into its stages (lane 4x + h: 64-dim block h of box
         // x), warp 6 V (lane x: box x, all four blocks); the block-table entry of each box is read
         // a tile before its use
         const bool is_k = warp == 5;
-        const int stages = is_k ? kT256KStages : kT256VStages;
+        const int stages = is_k ? kKStages : kVStages;
         const uint64_t policy = l2_policy_evict_first();
         const int x = is_k ? lane >> 2 : lane, dc = is_k ? lane & 3 : 0;
         auto fetch = [&](int j) {
@@ -299,7 +440,7 @@ __global__ void __launch_bounds__(kT256Threads, 1)
             bool bad = false;  // a missing page among the keys before that
             for (int bx = 0; bx < nbox; ++bx) bad |= ids[bx] < 0 && (bx << log2box) < first_past;
             if (first_past == KT && !bad) return;
-            const uint32_t dst = sV(j % kT256VStages) + (uint32_t)((lane >> 3) * box_t * 128 + (lane & 7) * 16);
+            const uint32_t dst = sV(j % kVStages) + (uint32_t)((lane >> 3) * box_t * 128 + (lane & 7) * 16);
             auto zero_key = [&](int k) {
                 st_shared_v4(dst + (uint32_t)((k >> log2box) * box_t * 512 + (k & (box_t - 1)) * 128), 0u, 0u, 0u, 0u);
             };
@@ -325,10 +466,10 @@ __global__ void __launch_bounds__(kT256Threads, 1)
         constexpr uint32_t kIdL = tc_idesc_bf16(kTcRows, 16, false);
         for (int j = 0; j <= n_tiles; ++j) {
             if (j < n_tiles) {  // S(j) = Q K(j)^T into S buffer j & 1
-                const int ks = j % kT256KStages, sb = j & 1;
+                const int ks = j % kKStages, sb = j & 1;
                 if (!__all_sync(0xffffffffu,
                                 (j > 0 || mbar_wait_bounded(q_full, 0, p.wait_limit_ns)) &&
-                                    mbar_wait_bounded(k_full(ks), (uint32_t)((j / kT256KStages) & 1),
+                                    mbar_wait_bounded(k_full(ks), (uint32_t)((j / kKStages) & 1),
                                                       p.wait_limit_ns) &&
                                     (j < 2 || mbar_wait_bounded(s_free(sb), (uint32_t)(((j >> 1) - 1) & 1),
                                                                 p.wait_limit_ns)))) {
@@ -351,8 +492,8 @@ __global__ void __launch_bounds__(kT256Threads, 1)
                 __syncwarp();
             }
             if (j >= 1) {  // O += P(j-1) V(j-1)
-                const int t = j - 1, vs = t % kT256VStages;
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(v_full(vs), (uint32_t)((t / kT256VStages) & 1),
+                const int t = j - 1, vs = t % kVStages;
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(v_full(vs), (uint32_t)((t / kVStages) & 1),
                                                                p.wait_limit_ns))) {
                     failed = true;
                     break;
@@ -536,7 +677,7 @@ __global__ void __launch_bounds__(kT256Threads, 1)
     }
     if (!direct) {  // the group's last split to finish merges the partials (also after a timeout,
                     // so the counter returns to 0 for the next call)
-        int *last = reinterpret_cast<int *>(smem_raw + T256Smem::tmem_slot + 4);
+        int *last = reinterpret_cast<int *>(smem_raw + Smem::tmem_slot + 4);
         __threadfence();
         __syncthreads();
         if (tid == 0)
@@ -545,7 +686,7 @@ __global__ void __launch_bounds__(kT256Threads, 1)
         __syncthreads();
         if (*last) {  // every warp merges rows warp, warp + W, ... of this CTA
             __threadfence();
-            for (int cr = warp; cr < nrows; cr += kT256Threads / 32) {
+            for (int cr = warp; cr < nrows; cr += kThreads / 32) {
                 const int rt = (row0 + cr) / G, rh = (row0 + cr) % G;
                 t256_merge_row_warp(p, n_chunks, (size_t)(q_base + rt) * p.Hq + kvh * G + rh, lane);
             }

@@ -410,8 +410,8 @@ def test_plan_reports_cluster_merge(lib):
 
 
 def test_prefill_plan_at_head_dim_256(lib):
-    # D = 256 on a bf16 cache: groups of more than 32 rows may take the 128-row tensor-core kernel of
-    # 64-key tiles; the fp8 cache at D = 256 stays on the mma.sync kernel
+    # D = 256: groups of more than 32 rows may take the 128-row tensor-core kernel of 64-key tiles
+    # (on the fp8 cache its instantiation with converter warps)
     try:
         pkv.set_prefill_tensor_cores("auto")
         p = pkv.prefill_plan_query(256, 32, 2, 256, 64, 32, 256 * 8, 8, 152)  # 128 rows per group
@@ -423,7 +423,8 @@ def test_prefill_plan_at_head_dim_256(lib):
             if q["num_splits"] > 1:
                 assert q["workspace_bytes"] >= q["num_splits"] * 18 * 16 * 256 * 4
         p8 = pkv.prefill_plan_query(256, 32, 2, 256, 64, 32, 256 * 8, 8, 152, cache="fp8")
-        assert p8["rows_per_block"] <= 32
+        assert p8["rows_per_block"] == 128 and p8["stage_tokens"] == 64 and p8["warps"] == 11, p8
+        assert p8["smem_bytes"] <= 232448 and p8["ring_stages"] == 1
         pkv.set_prefill_tensor_cores("off")
         assert pkv.prefill_plan_query(256, 32, 2, 256, 64, 32, 256 * 8, 8, 152)["rows_per_block"] <= 32
     finally:

@@ -461,3 +461,89 @@ def test_d256_tensor_core_path_at_full_size():
     eo, el = compare(case, out, lse, select=rows)
     assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
     assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+
+
+# fp8 cache at D = 256: the same kernel's instantiation with converter warps (codes and scales
+# staged by TMA, dequantised to bf16 tiles in the layout the bf16 copies land)
+
+@pytest.mark.parametrize("mode", ["always", "auto"])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("B,Hq,Hkv,D,P,q_lens,kv_lens", TC256, ids=lambda x: str(x).replace(" ", ""))
+def test_fp8_tensor_core_path_d256(B, Hq, Hkv, D, P, q_lens, kv_lens, causal, mode):
+    # against the fp8 oracle, and bit for bit the bf16 kernel on the dequantised cache where the
+    # call took the tensor cores (the converters write exactly the tiles its copies land)
+    case = make_prefill_case(_spec(B, Hq, Hkv, D, P, seed=9 * B + P + sum(q_lens)), q_lens, kv_lens, poison=True)
+    pools, deq = _fp8_pools(case)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    try:
+        pkv.set_prefill_tensor_cores(mode)
+        rows = max(q_lens) * (Hq // Hkv)
+        plan = pkv.prefill_plan_query(B, Hq, Hkv, D, P, case.max_pages, case.q.shape[0], max(q_lens), sms, cache="fp8")
+        takes_tc = rows > 32 and (mode == "always" or rows >= 128 or case.max_pages * P >= 8192)
+        assert (plan["rows_per_block"] == 128 and plan["stage_tokens"] == 64) == takes_tc, plan
+        out, lse = run_prefill(case, causal=causal, fp8=pools)
+        eo, el = compare(case, out, lse, causal=causal, fp8=pools)
+        assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+        if takes_tc:
+            ref_o, ref_l = run_prefill(deq, causal=causal)
+            assert torch.equal(out.view(torch.int16), ref_o.view(torch.int16)) and torch.equal(lse, ref_l)
+    finally:
+        pkv.set_prefill_tensor_cores("auto")
+
+
+@pytest.mark.parametrize("splits", [0, 3, 16])
+def test_fp8_d256_tensor_core_key_splits_and_bad_page(splits):
+    case = make_prefill_case(_spec(2, 32, 2, 256, 16, seed=53), [8, 4], [9000, 300], poison=True)
+    pools, deq = _fp8_pools(case)
+    try:
+        pkv.set_prefill_tensor_cores("always")
+        out, lse = run_prefill(case, num_splits=splits, fp8=pools)
+        rows = [(t, h) for t in range(12) for h in (0, 7, 31)]
+        eo, el = compare(case, out, lse, fp8=pools, select=rows)
+        assert eo <= OUT_TOL and el <= LSE_TOL, (splits, eo, el)
+        ref_o, ref_l = run_prefill(deq, num_splits=splits)
+        assert torch.equal(out.view(torch.int16), ref_o.view(torch.int16)) and torch.equal(lse, ref_l)
+        out2, _ = run_prefill(case, num_splits=splits, fp8=pools)  # the merge counters return to 0
+        assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+        bad = Case(**case.__dict__)
+        bt = case.block_table.clone()
+        bt[1, 2] = case.num_pages + 3
+        bad.block_table = bt
+        o_bad, _ = run_prefill(bad, num_splits=splits, fp8=pools, expect_status=-6)
+        assert torch.equal(o_bad[:8].view(torch.int16), out[:8].view(torch.int16))  # request 0 untouched
+        assert torch.isfinite(o_bad.float()).all()
+    finally:
+        pkv.set_prefill_tensor_cores("auto")
+
+
+def test_fp8_d256_tensor_core_path_at_full_size():
+    # the big-page G = 16 workload on the fp8 cache with 8 new tokens per sequence (128 rows per
+    # group): auto takes the D = 256 tensor-core kernel; sampled rows against the fp8 oracle, a
+    # second call equal bit for bit
+    from workloads import CONFIGS, draw_seq_lens
+    spec = CONFIGS["bigpage_g16"]
+    kv = draw_seq_lens(spec["lens"], spec["B"], spec["P"], spec["seed"])
+    case = make_prefill_case("bigpage_g16", [8] * spec["B"], kv)
+    _, k, v, _, _ = case.host_bits()
+    k8, ks = oracle.quantize_pool(k)
+    v8, vs = oracle.quantize_pool(v)
+    del k, v
+    pools = (k8, v8, ks, vs)
+    dcase = case.to("cuda")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    pkv.set_prefill_tensor_cores("auto")
+    plan = pkv.prefill_plan_query(case.B, case.Hq, case.Hkv, case.D, case.P, case.max_pages, case.q.shape[0], 8, sms,
+                                  cache="fp8")
+    assert plan["rows_per_block"] == 128 and plan["stage_tokens"] == 64 and plan["warps"] == 11, plan
+    out, lse = run_prefill(dcase, fp8=pools)
+    out2, lse2 = run_prefill(dcase, fp8=pools)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))
+    total_q = case.q.shape[0]
+    rows = [(t, h) for t in range(0, total_q, max(1, total_q // 16)) for h in (0, 17, case.Hq - 1)]
+    rows += [(total_q - 1, 5)]
+    eo, el = compare(case, out, lse, fp8=pools, select=rows)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    del case, dcase, pools, out, lse, out2, lse2
+    torch.cuda.empty_cache()
