@@ -453,6 +453,8 @@ def run_pkv(args) -> None:
         case = make_case(args.workload, device=dev)
     fp8 = args.cache == "fp8"
     pkv.set_prefill_tensor_cores({0: "off", 1: "auto", 2: "always", 3: "rows128"}[getattr(args, "tc", 1)])
+    if getattr(args, "cluster_merge", None) is not None:
+        pkv.set_cluster_merge(bool(args.cluster_merge))
     pools8 = None
     if fp8:  # quantise the pools on the device, then drop the bf16 copies
         pools8 = pkv.quantize_pool_fp8(case.k_cache, case.v_cache)
@@ -857,6 +859,9 @@ def main():
     ap.add_argument("--cache", default="bf16", choices=["bf16", "fp8"])
     ap.add_argument("--q-len", type=int, default=1,
                     help="new tokens per sequence (causal multi-token step); 1 = decode")
+    ap.add_argument("--cluster-merge", type=int, default=None, choices=[0, 1],
+                    help="decode split merge through a thread-block cluster (pkv_set_cluster_merge); "
+                         "default: the library's setting")
     ap.add_argument("--tc", type=int, default=1, choices=[0, 1, 2, 3],
                     help="several-rows calls: 0 = mma.sync kernel, 1 = library routing (pkv_set_prefill_tensor_cores "
                          "auto), 2 = tensor-core kernel wherever it applies (256 rows per CTA where the group has "

@@ -30,7 +30,7 @@ namespace pkv {
 std::atomic<int> g_pdl{0};
 bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
 std::atomic<int> g_prefill_tc{PKV_TC_AUTO};
-std::atomic<int> g_cluster_merge{0};
+std::atomic<int> g_cluster_merge{1};
 bool cluster_merge_enabled() { return g_cluster_merge.load(std::memory_order_relaxed) != 0; }
 
 namespace {

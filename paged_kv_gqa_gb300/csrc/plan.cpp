@@ -111,10 +111,12 @@ pkv_status make_plan(int B, int Hq, int Hkv, int D, int page_size, int max_pages
     if (num_splits > 0) {
         S = std::min(num_splits, max_stage_splits);
     } else {
-        // About one wave of blocks: enough splits that every resident slot gets one.
-        // Fewer (larger) blocks amortise each block's fixed start-up and epilogue cost;
-        // a batch that already has a block per slot is not split at all.
+        // About one wave of blocks: enough splits that every resident slot gets one, but no
+        // more blocks than are resident at once (a second, nearly empty wave costs a whole
+        // block's time).  Fewer (larger) blocks amortise each block's fixed start-up and
+        // epilogue cost; a batch that already has a block per slot is not split at all.
         S = std::max(1, (slots + units - 1) / units);
+        if ((long)units * S > (long)num_sms * per_sm) S = std::max(1, num_sms * per_sm / units);
         // Bound the bytes of one split so that no split becomes a straggler.  Where that
         // bound sets the count and the blocks span more than one wave of resident blocks,
         // take the count in [S, 1.5 S] that fills the last wave best (measured on GB300:
