@@ -77,8 +77,12 @@
 // workspace (FlashQuant wiki "CUDA Kernels", paged_decode.cu "Partial Output";
 // here normalised and in natural log), and the last split of the (b, kv head)
 // group to finish merges the group's partials in the same launch, so no second
-// kernel and no launch gap sit on the critical path.  A split that starts past
-// L_b exits at once and is never merged ("Early Exit for Empty Splits").
+// kernel and no launch gap sit on the critical path; on a grid of one wave with
+// 2-8 splits the splits of a group form a thread-block cluster instead and send
+// their partials into split 0's shared memory, which merges them the same way.
+// A split that starts past L_b exits at once and is never merged ("Early Exit for
+// Empty Splits").  A decode group wider than one block (G = 32 at D = 256) runs on
+// the several-rows instantiation with one row per sequence (no qo_indptr).
 #pragma once
 
 #include <cuda_bf16.h>
