@@ -56,3 +56,38 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
 
     bench.run_reference(Args())
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_line_on_rank_zero(monkeypatch, capsys):
+    """The reference arm's one JSON line: the oracle timed on the host cores, with the keys the
+    bench contract names."""
+    import json
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+
+    class Args:
+        workload, cache, steps, warmup, ref_seconds = "tiny", "bf16", 2, 3, 0.25
+
+    bench.run_reference(Args())
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["steps"] == 2 and line["warmup"] == 3 and line["higher_is_better"] is True
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    assert line["config"]["workload"] == "tiny"
+
+
+def test_reference_sample_fits_its_budget():
+    """Each step's sample fits the per-step budget at the measured rate (at least one row), so
+    that a run of any step count stays within a few minutes."""
+    from workloads import make_case
+    for name in ("tiny", "batch", "ragged"):
+        case = make_case(name)
+        lens = case.seq_lens.numpy()
+        rate = 0.4e9
+        for seconds in (0.01, 0.1, 1.0):
+            rows, _, threads = bench._reference_sample(case, seconds, rate)
+            assert 1 <= len(rows) <= case.B * case.Hq and 1 <= threads <= len(rows)
+            cost = [lens[b] * case.D * 4.0 / rate for b, _ in rows]
+            per_thread = max(sum(cost[i::threads]) for i in range(threads))
+            assert len(rows) == 1 or per_thread <= seconds + 1e-12
