@@ -117,6 +117,23 @@ PKV_API int pkv_set_programmatic_launch(int enable);
 PKV_API int pkv_set_cluster_merge(int enable);
 
 /*
+ * Adaptive split count (off at load).  enable != 0: a decode call with the automatic split
+ * count (paged_decode_attn, paged_decode_attn_fp8, paged_decode_attn_ex with num_splits = 0;
+ * B <= 1024) sizes its splits on the device from the batch's actual lengths instead of the
+ * block table's width (Atlas "CUDA Kernel Engineering", "The kernel inventory": adaptive split
+ * count): every block reads the B lengths and takes chunks of about (sum of the lengths x Hkv /
+ * block slots) keys, at least 512 KiB of cache bytes (and 256 keys), at most the planned chunk,
+ * and enough that no sequence needs more than the planned split count, so the grid, the
+ * workspace and the plan stay as pkv_plan_query reports them.  It pays where the table is much
+ * wider than the sequences and there are few (sequence, kv head) groups (measured on GB300: a
+ * 131072-key table holding four sequences of 2048 keys, 29.3 -> 23.2 us); it costs a pass over
+ * the lengths in every block, the empty splits of a wide table included (16 sequences of 1000
+ * keys on the same table: 25.5 -> 30.9 us), hence off by default.  Process-wide; returns the
+ * previous setting.
+ */
+PKV_API int pkv_set_adaptive_splits(int enable);
+
+/*
  * Tensor-core path of paged_prefill_attn and paged_prefill_attn_fp8 (D = 128 or 256,
  * scale > 0, more than 32 (token, query head) rows per (sequence, kv head) group, i.e.
  * max_q_len * Hq/Hkv > 32): the score and PV products run on tcgen05 (5th-generation tensor

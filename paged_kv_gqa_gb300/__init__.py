@@ -41,7 +41,7 @@ EXPORTED_SYMBOLS = [
     "paged_kv_append", "paged_decode_attn_fp8", "paged_kv_append_fp8", "pkv_plan_query_kv",
     "paged_decode_attn_workspace_size_kv", "paged_prefill_attn", "paged_prefill_attn_fp8",
     "pkv_plan_query_prefill", "paged_prefill_attn_workspace_size", "pkv_set_programmatic_launch",
-    "pkv_set_prefill_tensor_cores", "pkv_set_cluster_merge",
+    "pkv_set_prefill_tensor_cores", "pkv_set_cluster_merge", "pkv_set_adaptive_splits",
 ]
 
 KV_DTYPES = {"bf16": 0, "fp8": 1}
@@ -101,6 +101,7 @@ def load(path: str = LIB_PATH):
             "pkv_plan_query_prefill": (I, [I, I, I, I, I, I, I, I, I, I, I, ctypes.POINTER(PkvPlan)]),
             "pkv_set_programmatic_launch": (I, [I]),
             "pkv_set_cluster_merge": (I, [I]),
+            "pkv_set_adaptive_splits": (I, [I]),
             "pkv_set_prefill_tensor_cores": (I, [I]),
             "paged_prefill_attn_workspace_size": (I, [I, I, I, I, I, I, I, I, I, I, I, ctypes.POINTER(S)]),
             "paged_kv_append_fp8": (I, [P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, P]),
@@ -127,6 +128,13 @@ def set_cluster_merge(enable: bool) -> bool:
     """Decode calls with 2-8 splits merge them inside a thread-block cluster (on, the default)
     or through the workspace (off); returns the old setting."""
     return bool(load().pkv_set_cluster_merge(int(bool(enable))))
+
+
+def set_adaptive_splits(enable: bool) -> bool:
+    """Decode calls with the automatic split count size their splits on the device from the
+    batch's actual lengths (on) or from the block table's width (off, the default); returns
+    the old setting."""
+    return bool(load().pkv_set_adaptive_splits(int(bool(enable))))
 
 
 TC_MODES = {"off": 0, "auto": 1, "always": 2, "rows128": 3}

@@ -21,7 +21,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libpkv.so")
 
-SOURCES = ["api.cu", "decode_bf16.cu", "decode_fp8.cu", "prefill_bf16.cu", "prefill_fp8.cu", "plan.cpp",
+SOURCES = ["api.cu", "decode_bf16.cu", "decode_fp8.cu", "decode_adapt_bf16.cu", "decode_adapt_fp8.cu",
+           "prefill_bf16.cu", "prefill_fp8.cu", "plan.cpp",
            "tc_plan.cpp"]
 HEADERS = ["decode_kernel.cuh", "decode_launch.cuh", "launch_util.h", "merge_kernel.cuh", "append_kernel.cuh",
            "prefill_tc_kernel.cuh", "prefill_tc2_kernel.cuh", "prefill_tc256_kernel.cuh", "ptx.cuh", "plan.h",

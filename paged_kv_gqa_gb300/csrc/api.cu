@@ -32,6 +32,8 @@ bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
 std::atomic<int> g_prefill_tc{PKV_TC_AUTO};
 std::atomic<int> g_cluster_merge{1};
 bool cluster_merge_enabled() { return g_cluster_merge.load(std::memory_order_relaxed) != 0; }
+std::atomic<int> g_adaptive_splits{0};
+bool adaptive_splits_enabled() { return g_adaptive_splits.load(std::memory_order_relaxed) != 0; }
 
 namespace {
 
@@ -45,6 +47,10 @@ constexpr int kMqBlockRows = 32;
 constexpr long kTcShortGroupKeys = 8192;
 // Largest batch whose decode blocks rank the sequence lengths themselves (longest first).
 constexpr int kLongestFirstMaxB = 128;
+// Largest batch whose decode sizes its splits from the actual lengths on the device (every
+// block reads the B lengths: 8 loads a thread at most).
+constexpr int kAdaptMaxB = 1024;
+constexpr long kAdaptMinSplitBytes = 512l << 10;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -462,6 +468,20 @@ pkv_status decode_impl(const pkv_bf16 *q, const void *k_cache, const void *v_cac
     // B^2 / threads comparisons, so only for batches of at most kLongestFirstMaxB).
     p.longest_first = ((long)plan.grid_blocks > (long)sms * plan.blocks_per_sm && B > 1 &&
                        B <= kLongestFirstMaxB) ? 1 : 0;
+    // Decode with the automatic split count, when switched on (pkv_set_adaptive_splits): the
+    // kernel sizes the splits from the batch's actual lengths (a block reads every length, so only
+    // for batches of at most kAdaptMaxB), never below kAdaptMinSplitBytes of cache bytes
+    // (measured on GB300: shorter splits of short sequences cost more in start-up and merge than
+    // they gain) or kMinSplitTokens keys; where the planned chunk is no larger there is nothing to
+    // adapt.
+    {
+        const long token_bytes = kv8 ? 2l * D + 8 : 4l * D;
+        const long min_tokens = std::max<long>(kMinSplitTokens, kAdaptMinSplitBytes / token_bytes);
+        p.min_chunk = (int)((min_tokens + plan.stage_tokens - 1) / plan.stage_tokens * plan.stage_tokens);
+    }
+    const bool adapt = adaptive_splits_enabled() && !mq && num_splits == 0 && plan.num_splits > 1 &&
+                       B <= kAdaptMaxB && plan.chunk_tokens > p.min_chunk;
+    p.adapt_slots = adapt ? split_slots(sms, plan.blocks_per_sm, kv8) : 0;
 
     p.scale_log2 = (float)((double)scale * 1.4426950408889634074);
     p.wait_limit_ns = kWaitLimitNs;
@@ -477,6 +497,9 @@ pkv_status decode_impl(const pkv_bf16 *q, const void *k_cache, const void *v_cac
     if (mq || plan.q_tiles > 1)
         return kv8 ? launch_prefill_fp8(D, NT, mk, mv, p, plan, B, Hkv, device, stream)
                    : launch_prefill_bf16(D, NT, mk, mv, p, plan, B, Hkv, device, stream);
+    if (p.adapt_slots > 0)
+        return kv8 ? launch_decode_adapt_fp8(D, NT, mk, mv, p, plan, B, Hkv, device, stream)
+                   : launch_decode_adapt_bf16(D, NT, mk, mv, p, plan, B, Hkv, device, stream);
     return kv8 ? launch_decode_fp8(D, NT, mk, mv, p, plan, B, Hkv, device, stream)
                : launch_decode_bf16(D, NT, mk, mv, p, plan, B, Hkv, device, stream);
 }
@@ -531,6 +554,8 @@ int pkv_version(void) { return 100; }
 int pkv_set_programmatic_launch(int enable) { return g_pdl.exchange(enable ? 1 : 0); }
 
 int pkv_set_cluster_merge(int enable) { return g_cluster_merge.exchange(enable ? 1 : 0); }
+
+int pkv_set_adaptive_splits(int enable) { return g_adaptive_splits.exchange(enable ? 1 : 0); }
 
 int pkv_set_prefill_tensor_cores(int mode)
 {

@@ -119,6 +119,10 @@ struct DecodeParams {
                              // cluster and split 0 merges the partials in its shared memory
     int longest_first;       // 1 (grids of several waves, B <= kLongestFirstMaxB): grid row z
                              // serves the z-th longest sequence
+    int adapt_slots;         // > 0 (decode, automatic split count): the keys per split come from
+                             // the batch's lengths, about one block per slot (this many) over
+                             // its keys; chunk_tokens is then the largest chunk
+    int min_chunk;           // the smallest adaptive chunk (a multiple of the stage keys)
 
     float scale_log2;        // scale * log2(e)
     unsigned long long wait_limit_ns;
@@ -244,7 +248,7 @@ __device__ __forceinline__ void merge_write(__nv_bfloat16 *out_row, float *lse_r
     if (d == 0 && lse_row) *lse_row = m == ninf ? ninf : m + __logf(wsum);
 }
 
-template <int D, int NT, bool KV8, bool MQ>
+template <int D, int NT, bool KV8, bool MQ, bool ADAPT>
 __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
     decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const DecodeParams p)
@@ -299,14 +303,97 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
     }
     griddep_wait();
 
-    // ---- which sequence: longest first on grids of several waves ---------------
-    // Blocks are dispatched in index order as slots free up, so grid row z takes the z-th
-    // longest sequence (ties by index): the blocks of whole chunks start first and the short
-    // ones fill the last wave, instead of a long sequence's blocks starting last and running
-    // alone at the end.  The ranks are computed in the ring, before any copy lands there.
+    // ---- one pass over the batch's lengths (in the ring, before any copy lands there) ----
+    // Which sequence: on grids of several waves grid row z takes the z-th longest sequence (ties
+    // by index), so that the blocks of whole chunks start first and the short ones fill the last
+    // wave, instead of a long sequence's blocks starting last and running alone at the end.
+    // Adaptive split count (decode, automatic split count): the plan sizes the splits for
+    // sequences of the table's full width; from the batch's actual lengths every block takes
+    // chunks of about (total keys x Hkv / slots) keys, at least min_chunk, at most the planned
+    // chunk, and enough that no sequence needs more than the planned splits (Atlas "CUDA Kernel
+    // Engineering", "The kernel inventory": adaptive split count).  Every block computes the same
+    // value from the same lengths, so the splits of a group agree on their count.  An invalid
+    // length counts as empty.
     const int Lmax = p.max_pages * p.P;
     int b = (int)blockIdx.z;
-    if (p.longest_first) {
+    int chunk = p.chunk_tokens;
+    bool have_L = false;
+    int L_raw = 0;
+    if constexpr (ADAPT) {  // the adaptive instantiation (decode only) always takes this pass
+        constexpr bool adapt = !MQ;
+        int *lens = reinterpret_cast<int *>(base);        // [B <= 1024] raw lengths (longest first)
+        int *pick = reinterpret_cast<int *>(base + 4096);
+        int *own = pick + 1;                                // the raw length of sequence blockIdx.z
+        long long *wsum = reinterpret_cast<long long *>(base + 4104);
+        int *wmax = reinterpret_cast<int *>(base + 4104 + W * 8);
+        long long lsum = 0;
+        int lmax = 0;
+        for (int i = threadIdx.x; i < p.B; i += W * 32) {
+            const int li = p.seq_lens[i];
+            const int v = (li < 0 || li > Lmax) ? 0 : li;
+            if (p.longest_first) lens[i] = li;
+            if (i == b) *own = li;
+            lsum += v;
+            lmax = max(lmax, v);
+        }
+        __syncthreads();
+        if (adapt && !p.longest_first) {
+            // A later split that starts past the sequence even at the smallest chunk the rule below
+            // can give (min_chunk, or the planned chunk where that is smaller) has nothing to do.
+            // It must not leave unless it is empty at the chunk every block computes: split 0 of a
+            // cluster signals every non-empty split's shared memory.
+            const int own_len = *own, own_v = (own_len < 0 || own_len > Lmax) ? 0 : own_len;
+            const int lo = min(p.min_chunk, p.chunk_tokens);
+            if (c > 0 && (long long)c * lo >= own_v) return;
+        }
+        if (adapt) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+                lmax = max(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+            }
+            if (lane == 0) {
+                wsum[warp] = lsum;
+                wmax[warp] = lmax;
+            }
+            __syncthreads();
+            if (threadIdx.x == 0) {  // one thread divides; the others read the result
+                lsum = 0;
+                lmax = 0;
+#pragma unroll
+                for (int w = 0; w < W; ++w) {
+                    lsum += wsum[w];
+                    lmax = max(lmax, wmax[w]);
+                }
+                long long cc = (lsum * p.Hkv + p.adapt_slots - 1) / p.adapt_slots;
+                cc = max(cc, (long long)(lmax + p.num_splits - 1) / p.num_splits);
+                cc = max(cc, (long long)p.min_chunk);
+                cc = (cc + T - 1) / T * T;
+                *pick = (int)min(cc, (long long)p.chunk_tokens);
+            }
+            __syncthreads();
+            chunk = *pick;
+            __syncthreads();  // pick is reused by the ranking below
+        }
+        if (p.longest_first) {
+            for (int i = threadIdx.x; i < p.B; i += W * 32) {
+                const int ri = lens[i], li = (ri < 0 || ri > Lmax) ? 0 : ri;
+                int rank = 0;
+                for (int j = 0; j < p.B; ++j) {
+                    const int rj = lens[j], lj = (rj < 0 || rj > Lmax) ? 0 : rj;
+                    rank += (lj > li || (lj == li && j < i)) ? 1 : 0;
+                }
+                if (rank == (int)blockIdx.z) *pick = i;
+            }
+            __syncthreads();
+            b = *pick;
+            L_raw = lens[b];
+        } else {
+            L_raw = *own;
+        }
+        have_L = true;
+        __syncthreads();  // the ring is free again before the first copies
+    } else if (p.longest_first) {
         int *lens = reinterpret_cast<int *>(base);
         int *pick = lens + p.B;
         for (int i = threadIdx.x; i < p.B; i += W * 32) {
@@ -329,7 +416,7 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
     }
 
     // ---- length, split range ------------------------------------------------
-    int L = p.seq_lens[b];
+    int L = have_L ? L_raw : p.seq_lens[b];
     if (L < 0 || L > Lmax) {  // invalid length: the sequence is treated as empty
         if (threadIdx.x == 0 && c == 0 && kvh == 0) record_status(p.status, PKV_ERR_BAD_SEQ_LEN);
         L = 0;
@@ -363,7 +450,6 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
     // MQ with the causal mask: the last key block row r sees (keys past it get -inf)
     auto key_limit = [&](int r) -> int { return (MQ && p.causal) ? L - n_q + (row_begin + r) / G : L - 1; };
 
-    const int chunk = p.chunk_tokens;
     const int tok_begin = c * chunk;
     if (c > 0 && tok_begin >= L) return;  // empty split: the merge never reads it
     if (L == 0) {                          // empty sequence: out = 0, lse = -inf

@@ -21,18 +21,20 @@ namespace pkv {
                     const pkv_plan &plan, int B, int Hkv, int device, cudaStream_t stream);
 PKV_DECLARE_LAUNCH(launch_decode_bf16)
 PKV_DECLARE_LAUNCH(launch_decode_fp8)
+PKV_DECLARE_LAUNCH(launch_decode_adapt_bf16)
+PKV_DECLARE_LAUNCH(launch_decode_adapt_fp8)
 PKV_DECLARE_LAUNCH(launch_prefill_bf16)
 PKV_DECLARE_LAUNCH(launch_prefill_fp8)
 #undef PKV_DECLARE_LAUNCH
 
-template <int D, int NT, bool KV8, bool MQ>
+template <int D, int NT, bool KV8, bool MQ, bool ADAPT>
 pkv_status launch_decode_variant(const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
                                  const pkv_plan &plan, int B, int Hkv, int device, cudaStream_t stream)
 {
     static bool attr_set[64] = {};
     static int8_t cluster_ok[64][kMaxClusterSplits + 1] = {};  // 0 unknown, 1 resident, -1 not
     static std::mutex mu;
-    auto kern = decode_split_kernel<D, NT, KV8, MQ>;
+    auto kern = decode_split_kernel<D, NT, KV8, MQ, ADAPT>;
     if (device < 0 || device >= 64) return PKV_ERR_UNSUPPORTED;
     dim3 grid(Hkv * plan.q_tiles, plan.num_splits, B);
     dim3 block(plan.warps * 32);
@@ -65,17 +67,17 @@ pkv_status launch_decode_variant(const CUtensorMap &mk, const CUtensorMap &mv, c
 }
 
 // (a D = 256 block serves at most 16 rows: no 32-row variant there)
-#define PKV_V(DD, NN, KV8, MQ) launch_decode_variant<DD, NN, KV8, MQ>(mk, mv, p, plan, B, Hkv, device, stream)
-#define PKV_DECODE_DISPATCH(KV8, MQ)                         \
+#define PKV_V(DD, NN, KV8, MQ, AD) launch_decode_variant<DD, NN, KV8, MQ, AD>(mk, mv, p, plan, B, Hkv, device, stream)
+#define PKV_DECODE_DISPATCH(KV8, MQ, AD)                     \
     switch (D * 8 + NT) {                                    \
-        case 64 * 8 + 1: return PKV_V(64, 1, KV8, MQ);       \
-        case 64 * 8 + 2: return PKV_V(64, 2, KV8, MQ);       \
-        case 64 * 8 + 4: return PKV_V(64, 4, KV8, MQ);       \
-        case 128 * 8 + 1: return PKV_V(128, 1, KV8, MQ);     \
-        case 128 * 8 + 2: return PKV_V(128, 2, KV8, MQ);     \
-        case 128 * 8 + 4: return PKV_V(128, 4, KV8, MQ);     \
-        case 256 * 8 + 1: return PKV_V(256, 1, KV8, MQ);     \
-        case 256 * 8 + 2: return PKV_V(256, 2, KV8, MQ);     \
+        case 64 * 8 + 1: return PKV_V(64, 1, KV8, MQ, AD);       \
+        case 64 * 8 + 2: return PKV_V(64, 2, KV8, MQ, AD);       \
+        case 64 * 8 + 4: return PKV_V(64, 4, KV8, MQ, AD);       \
+        case 128 * 8 + 1: return PKV_V(128, 1, KV8, MQ, AD);     \
+        case 128 * 8 + 2: return PKV_V(128, 2, KV8, MQ, AD);     \
+        case 128 * 8 + 4: return PKV_V(128, 4, KV8, MQ, AD);     \
+        case 256 * 8 + 1: return PKV_V(256, 1, KV8, MQ, AD);     \
+        case 256 * 8 + 2: return PKV_V(256, 2, KV8, MQ, AD);     \
         default: return PKV_ERR_UNSUPPORTED;                 \
     }
 

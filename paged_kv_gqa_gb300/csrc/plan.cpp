@@ -26,7 +26,6 @@ namespace pkv {
 
 namespace {
 constexpr long kMaxSplitBytes = 2l << 20;  // cache bytes of one (b, kv head) split
-constexpr int kMinSplitTokens = 256;
 constexpr int kSmemPerSm = 233472;          // 228 KiB per SM on sm_100-class parts
 constexpr int kSmemPerBlockMax = 232448;    // 227 KiB opt-in maximum per block
 constexpr int kBlockReserve = 1024;         // shared memory the system reserves per block
@@ -104,7 +103,7 @@ pkv_status make_plan(int B, int Hq, int Hkv, int D, int page_size, int max_pages
     // twice the bytes per key, and fewer, longer splits amortise their start-up better
     // (measured on GB300: the batch workload runs fastest at 4-5 splits with three
     // blocks resident, at 8 with the fp8 cache).
-    const int slots = num_sms * (kv8 ? per_sm : std::min(per_sm, 2));
+    const int slots = split_slots(num_sms, per_sm, kv8);
 
     const int max_stage_splits = (max_tokens + t.T - 1) / t.T;
     int S;

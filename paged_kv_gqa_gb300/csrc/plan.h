@@ -35,6 +35,16 @@ RuntimeTiling tiling_for(int D);
 // Number of 8-wide head tiles (mma N tiles) for group size G.
 inline int head_tiles(int G) { return G <= 8 ? 1 : (G <= 16 ? 2 : 4); }
 
+// Fewest keys a split takes (the plan's rule, and the device's adaptive chunk).
+constexpr int kMinSplitTokens = 256;
+
+// The block slots the one-wave split rule counts: every resident block for the fp8 cache, at
+// most two per SM for a bf16 cache (fewer, longer splits amortise a block's start-up better).
+PKV_HD int split_slots(int num_sms, int blocks_per_sm, bool kv8)
+{
+    return num_sms * (kv8 ? blocks_per_sm : (blocks_per_sm < 2 ? blocks_per_sm : 2));
+}
+
 // Most (token, head) rows one decode block serves: 32, or 16 at D = 256, where the 32-row
 // variant's accumulators and query fragments exceed the register file and spill (measured:
 // ~2.6 KB of spills a thread, 9x slower than two 16-row blocks).

@@ -7,7 +7,7 @@ namespace pkv {
 pkv_status launch_prefill_bf16(int D, int NT, const CUtensorMap &mk, const CUtensorMap &mv, const DecodeParams &p,
                                const pkv_plan &plan, int B, int Hkv, int device, cudaStream_t stream)
 {
-    PKV_DECODE_DISPATCH(false, true)
+    PKV_DECODE_DISPATCH(false, true, false)
 }
 
 }  // namespace pkv

@@ -242,3 +242,43 @@ def test_cluster_merge_equals_workspace_merge(case_args, splits):
     assert torch.equal(a_lse.view(torch.int32), b_lse.view(torch.int32))
     eo, el = compare_with_oracle(case, a_out, a_lse, select=sample_rows(case, 12))
     assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+
+
+@pytest.mark.parametrize("adaptive", [True, False])
+@pytest.mark.parametrize("lens", [[2048, 1500, 3000, 77], [1, 0, 40000, 9], [3000, 40, 2000, 70000]])
+def test_adaptive_split_count_on_a_wide_table(lens, adaptive):
+    """A block table far wider than the batch's sequences (a pool sized for long contexts): the plan
+    sizes its splits for the full width; with the adaptive split count the kernel re-sizes them
+    from the actual lengths (more, shorter splits).  Against the oracle in full, and against one
+    split (the straddle check)."""
+    case = make_case(_spec(4, 64, 8, 128, 16, seed=61, max_pages=8192), seq_lens=lens, poison=True, device="cuda")
+    plan = pkv.plan_query(case.B, case.Hq, case.Hkv, case.D, case.P, case.max_pages,
+                          torch.cuda.get_device_properties(0).multi_processor_count)
+    assert plan["num_splits"] > 1 and plan["chunk_tokens"] > 2048, plan
+    prev = pkv.set_adaptive_splits(adaptive)
+    try:
+        out, lse = run_gpu(case)
+        out2, _ = run_gpu(case)  # the merge counters return to 0
+    finally:
+        pkv.set_adaptive_splits(prev)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    eo, el = compare_with_oracle(case, out, lse)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+    one_o, one_l = run_gpu(case, num_splits=1)
+    split_straddle_check(out.float().cpu().numpy(), one_o.float().cpu().numpy(), decode_oracle_rows(case))
+    assert max_abs_diff(lse.cpu().numpy(), one_l.cpu().numpy()) <= SPLIT_TOL
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,D,P,lens", SMALL, ids=lambda x: str(x).replace(" ", ""))
+def test_small_cases_with_adaptive_splits(B, Hq, Hkv, D, P, lens):
+    """The small cases again with the adaptive split count switched on (tables wider than the
+    longest sequence where the shape allows), against the oracle in full."""
+    case = make_case(_spec(B, Hq, Hkv, D, P, seed=B * 7 + D, max_pages=max(1, 2 * max(lens) // P + 3)),
+                     seq_lens=lens, poison=True)
+    prev = pkv.set_adaptive_splits(True)
+    try:
+        out, lse = run_gpu(case)
+    finally:
+        pkv.set_adaptive_splits(prev)
+    eo, el = compare_with_oracle(case, out, lse)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
