@@ -17,7 +17,8 @@ import torch
 import oracle
 import paged_kv_gqa_gb300 as pkv
 from paged_kv_gqa_gb300 import _build
-from gpu_util import LSE_TOL, OUT_TOL, max_abs_diff, run_gpu, sample_rows, split_invariance_violation
+from gpu_util import (LSE_TOL, OUT_TOL, SPLIT_TOL, max_abs_diff, run_gpu, sample_rows, split_invariance_violation,
+                      split_straddle_check)
 from test_parity import SMALL
 from workloads import CONFIG_ORDER, Case, bf16_bits, bits_to_bf16, make_case, used_slot_mask
 
@@ -332,3 +333,55 @@ def test_fp8_group_32_at_head_dim_256():
         out, lse = run_fp8(case, pools, num_splits=splits)
         eo, el = compare_fp8_with_oracle(case, pools, out, lse)
         assert eo <= OUT_TOL and el <= LSE_TOL, (splits, eo, el)
+
+
+@pytest.mark.parametrize("lens", [[2048, 1500, 3000, 77], [1, 0, 40000, 9], [3000, 40, 2000, 70000]])
+def test_fp8_adaptive_split_count_on_a_wide_table(lens):
+    """The fp8 cache under the adaptive split count, on a block table far wider than the batch's
+    sequences: against the fp8 oracle in full, repeatable bit for bit (the merge counters return
+    to zero), and held to the split-count bar against one split."""
+    case = make_case(_spec(4, 64, 8, 128, 16, seed=67, max_pages=8192), seq_lens=lens, poison=True)
+    pools = Fp8Pools(case)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = pkv.plan_query(case.B, case.Hq, case.Hkv, case.D, case.P, case.max_pages, sms, cache="fp8")
+    assert plan["num_splits"] > 1 and plan["chunk_tokens"] > 2048, plan
+    prev = pkv.set_adaptive_splits(True)
+    try:
+        out, lse = run_fp8(case, pools)
+        out2, lse2 = run_fp8(case, pools)
+    finally:
+        pkv.set_adaptive_splits(prev)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32))
+    eo, el = compare_fp8_with_oracle(case, pools, out, lse)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+    one_o, one_l = run_fp8(case, pools, num_splits=1)
+    q, _, _, bt, sl = case.host_bits()
+    rows = lambda idx: oracle.paged_decode_fp8(q, pools.k8, pools.v8, pools.ks, pools.vs, bt, sl, case.scale,
+                                               select=[tuple(r) for r in idx])[0]
+    split_straddle_check(out.float().cpu().numpy(), one_o.float().cpu().numpy(), rows)
+    assert max_abs_diff(lse.cpu().numpy(), one_l.cpu().numpy()) <= SPLIT_TOL
+
+
+@pytest.mark.parametrize("name", ["ragged", "long"])
+def test_fp8_workloads_with_adaptive_splits(name):
+    """Full-size workloads on the fp8 cache with the adaptive split count on: sampled rows against
+    the fp8 oracle and the split-count bar against the planned split."""
+    case = make_case(name)
+    pools = Fp8Pools(case, poison_scales=False)
+    dcase = case.to("cuda")
+    base_o, base_l = run_fp8(dcase, pools)
+    prev = pkv.set_adaptive_splits(True)
+    try:
+        out, lse = run_fp8(dcase, pools)
+    finally:
+        pkv.set_adaptive_splits(prev)
+    eo, el = compare_fp8_with_oracle(case, pools, out, lse, select=sample_rows(case, n=16, seed=6))
+    assert eo <= OUT_TOL and el <= LSE_TOL, (name, eo, el)
+    assert max_abs_diff(lse.cpu().numpy(), base_l.cpu().numpy()) <= SPLIT_TOL
+    q, _, _, bt, sl = case.host_bits()
+    rows = lambda idx: oracle.paged_decode_fp8(q, pools.k8, pools.v8, pools.ks, pools.vs, bt, sl, case.scale,
+                                               select=[tuple(r) for r in idx])[0]
+    split_straddle_check(out.float().cpu().numpy(), base_o.float().cpu().numpy(), rows)
+    del case, dcase, pools, out, lse, base_o, base_l
+    torch.cuda.empty_cache()

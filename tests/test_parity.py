@@ -269,6 +269,26 @@ def test_adaptive_split_count_on_a_wide_table(lens, adaptive):
     assert max_abs_diff(lse.cpu().numpy(), one_l.cpu().numpy()) <= SPLIT_TOL
 
 
+@pytest.mark.parametrize("name", ["batch", "ragged", "long"])
+def test_workloads_with_adaptive_splits(name):
+    """The full-size workloads with the adaptive split count switched on: sampled rows against the
+    oracle, and the whole output held to the split-count bar against the planned split (the two
+    calls differ at most in where the splits end, which only reorders the f32 sums)."""
+    case = make_case(name, device="cuda")
+    base_o, base_l = run_gpu(case)
+    prev = pkv.set_adaptive_splits(True)
+    try:
+        out, lse = run_gpu(case)
+    finally:
+        pkv.set_adaptive_splits(prev)
+    eo, el = compare_with_oracle(case, out, lse, select=sample_rows(case, n=16, seed=5))
+    assert eo <= OUT_TOL and el <= LSE_TOL, (name, eo, el)
+    assert max_abs_diff(lse.cpu().numpy(), base_l.cpu().numpy()) <= SPLIT_TOL
+    split_straddle_check(out.float().cpu().numpy(), base_o.float().cpu().numpy(), decode_oracle_rows(case))
+    del case, out, lse, base_o, base_l
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("B,Hq,Hkv,D,P,lens", SMALL, ids=lambda x: str(x).replace(" ", ""))
 def test_small_cases_with_adaptive_splits(B, Hq, Hkv, D, P, lens):
     """The small cases again with the adaptive split count switched on (tables wider than the

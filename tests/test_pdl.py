@@ -32,8 +32,11 @@ class Step:
     """One decode iteration on the batch shape: write each sequence's newest key and value
     (the last slot of its length), then attend over all its keys."""
 
-    def __init__(self, cache, seed):
-        c = make_case(dict(B=8, Hq=32, Hkv=8, D=128, P=16, lens=("uniform", 200, 3000), seed=seed), device="cuda")
+    def __init__(self, cache, seed, max_pages=None):
+        spec = dict(B=8, Hq=32, Hkv=8, D=128, P=16, lens=("uniform", 200, 3000), seed=seed)
+        if max_pages is not None:  # a table wider than the sequences (a pool sized for long contexts)
+            spec["max_pages"] = max_pages
+        c = make_case(spec, device="cuda")
         self.c = c
         self.cache = cache
         g = torch.Generator(device="cuda")
@@ -144,5 +147,48 @@ def test_pdl_inside_a_cuda_graph(cache):
         assert torch.equal(st.out.view(torch.int16), ref_o.view(torch.int16))
         assert torch.equal(st.lse.view(torch.int32), ref_l.view(torch.int32))
     pkv.set_programmatic_launch(False)
+    assert pkv.pkv_check_status(st.ws) == 0
+    assert_steps_match_oracle(st)
+
+
+@pytest.mark.parametrize("cache", ["bf16", "fp8"])
+def test_adaptive_splits_under_pdl_and_graph(cache):
+    """The adaptive split count (each block reads every length before it sizes the splits) on a
+    table far wider than the sequences, with PDL eagerly and inside a graph: equal bit for bit to
+    the serialised launches of the same mode, and held to the oracle."""
+    st = Step(cache, seed=13, max_pages=4096)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    c = st.c
+    plan = pkv.plan_query(c.B, c.Hq, c.Hkv, c.D, c.P, c.max_pages, sms, cache=cache)
+    assert plan["num_splits"] > 1 and plan["chunk_tokens"] > 2048, plan
+    prev = pkv.set_adaptive_splits(True)
+    try:
+        pkv.set_programmatic_launch(False)
+        st.reset()
+        st.run()
+        torch.cuda.synchronize()
+        ref_o, ref_l = st.out.clone(), st.lse.clone()
+        pkv.set_programmatic_launch(True)
+        st.reset()
+        st.run()
+        torch.cuda.synchronize()
+        assert torch.equal(st.out.view(torch.int16), ref_o.view(torch.int16))
+        assert torch.equal(st.lse.view(torch.int32), ref_l.view(torch.int32))
+        st.reset()
+        s = torch.cuda.Stream()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            st.run(stream=s)
+        for _ in range(2):
+            st.reset()
+            torch.cuda.synchronize()
+            graph.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(st.out.view(torch.int16), ref_o.view(torch.int16))
+            assert torch.equal(st.lse.view(torch.int32), ref_l.view(torch.int32))
+    finally:
+        pkv.set_programmatic_launch(False)
+        pkv.set_adaptive_splits(prev)
     assert pkv.pkv_check_status(st.ws) == 0
     assert_steps_match_oracle(st)
