@@ -4,7 +4,8 @@ Each case targets a place where a plausible kernel mistake would hide from the
 workload tests: a sharply peaked softmax (running maxima that jump by tens of
 units, deferred rescaling on the tensor-core path), a zero or negative scale
 (uniform and inverted weights), the largest group size at the largest head
-dimension, and a forced single split longer than one block's block-table slice.
+dimension, a forced single split longer than one block's block-table slice, and the
+largest sizes the entry points take (65535 sequences, G = 32 with 256-key pages).
 Bars as everywhere: max |out - oracle| <= 1.5e-2, max |lse - oracle| <= 1e-3.
 """
 import math
@@ -124,3 +125,37 @@ def test_peaked_softmax_several_rows(mode):
                                   k_bits=k, v_bits=v)
     o, l = out.float().cpu().numpy(), lse.cpu().numpy()
     assert np.abs(o - ro).max() <= OUT_TOL and np.abs(l - rl).max() <= LSE_TOL
+
+
+# The largest sizes the entry points take: 65535 sequences (the grid's z dimension), the
+# largest group (G = 32) at the largest head dimension and page size.
+MAXIMUM = [
+    # B, Hq, Hkv, D, P, lens
+    (65535, 4, 1, 64, 8, [(7 * i) % 23 for i in range(65535)]),
+    (1, 32, 1, 256, 256, [6000]),
+    (2, 32, 1, 128, 256, [20000, 1]),
+]
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,D,P,lens", MAXIMUM, ids=["B65535", "G32-D256-P256", "G32-D128-P256"])
+def test_maximum_sizes(B, Hq, Hkv, D, P, lens):
+    case = make_case(_spec(B, Hq, Hkv, D, P, seed=B % 1000 + D), seq_lens=lens, poison=True)
+    out, lse = run_gpu(case)
+    eo, el = compare_with_oracle(case, out, lse)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+    assert torch.isfinite(out.float()).all()
+
+
+def test_batch_past_the_grid_limit_is_rejected():
+    """65536 sequences: refused on the host with PKV_ERR_UNSUPPORTED before any launch (the
+    outputs keep their sentinel)."""
+    case = make_case(_spec(65536, 4, 1, 64, 8, seed=3), seq_lens=[1] * 65536).to("cuda")
+    ws = torch.zeros(1 << 20, dtype=torch.uint8, device="cuda")
+    out = torch.full((case.B, case.Hq, case.D), 7.0, dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((case.B, case.Hq), 7.0, dtype=torch.float32, device="cuda")
+    with pytest.raises(pkv.PkvError) as err:
+        pkv.paged_decode_attn(case.q, case.k_cache, case.v_cache, case.block_table, case.seq_lens, case.scale, out,
+                              lse, ws)
+    assert err.value.status == -2
+    torch.cuda.synchronize()
+    assert bool((out.float() == 7.0).all()) and bool((lse == 7.0).all())

@@ -385,3 +385,16 @@ def test_fp8_workloads_with_adaptive_splits(name):
     split_straddle_check(out.float().cpu().numpy(), base_o.float().cpu().numpy(), rows)
     del case, dcase, pools, out, lse, base_o, base_l
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("idx", [0, 1, 2], ids=["B65535", "G32-D256-P256", "G32-D128-P256"])
+def test_fp8_maximum_sizes(idx):
+    """The largest sizes the entry points take, on the fp8 cache, against the fp8 oracle in full."""
+    from test_edges import MAXIMUM
+    B, Hq, Hkv, D, P, lens = MAXIMUM[idx]
+    case = make_case(_spec(B, Hq, Hkv, D, P, seed=B % 997 + D), seq_lens=lens, poison=True)
+    pools = Fp8Pools(case)
+    out, lse = run_fp8(case, pools)
+    eo, el = compare_fp8_with_oracle(case, pools, out, lse)
+    assert eo <= OUT_TOL and el <= LSE_TOL, (eo, el)
+    assert torch.isfinite(out.float()).all()

@@ -45,7 +45,7 @@ SMALL = [
     (2, 32, 16, 64, 256, [600, 255]),
     (1, 4, 1, 256, 8, [1000]),
     (2, 24, 8, 128, 16, [100, 33]),   # G = 3 (padded head tile)
-    (300, 8, 2, 128, 16, [(7 * i) % 97 for i in range(300)]),  # more sequences than one launch takes
+    (300, 8, 2, 128, 16, [(7 * i) % 97 for i in range(300)]),  # more sequences than the longest-first order ranks (128)
 ]
 
 
