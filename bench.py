@@ -353,11 +353,13 @@ _REFERENCE_RUN_SECONDS = 150.0
 
 def _oracle_thread_rate(case, run_rows) -> float:
     """fp64 flops a second of one oracle thread on this host: one row of the longest sequence,
-    repeated for at least 20 ms (a warm-up as well)."""
+    once untimed (a warm-up: the first pass over the inputs runs slower), then repeated for at
+    least 20 ms."""
     import numpy as np
     lens = case.seq_lens.cpu().numpy().astype(np.int64)
     b = int(np.argmax(lens))
     flops = max(1, int(lens[b])) * case.D * 4.0
+    run_rows([(b, 0)])
     n, t = 0, 0.0
     while t < 0.02 or n == 0:
         t0 = time.perf_counter()
@@ -371,12 +373,15 @@ def _reference_sample(case, seconds, rate):
     """Rows (b, h) for a bounded CPU sample: the first n of a head-major order (head 0 of every
     sequence, then head 1, ...), n as large as keeps one oracle pass within `seconds` on this
     host's cores at `rate` fp64 flops a second per thread (the oracle's threads take the rows by
-    a fixed stride), and at least one row.  Returns (rows, description, threads used)."""
+    a fixed stride), and at least one row.  Where one row alone takes longer than `seconds`, the
+    pass may take as long as that row (the other threads take rows beside it in the same time).
+    Returns (rows, description, threads used)."""
     import numpy as np
     lens = case.seq_lens.cpu().numpy().astype(np.int64)
     order = [(b, h) for h in range(case.Hq) for b in range(case.B)]
     cost = np.array([lens[b] * case.D * 4.0 / rate for b, _ in order])
     cores = os.cpu_count() or 1
+    budget = max(seconds, float(cost[0]))
 
     def pass_seconds(n):
         t = min(cores, n)
@@ -385,7 +390,7 @@ def _reference_sample(case, seconds, rate):
     lo, hi = 1, len(order)
     while lo < hi:  # the largest n whose pass fits (pass time grows with n)
         mid = (lo + hi + 1) // 2
-        if pass_seconds(mid) <= seconds:
+        if pass_seconds(mid) <= budget:
             lo = mid
         else:
             hi = mid - 1
