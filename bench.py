@@ -93,16 +93,24 @@ def _kernel_name(tc_rows: int, fp8: bool, q_len: int, D: int = 128) -> str:
 
 
 def _roofline(args, case, q_len, fp8, tc_rows, peaks, gbs, mean_ms) -> dict:
-    """The roofline of the call's one kernel: the tensor cores for the tcgen05 kernels (causal
-    FLOPs over the measured bf16 peak), HBM bandwidth for the decode kernel (algorithmic bytes
-    over the measured copy bandwidth).  DRAM traffic comes from the committed ncu summary of
-    the same kernel and workload, taken on the current source, else null."""
+    """The roofline of the call's one kernel.  The decode kernel: HBM bandwidth (algorithmic
+    bytes over the measured copy bandwidth).  The tcgen05 kernels: whichever roof takes longer
+    at its peak, the tensor cores (causal FLOPs over the measured bf16 peak) or HBM (a long
+    table with few rows per group streams more bytes than the products take); the other roof's
+    fraction rides along under "secondary".  DRAM traffic comes from the committed ncu summary
+    of the same kernel and workload, taken on the current source, else null."""
     name = _kernel_name(tc_rows, fp8, q_len, case.D)
     if tc_rows:
-        tflops = causal_flops(case) / (mean_ms * 1e-3) / 1e12
-        return {"bound": "tensor", "achieved": round(tflops, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(tflops / peaks["bf16_tflops"], 4), "traffic": None, "kernel": name,
-                "peak_source": peaks["source"]}
+        flops = causal_flops(case)
+        tflops = flops / (mean_ms * 1e-3) / 1e12
+        tensor = {"bound": "tensor", "achieved": round(tflops, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                  "frac": round(tflops / peaks["bf16_tflops"], 4)}
+        hbm = {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+               "frac": round(gbs / peaks["hbm_gbs"], 4)}
+        t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
+        t_hbm = gbs * mean_ms * 1e-3 * 1e9 / (peaks["hbm_gbs"] * 1e9)  # algorithmic bytes at the HBM peak
+        main, other = (hbm, tensor) if t_hbm > t_tensor else (tensor, hbm)
+        return dict(main, traffic=None, kernel=name, peak_source=peaks["source"], secondary=other)
     traffic = profiled_traffic(profile_name(args.workload, args.cache)) if q_len == 1 else None
     return {"bound": "hbm", "achieved": round(gbs, 2), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(gbs / peaks["hbm_gbs"], 4), "traffic": traffic, "kernel": name,

@@ -78,16 +78,54 @@ def test_reference_arm_line_on_rank_zero(monkeypatch, capsys):
 
 
 def test_reference_sample_fits_its_budget():
-    """Each step's sample fits the per-step budget at the measured rate (at least one row), so
-    that a run of any step count stays within a few minutes."""
+    """Each step's sample fits the per-step budget at the measured rate, or, where the first row
+    alone outlasts it, the time of that row (the other threads take rows beside it), so that a
+    run of any step count stays within a few minutes."""
     from workloads import make_case
     for name in ("tiny", "batch", "ragged"):
         case = make_case(name)
         lens = case.seq_lens.numpy()
         rate = 0.4e9
-        for seconds in (0.01, 0.1, 1.0):
+        for seconds in (0.001, 0.01, 0.1, 1.0):
             rows, _, threads = bench._reference_sample(case, seconds, rate)
             assert 1 <= len(rows) <= case.B * case.Hq and 1 <= threads <= len(rows)
             cost = [lens[b] * case.D * 4.0 / rate for b, _ in rows]
             per_thread = max(sum(cost[i::threads]) for i in range(threads))
-            assert len(rows) == 1 or per_thread <= seconds + 1e-12
+            assert per_thread <= max(seconds, cost[0]) + 1e-12
+
+
+def test_reference_sample_keeps_every_thread_busy_on_long_rows(monkeypatch):
+    """One row of the long-context workload outlasts a short per-step budget: the step still
+    takes one row per host thread (the same wall time as one row), not a single row."""
+    import types
+    import torch
+    monkeypatch.setattr(bench.os, "cpu_count", lambda: 16)
+    # the long-context shape (only the lengths and sizes matter to the sample)
+    case = types.SimpleNamespace(B=4, Hq=64, D=128, seq_lens=torch.full((4,), 131072, dtype=torch.int32))
+    rate = 0.4e9
+    one_row = 131072 * case.D * 4.0 / rate
+    rows, _, threads = bench._reference_sample(case, one_row / 2, rate)
+    assert len(rows) == 16 and threads == 16
+
+
+def test_roofline_picks_the_binding_roof():
+    """A tensor-core call reports the roof that takes longer at its peak: HBM for a long table
+    with few rows per group, the tensor cores for a short table with many."""
+    from workloads import algorithmic_bytes, make_prefill_case
+    peaks = {"hbm_gbs": 6789.6, "bf16_tflops": 1874.7, "source": "measured"}
+
+    class Args:
+        workload, cache = "long", "bf16"
+
+    spec = dict(B=1, Hq=8, Hkv=1, D=128, P=16, lens=("fixed", 1), seed=0)
+    for L, q_len, want in ((65536, 8, "hbm"), (2048, 1024, "tensor")):
+        case = make_prefill_case(spec, [q_len], [L])
+        ms = 1.0
+        gbs = algorithmic_bytes(case)["total"] / (ms * 1e-3) / 1e9
+        r = bench._roofline(Args, case, q_len, False, 128, peaks, gbs, ms)
+        assert r["bound"] == want and r["secondary"]["bound"] != want
+        t_hbm = algorithmic_bytes(case)["total"] / (peaks["hbm_gbs"] * 1e9)
+        t_tensor = bench.causal_flops(case) / (peaks["bf16_tflops"] * 1e12)
+        assert (t_hbm > t_tensor) == (want == "hbm")
+        frac = {r["bound"]: r["frac"], r["secondary"]["bound"]: r["secondary"]["frac"]}
+        assert abs(frac["hbm"] - t_hbm / (ms * 1e-3)) < 1e-3 and abs(frac["tensor"] - t_tensor / (ms * 1e-3)) < 1e-3
