@@ -63,7 +63,8 @@ typedef enum {
     PKV_OK = 0,
     PKV_ERR_INVALID_ARG = -1,         /* null pointer, non-positive size, Hq % Hkv != 0, seq bound */
     PKV_ERR_UNSUPPORTED = -2,         /* D not in {64,128,256}, page_size not a power of two in
-                                         [8,256], group size Hq/Hkv > 32, no sm_103a device */
+                                         [8,256], group size Hq/Hkv > 32, B > 65535 (the
+                                         sequences are a launch dimension), no sm_103a device */
     PKV_ERR_MISALIGNED = -3,          /* a device pointer is not 16-byte aligned */
     PKV_ERR_WORKSPACE_TOO_SMALL = -4, /* workspace_bytes below the size query's answer */
     PKV_ERR_CUDA = -5,                /* a CUDA runtime/driver call failed */
