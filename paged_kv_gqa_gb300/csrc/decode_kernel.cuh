@@ -300,6 +300,16 @@ __global__ void __launch_bounds__(Tiling<D>::W * 32, target_blocks(D, NT, KV8))
     if (threadIdx.x == 0) {
         prefetch_tensor_map(&tmK);
         prefetch_tensor_map(&tmV);
+        // The block's length and the first lines of its block-table slice into L2 now, so that
+        // the table read that depends on the length finds them there.  Safe before the wait: a
+        // line the previous kernel writes later is updated in L2, which serves every later read.
+        if (!ADAPT && !p.longest_first) {
+            prefetch_l2(p.seq_lens + blockIdx.z);
+            const long pg = ((long)blockIdx.y * p.chunk_tokens) >> p.log2P;
+            const int *row = p.block_table + (size_t)blockIdx.z * p.max_pages;
+            if (pg < p.max_pages) prefetch_l2(row + pg);
+            if (pg + 32 < p.max_pages) prefetch_l2(row + pg + 32);
+        }
     }
     griddep_wait();
 
