@@ -50,3 +50,32 @@ def test_algorithmic_bytes_tiny():
     assert ab["kv"] == 2 * 256 * 2 * 64 * 2
     assert ab["total"] == ab["kv"] + 2 * 8 * 64 * 2 + 8 * 4 + 16 * 4 + 4
     assert ab["tail_bytes"] == 0
+
+
+def test_profile_summaries_agree_with_the_workloads():
+    """Every committed ncu summary of the decode kernel names the algorithmic bytes the workload
+    definition gives (recomputed here from the seeded lengths), and its DRAM traffic lies between
+    those bytes and 4% above them (every K/V byte read once)."""
+    import glob
+    import os
+    import re
+    import types
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    paths = sorted(glob.glob(os.path.join(root, "profiles", "decode_split_kernel_*.md")))
+    assert paths
+    for path in paths:
+        tag = os.path.basename(path)[len("decode_split_kernel_"):-len(".md")]
+        cache = "fp8" if tag.endswith("_fp8") else "bf16"
+        name = tag[:-len("_fp8")] if cache == "fp8" else tag
+        spec = CONFIGS[name]
+        lens = draw_seq_lens(spec["lens"], spec["B"], spec["P"], spec["seed"])
+        light = types.SimpleNamespace(B=spec["B"], Hq=spec["Hq"], Hkv=spec["Hkv"], D=spec["D"], P=spec["P"],
+                                      seq_lens=torch.from_numpy(lens), qo_indptr=None)
+        want = algorithmic_bytes(light, cache=cache)["total"]
+        text = open(path).read()
+        got = int(re.search(r"algorithmic bytes per launch: ([\d,]+) B", text).group(1).replace(",", ""))
+        traffic = int(re.search(r"dram_bytes_per_launch: `(\d+)`", text).group(1))
+        assert got == want, (tag, got, want)
+        assert want <= traffic <= 1.04 * want, (tag, traffic / want)
+        assert re.search(r"kernel_source_hash: `[0-9a-f]{16}`", text), tag
